@@ -1,0 +1,221 @@
+/*
+ * proj.h -- C ABI of libproj: weight-bandwidth-bound dense projections on
+ * GB300 (sm_103a).
+ *
+ * The operation (muse_bf16_proj guide, ch. 1, §1.1 "What is computed"):
+ *
+ *     out[i, n] = sum over k of x[i, k] * W[n, k]        (out = x @ W.T, no bias)
+ *
+ * for five fixed layers (§1.1 table):
+ *
+ *     layer      N x K         W dtype   out dtype
+ *     qkv_gate   2304 x 8192   bf16      bf16
+ *     o          8192 x 1024   bf16      bf16
+ *     pooler     4096 x 8192   bf16      bf16
+ *     unpooler   8192 x 4096   bf16      bf16   (only rows 0..1023 at m <= 8)
+ *     router      256 x 8192   fp32      fp32
+ *
+ * Accumulation is in fp32; the dense layers round the fp32 sum to bf16
+ * (round-to-nearest-even) on output.  The router multiplies the bf16 input
+ * (widened exactly to fp32) by its fp32 weights with fp32 fused multiply-adds
+ * (no TF32, no bf16 split of the weights).
+ *
+ * Interface shape (guide ch. 1, §1.6 "Rules that shaped the code"):
+ * prepare(weights) runs once, untimed, and may repack or losslessly recode
+ * W; the timed call is replayed as a CUDA graph, so it branches on shapes
+ * only, performs no host synchronisation, no allocation and no memset, and
+ * caches nothing derived from x.  Split-K bookkeeping is reset on the GPU.
+ *
+ * Threading: a handle is not thread-safe and must not run on two streams
+ * at the same time (its split-K workspace and counters are shared by calls).
+ * Different handles are independent.
+ *
+ * Errors: every call validates its arguments before touching the GPU and
+ * returns a proj_status (or NULL + proj_last_status() for constructors).
+ * A CUDA error raised while enqueuing maps to PROJ_ECUDA.  Nothing aborts
+ * the process and no C++ exception crosses this boundary.
+ */
+#ifndef PROJ_H_
+#define PROJ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque, library-owned state of one prepared layer. */
+typedef struct proj_ctx *proj_handle;
+
+/* A CUDA stream (cudaStream_t / CUstream).  NULL means the legacy default
+ * stream of the calling thread. */
+typedef struct CUstream_st *proj_stream;
+
+enum proj_layer {
+    PROJ_QKV_GATE = 0,
+    PROJ_O = 1,
+    PROJ_POOLER = 2,
+    PROJ_UNPOOLER = 3,
+    PROJ_ROUTER = 4
+};
+
+enum proj_dtype { PROJ_BF16 = 0, PROJ_FP32 = 1 };
+
+enum proj_flags {
+    /* Also keep a lossless 12-bit exponent-window copy of a bf16 W and use
+     * it for the token counts its kernel covers (project report, "Round 5 --
+     * lossless 12-bit compressed weights", "Format"): per weight the raw low
+     * byte plus a 4-bit (sign, 3-bit window code) field; the 8 window values
+     * of the 7 high exponent bits are chosen per matrix to cover the most
+     * weights; weights outside the window are restored exactly from a
+     * per-tile escape list.  Results are bit-identical to the uncompressed
+     * kernel.  If any tile holds more escapes than the format's per-tile
+     * capacity, the encoding is declined and the handle runs uncompressed
+     * (proj_info reports it). */
+    PROJ_ENCODE_EXPWIN12 = 1u << 0
+};
+
+enum proj_status {
+    PROJ_OK = 0,
+    PROJ_EINVAL = 1,        /* bad argument (NULL, wrong shape or dtype, m < 0) */
+    PROJ_EUNSUPPORTED = 2,  /* valid request this build does not serve (m > m_max) */
+    PROJ_EALIGN = 3,        /* a pointer is not 16-byte aligned */
+    PROJ_ENOMEM = 4,        /* device or host allocation failed (prepare only) */
+    PROJ_ECUDA = 5,         /* a CUDA call failed; see proj_last_cuda_error() */
+    PROJ_EDEVICE = 6        /* a kernel reported a fault in its status word */
+};
+
+/* Variant selection for proj_run_ex (testing and tuning). */
+enum proj_variant {
+    PROJ_VARIANT_AUTO = 0,      /* the dispatch table's choice */
+    PROJ_VARIANT_DENSE = 1,     /* uncompressed weights */
+    PROJ_VARIANT_EXPWIN12 = 2   /* 12-bit weights (handle must hold them) */
+};
+
+typedef struct proj_run_opts {
+    int variant;    /* enum proj_variant */
+    int grid;       /* CTAs of the split-K partition; 0 = dispatch table */
+    int stages;     /* reserved, 0 */
+    int reserved;
+} proj_run_opts;
+
+typedef struct proj_info_t {
+    int layer;               /* enum proj_layer */
+    int dtype;               /* enum proj_dtype of W */
+    int64_t N, K;
+    int64_t m_max;
+    int expwin12;            /* 1 if the 12-bit copy is present and used */
+    int expwin12_declined;   /* 1 if requested but declined (escape overflow) */
+    int expwin12_e0;         /* window base: high7 in [e0, e0 + 7] */
+    int64_t expwin12_escapes;        /* weights outside the window */
+    int64_t expwin12_bytes;          /* bytes of the 12-bit stream incl. escapes */
+    int64_t dense_bytes;             /* bytes of the packed uncompressed W */
+    int64_t workspace_bytes;         /* split-K partials + counters */
+    int num_sms;
+    int reserved[7];
+} proj_info_t;
+
+/*
+ * Prepare a layer.  Untimed; may allocate and synchronise.
+ *   layer : enum proj_layer.
+ *   W     : device pointer to row-major [N, K] weights, 16-byte aligned;
+ *           bf16 for every layer but the router, fp32 for the router.  It is
+ *           only read, and fully consumed before return: the caller may free
+ *           it afterwards.
+ *   N, K  : must equal the layer's fixed shape (table above).
+ *   dtype : PROJ_FP32 for the router, PROJ_BF16 otherwise.
+ * Returns NULL on error; proj_last_status() then says why.
+ */
+proj_handle proj_prepare(int layer, const void *W, int64_t N, int64_t K, int dtype);
+
+/*
+ * As proj_prepare, plus:
+ *   flags  : enum proj_flags.
+ *   m_max  : largest token count proj_run will be called with; sizes the
+ *            workspace.  0 selects the default, 1024.
+ *   status : optional out-parameter (may be NULL).
+ */
+proj_handle proj_prepare_ex(int layer, const void *W, int64_t N, int64_t K, int dtype,
+                            uint32_t flags, int64_t m_max, int *status);
+
+/*
+ * Timed call.  Enqueues the projection on `stream` and returns; no
+ * allocation, no host synchronisation, no memset; capturable in a CUDA graph.
+ * Branches on m only.
+ *   x   : device pointer, bf16 row-major [m, K], contiguous, 16-byte aligned.
+ *   m   : token count, 0 <= m <= m_max (m = 0 returns PROJ_OK, no launch).
+ *   out : device pointer, row-major [m, proj_out_features(h, m)], contiguous,
+ *         16-byte aligned; bf16 for the dense layers, fp32 for the router.
+ *         Every element is written.
+ * x and out must not overlap.  Returns PROJ_OK or an error status.
+ */
+int proj_run(proj_handle h, const void *x, int64_t m, void *out, proj_stream stream);
+
+/* proj_run with an explicit variant and split-K grid (opts may be NULL). */
+int proj_run_ex(proj_handle h, const void *x, int64_t m, void *out, proj_stream stream,
+                const proj_run_opts *opts);
+
+/*
+ * End-to-end call on HOST buffers: copies x_host [m, K] bf16 to a
+ * handle-owned device buffer, runs the projection, and copies the result to
+ * out_host [m, proj_out_features(h, m)], all enqueued on `stream`.  The
+ * copies are asynchronous for page-locked host memory; the caller
+ * synchronises `stream` before reading out_host.  Same m rules as proj_run.
+ */
+int proj_run_host(proj_handle h, const void *x_host, int64_t m, void *out_host,
+                  proj_stream stream);
+
+/* Output width at m tokens: N, except the unpooler's 1024 at m <= 8
+ * (guide ch. 1, §1.1 table).  Returns -1 for a NULL handle. */
+int64_t proj_out_features(proj_handle h, int64_t m);
+
+/* Fill *info with the handle's facts.  Returns PROJ_OK or PROJ_EINVAL. */
+int proj_info(proj_handle h, proj_info_t *info);
+
+/*
+ * Describe the kernel and launch shape proj_run would use at m (for
+ * reports): writes a NUL-terminated string of at most `cap` bytes to `buf`.
+ */
+int proj_describe(proj_handle h, int64_t m, char *buf, size_t cap);
+
+/*
+ * Decode the handle's packed weights back to row-major [N, K] at W_out
+ * (device, same dtype as prepared).  With the 12-bit copy present it
+ * decodes that copy, so a bitwise comparison with the original W checks
+ * that the recode is lossless.  Enqueued on `stream`.
+ */
+int proj_unpack_weights(proj_handle h, int variant, void *W_out, proj_stream stream);
+
+/* Read and clear the handle's device status word (synchronises `stream`).
+ * Returns PROJ_OK or PROJ_EDEVICE; *code receives the raw word if non-NULL. */
+int proj_device_status(proj_handle h, proj_stream stream, uint32_t *code);
+
+/* Free everything the handle owns (synchronises the device first). */
+void proj_destroy(proj_handle h);
+
+/* Status of the last failing call on this thread, and its text. */
+int proj_last_status(void);
+const char *proj_status_string(int status);
+/* Last CUDA error string recorded on this thread ("" if none). */
+const char *proj_last_cuda_error(void);
+
+/*
+ * Streaming read of `bytes` bytes at device pointer `buf` (16-byte aligned,
+ * bytes a multiple of 16), with every byte reaching the SMs: the HBM read
+ * floor of the timing harness, and, on a buffer larger than L2, the flush
+ * that makes the next call cold.  Writes one 32-bit checksum per CTA to
+ * `sink` (device, >= grid words).  grid = 0 picks one CTA per SM.
+ * mode 0 = 128-bit register loads, mode 1 = bulk copies into shared memory.
+ */
+int proj_read_floor(const void *buf, int64_t bytes, void *sink, int grid, int mode,
+                    proj_stream stream);
+
+/* Number of SMs of the current device (0 on error). */
+int proj_num_sms(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PROJ_H_ */
