@@ -1,0 +1,588 @@
+// api.cu -- the C ABI of libproj (declared in include/proj.h).
+//
+// prepare (untimed) validates the layer's fixed shape, repacks W into the
+// kernels' tile layouts, optionally builds the 12-bit exponent-window copy,
+// and allocates the split-K workspace and counters (zeroed once; the kernels
+// return every counter to zero).  run validates, picks a kernel from the
+// token count alone, encodes the x tensor map and launches one kernel.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "../../include/proj.h"
+#include "kernels.h"
+
+using namespace proj;
+
+namespace {
+
+// ------------------------------------------------------------------ errors --
+thread_local int g_last_status = PROJ_OK;
+thread_local char g_last_cuda[256] = "";
+
+int fail(int status) {
+  g_last_status = status;
+  return status;
+}
+
+int fail_cuda(cudaError_t e, const char* what) {
+  std::snprintf(g_last_cuda, sizeof g_last_cuda, "%s: %s", what, cudaGetErrorString(e));
+  g_last_status = PROJ_ECUDA;
+  return PROJ_ECUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ------------------------------------------------------------ layer table --
+struct LayerShape {
+  int64_t N, K;
+  int dtype;
+};
+// muse_bf16_proj guide, ch. 1, §1.1 table.
+constexpr LayerShape kLayers[5] = {
+    {2304, 8192, PROJ_BF16},  // qkv_gate
+    {8192, 1024, PROJ_BF16},  // o
+    {4096, 8192, PROJ_BF16},  // pooler
+    {8192, 4096, PROJ_BF16},  // unpooler
+    {256, 8192, PROJ_FP32},   // router
+};
+constexpr int64_t kUnpoolerSliceRows = 1024;
+constexpr int64_t kUnpoolerSliceMaxM = 8;
+constexpr int64_t kDefaultMMax = 1024;
+
+// --------------------------------------------------------- tensor maps -----
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// x: bf16 [m, K] row-major; box = 64 columns x box_rows rows.
+bool make_x_map(CUtensorMap* map, const void* x, int64_t m, int64_t K, int box_rows,
+                bool swizzle128) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(m)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int bn_for_m(int64_t m) {
+  if (m <= 16) return 16;
+  if (m <= 32) return 32;
+  if (m <= 64) return 64;
+  if (m <= 128) return 128;
+  return 256;
+}
+
+int tm_for_m(int64_t m) {
+  if (m <= 4) return 4;
+  if (m <= 8) return 8;
+  if (m <= 16) return 16;
+  if (m <= 32) return 32;
+  return 64;
+}
+
+// Token counts up to which the 12-bit copy is used by the dispatch table.
+constexpr int64_t kExpwinAutoMaxM = 16;
+constexpr int64_t kExpwinMaxM = 32;
+
+struct Plan {
+  bool router;
+  bool expwin;
+  int bn;       // BN (tensor core) or TM (router)
+  int64_t n_out;
+  int T, KB, MT;
+  int G;
+};
+
+}  // namespace
+
+struct proj_ctx {
+  int layer = 0, dtype = 0;
+  int64_t N = 0, K = 0, m_max = 0;
+  int device = 0, num_sms = 0;
+  uint8_t* w_dense = nullptr;
+  size_t w_dense_bytes = 0;
+  uint8_t* w_exp = nullptr;
+  size_t w_exp_bytes = 0;
+  int e0 = 0;
+  int64_t n_esc = 0;
+  int exp_declined = 0;
+  float* ws = nullptr;
+  size_t ws_bytes = 0;
+  uint32_t* counters = nullptr;
+  size_t counters_bytes = 0;
+  uint32_t* status = nullptr;
+  void* x_stage = nullptr;
+  void* out_stage = nullptr;
+  struct MapEntry {
+    const void* x;
+    int64_t m;
+    int box;
+    bool swz;
+    CUtensorMap map;
+  } maps[8];
+  int n_maps = 0, next_map = 0;
+};
+
+namespace {
+
+void free_ctx(proj_ctx* h) {
+  if (!h) return;
+  cudaFree(h->w_dense);
+  cudaFree(h->w_exp);
+  cudaFree(h->ws);
+  cudaFree(h->counters);
+  cudaFree(h->status);
+  cudaFree(h->x_stage);
+  cudaFree(h->out_stage);
+  delete h;
+}
+
+const CUtensorMap* get_map(proj_ctx* h, const void* x, int64_t m, int box, bool swz) {
+  for (int i = 0; i < h->n_maps; ++i) {
+    auto& e = h->maps[i];
+    if (e.x == x && e.m == m && e.box == box && e.swz == swz) return &e.map;
+  }
+  auto& e = h->maps[h->next_map];
+  if (!make_x_map(&e.map, x, m, h->K, box, swz)) return nullptr;
+  e.x = x;
+  e.m = m;
+  e.box = box;
+  e.swz = swz;
+  h->next_map = (h->next_map + 1) % 8;
+  h->n_maps = std::min(h->n_maps + 1, 8);
+  return &e.map;
+}
+
+int64_t out_rows(const proj_ctx* h, int64_t m) {
+  if (h->layer == PROJ_UNPOOLER && m <= kUnpoolerSliceMaxM) return kUnpoolerSliceRows;
+  return h->N;
+}
+
+int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl) {
+  const int variant = opts ? opts->variant : PROJ_VARIANT_AUTO;
+  pl->router = (h->layer == PROJ_ROUTER);
+  pl->n_out = out_rows(h, m);
+  if (pl->router) {
+    if (variant == PROJ_VARIANT_EXPWIN12) return PROJ_EUNSUPPORTED;
+    pl->expwin = false;
+    pl->bn = tm_for_m(m);
+    pl->T = static_cast<int>(h->N / kRtRows);
+    pl->KB = static_cast<int>(h->K / kRtK);
+  } else {
+    bool use_exp = false;
+    if (variant == PROJ_VARIANT_EXPWIN12) {
+      if (!h->w_exp || m > kExpwinMaxM) return PROJ_EUNSUPPORTED;
+      use_exp = true;
+    } else if (variant == PROJ_VARIANT_AUTO) {
+      use_exp = h->w_exp && m <= kExpwinAutoMaxM;
+    } else if (variant != PROJ_VARIANT_DENSE) {
+      return PROJ_EINVAL;
+    }
+    pl->expwin = use_exp;
+    pl->bn = bn_for_m(m);
+    pl->T = static_cast<int>(pl->n_out / kTileRows);
+    pl->KB = static_cast<int>(h->K / kTileK);
+  }
+  pl->MT = static_cast<int>((m + pl->bn - 1) / pl->bn);
+  const int64_t U = static_cast<int64_t>(pl->MT) * pl->T * pl->KB;
+  int64_t G = h->num_sms;
+  if (opts && opts->grid > 0) G = std::min<int64_t>(opts->grid, h->num_sms);
+  pl->G = static_cast<int>(std::min<int64_t>(G, U));
+  return PROJ_OK;
+}
+
+int choose_window(const uint32_t hist[128]) {
+  int best_e0 = 0;
+  int64_t best = -1;
+  for (int e0 = 0; e0 <= 120; ++e0) {
+    int64_t c = 0;
+    for (int j = 0; j < 8; ++j) c += hist[e0 + j];
+    if (c > best) {
+      best = c;
+      best_e0 = e0;
+    }
+  }
+  return best_e0;
+}
+
+template <typename T>
+cudaError_t dmalloc(T** p, size_t bytes) {
+  return cudaMalloc(reinterpret_cast<void**>(p), bytes ? bytes : 16);
+}
+
+}  // namespace
+
+// ============================================================================
+extern "C" {
+
+int proj_last_status(void) { return g_last_status; }
+
+const char* proj_last_cuda_error(void) { return g_last_cuda; }
+
+const char* proj_status_string(int status) {
+  switch (status) {
+    case PROJ_OK: return "ok";
+    case PROJ_EINVAL: return "invalid argument";
+    case PROJ_EUNSUPPORTED: return "unsupported request";
+    case PROJ_EALIGN: return "pointer not 16-byte aligned";
+    case PROJ_ENOMEM: return "out of memory";
+    case PROJ_ECUDA: return "CUDA error";
+    case PROJ_EDEVICE: return "device-side fault reported";
+  }
+  return "unknown status";
+}
+
+int proj_num_sms(void) {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+proj_handle proj_prepare_ex(int layer, const void* W, int64_t N, int64_t K, int dtype,
+                            uint32_t flags, int64_t m_max, int* status) {
+  auto bail = [&](int st) -> proj_handle {
+    fail(st);
+    if (status) *status = st;
+    return nullptr;
+  };
+  if (layer < 0 || layer > 4) return bail(PROJ_EINVAL);
+  const LayerShape& ls = kLayers[layer];
+  if (N != ls.N || K != ls.K || dtype != ls.dtype) return bail(PROJ_EINVAL);
+  if (!W) return bail(PROJ_EINVAL);
+  if (!aligned16(W)) return bail(PROJ_EALIGN);
+  if (flags & ~static_cast<uint32_t>(PROJ_ENCODE_EXPWIN12)) return bail(PROJ_EINVAL);
+  if (m_max < 0) return bail(PROJ_EINVAL);
+  if (m_max == 0) m_max = kDefaultMMax;
+
+  proj_ctx* h = new (std::nothrow) proj_ctx();
+  if (!h) return bail(PROJ_ENOMEM);
+  h->layer = layer;
+  h->dtype = dtype;
+  h->N = N;
+  h->K = K;
+  h->m_max = m_max;
+  auto bail_cuda = [&](cudaError_t e, const char* what) -> proj_handle {
+    fail_cuda(e, what);
+    free_ctx(h);
+    const int st = (e == cudaErrorMemoryAllocation) ? PROJ_ENOMEM : PROJ_ECUDA;
+    g_last_status = st;
+    if (status) *status = st;
+    return nullptr;
+  };
+  cudaError_t e;
+  if ((e = cudaGetDevice(&h->device)) != cudaSuccess) return bail_cuda(e, "cudaGetDevice");
+  if ((e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device)) !=
+      cudaSuccess)
+    return bail_cuda(e, "cudaDeviceGetAttribute");
+  if ((e = tc_init_attributes()) != cudaSuccess) return bail_cuda(e, "tc attributes");
+  if ((e = router_init_attributes()) != cudaSuccess) return bail_cuda(e, "router attributes");
+  if (!encode_fn()) return bail_cuda(cudaErrorNotSupported, "cuTensorMapEncodeTiled");
+
+  cudaStream_t s;
+  if ((e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking)) != cudaSuccess)
+    return bail_cuda(e, "cudaStreamCreate");
+  auto done = [&]() { cudaStreamDestroy(s); };
+
+  const int64_t sms = h->num_sms;
+  if (layer == PROJ_ROUTER) {
+    h->w_dense_bytes = static_cast<size_t>(N) * K * 4;
+    if ((e = dmalloc(&h->w_dense, h->w_dense_bytes)) != cudaSuccess) {
+      done();
+      return bail_cuda(e, "cudaMalloc(weights)");
+    }
+    if ((e = pack_router_tiles(static_cast<const float*>(W), static_cast<int>(N),
+                               static_cast<int>(K), h->w_dense, s)) != cudaSuccess) {
+      done();
+      return bail_cuda(e, "pack router");
+    }
+    const int tm_max = tm_for_m(std::min<int64_t>(m_max, 64));
+    h->ws_bytes = static_cast<size_t>(2 * sms) * 64 * tm_max * 4;
+    const int64_t mt_max = (m_max + 63) / 64;
+    h->counters_bytes = static_cast<size_t>(std::max<int64_t>(mt_max, 1) * (N / kRtRows)) * 4;
+  } else {
+    h->w_dense_bytes = static_cast<size_t>(N) * K * 2;
+    if ((e = dmalloc(&h->w_dense, h->w_dense_bytes)) != cudaSuccess) {
+      done();
+      return bail_cuda(e, "cudaMalloc(weights)");
+    }
+    if ((e = pack_bf16_tiles(static_cast<const uint16_t*>(W), static_cast<int>(N),
+                             static_cast<int>(K), h->w_dense, s)) != cudaSuccess) {
+      done();
+      return bail_cuda(e, "pack bf16");
+    }
+    if (flags & PROJ_ENCODE_EXPWIN12) {
+      uint32_t* dev_hist = nullptr;
+      uint32_t* dev_flag = nullptr;  // [0] overflow, [2..3] escape count (u64)
+      if ((e = dmalloc(&dev_hist, 128 * 4)) != cudaSuccess ||
+          (e = dmalloc(&dev_flag, 16)) != cudaSuccess) {
+        cudaFree(dev_hist);
+        done();
+        return bail_cuda(e, "cudaMalloc(hist)");
+      }
+      uint32_t hist[128];
+      uint32_t flag[4];
+      const size_t rec_bytes =
+          static_cast<size_t>(N / kTileRows) * (K / kTileK) * static_cast<size_t>(kRecBytes);
+      bool ok = (e = cudaMemsetAsync(dev_hist, 0, 128 * 4, s)) == cudaSuccess &&
+                (e = cudaMemsetAsync(dev_flag, 0, 16, s)) == cudaSuccess &&
+                (e = high7_histogram(static_cast<const uint16_t*>(W), N * K, dev_hist, s)) ==
+                    cudaSuccess &&
+                (e = cudaMemcpyAsync(hist, dev_hist, sizeof hist, cudaMemcpyDeviceToHost, s)) ==
+                    cudaSuccess &&
+                (e = cudaStreamSynchronize(s)) == cudaSuccess;
+      if (ok) {
+        h->e0 = choose_window(hist);
+        h->w_exp_bytes = rec_bytes;
+        ok = (e = dmalloc(&h->w_exp, rec_bytes)) == cudaSuccess &&
+             (e = cudaMemsetAsync(h->w_exp, 0, rec_bytes, s)) == cudaSuccess &&
+             (e = encode_expwin12(static_cast<const uint16_t*>(W), static_cast<int>(N),
+                                  static_cast<int>(K), h->e0, h->w_exp, dev_flag,
+                                  reinterpret_cast<unsigned long long*>(dev_flag + 2), s)) ==
+                 cudaSuccess &&
+             (e = cudaMemcpyAsync(flag, dev_flag, sizeof flag, cudaMemcpyDeviceToHost, s)) ==
+                 cudaSuccess &&
+             (e = cudaStreamSynchronize(s)) == cudaSuccess;
+      }
+      cudaFree(dev_hist);
+      cudaFree(dev_flag);
+      if (!ok) {
+        done();
+        return bail_cuda(e, "12-bit encode");
+      }
+      uint64_t nesc;
+      std::memcpy(&nesc, &flag[2], 8);
+      h->n_esc = static_cast<int64_t>(nesc);
+      if (flag[0]) {  // some tile has more escapes than its block holds
+        cudaFree(h->w_exp);
+        h->w_exp = nullptr;
+        h->w_exp_bytes = 0;
+        h->exp_declined = 1;
+      }
+    }
+    const int bn_max = bn_for_m(std::min<int64_t>(m_max, 256));
+    h->ws_bytes = static_cast<size_t>(2 * sms) * bn_max * kTileRows * 4;
+    const int64_t mt_max = (m_max + 255) / 256;
+    h->counters_bytes = static_cast<size_t>(std::max<int64_t>(mt_max, 1) * (N / kTileRows)) * 4;
+  }
+  const size_t out_elem = (layer == PROJ_ROUTER) ? 4 : 2;
+  if ((e = dmalloc(&h->ws, h->ws_bytes)) != cudaSuccess ||
+      (e = dmalloc(&h->counters, h->counters_bytes)) != cudaSuccess ||
+      (e = dmalloc(&h->status, 16)) != cudaSuccess ||
+      (e = dmalloc(&h->x_stage, static_cast<size_t>(m_max) * K * 2)) != cudaSuccess ||
+      (e = dmalloc(&h->out_stage, static_cast<size_t>(m_max) * N * out_elem)) != cudaSuccess) {
+    done();
+    return bail_cuda(e, "cudaMalloc(workspace)");
+  }
+  if ((e = cudaMemsetAsync(h->counters, 0, h->counters_bytes, s)) != cudaSuccess ||
+      (e = cudaMemsetAsync(h->status, 0, 16, s)) != cudaSuccess ||
+      (e = cudaStreamSynchronize(s)) != cudaSuccess) {
+    done();
+    return bail_cuda(e, "prepare sync");
+  }
+  done();
+  if (status) *status = PROJ_OK;
+  return h;
+}
+
+proj_handle proj_prepare(int layer, const void* W, int64_t N, int64_t K, int dtype) {
+  return proj_prepare_ex(layer, W, N, K, dtype, 0u, 0, nullptr);
+}
+
+int64_t proj_out_features(proj_handle h, int64_t m) {
+  if (!h) return -1;
+  return out_rows(h, m);
+}
+
+int proj_run_ex(proj_handle h, const void* x, int64_t m, void* out, proj_stream stream,
+                const proj_run_opts* opts) {
+  if (!h) return fail(PROJ_EINVAL);
+  if (m < 0) return fail(PROJ_EINVAL);
+  if (m > h->m_max) return fail(PROJ_EUNSUPPORTED);
+  if (m == 0) return PROJ_OK;
+  if (!x || !out) return fail(PROJ_EINVAL);
+  if (!aligned16(x) || !aligned16(out)) return fail(PROJ_EALIGN);
+  Plan pl;
+  int st = make_plan(h, m, opts, &pl);
+  if (st != PROJ_OK) return fail(st);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const CUtensorMap* map = get_map(h, x, m, pl.bn, !pl.router);
+  if (!map) return fail_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(x)");
+  cudaError_t e;
+  if (pl.router) {
+    RouterParams p;
+    p.w = h->w_dense;
+    p.out = static_cast<float*>(out);
+    p.ws = h->ws;
+    p.counters = h->counters;
+    p.status = h->status;
+    p.m = static_cast<int>(m);
+    p.T = pl.T;
+    p.KB = pl.KB;
+    p.MT = pl.MT;
+    p.G = pl.G;
+    e = router_launch(pl.bn, *map, p, s);
+  } else {
+    TcParams p;
+    p.w = pl.expwin ? h->w_exp : h->w_dense;
+    p.out = out;
+    p.ws = h->ws;
+    p.counters = h->counters;
+    p.status = h->status;
+    p.m = static_cast<int>(m);
+    p.n_out = static_cast<int>(pl.n_out);
+    p.K = static_cast<int>(h->K);
+    p.T = pl.T;
+    p.KB = pl.KB;
+    p.MT = pl.MT;
+    p.G = pl.G;
+    p.e0x4 = static_cast<uint32_t>(h->e0) * 0x01010101u;
+    e = tc_launch(pl.bn, pl.expwin, *map, p, s);
+  }
+  if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
+  return PROJ_OK;
+}
+
+int proj_run(proj_handle h, const void* x, int64_t m, void* out, proj_stream stream) {
+  return proj_run_ex(h, x, m, out, stream, nullptr);
+}
+
+int proj_run_host(proj_handle h, const void* x_host, int64_t m, void* out_host,
+                  proj_stream stream) {
+  if (!h) return fail(PROJ_EINVAL);
+  if (m < 0) return fail(PROJ_EINVAL);
+  if (m > h->m_max) return fail(PROJ_EUNSUPPORTED);
+  if (m == 0) return PROJ_OK;
+  if (!x_host || !out_host) return fail(PROJ_EINVAL);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t xb = static_cast<size_t>(m) * h->K * 2;
+  const size_t ob = static_cast<size_t>(m) * out_rows(h, m) * (h->layer == PROJ_ROUTER ? 4 : 2);
+  cudaError_t e = cudaMemcpyAsync(h->x_stage, x_host, xb, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return fail_cuda(e, "copy x to device");
+  int st = proj_run_ex(h, h->x_stage, m, h->out_stage, stream, nullptr);
+  if (st != PROJ_OK) return st;
+  e = cudaMemcpyAsync(out_host, h->out_stage, ob, cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return fail_cuda(e, "copy out to host");
+  return PROJ_OK;
+}
+
+int proj_info(proj_handle h, proj_info_t* info) {
+  if (!h || !info) return fail(PROJ_EINVAL);
+  std::memset(info, 0, sizeof *info);
+  info->layer = h->layer;
+  info->dtype = h->dtype;
+  info->N = h->N;
+  info->K = h->K;
+  info->m_max = h->m_max;
+  info->expwin12 = h->w_exp ? 1 : 0;
+  info->expwin12_declined = h->exp_declined;
+  info->expwin12_e0 = h->e0;
+  info->expwin12_escapes = h->n_esc;
+  info->expwin12_bytes = h->w_exp ? (h->N * h->K * 3) / 2 + h->n_esc * 4 : 0;
+  info->dense_bytes = static_cast<int64_t>(h->w_dense_bytes);
+  info->workspace_bytes = static_cast<int64_t>(h->ws_bytes + h->counters_bytes);
+  info->num_sms = h->num_sms;
+  return PROJ_OK;
+}
+
+int proj_describe(proj_handle h, int64_t m, char* buf, size_t cap) {
+  if (!h || !buf || cap == 0 || m < 1) return fail(PROJ_EINVAL);
+  Plan pl;
+  int st = make_plan(h, m, nullptr, &pl);
+  if (st != PROJ_OK) return fail(st);
+  if (pl.router) {
+    std::snprintf(buf, cap, "router_fma TM=%d stages=8 G=%d T=%d KB=%d MT=%d", pl.bn, pl.G, pl.T,
+                  pl.KB, pl.MT);
+  } else {
+    std::snprintf(buf, cap, "tc_%s BN=%d stages=%d G=%d T=%d KB=%d MT=%d n_out=%lld",
+                  pl.expwin ? "expwin12" : "dense", pl.bn, tc_stages(pl.bn, pl.expwin), pl.G,
+                  pl.T, pl.KB, pl.MT, static_cast<long long>(pl.n_out));
+  }
+  return PROJ_OK;
+}
+
+int proj_unpack_weights(proj_handle h, int variant, void* W_out, proj_stream stream) {
+  if (!h || !W_out) return fail(PROJ_EINVAL);
+  if (!aligned16(W_out)) return fail(PROJ_EALIGN);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (h->layer == PROJ_ROUTER) {
+    if (variant == PROJ_VARIANT_EXPWIN12) return fail(PROJ_EUNSUPPORTED);
+    e = unpack_router_tiles(h->w_dense, static_cast<int>(h->N), static_cast<int>(h->K),
+                            static_cast<float*>(W_out), s);
+  } else if (variant == PROJ_VARIANT_EXPWIN12 ||
+             (variant == PROJ_VARIANT_AUTO && h->w_exp != nullptr)) {
+    if (!h->w_exp) return fail(PROJ_EUNSUPPORTED);
+    e = decode_expwin12(h->w_exp, static_cast<int>(h->N), static_cast<int>(h->K), h->e0,
+                        static_cast<uint16_t*>(W_out), s);
+  } else {
+    e = unpack_bf16_tiles(h->w_dense, static_cast<int>(h->N), static_cast<int>(h->K),
+                          static_cast<uint16_t*>(W_out), s);
+  }
+  if (e != cudaSuccess) return fail_cuda(e, "unpack");
+  return PROJ_OK;
+}
+
+int proj_device_status(proj_handle h, proj_stream stream, uint32_t* code) {
+  if (!h) return fail(PROJ_EINVAL);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  cudaError_t e;
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return fail_cuda(e, "sync");
+  if ((e = cudaMemcpy(&word, h->status, 4, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return fail_cuda(e, "read status");
+  if ((e = cudaMemset(h->status, 0, 4)) != cudaSuccess) return fail_cuda(e, "clear status");
+  if (code) *code = word;
+  return word ? fail(PROJ_EDEVICE) : PROJ_OK;
+}
+
+void proj_destroy(proj_handle h) {
+  if (!h) return;
+  cudaDeviceSynchronize();
+  free_ctx(h);
+}
+
+int proj_read_floor(const void* buf, int64_t bytes, void* sink, int grid, int mode,
+                    proj_stream stream) {
+  if (!buf || !sink || bytes <= 0 || (bytes % 16) != 0 || grid < 0 || mode < 0 || mode > 1)
+    return fail(PROJ_EINVAL);
+  if (!aligned16(buf) || (reinterpret_cast<uintptr_t>(sink) & 3u)) return fail(PROJ_EALIGN);
+  if (grid == 0) {
+    const int sms = proj_num_sms();
+    if (sms <= 0) return fail_cuda(cudaErrorNoDevice, "proj_num_sms");
+    grid = (mode == 0) ? 2 * sms : sms;
+  }
+  cudaError_t e = read_floor_launch(buf, bytes, static_cast<uint32_t*>(sink), grid, mode,
+                                    reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "read floor launch");
+  return PROJ_OK;
+}
+
+}  // extern "C"

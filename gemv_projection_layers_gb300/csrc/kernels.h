@@ -1,0 +1,118 @@
+// kernels.h -- host-side interface between the C ABI (api.cu) and the kernel
+// translation units.  Internal to libproj.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace proj {
+
+// ----------------------------------------------------------------------------
+// Packed bf16 weights for the tensor-core path.
+//
+// W [N, K] row-major is cut into tiles of 128 rows x 64 columns.  Tile (t, kb)
+// covers rows [128 t, 128 t + 128) and columns [64 kb, 64 kb + 64) and is
+// stored contiguously at byte offset (t * KB + kb) * 16384, already in the
+// shared-memory image the MMA reads: row r at byte r * 128, its 16-byte chunk
+// c (columns 8c .. 8c + 7) at chunk position c ^ (r & 7) -- the 128-byte
+// swizzle.  One bulk copy per tile lands it ready for tcgen05.mma.
+// ----------------------------------------------------------------------------
+constexpr int kTileRows = 128;
+constexpr int kTileK = 64;
+constexpr int kTileBytes = kTileRows * kTileK * 2;  // 16384
+
+// 12-bit exponent-window record of one tile (same tiling):
+//   [0, 8192)      low bytes, chunk-major: chunk (r, c) at (8 r + c) * 8,
+//                  bytes in column order;
+//   [8192, 12288)  nibbles, chunk (r, c) at 8192 + (8 r + c) * 4: byte b of the
+//                  32-bit word holds the nibble of column 8c + b in bits 0-3 and
+//                  that of column 8c + 4 + b in bits 4-7; nibble = sign << 3 |
+//                  code, high byte = sign << 7 | (e0 + code);
+//   [12288, 12352) escape block: word 0 = count (<= kEscCap), then count
+//                  words (position << 8 | original high byte), position =
+//                  64 r + column within the tile.
+constexpr int kRecBytes = 12352;
+constexpr int kRecLowOff = 0;
+constexpr int kRecNibOff = 8192;
+constexpr int kRecEscOff = 12288;
+constexpr int kEscCap = 15;
+
+// Router (fp32) tiles: 64 rows x 64 columns, 16384 bytes, tile (t, kb) at
+// (t * 128 + kb) * 16384; row r at r * 256, its float4 q (columns 4q .. 4q+3)
+// at slot q ^ (r & 7).
+constexpr int kRtRows = 64;
+constexpr int kRtK = 64;
+constexpr int kRtBytes = kRtRows * kRtK * 4;
+
+struct TcParams {
+  const uint8_t* w;     // packed tiles or 12-bit records
+  void* out;            // bf16 [m, n_out]
+  float* ws;            // split-K partials: [2 G][BN][128] fp32
+  uint32_t* counters;   // [MT * T], zero between calls
+  uint32_t* status;     // device status word
+  int m;
+  int n_out;            // rows of W computed (multiple of 128)
+  int K;
+  int T;                // n_out / 128
+  int KB;               // K / 64
+  int MT;               // ceil(m / BN)
+  int G;                // CTAs (the split-K partition)
+  uint32_t e0x4;        // 12-bit window base replicated into 4 bytes
+};
+
+struct RouterParams {
+  const uint8_t* w;     // packed router tiles
+  float* out;           // fp32 [m, 256]
+  float* ws;            // [2 G][64 * TM] fp32
+  uint32_t* counters;   // [MT * 4]
+  uint32_t* status;
+  int m;
+  int T;                // 4
+  int KB;               // 128
+  int MT;               // ceil(m / TM)
+  int G;
+};
+
+// Tensor-core path: BN in {16, 32, 64, 128, 256}; expwin12 for BN in {16, 32}.
+bool tc_supported(int BN, bool expwin);
+int tc_threads(bool expwin);
+size_t tc_smem_bytes(int BN, bool expwin);
+int tc_stages(int BN, bool expwin);
+cudaError_t tc_init_attributes();
+cudaError_t tc_launch(int BN, bool expwin, const CUtensorMap& tmap_x, const TcParams& p,
+                      cudaStream_t s);
+
+// Router FP32-FMA path: TM in {4, 8, 16, 32, 64}.
+bool router_supported(int TM);
+size_t router_smem_bytes(int TM);
+cudaError_t router_init_attributes();
+cudaError_t router_launch(int TM, const CUtensorMap& tmap_x, const RouterParams& p,
+                          cudaStream_t s);
+
+// Prepare-time kernels (prep.cu).
+cudaError_t pack_bf16_tiles(const uint16_t* W, int N, int K, uint8_t* dst, cudaStream_t s);
+cudaError_t unpack_bf16_tiles(const uint8_t* src, int N, int K, uint16_t* W, cudaStream_t s);
+cudaError_t high7_histogram(const uint16_t* W, int64_t n, uint32_t* hist128, cudaStream_t s);
+cudaError_t encode_expwin12(const uint16_t* W, int N, int K, int e0, uint8_t* dst,
+                            uint32_t* overflow, unsigned long long* n_esc, cudaStream_t s);
+cudaError_t decode_expwin12(const uint8_t* src, int N, int K, int e0, uint16_t* W,
+                            cudaStream_t s);
+cudaError_t pack_router_tiles(const float* W, int N, int K, uint8_t* dst, cudaStream_t s);
+cudaError_t unpack_router_tiles(const uint8_t* src, int N, int K, float* W, cudaStream_t s);
+
+// Streaming read (read.cu).
+cudaError_t read_floor_launch(const void* buf, int64_t bytes, uint32_t* sink, int grid, int mode,
+                              cudaStream_t s);
+
+// Split-K partition shared by every kernel: CTA c owns work units
+// [c U / G, (c + 1) U / G) of the linear order (tile, k-block).
+__host__ __device__ inline int64_t part_begin(int64_t c, int64_t U, int64_t G) {
+  return c * U / G;
+}
+// The CTA whose range holds unit u.
+__host__ __device__ inline int64_t part_owner(int64_t u, int64_t U, int64_t G) {
+  return ((u + 1) * G - 1) / U;
+}
+
+}  // namespace proj

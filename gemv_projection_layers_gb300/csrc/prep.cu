@@ -1,0 +1,246 @@
+// prep.cu -- prepare-time (untimed) weight transforms, all lossless:
+//   * bf16 W -> 128 x 64 tiles in the swizzled shared-memory image (and back);
+//   * histogram of the 7 high exponent bits, and the 12-bit exponent-window
+//     encoder/decoder (muse_bf16_proj project report, "Round 5 -- lossless
+//     12-bit compressed weights", "Format");
+//   * router fp32 W -> 64 x 64 swizzled tiles (and back).
+// The tile and record layouts are defined in kernels.h.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace proj {
+namespace {
+
+__device__ __forceinline__ size_t tile_chunk_offset(int r, int c) {
+  return static_cast<size_t>(r) * 128 + (static_cast<size_t>(c ^ (r & 7)) << 4);
+}
+
+// One thread per 16-byte chunk (8 bf16) of W.
+__global__ void pack_bf16_kernel(const uint16_t* __restrict__ W, int N, int K,
+                                 uint8_t* __restrict__ dst) {
+  const int64_t chunks = static_cast<int64_t>(N) * (K / 8);
+  const int KB = K / kTileK;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < chunks;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int n = static_cast<int>(i / (K / 8));
+    const int k8 = static_cast<int>(i % (K / 8));
+    const int t = n / kTileRows, r = n % kTileRows;
+    const int kb = k8 / 8, c = k8 % 8;
+    const uint4 v = *reinterpret_cast<const uint4*>(W + static_cast<size_t>(n) * K + k8 * 8);
+    uint8_t* tile = dst + (static_cast<size_t>(t) * KB + kb) * kTileBytes;
+    *reinterpret_cast<uint4*>(tile + tile_chunk_offset(r, c)) = v;
+  }
+}
+
+__global__ void unpack_bf16_kernel(const uint8_t* __restrict__ src, int N, int K,
+                                   uint16_t* __restrict__ W) {
+  const int64_t chunks = static_cast<int64_t>(N) * (K / 8);
+  const int KB = K / kTileK;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < chunks;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int n = static_cast<int>(i / (K / 8));
+    const int k8 = static_cast<int>(i % (K / 8));
+    const int t = n / kTileRows, r = n % kTileRows;
+    const int kb = k8 / 8, c = k8 % 8;
+    const uint8_t* tile = src + (static_cast<size_t>(t) * KB + kb) * kTileBytes;
+    *reinterpret_cast<uint4*>(W + static_cast<size_t>(n) * K + k8 * 8) =
+        *reinterpret_cast<const uint4*>(tile + tile_chunk_offset(r, c));
+  }
+}
+
+__global__ void high7_hist_kernel(const uint16_t* __restrict__ W, int64_t n,
+                                  uint32_t* __restrict__ hist) {
+  __shared__ uint32_t h[128];
+  for (int i = threadIdx.x; i < 128; i += blockDim.x) h[i] = 0;
+  __syncthreads();
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    atomicAdd(&h[(W[i] >> 8) & 0x7F], 1u);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < 128; i += blockDim.x)
+    if (h[i]) atomicAdd(&hist[i], h[i]);
+}
+
+// One thread per chunk of 8 weights.  The record's escape block must be
+// zeroed before the launch (its count is accumulated atomically).
+__global__ void encode_expwin12_kernel(const uint16_t* __restrict__ W, int N, int K, int e0,
+                                       uint8_t* __restrict__ dst, uint32_t* overflow,
+                                       unsigned long long* n_esc) {
+  const int64_t chunks = static_cast<int64_t>(N) * (K / 8);
+  const int KB = K / kTileK;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < chunks;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int n = static_cast<int>(i / (K / 8));
+    const int k8 = static_cast<int>(i % (K / 8));
+    const int t = n / kTileRows, r = n % kTileRows;
+    const int kb = k8 / 8, c = k8 % 8;
+    const uint4 v = *reinterpret_cast<const uint4*>(W + static_cast<size_t>(n) * K + k8 * 8);
+    const uint16_t w[8] = {
+        static_cast<uint16_t>(v.x & 0xFFFF), static_cast<uint16_t>(v.x >> 16),
+        static_cast<uint16_t>(v.y & 0xFFFF), static_cast<uint16_t>(v.y >> 16),
+        static_cast<uint16_t>(v.z & 0xFFFF), static_cast<uint16_t>(v.z >> 16),
+        static_cast<uint16_t>(v.w & 0xFFFF), static_cast<uint16_t>(v.w >> 16)};
+    uint8_t* rec = dst + (static_cast<size_t>(t) * KB + kb) * kRecBytes;
+    const int ch = r * 8 + c;
+    uint32_t lo0 = 0, lo1 = 0, nb = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t b = w[j];
+      const uint32_t lo = b & 0xFF;
+      const int h7 = static_cast<int>((b >> 8) & 0x7F);
+      const uint32_t sgn = b >> 15;
+      int code = h7 - e0;
+      const bool esc = code < 0 || code > 7;
+      code = code < 0 ? 0 : (code > 7 ? 7 : code);
+      const uint32_t nib = (sgn << 3) | static_cast<uint32_t>(code);
+      if (j < 4) {
+        lo0 |= lo << (8 * j);
+        nb |= nib << (8 * j);
+      } else {
+        lo1 |= lo << (8 * (j - 4));
+        nb |= nib << (8 * (j - 4) + 4);
+      }
+      if (esc) {
+        uint32_t* blk = reinterpret_cast<uint32_t*>(rec + kRecEscOff);
+        const uint32_t slot = atomicAdd(blk, 1u);
+        atomicAdd(n_esc, 1ull);
+        if (slot < static_cast<uint32_t>(kEscCap)) {
+          const uint32_t pos = static_cast<uint32_t>(r * 64 + c * 8 + j);
+          blk[1 + slot] = (pos << 8) | (b >> 8);
+        } else {
+          atomicOr(overflow, 1u);
+        }
+      }
+    }
+    *reinterpret_cast<uint2*>(rec + kRecLowOff + ch * 8) = make_uint2(lo0, lo1);
+    *reinterpret_cast<uint32_t*>(rec + kRecNibOff + ch * 4) = nb;
+  }
+}
+
+// Decode records back to row-major bf16 (the same arithmetic the tensor-core
+// kernel's decode warps run, then the escape patch).
+__global__ void decode_expwin12_kernel(const uint8_t* __restrict__ src, int N, int K,
+                                       uint32_t e0x4, uint16_t* __restrict__ W) {
+  const int64_t chunks = static_cast<int64_t>(N) * (K / 8);
+  const int KB = K / kTileK;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < chunks;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int n = static_cast<int>(i / (K / 8));
+    const int k8 = static_cast<int>(i % (K / 8));
+    const int t = n / kTileRows, r = n % kTileRows;
+    const int kb = k8 / 8, c = k8 % 8;
+    const uint8_t* rec = src + (static_cast<size_t>(t) * KB + kb) * kRecBytes;
+    const int ch = r * 8 + c;
+    const uint2 lo = *reinterpret_cast<const uint2*>(rec + kRecLowOff + ch * 8);
+    const uint32_t nb = *reinterpret_cast<const uint32_t*>(rec + kRecNibOff + ch * 4);
+    const uint32_t v0 = nb & 0x0F0F0F0Fu;
+    const uint32_t v1 = (nb >> 4) & 0x0F0F0F0Fu;
+    const uint32_t h0 = ((v0 & 0x07070707u) + e0x4) | ((v0 << 4) & 0x80808080u);
+    const uint32_t h1 = ((v1 & 0x07070707u) + e0x4) | ((v1 << 4) & 0x80808080u);
+    uint4 o;
+    o.x = __byte_perm(lo.x, h0, 0x5140);
+    o.y = __byte_perm(lo.x, h0, 0x7362);
+    o.z = __byte_perm(lo.y, h1, 0x5140);
+    o.w = __byte_perm(lo.y, h1, 0x7362);
+    uint16_t w[8] = {
+        static_cast<uint16_t>(o.x & 0xFFFF), static_cast<uint16_t>(o.x >> 16),
+        static_cast<uint16_t>(o.y & 0xFFFF), static_cast<uint16_t>(o.y >> 16),
+        static_cast<uint16_t>(o.z & 0xFFFF), static_cast<uint16_t>(o.z >> 16),
+        static_cast<uint16_t>(o.w & 0xFFFF), static_cast<uint16_t>(o.w >> 16)};
+    const uint32_t* esc = reinterpret_cast<const uint32_t*>(rec + kRecEscOff);
+    const uint32_t cnt = min(esc[0], static_cast<uint32_t>(kEscCap));
+    for (uint32_t e = 0; e < cnt; ++e) {
+      const uint32_t ent = esc[1 + e];
+      const uint32_t pos = ent >> 8;
+      if (static_cast<int>(pos >> 6) == r && static_cast<int>((pos & 63) >> 3) == c) {
+        const int j = pos & 7;
+        w[j] = static_cast<uint16_t>((w[j] & 0x00FF) | ((ent & 0xFF) << 8));
+      }
+    }
+    uint4 out;
+    out.x = w[0] | (static_cast<uint32_t>(w[1]) << 16);
+    out.y = w[2] | (static_cast<uint32_t>(w[3]) << 16);
+    out.z = w[4] | (static_cast<uint32_t>(w[5]) << 16);
+    out.w = w[6] | (static_cast<uint32_t>(w[7]) << 16);
+    *reinterpret_cast<uint4*>(W + static_cast<size_t>(n) * K + k8 * 8) = out;
+  }
+}
+
+// Router: one thread per float4 of W.
+__global__ void pack_router_kernel(const float* __restrict__ W, int N, int K,
+                                   uint8_t* __restrict__ dst) {
+  const int64_t quads = static_cast<int64_t>(N) * (K / 4);
+  const int KB = K / kRtK;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < quads;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int n = static_cast<int>(i / (K / 4));
+    const int k4 = static_cast<int>(i % (K / 4));
+    const int t = n / kRtRows, r = n % kRtRows;
+    const int kb = k4 / 16, q = k4 % 16;
+    const float4 v = *reinterpret_cast<const float4*>(W + static_cast<size_t>(n) * K + k4 * 4);
+    uint8_t* tile = dst + (static_cast<size_t>(t) * KB + kb) * kRtBytes;
+    *reinterpret_cast<float4*>(tile + r * 256 + ((q ^ (r & 7)) << 4)) = v;
+  }
+}
+
+__global__ void unpack_router_kernel(const uint8_t* __restrict__ src, int N, int K,
+                                     float* __restrict__ W) {
+  const int64_t quads = static_cast<int64_t>(N) * (K / 4);
+  const int KB = K / kRtK;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < quads;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int n = static_cast<int>(i / (K / 4));
+    const int k4 = static_cast<int>(i % (K / 4));
+    const int t = n / kRtRows, r = n % kRtRows;
+    const int kb = k4 / 16, q = k4 % 16;
+    const uint8_t* tile = src + (static_cast<size_t>(t) * KB + kb) * kRtBytes;
+    *reinterpret_cast<float4*>(W + static_cast<size_t>(n) * K + k4 * 4) =
+        *reinterpret_cast<const float4*>(tile + r * 256 + ((q ^ (r & 7)) << 4));
+  }
+}
+
+constexpr int kPrepBlock = 256;
+constexpr int kPrepGrid = 152 * 8;
+
+}  // namespace
+
+cudaError_t pack_bf16_tiles(const uint16_t* W, int N, int K, uint8_t* dst, cudaStream_t s) {
+  pack_bf16_kernel<<<kPrepGrid, kPrepBlock, 0, s>>>(W, N, K, dst);
+  return cudaGetLastError();
+}
+
+cudaError_t unpack_bf16_tiles(const uint8_t* src, int N, int K, uint16_t* W, cudaStream_t s) {
+  unpack_bf16_kernel<<<kPrepGrid, kPrepBlock, 0, s>>>(src, N, K, W);
+  return cudaGetLastError();
+}
+
+cudaError_t high7_histogram(const uint16_t* W, int64_t n, uint32_t* hist128, cudaStream_t s) {
+  high7_hist_kernel<<<kPrepGrid, kPrepBlock, 0, s>>>(W, n, hist128);
+  return cudaGetLastError();
+}
+
+cudaError_t encode_expwin12(const uint16_t* W, int N, int K, int e0, uint8_t* dst,
+                            uint32_t* overflow, unsigned long long* n_esc, cudaStream_t s) {
+  encode_expwin12_kernel<<<kPrepGrid, kPrepBlock, 0, s>>>(W, N, K, e0, dst, overflow, n_esc);
+  return cudaGetLastError();
+}
+
+cudaError_t decode_expwin12(const uint8_t* src, int N, int K, int e0, uint16_t* W,
+                            cudaStream_t s) {
+  const uint32_t e0x4 = static_cast<uint32_t>(e0) * 0x01010101u;
+  decode_expwin12_kernel<<<kPrepGrid, kPrepBlock, 0, s>>>(src, N, K, e0x4, W);
+  return cudaGetLastError();
+}
+
+cudaError_t pack_router_tiles(const float* W, int N, int K, uint8_t* dst, cudaStream_t s) {
+  pack_router_kernel<<<kPrepGrid, kPrepBlock, 0, s>>>(W, N, K, dst);
+  return cudaGetLastError();
+}
+
+cudaError_t unpack_router_tiles(const uint8_t* src, int N, int K, float* W, cudaStream_t s) {
+  unpack_router_kernel<<<kPrepGrid, kPrepBlock, 0, s>>>(src, N, K, W);
+  return cudaGetLastError();
+}
+
+}  // namespace proj

@@ -1,0 +1,115 @@
+// read.cu -- the HBM read floor: a kernel that only streams bytes into the SMs.
+//
+// The pages measure the practical ceiling of a weight stream with a
+// hand-written cold-L2 read kernel and a bulk-copy streaming kernel, and find
+// both reach the same time (muse_bf16_proj project report, "Method /
+// tooling" and "Round 2").  Both forms are here: mode 0 streams with 128-bit
+// non-allocating loads into registers, mode 1 with 1-D bulk copies into a
+// shared-memory ring.  Each CTA reads one contiguous range; a checksum per
+// CTA keeps the loads alive.  Run over a buffer larger than L2 it is also the
+// flush that makes the next call's weights cold.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace proj {
+namespace {
+
+constexpr int kRegThreads = 512;
+constexpr int kRegUnroll = 8;
+
+__global__ void __launch_bounds__(kRegThreads)
+    read_regs_kernel(const uint4* __restrict__ buf, int64_t n16, uint32_t* __restrict__ sink) {
+  const int64_t b = part_begin(blockIdx.x, n16, gridDim.x);
+  const int64_t e = part_begin(blockIdx.x + 1, n16, gridDim.x);
+  uint32_t acc = 0;
+  for (int64_t i = b + threadIdx.x; i < e; i += static_cast<int64_t>(kRegThreads) * kRegUnroll) {
+    uint4 v[kRegUnroll];
+#pragma unroll
+    for (int u = 0; u < kRegUnroll; ++u) {
+      const int64_t j = i + static_cast<int64_t>(u) * kRegThreads;
+      v[u] = j < e ? ld_stream_v4(buf + j) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kRegUnroll; ++u) acc ^= v[u].x ^ v[u].y ^ v[u].z ^ v[u].w;
+  }
+  __shared__ uint32_t red[kRegThreads / 32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc ^= __shfl_xor_sync(0xffffffffu, acc, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t r = 0;
+    for (int w = 0; w < kRegThreads / 32; ++w) r ^= red[w];
+    sink[blockIdx.x] = r;
+  }
+}
+
+constexpr int kBulkStages = 12;
+constexpr int kBulkChunk = 16384;
+constexpr size_t kBulkSmem = 1024 + kBulkStages * kBulkChunk + kBulkStages * 8;
+
+__global__ void __launch_bounds__(32)
+    read_bulk_kernel(const uint8_t* __restrict__ buf, int64_t n16, uint32_t* __restrict__ sink,
+                     uint32_t* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t bar0 = smem_u32(smem + kBulkStages * kBulkChunk);
+  const int64_t b = part_begin(blockIdx.x, n16, gridDim.x) * 16;
+  const int64_t e = part_begin(blockIdx.x + 1, n16, gridDim.x) * 16;
+  const int64_t nchunks = (e - b + kBulkChunk - 1) / kBulkChunk;
+  if (threadIdx.x != 0) return;
+  for (int s = 0; s < kBulkStages; ++s) mbar_init(bar0 + 8 * s, 1);
+  fence_mbar_init();
+  const uint64_t pol = policy_evict_first();
+  auto issue = [&](int64_t j) {
+    const int64_t off = b + j * kBulkChunk;
+    const int64_t left = e - off;
+    const uint32_t bytes = static_cast<uint32_t>(left < kBulkChunk ? left : kBulkChunk);
+    const int s = static_cast<int>(j % kBulkStages);
+    mbar_arrive_expect_tx(bar0 + 8 * s, bytes);
+    bulk_g2s(smem_u32(smem + s * kBulkChunk), buf + off, bytes, bar0 + 8 * s, pol);
+  };
+  int64_t issued = 0;
+  for (; issued < nchunks && issued < kBulkStages; ++issued) issue(issued);
+  uint32_t acc = 0;
+  for (int64_t j = 0; j < nchunks; ++j) {
+    const int s = static_cast<int>(j % kBulkStages);
+    if (!mbar_wait(bar0 + 8 * s, static_cast<uint32_t>((j / kBulkStages) & 1), status,
+                   kStatusTimeoutProducer)) {
+      break;
+    }
+    acc ^= *reinterpret_cast<const uint32_t*>(smem + s * kBulkChunk);
+    if (issued < nchunks) issue(issued++);
+  }
+  // Drain (normally a no-op: every issued chunk has been waited on).
+  for (int64_t j = issued > kBulkStages ? issued - kBulkStages : 0; j < issued; ++j)
+    mbar_wait(bar0 + 8 * static_cast<int>(j % kBulkStages),
+              static_cast<uint32_t>((j / kBulkStages) & 1), status, kStatusTimeoutDrain);
+  sink[blockIdx.x] = acc;
+}
+
+}  // namespace
+
+cudaError_t read_floor_launch(const void* buf, int64_t bytes, uint32_t* sink, int grid, int mode,
+                              cudaStream_t s) {
+  const int64_t n16 = bytes / 16;
+  if (mode == 0) {
+    read_regs_kernel<<<grid, kRegThreads, 0, s>>>(static_cast<const uint4*>(buf), n16, sink);
+    return cudaGetLastError();
+  }
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(read_bulk_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kBulkSmem));
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  // The status word for the bulk form lives in the tail of the sink buffer.
+  read_bulk_kernel<<<grid, 32, kBulkSmem, s>>>(static_cast<const uint8_t*>(buf), n16, sink,
+                                               sink + grid);
+  return cudaGetLastError();
+}
+
+}  // namespace proj

@@ -205,7 +205,8 @@ const char *proj_last_cuda_error(void);
  * bytes a multiple of 16), with every byte reaching the SMs: the HBM read
  * floor of the timing harness, and, on a buffer larger than L2, the flush
  * that makes the next call cold.  Writes one 32-bit checksum per CTA to
- * `sink` (device, >= grid words).  grid = 0 picks one CTA per SM.
+ * `sink` (device, >= grid + 1 words; the last one is a status word).
+ * grid = 0 picks two CTAs per SM for mode 0 and one for mode 1.
  * mode 0 = 128-bit register loads, mode 1 = bulk copies into shared memory.
  */
 int proj_read_floor(const void *buf, int64_t bytes, void *sink, int grid, int mode,

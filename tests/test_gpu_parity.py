@@ -1,0 +1,259 @@
+"""GPU parity: the CUDA path through the C ABI against the FP64 oracle.
+
+Contract (muse_bf16_proj guide, ch. 1, §1.5 "What counts as correct"):
+relative L2 per output <= 1e-2 (router 1e-4), probe rows within 1e-3 (and,
+stronger, exactly equal to the scaled weight column), no row over 5x the
+bound, no NaN/Inf.  Shapes: the five layers at the six scored token counts
+and the awkward ones (§1.2), two weight seeds, normal and outlier inputs.
+Small m is compared in full; large m on sampled token rows (all of their
+outputs), which always include the probe rows.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from gemv_projection_layers_gb300 import binding as B
+from gemv_projection_layers_gb300 import workloads as wl
+from oracle import oracle
+
+pytestmark = pytest.mark.gpu
+
+FULL_ORACLE_MAX_M = 33
+SAMPLED_ROWS = 20
+M_SCORED = (1, 8, 16, 32, 128, 256)
+M_AWKWARD = (5, 7, 9, 33, 130, 512, 1000)
+
+
+@pytest.fixture(scope="module")
+def dev():
+    assert torch.cuda.is_available()
+    B.load()
+    return torch.device("cuda:0")
+
+
+_cache = {}
+
+
+def prepared(layer, seed, flags=0):
+    key = (layer, seed, flags)
+    if key not in _cache:
+        spec = wl.LAYER_BY_NAME[layer]
+        Wnp = wl.make_weights(layer, seed)
+        if spec.weight_dtype == "fp32":
+            Wd = torch.from_numpy(Wnp).cuda()
+            dt = B.PROJ_FP32
+        else:
+            Wd = torch.from_numpy(Wnp.view(np.int16)).cuda().view(torch.bfloat16)
+            dt = B.PROJ_BF16
+        h = B.proj_prepare_ex(spec.index, Wd, spec.N, spec.K, dt, flags, 1024)
+        _cache[key] = (h, Wnp, Wd)
+    return _cache[key]
+
+
+def to_dev_x(x_bits):
+    return torch.from_numpy(np.ascontiguousarray(x_bits).view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def run(layer, h, x_dev, m, **kw):
+    spec = wl.LAYER_BY_NAME[layer]
+    n_out = B.proj_out_features(h, m)
+    dt = torch.float32 if spec.out_dtype == "fp32" else torch.bfloat16
+    out = torch.full((m, n_out), float("nan"), dtype=dt, device="cuda")
+    if kw:
+        B.proj_run_ex(h, x_dev, m, out, torch.cuda.current_stream(), **kw)
+    else:
+        B.proj_run(h, x_dev, m, out, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    return out
+
+
+def out_f64(out):
+    return out.float().cpu().numpy().astype(np.float64)
+
+
+def reference_rows(layer, act, W, rows):
+    """FP64 reference of whole output rows (tokens) `rows`."""
+    return oracle.reference(layer, act.x_bits[rows], W)
+
+
+def check_case(layer, seed, outliers, m, h=None, W=None, **kw):
+    if h is None:
+        h, W, _ = prepared(layer, seed)
+    act = wl.make_activations(layer, m, seed, outliers)
+    out = out_f64(run(layer, h, to_dev_x(act.x_bits), m, **kw))
+    if m <= FULL_ORACLE_MAX_M:
+        rows = np.arange(m)
+    else:
+        rng = np.random.default_rng(m * 7 + seed)
+        pick = rng.choice(m, size=min(SAMPLED_ROWS, m), replace=False)
+        rows = np.unique(np.concatenate([pick, [m - 1], act.probe_rows])).astype(np.int64)
+    ref = reference_rows(layer, act, W, rows)
+    probe_local = [int(np.flatnonzero(rows == p)[0]) for p in act.probe_rows]
+    res = oracle.check(layer, out[rows], ref, probe_local)
+    assert res["ok"], (layer, seed, outliers, m, res)
+    # probe rows: exactly the scaled weight column (bf16 out: exact in bf16)
+    n_out = out.shape[1]
+    for r, c, e, s in zip(act.probe_rows, act.probe_cols, act.probe_exp, act.probe_sign):
+        if W.dtype == np.float32:
+            col = W[:n_out, c].astype(np.float64)
+        else:
+            col = oracle.bf16_bits_to_f64(W[:n_out, c])
+        assert np.array_equal(out[r], float(s) * 2.0 ** int(e) * col), (layer, m, int(r))
+    return out
+
+
+@pytest.mark.parametrize("m", M_SCORED + M_AWKWARD)
+@pytest.mark.parametrize("layer", [s.name for s in wl.LAYERS])
+def test_parity_all_shapes(dev, layer, m):
+    combos = [(0, False), (1, True)]
+    if m <= FULL_ORACLE_MAX_M:
+        combos += [(0, True), (1, False)]
+    for seed, outl in combos:
+        check_case(layer, seed, outl, m)
+
+
+@pytest.mark.parametrize("layer,m", [("o", 1), ("o", 33), ("router", 1), ("router", 33),
+                                     ("unpooler", 8), ("qkv_gate", 130)])
+def test_split_partitions_and_determinism(dev, layer, m):
+    h, W, _ = prepared(layer, 0)
+    sms = B.proj_num_sms()
+    for grid in (1, 7, 64, sms - 1, sms):
+        a = check_case(layer, 0, True, m, h=h, W=W, grid=grid)
+        b = check_case(layer, 0, True, m, h=h, W=W, grid=grid)
+        assert np.array_equal(a, b), (layer, m, grid)
+    assert B.proj_device_status(h) == 0
+
+
+@pytest.mark.parametrize("layer,m", [("qkv_gate", 16), ("router", 1), ("pooler", 256),
+                                     ("unpooler", 8), ("router", 130)])
+def test_graph_replay_with_fresh_inputs(dev, layer, m):
+    """Split-K counters must return to zero: replays on new x stay correct
+    (muse_bf16_proj notebook, n. 19 "Split-K and the cost of combining work")."""
+    spec = wl.LAYER_BY_NAME[layer]
+    h, W, _ = prepared(layer, 1)
+    n_out = B.proj_out_features(h, m)
+    dt = torch.float32 if spec.out_dtype == "fp32" else torch.bfloat16
+    xs = torch.zeros((m, spec.K), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros((m, n_out), dtype=dt, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        B.proj_run(h, xs, m, out, s)  # warm-up (tensor map cached for this buffer)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        B.proj_run(h, xs, m, out, torch.cuda.current_stream())
+    for rep in range(4):
+        act = wl.make_activations(layer, m, 100 + rep, outliers=bool(rep & 1))
+        xs.copy_(to_dev_x(act.x_bits))
+        g.replay()
+        torch.cuda.synchronize()
+        o = out_f64(out)
+        rows = np.arange(m) if m <= FULL_ORACLE_MAX_M else np.unique(
+            np.concatenate([np.arange(0, m, max(1, m // 16)), act.probe_rows]))
+        ref = reference_rows(layer, act, W, rows)
+        probe_local = [int(np.flatnonzero(rows == p)[0]) for p in act.probe_rows]
+        res = oracle.check(layer, o[rows], ref, probe_local)
+        assert res["ok"], (layer, m, rep, res)
+    assert B.proj_device_status(h) == 0
+
+
+@pytest.mark.parametrize("layer", ["qkv_gate", "o", "pooler", "unpooler", "router"])
+def test_unpack_is_lossless(dev, layer):
+    h, W, Wd = prepared(layer, 0)
+    back = torch.empty_like(Wd)
+    B.proj_unpack_weights(h, B.PROJ_VARIANT_DENSE, back)
+    torch.cuda.synchronize()
+    assert torch.equal(back.view(torch.int16) if back.dtype == torch.bfloat16 else back,
+                       Wd.view(torch.int16) if Wd.dtype == torch.bfloat16 else Wd)
+
+
+@pytest.mark.parametrize("layer", ["qkv_gate", "o", "pooler", "unpooler"])
+def test_expwin12_lossless_and_bit_identical(dev, layer):
+    """12-bit exponent-window weights (muse_bf16_proj project report, Round 5):
+    window and escapes as the oracle's codec, lossless decode, and outputs
+    bit-identical to the uncompressed kernel at the same partition."""
+    for seed in (0, 1):
+        h, W, Wd = prepared(layer, seed, B.PROJ_ENCODE_EXPWIN12)
+        info = B.proj_info(h)
+        assert info["expwin12"] == 1 and info["expwin12_declined"] == 0
+        e0 = oracle.expwin12_window(W)
+        _, _, esc, _ = oracle.expwin12_encode(W, e0)
+        assert info["expwin12_e0"] == e0
+        assert info["expwin12_escapes"] == esc.size
+        back = torch.empty_like(Wd)
+        B.proj_unpack_weights(h, B.PROJ_VARIANT_EXPWIN12, back)
+        torch.cuda.synchronize()
+        assert torch.equal(back.view(torch.int16), Wd.view(torch.int16))
+        for m in (1, 8, 16, 32):
+            act = wl.make_activations(layer, m, seed + 5, outliers=True)
+            x = to_dev_x(act.x_bits)
+            for grid in (0, 37):
+                a = run(layer, h, x, m, variant=B.PROJ_VARIANT_DENSE, grid=grid)
+                b = run(layer, h, x, m, variant=B.PROJ_VARIANT_EXPWIN12, grid=grid)
+                assert torch.equal(a.view(torch.int16), b.view(torch.int16)), (layer, seed, m, grid)
+            check_case(layer, seed, True, m, h=h, W=W, variant=B.PROJ_VARIANT_EXPWIN12)
+        # one-hot rows on escaped columns reproduce the column exactly
+        K = W.shape[1]
+        n_out = B.proj_out_features(h, 8)
+        cols = np.unique(esc[(esc // K) < n_out] % K)[:8]
+        x = np.zeros((len(cols), K), np.uint16)
+        x[np.arange(len(cols)), cols] = 0x3F80  # 1.0
+        o = out_f64(run(layer, h, to_dev_x(x), len(cols), variant=B.PROJ_VARIANT_EXPWIN12))
+        for i, c in enumerate(cols):
+            assert np.array_equal(o[i], oracle.bf16_bits_to_f64(W[:o.shape[1], c]))
+        assert B.proj_device_status(h) == 0
+
+
+def test_run_host_matches_device_run(dev):
+    for layer, m in (("o", 1), ("router", 16), ("unpooler", 8), ("pooler", 130)):
+        spec = wl.LAYER_BY_NAME[layer]
+        h, W, _ = prepared(layer, 0)
+        act = wl.make_activations(layer, m, 3, False)
+        dev_out = run(layer, h, to_dev_x(act.x_bits), m)
+        x_host = torch.from_numpy(act.x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+        host_out = torch.empty(dev_out.shape, dtype=dev_out.dtype).pin_memory()
+        s = torch.cuda.current_stream()
+        B.proj_run_host(h, x_host, m, host_out, s)
+        s.synchronize()
+        assert torch.equal(host_out.view(torch.int16) if spec.out_dtype == "bf16" else host_out,
+                           dev_out.cpu().view(torch.int16) if spec.out_dtype == "bf16"
+                           else dev_out.cpu())
+
+
+def test_edge_arguments(dev):
+    h, W, _ = prepared("o", 0)
+    x = torch.zeros((4, 1024), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros((4, 8192), dtype=torch.bfloat16, device="cuda")
+    B.proj_run(h, x, 0, out)  # m = 0: no launch, no error
+    with pytest.raises(B.ProjError) as e:
+        B.proj_run(h, x, 1025, out)
+    assert e.value.status == B.PROJ_EUNSUPPORTED
+    with pytest.raises(B.ProjError) as e:
+        B.proj_run(h, x.data_ptr() + 2, 1, out)
+    assert e.value.status == B.PROJ_EALIGN
+    assert B.proj_out_features(prepared("unpooler", 0)[0], 8) == 1024
+    assert B.proj_out_features(prepared("unpooler", 0)[0], 9) == 8192
+    assert "BN=16" in B.proj_describe(h, 1)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_read_floor_checksums(dev, mode):
+    nbytes = 48 * 1024 * 1024 + 4096
+    g = torch.Generator().manual_seed(5)
+    buf = torch.randint(-2**31, 2**31 - 1, (nbytes // 4,), dtype=torch.int32, generator=g)
+    grid = 37
+    sink = torch.zeros(grid + 1, dtype=torch.int32, device="cuda")
+    B.proj_read_floor(buf.cuda(), nbytes, sink, grid, mode)
+    torch.cuda.synchronize()
+    words = buf.numpy().view(np.uint32)
+    n16 = nbytes // 16
+    for c in range(grid):
+        b, e = c * n16 // grid, (c + 1) * n16 // grid
+        seg = words[4 * b:4 * e]
+        if mode == 0:
+            expect = np.bitwise_xor.reduce(seg) if seg.size else 0
+        else:
+            expect = np.bitwise_xor.reduce(seg[::4096]) if seg.size else 0
+        assert int(sink[c].item()) & 0xFFFFFFFF == int(expect), c
+    assert int(sink[grid].item()) == 0
