@@ -1,0 +1,570 @@
+"""Benchmark: microseconds per load (sum of the five layers, cold L2, CUDA
+graph replay) and achieved HBM bandwidth against the measured peak.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--load decode1] [--no-extras]
+
+One step = one load: the five layers (qkv_gate, o, pooler, unpooler, router)
+at the load's token count, each a captured single-kernel CUDA graph replayed
+back to back on one stream.  Before every step a read of 4x the L2 size
+(the library's own streaming-read kernel) evicts the weights, outside the
+timed events (muse_bf16_proj guide, ch. 10, §10.1 "How we measure": graph
+capture after 3 warm-ups, a read larger than L2 before each replay).  Events
+bracket each layer, so every layer's cold-L2 duration is measured inside the
+timed region.
+
+--impl reference times the CPU FP64 oracle (the only other program that
+computes this result here) on the same load.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from gemv_projection_layers_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "us per load (sum of 5 layers, cold L2, graph replay)"
+UNIT = "us/load"
+HEADLINE_LOAD = "decode1"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ----------------------------------------------------------------- helpers --
+
+def algorithmic_bytes(spec, m: int, n_out: int, w_bytes_per_elem: float, n_esc: int = 0) -> float:
+    """Weights of the rows computed + bf16 x + output (escape entries, 4 B
+    each, count as weight bytes of the 12-bit form)."""
+    ob = 4 if spec.out_dtype == "fp32" else 2
+    return n_out * spec.K * w_bytes_per_elem + n_esc * 4 + m * spec.K * 2 + m * n_out * ob
+
+
+def flops(spec, m: int, n_out: int) -> float:
+    return 2.0 * m * n_out * spec.K
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 1900.0)), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, flags in rows for i, f in enumerate(flags)
+                          if f.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows),
+                "samples": len(rows), "reasons": reasons}
+
+
+# --------------------------------------------------------------- our path --
+
+class Layer:
+    def __init__(self, spec, h, info):
+        self.spec, self.h, self.info = spec, h, info
+
+
+class Shape:
+    """One layer at one token count: resident x and out buffers."""
+
+    def __init__(self, B, torch, L, m, seed=0):
+        self.L, self.spec, self.h, self.m = L, L.spec, L.h, m
+        act = wl.make_activations(L.spec, m, seed, outliers=False)
+        self.x = torch.from_numpy(act.x_bits.view(np.int16)).cuda().view(torch.bfloat16)
+        self.n_out = B.proj_out_features(L.h, m)
+        odt = torch.float32 if L.spec.out_dtype == "fp32" else torch.bfloat16
+        self.out = torch.empty((m, self.n_out), dtype=odt, device="cuda")
+        self.desc = B.proj_describe(L.h, m)
+
+
+def setup_layers(B, torch, expwin: bool, seed: int = 0):
+    layers = []
+    for spec in wl.LAYERS:
+        Wnp = wl.make_weights(spec, seed)
+        if spec.weight_dtype == "fp32":
+            Wd = torch.from_numpy(Wnp).cuda()
+            dt, flags = B.PROJ_FP32, 0
+        else:
+            Wd = torch.from_numpy(Wnp.view(np.int16)).cuda().view(torch.bfloat16)
+            dt = B.PROJ_BF16
+            flags = B.PROJ_ENCODE_EXPWIN12 if expwin else 0
+        h = B.proj_prepare_ex(spec.index, Wd, spec.N, spec.K, dt, flags, 1024)
+        del Wd
+        layers.append(Layer(spec, h, B.proj_info(h)))
+    torch.cuda.synchronize()
+    return layers
+
+
+def _external_events_supported(torch) -> bool:
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+        return True
+    except TypeError:
+        return False
+
+
+class LoadGraph:
+    """The five layers of one load captured in one CUDA graph, with timing
+    events recorded between the kernels when torch supports external events
+    (otherwise one graph per layer, timed back to back)."""
+
+    def __init__(self, B, torch, shapes, stream):
+        self.shapes = shapes
+        self.stream = stream
+        with torch.cuda.stream(stream):  # 3 warm-ups before capture (guide ch. 10, §10.1)
+            for _ in range(3):
+                for S in shapes:
+                    B.proj_run(S.h, S.x, S.m, S.out, stream)
+        torch.cuda.synchronize()
+        self.inner = _external_events_supported(torch)
+        n = len(shapes)
+        if self.inner:
+            self.ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n + 1)]
+            self.graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.graph, stream=stream):
+                self.ev[0].record(stream)
+                for i, S in enumerate(shapes):
+                    B.proj_run(S.h, S.x, S.m, S.out, stream)
+                    self.ev[i + 1].record(stream)
+            self.graphs = None
+        else:
+            self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+            self.graphs = []
+            for S in shapes:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    B.proj_run(S.h, S.x, S.m, S.out, stream)
+                self.graphs.append(g)
+            self.graph = None
+        torch.cuda.synchronize()
+
+    def step(self, B, torch, flush, sink):
+        """flush (untimed) -> events -> replay; returns (outer us, per-layer us)."""
+        s = self.stream
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            B.proj_read_floor(flush, flush.numel() * 4, sink, 0, 0, s)
+            a.record(s)
+            if self.graph is not None:
+                self.graph.replay()
+            else:
+                self.ev[0].record(s)
+                for i, g in enumerate(self.graphs):
+                    g.replay()
+                    self.ev[i + 1].record(s)
+            b.record(s)
+        s.synchronize()
+        per = [self.ev[i].elapsed_time(self.ev[i + 1]) * 1e3 for i in range(len(self.shapes))]
+        return a.elapsed_time(b) * 1e3, per
+
+
+def time_load(B, torch, lg, flush, sink, steps):
+    outer, per = [], []
+    for _ in range(steps):
+        o, p = lg.step(B, torch, flush, sink)
+        outer.append(o)
+        per.append(p)
+    return np.array(outer), np.array(per)
+
+
+def time_read_floor(B, torch, nbytes_list, flush, sink, stream, reps, mode=0):
+    """Cold-L2 read of exactly `nbytes` (one graph per size), median us."""
+    res = {}
+    buf = torch.empty(max(nbytes_list) // 4 + 16, dtype=torch.int32, device="cuda")
+    buf.fill_(1)
+    sink2 = torch.zeros(2 * B.proj_num_sms() + 8, dtype=torch.int32, device="cuda")
+    for nb in nbytes_list:
+        nb16 = nb - nb % 16
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                B.proj_read_floor(buf, nb16, sink2, 0, mode, stream)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            B.proj_read_floor(buf, nb16, sink2, 0, mode, stream)
+        ts = []
+        with torch.cuda.stream(stream):
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(reps)]
+            for a, b in evs:
+                B.proj_read_floor(flush, flush.numel() * 4, sink, 0, 0, stream)
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+        stream.synchronize()
+        ts = [a.elapsed_time(b) * 1e3 for a, b in evs]
+        res[nb] = float(np.median(ts))
+    return res
+
+
+def time_empty_graph(B, torch, flush, sink, stream, reps):
+    """Replay cost of a graph holding one tiny kernel (a 16-byte read)."""
+    tiny = torch.zeros(64, dtype=torch.int32, device="cuda")
+    s2 = torch.zeros(8, dtype=torch.int32, device="cuda")
+    with torch.cuda.stream(stream):
+        B.proj_read_floor(tiny, 16, s2, 1, 0, stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        B.proj_read_floor(tiny, 16, s2, 1, 0, stream)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    with torch.cuda.stream(stream):
+        for a, b in evs:
+            B.proj_read_floor(flush, flush.numel() * 4, sink, 0, 0, stream)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+    stream.synchronize()
+    return float(np.median([a.elapsed_time(b) * 1e3 for a, b in evs]))
+
+
+def time_e2e(B, torch, shapes, flush, sink, stream, steps):
+    """Through proj_run_host: pinned host x in, pinned host out, per step."""
+    hosts = []
+    for S in shapes:
+        xh = S.x.cpu().pin_memory()
+        oh = torch.empty(S.out.shape, dtype=S.out.dtype).pin_memory()
+        hosts.append((xh, oh))
+    h2d = sum(xh.numel() * xh.element_size() for xh, _ in hosts)
+    d2h = sum(oh.numel() * oh.element_size() for _, oh in hosts)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            for S, (xh, oh) in zip(shapes, hosts):
+                B.proj_run_host(S.h, xh, S.m, oh, stream)
+    stream.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for a, b in evs:
+            B.proj_read_floor(flush, flush.numel() * 4, sink, 0, 0, stream)
+            a.record(stream)
+            for S, (xh, oh) in zip(shapes, hosts):
+                B.proj_run_host(S.h, xh, S.m, oh, stream)
+            b.record(stream)
+    stream.synchronize()
+    ts = [a.elapsed_time(b) * 1e3 for a, b in evs]
+    return float(np.mean(ts)), h2d, d2h
+
+
+def time_direct_kernel(B, torch, S, flush, sink, stream, reps):
+    """Event-bracketed direct launch after a flush (kernel duration, cold)."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    with torch.cuda.stream(stream):
+        for a, b in evs:
+            B.proj_read_floor(flush, flush.numel() * 4, sink, 0, 0, stream)
+            a.record(stream)
+            B.proj_run(S.h, S.x, S.m, S.out, stream)
+            b.record(stream)
+    stream.synchronize()
+    return float(np.mean([a.elapsed_time(b) * 1e3 for a, b in evs]))
+
+
+def weight_bytes(S) -> tuple[float, int]:
+    """(bytes per weight element read, escape entries read) for a shape."""
+    if S.spec.weight_dtype == "fp32":
+        return 4.0, 0
+    if "expwin12" in S.desc:
+        return 1.5, int(S.L.info["expwin12_escapes"] * S.n_out / S.spec.N)
+    return 2.0, 0
+
+
+def cpu_baseline(load_m: int, budget_s: float = 10.0, seed: int = 0):
+    """The oracle as it stands, on the host cores, over whole loads."""
+    from oracle import oracle
+    Ws = [wl.make_weights(s, seed) for s in wl.LAYERS]
+    acts = [wl.make_activations(s, load_m, seed) for s in wl.LAYERS]
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        for s, W, a in zip(wl.LAYERS, Ws, acts):
+            oracle.reference(s.name, a.x_bits, W)
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return dt / n * 1e6, oracle.threads(), n
+
+
+def traffic_from_profiles(kernel_key: str):
+    """DRAM bytes per launch recorded from an ncu capture, if still current."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        d = json.load(open(p))
+        e = d.get(kernel_key)
+        if not e:
+            return None
+        import hashlib
+        src = os.path.join(ROOT, e["source"])
+        if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != e["source_sha"]:
+            return None
+        return float(e["bytes_per_launch"])
+    except Exception:
+        return None
+
+
+def run_ours(args):
+    import torch
+    from gemv_projection_layers_gb300 import binding as B
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    B.load()  # fails loudly if the CUDA library is missing
+
+    stream = torch.cuda.Stream()
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    flush = torch.ones(l2 + 4096, dtype=torch.int32, device="cuda")  # 4x L2 bytes
+    sink = torch.zeros(2 * B.proj_num_sms() + 8, dtype=torch.int32, device="cuda")
+    layers = setup_layers(B, torch, expwin=not args.dense)
+
+    loads = [args.load] + ([n for n, _ in wl.LOADS if n != args.load] if args.all_loads else [])
+    graphs = {}
+    for ld in loads:
+        shapes = [Shape(B, torch, L, wl.LOAD_M[ld]) for L in layers]
+        graphs[ld] = LoadGraph(B, torch, shapes, stream)
+    lg = graphs[args.load]
+    m = wl.LOAD_M[args.load]
+
+    time_load(B, torch, lg, flush, sink, max(3, args.warmup))
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    outer, per = time_load(B, torch, lg, flush, sink, args.steps)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+
+    mean_us = float(outer.mean())
+    if world > 1:
+        t = torch.tensor([mean_us], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        mean_us = float(t.item())
+    layer_us = per.mean(axis=0)
+
+    hbm_gbs, bf16_tf, peak_src = load_peaks()
+    di = int(np.argmax(layer_us))  # dominant kernel: largest share of the load
+    D = lg.shapes[di]
+    wbpe, nesc = weight_bytes(D)
+    dom_bytes = algorithmic_bytes(D.spec, m, D.n_out, wbpe, nesc)
+    dom_us = float(layer_us[di])
+    achieved = dom_bytes / (dom_us * 1e-6) / 1e9
+    kernel_key = f"{D.spec.name}_m{m}_{'expwin12' if wbpe == 1.5 else 'dense'}"
+    slice_rows = lg.shapes[3].n_out
+
+    result = {
+        "metric": METRIC,
+        "value": round(mean_us / world, 3),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(mean_us / 1e3, 6),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded: x ~ N(0,1) bf16, W ~ N(0,1/K))",
+        "config": {
+            "workload": f"{args.load} load: m={m} through qkv_gate 2304x8192, o 8192x1024, "
+                        f"pooler 4096x8192, unpooler {slice_rows}x4096, router fp32 256x8192",
+            "m": m,
+            "l2": f"flushed before every step by a {4 * l2 >> 20} MiB read (4x L2), "
+                  "outside the events",
+            "timing": "one CUDA graph per load (5 kernels); value = event pair around the "
+                      "replay (includes one graph launch); per-layer = event nodes inside "
+                      "the graph" if lg.inner else
+                      "one CUDA graph per layer replayed back to back; value includes 5 "
+                      "graph launches",
+            "weights": "dense bf16" if args.dense else "12-bit exponent-window for bf16 "
+                                                       "layers at m<=16, dense otherwise",
+            "parallelism": f"replicas x{world}",
+        },
+        "kernel_sum_us": round(float(layer_us.sum()), 3),
+        "per_layer_us": {S.spec.name: round(float(u), 3) for S, u in zip(lg.shapes, layer_us)},
+        "kernels": {S.spec.name: S.desc for S in lg.shapes},
+        "roofline": {
+            "bound": "hbm",
+            "kernel": f"{D.spec.name} ({D.desc})",
+            "achieved": round(achieved, 1),
+            "peak": hbm_gbs,
+            "unit": "GB/s",
+            "frac": round(achieved / hbm_gbs, 4),
+            "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                           if peak_src == "measured" else "fallback 6.8 TB/s",
+            "algorithmic_bytes": int(dom_bytes),
+            "duration_us": round(dom_us, 3),
+            "traffic": traffic_from_profiles(kernel_key),
+        },
+        "clocks": clk,
+        "gpu_launches": int(args.steps * (len(layers) + 1)),
+        "timed_wall_s": round(t_wall, 4),
+    }
+
+    if args.all_loads and rank == 0:
+        loads_out = {}
+        for ld in loads:
+            o, pl = time_load(B, torch, graphs[ld], flush, sink, max(20, min(args.steps, 100)))
+            loads_out[ld] = {"us": round(float(o.mean()), 2),
+                             "kernel_sum_us": round(float(pl.mean(axis=0).sum()), 2),
+                             "per_layer_us": {S.spec.name: round(float(u), 2) for S, u in
+                                              zip(graphs[ld].shapes, pl.mean(axis=0))}}
+        result["loads"] = loads_out
+
+    if not args.no_extras and rank == 0:
+        e2e_us, h2d, d2h = time_e2e(B, torch, lg.shapes, flush, sink, stream, args.steps)
+        result["e2e"] = {"value": round(e2e_us, 3), "unit": UNIT,
+                         "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+        wb = {}
+        for S in lg.shapes:
+            bpe, ne = weight_bytes(S)
+            wb[S.spec.name] = int(S.n_out * S.spec.K * bpe + ne * 4)
+        floors = time_read_floor(B, torch, sorted(set(wb.values())), flush, sink, stream,
+                                 max(20, min(args.steps, 100)))
+        ov = time_empty_graph(B, torch, flush, sink, stream, 50)
+        result["read_floor_us"] = {k: round(floors[v], 3) for k, v in wb.items()}
+        result["empty_graph_us"] = round(ov, 3)
+        if lg.inner:
+            # kernel-only layer times vs the read kernel net of its replay cost
+            result["floor_fraction"] = {k: round(max(floors[wb[k]] - ov, 0.0) / float(u), 3)
+                                        for k, u in zip(wb, layer_us)}
+        result["direct_launch_us"] = {S.spec.name: round(time_direct_kernel(
+            B, torch, S, flush, sink, stream, 20), 3) for S in lg.shapes}
+        cb_us, cores, n = cpu_baseline(m, budget_s=args.cpu_seconds)
+        result["cpu_baseline"] = {"value": round(cb_us, 1), "unit": UNIT, "cores": cores,
+                                  "kind": "oracle",
+                                  "sample": f"{n} whole {args.load} loads (FP64 C oracle, "
+                                            f"{args.cpu_seconds:.0f} s budget)"}
+    for L in layers:
+        B.proj_destroy(L.h)
+    if rank == 0:
+        print(json.dumps(result))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_reference(args):
+    """The oracle (CPU, FP64) timed on the same load; rank 0 only."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from oracle import oracle
+    m = wl.LOAD_M[args.load]
+    Ws = [wl.make_weights(s, 0) for s in wl.LAYERS]
+    acts = [wl.make_activations(s, m, 0) for s in wl.LAYERS]
+    for _ in range(max(1, args.warmup)):
+        for s, W, a in zip(wl.LAYERS, Ws, acts):
+            oracle.reference(s.name, a.x_bits, W)
+    ts = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        for s, W, a in zip(wl.LAYERS, Ws, acts):
+            oracle.reference(s.name, a.x_bits, W)
+        ts.append((time.perf_counter() - t0) * 1e6)
+    v = float(np.mean(ts))
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": UNIT,
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(v / 1e3, 4), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.load} load: m={m}, five layers", "m": m},
+        "cpu_baseline": {"value": round(v, 1), "unit": UNIT, "cores": oracle.threads(),
+                         "kind": "oracle", "sample": f"one whole {args.load} load per step"},
+        "e2e": {"value": round(v, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }))
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--load", choices=[n for n, _ in wl.LOADS], default=HEADLINE_LOAD)
+    ap.add_argument("--dense", action="store_true", help="no 12-bit weights")
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--all-loads", action=argparse.BooleanOptionalAction, default=True,
+                    help="also time the other five loads (reported under 'loads')")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

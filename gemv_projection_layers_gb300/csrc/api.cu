@@ -111,9 +111,16 @@ int tm_for_m(int64_t m) {
 constexpr int64_t kExpwinAutoMaxM = 16;
 constexpr int64_t kExpwinMaxM = 32;
 
+// Split-K combine by token count: the owner sums the others' partials while
+// its last segment streams (short tail, but one CTA reads S - 1 partials);
+// the distributed form spreads that reading over the contributors.
+constexpr int64_t kTcOwnerMaxM = 8;
+constexpr int64_t kRouterOwnerMaxM = 4;
+
 struct Plan {
   bool router;
   bool expwin;
+  int reduce;   // 0 owner, 1 distributed
   int bn;       // BN (tensor core) or TM (router)
   int64_t n_out;
   int T, KB, MT;
@@ -210,6 +217,18 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
     pl->T = static_cast<int>(pl->n_out / kTileRows);
     pl->KB = static_cast<int>(h->K / kTileK);
   }
+  const int rq = opts ? opts->reduce : PROJ_REDUCE_AUTO;
+  if (rq == PROJ_REDUCE_AUTO) {
+    pl->reduce = (m <= (pl->router ? kRouterOwnerMaxM : kTcOwnerMaxM)) ? 0 : 1;
+  } else if (rq == PROJ_REDUCE_OWNER) {
+    if (!pl->router && pl->bn > 32) return PROJ_EUNSUPPORTED;
+    pl->reduce = 0;
+  } else if (rq == PROJ_REDUCE_DISTRIBUTED) {
+    pl->reduce = 1;
+  } else {
+    return PROJ_EINVAL;
+  }
+  if (opts && opts->reserved != 0) return PROJ_EINVAL;
   pl->MT = static_cast<int>((m + pl->bn - 1) / pl->bn);
   const int64_t U = static_cast<int64_t>(pl->MT) * pl->T * pl->KB;
   int64_t G = h->num_sms;
@@ -448,6 +467,7 @@ int proj_run_ex(proj_handle h, const void* x, int64_t m, void* out, proj_stream 
     p.KB = pl.KB;
     p.MT = pl.MT;
     p.G = pl.G;
+    p.reduce = pl.reduce;
     e = router_launch(pl.bn, *map, p, s);
   } else {
     TcParams p;
@@ -464,6 +484,7 @@ int proj_run_ex(proj_handle h, const void* x, int64_t m, void* out, proj_stream 
     p.MT = pl.MT;
     p.G = pl.G;
     p.e0x4 = static_cast<uint32_t>(h->e0) * 0x01010101u;
+    p.reduce = pl.reduce;
     e = tc_launch(pl.bn, pl.expwin, *map, p, s);
   }
   if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
@@ -518,12 +539,13 @@ int proj_describe(proj_handle h, int64_t m, char* buf, size_t cap) {
   int st = make_plan(h, m, nullptr, &pl);
   if (st != PROJ_OK) return fail(st);
   if (pl.router) {
-    std::snprintf(buf, cap, "router_fma TM=%d stages=8 G=%d T=%d KB=%d MT=%d", pl.bn, pl.G, pl.T,
-                  pl.KB, pl.MT);
+    std::snprintf(buf, cap, "router_fma TM=%d stages=8 G=%d T=%d KB=%d MT=%d reduce=%s", pl.bn,
+                  pl.G, pl.T, pl.KB, pl.MT, pl.reduce ? "distributed" : "owner");
   } else {
-    std::snprintf(buf, cap, "tc_%s BN=%d stages=%d G=%d T=%d KB=%d MT=%d n_out=%lld",
+    std::snprintf(buf, cap, "tc_%s BN=%d stages=%d G=%d T=%d KB=%d MT=%d n_out=%lld reduce=%s",
                   pl.expwin ? "expwin12" : "dense", pl.bn, tc_stages(pl.bn, pl.expwin), pl.G,
-                  pl.T, pl.KB, pl.MT, static_cast<long long>(pl.n_out));
+                  pl.T, pl.KB, pl.MT, static_cast<long long>(pl.n_out),
+                  pl.reduce ? "distributed" : "owner");
   }
   return PROJ_OK;
 }

@@ -7,58 +7,56 @@
 //
 // * Operand roles are swapped: 128 weight rows are the MMA's M side (A,
 //   K-major, from shared memory), the m tokens are its N side (B, N = BN =
-//   m rounded up to 16..256), so even m = 1 runs one tcgen05.mma.kind::f16
-//   M128 x N16 x K16 per 16 columns with fp32 accumulation in tensor memory.
+//   m rounded up to 16..256), so even m = 1 runs tcgen05.mma.kind::f16
+//   M128 x N16 x K16 with fp32 accumulation in tensor memory.
 // * Weights stream HBM -> shared memory with 1-D bulk copies of prepacked,
 //   pre-swizzled 16 KB tiles (one copy per 128 x 64 tile, evict-first), x
 //   with a 2-D TMA load whose out-of-range rows read as zero (ragged m).
-//   A deep mbarrier ring (4-12 stages) keeps >= 64 KB in flight per SM,
-//   enough to cover HBM latency at the per-SM share of bandwidth.
-// * Exactly one CTA per SM, 152 on GB300, and a split-K partition that
-//   gives every CTA the same number of (tile, k-block) units: the CTAs cut
-//   the linear order of units into G equal ranges (so a tile may be shared
-//   by several CTAs).  A CTA that finishes a whole tile writes bf16 output
-//   directly; a shared tile's CTAs write fp32 partials, bump a per-tile
-//   counter (acq_rel), and the last to arrive sums the partials in fixed CTA
-//   order (= ascending k), writes the output and resets the counter to zero
-//   on the GPU (muse_bf16_proj notebook, n. 19 "Split-K and the cost of
-//   combining work", last-arriving-block design; guide ch. 1, §1.6: counters
-//   are reset on the GPU).  No spin-wait on another CTA, one launch per call,
-//   deterministic results.
+//   A deep mbarrier ring keeps 100-200 KB in flight per SM.
+// * Exactly one CTA per SM (cooperative launch) and a split-K partition
+//   that gives every CTA the same number of (tile, k-block) units; tiles
+//   shared by several CTAs are combined in fixed CTA order (splitk.cuh):
+//   owner mode for small m (the owner pre-sums the other contributors'
+//   partials while its own last segment streams), distributed mode for large
+//   m (each contributor reduces 1/S of the tile).  Counters return to zero
+//   on the GPU (guide ch. 1, §1.6).  One launch per call, deterministic.
 // * Warp roles: warp 0 issues copies, warp 1 issues MMAs (and owns the
 //   tensor memory), warps 2-5 drain the accumulators; the 12-bit variant adds
-//   warps 6-9, which decode each record into the swizzled bf16 tile in shared
-//   memory and patch its escapes before the MMA reads it, so the MMA inputs
-//   -- and therefore the outputs -- are bit-identical to the dense kernel's
-//   (project report, "Round 5 -- lossless 12-bit compressed weights").
+//   warps 6-9, which decode each record from a deep ring of encoded stages
+//   into a short ring of swizzled bf16 tiles and patch the escapes before the
+//   MMA reads them, so the MMA inputs -- and the outputs -- are bit-identical
+//   to the dense kernel's (project report, "Round 5 -- lossless 12-bit
+//   compressed weights").
 // * The accumulator is double-buffered in tensor memory so the epilogue of
 //   one tile overlaps the MMAs of the next.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "splitk.cuh"
 
 namespace proj {
 namespace {
 
-constexpr int kSmemLimit = 232448;  // max dynamic shared memory per block
+constexpr int kSmemLimit = 232448;        // max dynamic shared memory per block
 constexpr int kSmemReserve = 1024 + 512;  // alignment slack + barriers
 
 template <int BN, bool EXPWIN>
 struct Cfg {
   static constexpr int kXBytes = BN * 128;
-  static constexpr int kStageBytes = kTileBytes + kXBytes + (EXPWIN ? kRecBytes : 0);
-  static constexpr int kStagesFit = (kSmemLimit - kSmemReserve) / kStageBytes;
-  static constexpr int kStages = kStagesFit > 12 ? 12 : kStagesFit;
+  static constexpr int SA = EXPWIN ? 4 : 0;  // decoded-tile ring (12-bit only)
+  static constexpr int kCopyStage = (EXPWIN ? kRecBytes : kTileBytes) + kXBytes;
+  static constexpr int kFit = (kSmemLimit - kSmemReserve - SA * kTileBytes) / kCopyStage;
+  static constexpr int SE = kFit > 12 ? 12 : kFit;  // copy ring
   static constexpr int kThreads = EXPWIN ? 320 : 192;
   static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
-  static constexpr int kABytes = kStages * kTileBytes;
-  static constexpr int kBBytes = kStages * kXBytes;
-  static constexpr int kEBytes = EXPWIN ? kStages * kRecBytes : 0;
-  static constexpr int kNumBars = 3 * kStages + 4;
+  static constexpr int kABytes = (EXPWIN ? SA : SE) * kTileBytes;
+  static constexpr int kBBytes = SE * kXBytes;
+  static constexpr int kEBytes = EXPWIN ? SE * kRecBytes : 0;
+  static constexpr int kNumBars = 2 * SE + 2 * SA + 4;
   static constexpr size_t kSmem = 1024 + kABytes + kBBytes + kEBytes + kNumBars * 8 + 16;
   static constexpr uint32_t kIdesc = idesc_bf16_f32(128, BN);
-  static_assert(kStages >= 3, "pipeline too shallow");
+  static_assert(SE >= 4, "pipeline too shallow");
   static_assert(kSmem <= kSmemLimit, "shared memory budget");
   static_assert((kXBytes % 1024) == 0, "x tile must keep 1024-byte alignment");
 };
@@ -93,11 +91,60 @@ __device__ __forceinline__ uint4 expwin_decode8(uint2 lo, uint32_t nb, uint32_t 
   return o;
 }
 
+// Owner mode: sum, in CTA order, the partials of contributors c_first + 1 ..
+// c_last for row r and tokens [0, mv) into pre[] (ws slot = contributor).
+template <int BN>
+__device__ __forceinline__ void owner_presum(const float* __restrict__ ws, int64_t cf, int64_t cl,
+                                             int mv, int r, float (&pre)[BN]) {
+  constexpr int64_t kStride = static_cast<int64_t>(BN) * kTileRows;
+#pragma unroll
+  for (int j = 0; j < BN; ++j) pre[j] = 0.f;
+  if (mv <= 2) {
+    // few tokens: many contributors per batch
+    for (int64_t c = cf + 1; c <= cl; c += 16) {
+      float v[16][2];
+#pragma unroll
+      for (int a = 0; a < 16; ++a)
+#pragma unroll
+        for (int b = 0; b < 2; ++b)
+          v[a][b] = (c + a <= cl && b < mv) ? __ldcg(ws + (c + a) * kStride + b * kTileRows + r)
+                                            : 0.f;
+#pragma unroll
+      for (int a = 0; a < 16; ++a) {
+        pre[0] += v[a][0];
+        if (BN > 1) pre[1] += v[a][1];
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j0 = 0; j0 < BN; j0 += 8) {
+      if (j0 < mv) {
+        for (int64_t c = cf + 1; c <= cl; c += 4) {
+          float v[4][8];
+#pragma unroll
+          for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 8; ++b)
+              v[a][b] = (c + a <= cl && j0 + b < mv)
+                            ? __ldcg(ws + (c + a) * kStride + (j0 + b) * kTileRows + r)
+                            : 0.f;
+#pragma unroll
+          for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 8; ++b) pre[j0 + b] += v[a][b];
+        }
+      }
+    }
+  }
+}
+
 template <int BN, bool EXPWIN>
 __global__ void __launch_bounds__(Cfg<BN, EXPWIN>::kThreads, 1)
     tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcParams p) {
   using C = Cfg<BN, EXPWIN>;
-  constexpr int S = C::kStages;
+  constexpr int SE = C::SE;
+  constexpr int SA = C::SA;
+  constexpr bool kOwnerOk = (BN <= 32);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -106,26 +153,31 @@ __global__ void __launch_bounds__(Cfg<BN, EXPWIN>::kThreads, 1)
   uint8_t* sE = sB + C::kBBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sE + C::kEBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
-  volatile uint32_t* last_flag = tmem_slot + 1;
 
   const uint32_t full0 = smem_u32(bars);
-  const uint32_t empty0 = full0 + 8 * S;
-  const uint32_t dec0 = empty0 + 8 * S;
-  const uint32_t accf0 = dec0 + 8 * S;
+  const uint32_t empty0 = full0 + 8 * SE;
+  const uint32_t decf0 = empty0 + 8 * SE;
+  const uint32_t dece0 = decf0 + 8 * SA;
+  const uint32_t accf0 = dece0 + 8 * SA;
   const uint32_t acce0 = accf0 + 16;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t G = p.G;
   const int64_t U = static_cast<int64_t>(p.MT) * p.T * p.KB;
-  const int64_t u0 = part_begin(blockIdx.x, U, G);
-  const int64_t u1 = part_begin(blockIdx.x + 1, U, G);
+  const int64_t cta = blockIdx.x;
+  const int64_t u0 = part_begin(cta, U, G);
+  const int64_t u1 = part_begin(cta + 1, U, G);
+  const bool owner_mode = kOwnerOk && p.reduce == 0;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
+    for (int s = 0; s < SE; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
-      mbar_init(dec0 + 8 * s, 1);
+    }
+    for (int s = 0; s < SA; ++s) {
+      mbar_init(decf0 + 8 * s, 1);
+      mbar_init(dece0 + 8 * s, 1);
     }
     mbar_init(accf0, 1);
     mbar_init(accf0 + 8, 1);
@@ -147,8 +199,8 @@ __global__ void __launch_bounds__(Cfg<BN, EXPWIN>::kThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      int stage = 0;
-      uint32_t phase = 0;
+      int e = 0;
+      uint32_t ph = 0;
       int64_t issued = 0;
       int64_t u = u0;
       Seg sg;
@@ -157,42 +209,41 @@ __global__ void __launch_bounds__(Cfg<BN, EXPWIN>::kThreads, 1)
         const int t = sg.tile / p.MT;
         const int mt = sg.tile % p.MT;
         for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
-          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, p.status, kStatusTimeoutProducer)) {
+          if (!mbar_wait(empty0 + 8 * e, ph ^ 1, p.status, kStatusTimeoutProducer)) {
             ok = false;
             break;
           }
-          const uint32_t fb = full0 + 8 * stage;
+          const uint32_t fb = full0 + 8 * e;
           const size_t tile_idx = static_cast<size_t>(t) * p.KB + kb;
           if (EXPWIN) {
             mbar_arrive_expect_tx(fb, kRecBytes + C::kXBytes);
-            bulk_g2s(smem_u32(sE + stage * kRecBytes), p.w + tile_idx * kRecBytes, kRecBytes, fb,
+            bulk_g2s(smem_u32(sE + e * kRecBytes), p.w + tile_idx * kRecBytes, kRecBytes, fb,
                      pol);
           } else {
             mbar_arrive_expect_tx(fb, kTileBytes + C::kXBytes);
-            bulk_g2s(smem_u32(sA + stage * kTileBytes), p.w + tile_idx * kTileBytes, kTileBytes,
-                     fb, pol);
+            bulk_g2s(smem_u32(sA + e * kTileBytes), p.w + tile_idx * kTileBytes, kTileBytes, fb,
+                     pol);
           }
-          tma_load_2d(smem_u32(sB + stage * C::kXBytes), &tmap_x, kb * kTileK, mt * BN, fb);
+          tma_load_2d(smem_u32(sB + e * C::kXBytes), &tmap_x, kb * kTileK, mt * BN, fb);
           ++issued;
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1;
+          if (++e == SE) {
+            e = 0;
+            ph ^= 1;
           }
         }
       }
       // Drain: every copy issued must have landed before the CTA may exit.
-      const int64_t n = issued < S ? issued : S;
+      const int64_t n = issued < SE ? issued : SE;
       for (int64_t j = 0; j < n; ++j) {
         const int64_t idx = issued - 1 - j;
-        mbar_wait(full0 + 8 * static_cast<int>(idx % S), static_cast<uint32_t>((idx / S) & 1),
+        mbar_wait(full0 + 8 * static_cast<int>(idx % SE), static_cast<uint32_t>((idx / SE) & 1),
                   p.status, kStatusTimeoutDrain);
       }
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
+      int64_t j = 0;  // running unit index
       int64_t u = u0;
       Seg sg;
       int segi = 0;
@@ -202,28 +253,32 @@ __global__ void __launch_bounds__(Cfg<BN, EXPWIN>::kThreads, 1)
         if (!mbar_wait(acce0 + 8 * buf, ((segi >> 1) & 1) ^ 1, p.status, kStatusTimeoutMma)) break;
         tc_fence_after();
         const uint32_t d = tmem + buf * BN;
-        for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
-          if (!mbar_wait(full0 + 8 * stage, phase, p.status, kStatusTimeoutMma)) {
+        for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++j) {
+          const int e = static_cast<int>(j % SE);
+          if (!mbar_wait(full0 + 8 * e, static_cast<uint32_t>((j / SE) & 1), p.status,
+                         kStatusTimeoutMma)) {
             ok = false;
             break;
           }
-          if (EXPWIN && !mbar_wait(dec0 + 8 * stage, phase, p.status, kStatusTimeoutMma)) {
-            ok = false;
-            break;
+          int a_idx = e;
+          if (EXPWIN) {
+            a_idx = static_cast<int>(j % SA);
+            if (!mbar_wait(decf0 + 8 * a_idx, static_cast<uint32_t>((j / SA) & 1), p.status,
+                           kStatusTimeoutMma)) {
+              ok = false;
+              break;
+            }
           }
           tc_fence_after();
-          const uint32_t a = smem_u32(sA + stage * kTileBytes);
-          const uint32_t b = smem_u32(sB + stage * C::kXBytes);
+          const uint32_t a = smem_u32(sA + a_idx * kTileBytes);
+          const uint32_t b = smem_u32(sB + e * C::kXBytes);
 #pragma unroll
           for (int k = 0; k < kTileK / 16; ++k) {
             tc_mma_f16(d, smem_desc_sw128(a + 32 * k), smem_desc_sw128(b + 32 * k), C::kIdesc,
                        (kb > sg.kb0 || k > 0) ? 1u : 0u);
           }
-          tc_commit(empty0 + 8 * stage);
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1;
-          }
+          tc_commit(empty0 + 8 * e);
+          if (EXPWIN) tc_commit(dece0 + 8 * a_idx);
         }
         if (!ok) break;
         tc_commit(accf0 + 8 * buf);
@@ -236,85 +291,127 @@ __global__ void __launch_bounds__(Cfg<BN, EXPWIN>::kThreads, 1)
     const int r = q * 32 + lane;
     const int etid = threadIdx.x - 64;  // 0..127
     const int64_t first_tile = u0 / p.KB;
+    constexpr int64_t kSlot = static_cast<int64_t>(BN) * kTileRows;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+    int pend[2];
+    int npend = 0;
     int64_t u = u0;
     Seg sg;
     int segi = 0;
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
-    while (next_seg(u, u1, p.KB, sg)) {
+    bool ok = true;
+    while (ok && next_seg(u, u1, p.KB, sg)) {
       const int buf = segi & 1;
-      if (!mbar_wait(accf0 + 8 * buf, (segi >> 1) & 1, p.status, kStatusTimeoutEpilogue)) break;
-      tc_fence_after();
       const int t = sg.tile / p.MT;
       const int mt = sg.tile % p.MT;
       const int mv = min(BN, p.m - mt * BN);
       const bool whole = (sg.kb0 == 0 && sg.kb1 == p.KB);
+      const bool owner = owner_mode && !whole && sg.kb0 == 0;
+      __nv_bfloat16* outp = out + static_cast<size_t>(mt) * BN * p.n_out +
+                            static_cast<size_t>(t) * kTileRows + r;
+      float pre[kOwnerOk ? BN : 1];
+      if constexpr (kOwnerOk) {
+        if (owner) {
+          const TileSplit ts = tile_split(sg.tile, p.KB, U, G);
+          ok = spin_until_ge(p.counters + sg.tile, static_cast<uint32_t>(ts.c_last - ts.c_first),
+                             p.status);
+          owner_presum<BN>(p.ws, ts.c_first, ts.c_last, mv, r, pre);
+        }
+      }
+      if (!mbar_wait(accf0 + 8 * buf, (segi >> 1) & 1, p.status, kStatusTimeoutEpilogue)) break;
+      tc_fence_after();
       const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
-      const size_t out_col = static_cast<size_t>(t) * kTileRows + r;
-      const size_t out_row0 = static_cast<size_t>(mt) * BN;
-      float* slot = p.ws + (2 * static_cast<int64_t>(blockIdx.x) + (sg.tile == first_tile ? 0 : 1)) *
-                               (static_cast<int64_t>(BN) * kTileRows);
-#pragma unroll 1
+      float* slot = p.ws + (owner_mode ? cta : 2 * cta + (sg.tile == first_tile ? 0 : 1)) * kSlot;
+#pragma unroll
       for (int c0 = 0; c0 < BN; c0 += 16) {
-        if (c0 >= mv) break;
-        float v[16];
-        tmem_ld16(taddr + c0, v);
-        tmem_ld_wait();
-        if (whole) {
+        if (c0 < mv) {
+          float v[16];
+          tmem_ld16(taddr + c0, v);
+          tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (c0 + j < mv)
-              out[(out_row0 + c0 + j) * p.n_out + out_col] = __float2bfloat16_rn(v[j]);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (c0 + j < mv) slot[(c0 + j) * kTileRows + r] = v[j];
+          for (int jj = 0; jj < 16; ++jj) {
+            const int j = c0 + jj;
+            if (j < mv) {
+              if (whole) {
+                outp[static_cast<size_t>(j) * p.n_out] = __float2bfloat16_rn(v[jj]);
+              } else if (owner) {
+                if constexpr (kOwnerOk)
+                  outp[static_cast<size_t>(j) * p.n_out] = __float2bfloat16_rn(v[jj] + pre[j]);
+              } else {
+                slot[j * kTileRows + r] = v[jj];
+              }
+            }
+          }
         }
       }
       tc_fence_before();
       mbar_arrive(acce0 + 8 * buf);
       if (!whole) {
-        __threadfence();
-        named_bar_sync(1, 128);
-        const int64_t tu0 = static_cast<int64_t>(sg.tile) * p.KB;
-        const int64_t c_first = part_owner(tu0, U, G);
-        const int64_t c_last = part_owner(tu0 + p.KB - 1, U, G);
-        if (etid == 0) {
-          const uint32_t old = atom_add_acq_rel_gpu(p.counters + sg.tile, 1u);
-          *last_flag = (old == static_cast<uint32_t>(c_last - c_first)) ? 1u : 0u;
-        }
-        named_bar_sync(1, 128);
-        if (*last_flag) {
-          __threadfence();
-          for (int j = 0; j < mv; ++j) {
-            float acc = 0.f;
-            for (int64_t c = c_first; c <= c_last; ++c) {
-              const int64_t s = 2 * c + ((part_begin(c, U, G) / p.KB) == sg.tile ? 0 : 1);
-              acc += __ldcg(p.ws + s * (static_cast<int64_t>(BN) * kTileRows) + j * kTileRows + r);
-            }
-            out[(out_row0 + j) * p.n_out + out_col] = __float2bfloat16_rn(acc);
-          }
+        if (owner) {
+          named_bar_sync(1, 128);
           if (etid == 0) p.counters[sg.tile] = 0u;
+        } else {
+          __threadfence();
+          named_bar_sync(1, 128);
+          if (etid == 0) red_release_gpu_add(p.counters + sg.tile, 1u);
+          if (!owner_mode) pend[npend++] = sg.tile;
         }
-        named_bar_sync(1, 128);
       }
       ++segi;
+    }
+    // distributed mode: reduce this CTA's share of each split tile it touched
+    for (int i = 0; ok && i < npend; ++i) {
+      const int tile = pend[i];
+      const TileSplit ts = tile_split(tile, p.KB, U, G);
+      const int64_t S = ts.c_last - ts.c_first + 1;
+      if (!spin_until_ge(p.counters + tile, static_cast<uint32_t>(S), p.status)) break;
+      const int t = tile / p.MT;
+      const int mt = tile % p.MT;
+      const int mv = min(BN, p.m - mt * BN);
+      const int64_t n = static_cast<int64_t>(kTileRows) * mv;
+      const int64_t me = cta - ts.c_first;
+      const int64_t o0 = me * n / S, o1 = (me + 1) * n / S;
+      const int64_t s_first =
+          2 * ts.c_first + ((part_begin(ts.c_first, U, G) / p.KB) == tile ? 0 : 1);
+      for (int64_t o = o0 + etid; o < o1; o += 128) {
+        const int j = static_cast<int>(o / kTileRows), rr = static_cast<int>(o % kTileRows);
+        const float* base = p.ws + j * kTileRows + rr;
+        float acc = __ldcg(base + s_first * kSlot);
+        for (int64_t c = ts.c_first + 1; c <= ts.c_last; c += 8) {
+          float v[8];
+#pragma unroll
+          for (int a = 0; a < 8; ++a) v[a] = (c + a <= ts.c_last) ? __ldcg(base + 2 * (c + a) * kSlot) : 0.f;
+#pragma unroll
+          for (int a = 0; a < 8; ++a) acc += v[a];
+        }
+        out[(static_cast<size_t>(mt) * BN + j) * p.n_out + static_cast<size_t>(t) * kTileRows + rr] =
+            __float2bfloat16_rn(acc);
+      }
+      named_bar_sync(1, 128);
+      if (etid == 0) {
+        const uint32_t old = atomicAdd(p.counters + tile, 1u);
+        if (old == static_cast<uint32_t>(2 * S - 1)) p.counters[tile] = 0u;
+      }
     }
   } else if (EXPWIN) {
     // -------------------------------------------------------------- decode
     const int dtid = threadIdx.x - 192;  // 0..127
-    int stage = 0;
-    uint32_t phase = 0;
+    int64_t j = 0;
     int64_t u = u0;
     Seg sg;
     bool ok = true;
     while (ok && next_seg(u, u1, p.KB, sg)) {
-      for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
-        if (!mbar_wait(full0 + 8 * stage, phase, p.status, kStatusTimeoutDecode)) {
+      for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++j) {
+        const int e = static_cast<int>(j % SE);
+        const int ai = static_cast<int>(j % (SA > 0 ? SA : 1));
+        if (!mbar_wait(full0 + 8 * e, static_cast<uint32_t>((j / SE) & 1), p.status,
+                       kStatusTimeoutDecode) ||
+            !mbar_wait(dece0 + 8 * ai, static_cast<uint32_t>(((j / (SA > 0 ? SA : 1)) & 1) ^ 1),
+                       p.status, kStatusTimeoutDecode)) {
           ok = false;
           break;
         }
-        const uint8_t* rec = sE + stage * kRecBytes;
-        uint8_t* a = sA + stage * kTileBytes;
+        const uint8_t* rec = sE + e * kRecBytes;
+        uint8_t* a = sA + ai * kTileBytes;
 #pragma unroll 4
         for (int ch = dtid; ch < 1024; ch += 128) {
           const int rr = ch >> 3, cc = ch & 7;
@@ -327,19 +424,15 @@ __global__ void __launch_bounds__(Cfg<BN, EXPWIN>::kThreads, 1)
         const uint32_t* esc = reinterpret_cast<const uint32_t*>(rec + kRecEscOff);
         const uint32_t cnt = esc[0];
         if (dtid < static_cast<int>(cnt) && dtid < kEscCap) {
-          const uint32_t e = esc[1 + dtid];
-          const uint32_t pos = e >> 8;
+          const uint32_t ent = esc[1 + dtid];
+          const uint32_t pos = ent >> 8;
           const int rr = static_cast<int>(pos >> 6), kk = static_cast<int>(pos & 63);
           a[rr * 128 + (((kk >> 3) ^ (rr & 7)) << 4) + (kk & 7) * 2 + 1] =
-              static_cast<uint8_t>(e & 0xFF);
+              static_cast<uint8_t>(ent & 0xFF);
         }
         fence_proxy_async_smem();
         named_bar_sync(2, 128);
-        if (dtid == 0) mbar_arrive(dec0 + 8 * stage);
-        if (++stage == S) {
-          stage = 0;
-          phase ^= 1;
-        }
+        if (dtid == 0) mbar_arrive(decf0 + 8 * ai);
       }
     }
   }
@@ -360,8 +453,17 @@ cudaError_t set_attr() {
 
 template <int BN, bool EXPWIN>
 cudaError_t launch(const CUtensorMap& tmap, const TcParams& p, cudaStream_t s) {
-  tc_kernel<BN, EXPWIN><<<p.G, Cfg<BN, EXPWIN>::kThreads, Cfg<BN, EXPWIN>::kSmem, s>>>(tmap, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.G);
+  cfg.blockDim = dim3(Cfg<BN, EXPWIN>::kThreads);
+  cfg.dynamicSmemBytes = Cfg<BN, EXPWIN>::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tc_kernel<BN, EXPWIN>, tmap, p);
 }
 
 }  // namespace
@@ -373,39 +475,31 @@ bool tc_supported(int BN, bool expwin) {
 
 int tc_threads(bool expwin) { return expwin ? 320 : 192; }
 
+#define PROJ_TC_SWITCH(BN, EXPWIN, ...)              \
+  do {                                                  \
+    if (EXPWIN) {                                       \
+      switch (BN) {                                     \
+        case 16: { constexpr int kB = 16; constexpr bool kE = true; __VA_ARGS__; } \
+        case 32: { constexpr int kB = 32; constexpr bool kE = true; __VA_ARGS__; } \
+      }                                                 \
+    } else {                                            \
+      switch (BN) {                                     \
+        case 16: { constexpr int kB = 16; constexpr bool kE = false; __VA_ARGS__; } \
+        case 32: { constexpr int kB = 32; constexpr bool kE = false; __VA_ARGS__; } \
+        case 64: { constexpr int kB = 64; constexpr bool kE = false; __VA_ARGS__; } \
+        case 128: { constexpr int kB = 128; constexpr bool kE = false; __VA_ARGS__; } \
+        case 256: { constexpr int kB = 256; constexpr bool kE = false; __VA_ARGS__; } \
+      }                                                 \
+    }                                                   \
+  } while (0)
+
 size_t tc_smem_bytes(int BN, bool expwin) {
-  if (expwin) {
-    switch (BN) {
-      case 16: return Cfg<16, true>::kSmem;
-      case 32: return Cfg<32, true>::kSmem;
-    }
-    return 0;
-  }
-  switch (BN) {
-    case 16: return Cfg<16, false>::kSmem;
-    case 32: return Cfg<32, false>::kSmem;
-    case 64: return Cfg<64, false>::kSmem;
-    case 128: return Cfg<128, false>::kSmem;
-    case 256: return Cfg<256, false>::kSmem;
-  }
+  PROJ_TC_SWITCH(BN, expwin, return Cfg<kB, kE>::kSmem);
   return 0;
 }
 
 int tc_stages(int BN, bool expwin) {
-  if (expwin) {
-    switch (BN) {
-      case 16: return Cfg<16, true>::kStages;
-      case 32: return Cfg<32, true>::kStages;
-    }
-    return 0;
-  }
-  switch (BN) {
-    case 16: return Cfg<16, false>::kStages;
-    case 32: return Cfg<32, false>::kStages;
-    case 64: return Cfg<64, false>::kStages;
-    case 128: return Cfg<128, false>::kStages;
-    case 256: return Cfg<256, false>::kStages;
-  }
+  PROJ_TC_SWITCH(BN, expwin, return Cfg<kB, kE>::SE);
   return 0;
 }
 
@@ -423,20 +517,7 @@ cudaError_t tc_init_attributes() {
 
 cudaError_t tc_launch(int BN, bool expwin, const CUtensorMap& tmap, const TcParams& p,
                       cudaStream_t s) {
-  if (expwin) {
-    switch (BN) {
-      case 16: return launch<16, true>(tmap, p, s);
-      case 32: return launch<32, true>(tmap, p, s);
-    }
-    return cudaErrorInvalidValue;
-  }
-  switch (BN) {
-    case 16: return launch<16, false>(tmap, p, s);
-    case 32: return launch<32, false>(tmap, p, s);
-    case 64: return launch<64, false>(tmap, p, s);
-    case 128: return launch<128, false>(tmap, p, s);
-    case 256: return launch<256, false>(tmap, p, s);
-  }
+  PROJ_TC_SWITCH(BN, expwin, return (launch<kB, kE>(tmap, p, s)));
   return cudaErrorInvalidValue;
 }
 

@@ -48,7 +48,7 @@ constexpr int kRtBytes = kRtRows * kRtK * 4;
 struct TcParams {
   const uint8_t* w;     // packed tiles or 12-bit records
   void* out;            // bf16 [m, n_out]
-  float* ws;            // split-K partials: [2 G][BN][128] fp32
+  float* ws;            // split-K partials: [2 G][BN][128] fp32 (slot stride BN * 128)
   uint32_t* counters;   // [MT * T], zero between calls
   uint32_t* status;     // device status word
   int m;
@@ -59,6 +59,7 @@ struct TcParams {
   int MT;               // ceil(m / BN)
   int G;                // CTAs (the split-K partition)
   uint32_t e0x4;        // 12-bit window base replicated into 4 bytes
+  int reduce;           // split-K combine: 0 = owner, 1 = distributed
 };
 
 struct RouterParams {
@@ -72,6 +73,7 @@ struct RouterParams {
   int KB;               // 128
   int MT;               // ceil(m / TM)
   int G;
+  int reduce;           // split-K combine: 0 = owner, 1 = distributed
 };
 
 // Tensor-core path: BN in {16, 32, 64, 128, 256}; expwin12 for BN in {16, 32}.

@@ -5,19 +5,20 @@
 // (muse_bf16_proj guide, ch. 1, §1.1; the router's tighter 0.01 % bound,
 // §1.5, is why its weights keep full fp32 precision).
 //
-// Design: one CTA per SM; the (m-tile, 64-row tile, 64-column block) units
-// are cut into G equal ranges as in the tensor-core path (the router has
-// only 256 rows, so K must be split to fill 152 SMs: muse_bf16_proj
-// notebook, n. 12 "Why the router needs special care").  Thread 0 streams
-// the 16 KB prepacked weight tiles with bulk copies and the bf16 x block with
-// a 2-D TMA load into an 8-stage ring; all 256 threads widen x to fp32 in a
-// swizzled shared buffer and run a 4-row x 4-token register tile of FMAs per
-// thread.  For small token tiles the threads also split each 64-column block
-// into k-groups (KS = 64 / TM), reduced through shared memory in fixed order
-// at the end of a segment.  Shared tiles finish through the same fixed-order
-// last-arriver reduction as the tensor-core path.
+// Design: one CTA per SM (cooperative launch); the (m-tile, 64-row tile,
+// 64-column block) units are cut into G equal ranges as in the tensor-core
+// path (the router has only 256 rows, so K must be split to fill 152 SMs:
+// muse_bf16_proj notebook, n. 12 "Why the router needs special care").
+// Thread 0 streams the 16 KB prepacked weight tiles with bulk copies and the
+// bf16 x block with a 2-D TMA load into an 8-stage ring; all 256 threads
+// widen x to fp32 in a swizzled shared buffer and run a 4-row x 4-token
+// register tile of FMAs per thread.  For small token tiles the threads also
+// split each 64-column block into k-groups (KS = 64 / TM), reduced through
+// shared memory in fixed order at the end of a segment.  Shared tiles are
+// combined in fixed CTA order (splitk.cuh, owner or distributed mode).
 #include "kernels.h"
 #include "ptx.cuh"
+#include "splitk.cuh"
 
 namespace proj {
 namespace {
@@ -35,7 +36,7 @@ struct RCfg {
   static constexpr int kGroupThreads = kThreads / KS; // = 4 TM
   static constexpr int kKPerGroup = 64 / KS;          // columns per k-group per stage
   static constexpr size_t kSmem =
-      1024 + kStages * kStageBytes + kXfBytes + kRedFloats * 4 + 2 * kStages * 8 + 16;
+      1024 + kStages * kStageBytes + kXfBytes + kRedFloats * 4 + kStages * 8 + 16;
   static_assert(kSmem <= 232448, "shared memory budget");
 };
 
@@ -43,6 +44,7 @@ template <int TM>
 __global__ void __launch_bounds__(kThreads, 1)
     router_kernel(const __grid_constant__ CUtensorMap tmap_x, const RouterParams p) {
   using C = RCfg<TM>;
+  constexpr int64_t kSlot = 64 * TM;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -51,7 +53,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* sXf = reinterpret_cast<float*>(sXb + kStages * C::kXbBytes);
   float* sRed = sXf + TM * 64;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sRed + kRedFloats);
-  volatile uint32_t* last_flag = reinterpret_cast<uint32_t*>(bars + kStages);
   const uint32_t full0 = smem_u32(bars);
 
   const int tid = threadIdx.x;
@@ -61,10 +62,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tt = g >> 4;        // tokens tt + (TM / 4) j
   const int64_t G = p.G;
   const int64_t U = static_cast<int64_t>(p.MT) * p.T * p.KB;
-  const int64_t u0 = part_begin(blockIdx.x, U, G);
-  const int64_t u1 = part_begin(blockIdx.x + 1, U, G);
+  const int64_t cta = blockIdx.x;
+  const int64_t u0 = part_begin(cta, U, G);
+  const int64_t u1 = part_begin(cta + 1, U, G);
   const int64_t nunits = u1 - u0;
   const int64_t first_tile = u0 / p.KB;
+  const bool owner_mode = (p.reduce == 0);
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(full0 + 8 * s, 1);
@@ -99,6 +102,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   bool ok = true;
   int seg_kb0 = 0;
+  int pend[2];
+  int npend = 0;
   for (int64_t j = 0; j < nunits; ++j) {
     const int64_t u = u0 + j;
     const int tile = static_cast<int>(u / p.KB);
@@ -168,6 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = tile / p.MT, mt = tile % p.MT;
     const int mv = min(TM, p.m - mt * TM);
     const bool whole = (seg_kb0 == 0 && kb == p.KB - 1);
+    const bool owner = owner_mode && !whole && seg_kb0 == 0;
     // k-group partials -> sRed[kg][row][token], then fixed-order sum over kg.
 #pragma unroll
     for (int a = 0; a < 4; ++a)
@@ -177,46 +183,82 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc[a][b] = 0.f;
       }
     __syncthreads();
-    float* slot = p.ws + (2 * static_cast<int64_t>(blockIdx.x) + (tile == first_tile ? 0 : 1)) *
-                             (64 * TM);
+    TileSplit ts{0, 0};
+    if (owner) {
+      ts = tile_split(tile, p.KB, U, G);
+      if (!spin_until_ge(p.counters + tile, static_cast<uint32_t>(ts.c_last - ts.c_first),
+                         p.status))
+        ok = false;
+    }
+    float* slot = p.ws + (owner_mode ? cta : 2 * cta + (tile == first_tile ? 0 : 1)) * kSlot;
     for (int o = tid; o < 64 * TM; o += kThreads) {
-      const int r = o / TM, i = o % TM;
+      const int r = o % 64, i = o / 64;
+      if (i >= mv) continue;
       float v = 0.f;
       for (int gk = 0; gk < C::KS; ++gk) v += sRed[(gk * 64 + r) * TM + i];
-      if (i < mv) {
-        if (whole) {
-          p.out[(static_cast<size_t>(mt) * TM + i) * 256 + t * 64 + r] = v;
-        } else {
-          slot[i * 64 + r] = v;
+      float* dst = p.out + (static_cast<size_t>(mt) * TM + i) * 256 + t * 64 + r;
+      if (whole) {
+        *dst = v;
+      } else if (owner) {
+        const float* base = p.ws + i * 64 + r;
+        float pre = 0.f;
+        for (int64_t c = ts.c_first + 1; c <= ts.c_last; c += 8) {
+          float w8[8];
+#pragma unroll
+          for (int a = 0; a < 8; ++a) w8[a] = (c + a <= ts.c_last) ? __ldcg(base + (c + a) * kSlot) : 0.f;
+#pragma unroll
+          for (int a = 0; a < 8; ++a) pre += w8[a];
         }
+        *dst = v + pre;
+      } else {
+        slot[i * 64 + r] = v;
       }
     }
     if (!whole) {
-      __threadfence();
-      __syncthreads();
-      const int64_t tu0 = static_cast<int64_t>(tile) * p.KB;
-      const int64_t c_first = part_owner(tu0, U, G);
-      const int64_t c_last = part_owner(tu0 + p.KB - 1, U, G);
-      if (tid == 0) {
-        const uint32_t old = atom_add_acq_rel_gpu(p.counters + tile, 1u);
-        *last_flag = (old == static_cast<uint32_t>(c_last - c_first)) ? 1u : 0u;
-      }
-      __syncthreads();
-      if (*last_flag) {
-        __threadfence();
-        for (int o = tid; o < 64 * mv; o += kThreads) {
-          const int i = o / 64, r = o % 64;
-          float v = 0.f;
-          for (int64_t c = c_first; c <= c_last; ++c) {
-            const int64_t sl = 2 * c + ((part_begin(c, U, G) / p.KB) == tile ? 0 : 1);
-            v += __ldcg(p.ws + sl * (64 * TM) + i * 64 + r);
-          }
-          p.out[(static_cast<size_t>(mt) * TM + i) * 256 + t * 64 + r] = v;
-        }
+      if (owner) {
+        __syncthreads();
         if (tid == 0) p.counters[tile] = 0u;
+      } else {
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) red_release_gpu_add(p.counters + tile, 1u);
+        if (!owner_mode) pend[npend++] = tile;
       }
     }
-    __syncthreads();  // sRed and last_flag reuse
+    __syncthreads();  // sRed reuse
+  }
+
+  // distributed mode: this CTA's share of each split tile it touched
+  for (int i = 0; ok && i < npend; ++i) {
+    const int tile = pend[i];
+    const TileSplit ts = tile_split(tile, p.KB, U, G);
+    const int64_t S = ts.c_last - ts.c_first + 1;
+    if (!spin_until_ge(p.counters + tile, static_cast<uint32_t>(S), p.status)) break;
+    const int t = tile / p.MT, mt = tile % p.MT;
+    const int mv = min(TM, p.m - mt * TM);
+    const int64_t n = 64 * static_cast<int64_t>(mv);
+    const int64_t me = cta - ts.c_first;
+    const int64_t o0 = me * n / S, o1 = (me + 1) * n / S;
+    const int64_t s_first =
+        2 * ts.c_first + ((part_begin(ts.c_first, U, G) / p.KB) == tile ? 0 : 1);
+    for (int64_t o = o0 + tid; o < o1; o += kThreads) {
+      const int ii = static_cast<int>(o / 64), r = static_cast<int>(o % 64);
+      const float* base = p.ws + ii * 64 + r;
+      float v = __ldcg(base + s_first * kSlot);
+      for (int64_t c = ts.c_first + 1; c <= ts.c_last; c += 8) {
+        float w8[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) w8[a] = (c + a <= ts.c_last) ? __ldcg(base + 2 * (c + a) * kSlot) : 0.f;
+#pragma unroll
+        for (int a = 0; a < 8; ++a) v += w8[a];
+      }
+      p.out[(static_cast<size_t>(mt) * TM + ii) * 256 + t * 64 + r] = v;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      const uint32_t old = atomicAdd(p.counters + tile, 1u);
+      if (old == static_cast<uint32_t>(2 * S - 1)) p.counters[tile] = 0u;
+    }
   }
 
   // Drain copies still in flight (only after an abort): the last kStages
@@ -237,8 +279,17 @@ cudaError_t set_attr() {
 
 template <int TM>
 cudaError_t launch(const CUtensorMap& tmap, const RouterParams& p, cudaStream_t s) {
-  router_kernel<TM><<<p.G, kThreads, RCfg<TM>::kSmem, s>>>(tmap, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.G);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = RCfg<TM>::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, router_kernel<TM>, tmap, p);
 }
 
 }  // namespace

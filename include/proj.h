@@ -93,11 +93,20 @@ enum proj_variant {
     PROJ_VARIANT_EXPWIN12 = 2   /* 12-bit weights (handle must hold them) */
 };
 
+/* How CTAs sharing a tile combine their fp32 partials (both deterministic:
+ * the summation order depends only on the partition). */
+enum proj_reduce {
+    PROJ_REDUCE_AUTO = 0,        /* the dispatch table's choice */
+    PROJ_REDUCE_OWNER = 1,       /* the CTA holding the tile's first k-range sums
+                                    the others' partials (small m) */
+    PROJ_REDUCE_DISTRIBUTED = 2  /* every contributor sums 1/S of the tile */
+};
+
 typedef struct proj_run_opts {
     int variant;    /* enum proj_variant */
-    int grid;       /* CTAs of the split-K partition; 0 = dispatch table */
-    int stages;     /* reserved, 0 */
-    int reserved;
+    int grid;       /* CTAs of the split-K partition (1 .. SMs); 0 = dispatch table */
+    int reduce;     /* enum proj_reduce; owner mode needs m <= 32 on bf16 layers */
+    int reserved;   /* 0 */
 } proj_run_opts;
 
 typedef struct proj_info_t {

@@ -114,15 +114,31 @@ def test_parity_all_shapes(dev, layer, m):
 
 
 @pytest.mark.parametrize("layer,m", [("o", 1), ("o", 33), ("router", 1), ("router", 33),
-                                     ("unpooler", 8), ("qkv_gate", 130)])
+                                     ("unpooler", 8), ("qkv_gate", 130), ("pooler", 16),
+                                     ("router", 256)])
 def test_split_partitions_and_determinism(dev, layer, m):
+    """Every partition and both split-K combine modes meet the contract and
+    are bitwise reproducible."""
     h, W, _ = prepared(layer, 0)
     sms = B.proj_num_sms()
-    for grid in (1, 7, 64, sms - 1, sms):
-        a = check_case(layer, 0, True, m, h=h, W=W, grid=grid)
-        b = check_case(layer, 0, True, m, h=h, W=W, grid=grid)
-        assert np.array_equal(a, b), (layer, m, grid)
+    modes = [B.PROJ_REDUCE_DISTRIBUTED]
+    if layer == "router" or m <= 32:
+        modes.append(B.PROJ_REDUCE_OWNER)
+    for reduce in modes:
+        for grid in (1, 7, 64, sms - 1, sms):
+            a = check_case(layer, 0, True, m, h=h, W=W, grid=grid, reduce=reduce)
+            b = check_case(layer, 0, True, m, h=h, W=W, grid=grid, reduce=reduce)
+            assert np.array_equal(a, b), (layer, m, grid, reduce)
     assert B.proj_device_status(h) == 0
+
+
+def test_owner_mode_rejected_for_wide_token_tiles(dev):
+    h, W, _ = prepared("pooler", 0)
+    x = torch.zeros((64, 8192), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros((64, 4096), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(B.ProjError) as e:
+        B.proj_run_ex(h, x, 64, out, reduce=B.PROJ_REDUCE_OWNER)
+    assert e.value.status == B.PROJ_EUNSUPPORTED
 
 
 @pytest.mark.parametrize("layer,m", [("qkv_gate", 16), ("router", 1), ("pooler", 256),
@@ -188,10 +204,13 @@ def test_expwin12_lossless_and_bit_identical(dev, layer):
         for m in (1, 8, 16, 32):
             act = wl.make_activations(layer, m, seed + 5, outliers=True)
             x = to_dev_x(act.x_bits)
-            for grid in (0, 37):
-                a = run(layer, h, x, m, variant=B.PROJ_VARIANT_DENSE, grid=grid)
-                b = run(layer, h, x, m, variant=B.PROJ_VARIANT_EXPWIN12, grid=grid)
-                assert torch.equal(a.view(torch.int16), b.view(torch.int16)), (layer, seed, m, grid)
+            for grid, reduce in ((0, 0), (37, B.PROJ_REDUCE_OWNER),
+                                 (0, B.PROJ_REDUCE_DISTRIBUTED)):
+                a = run(layer, h, x, m, variant=B.PROJ_VARIANT_DENSE, grid=grid, reduce=reduce)
+                b = run(layer, h, x, m, variant=B.PROJ_VARIANT_EXPWIN12, grid=grid,
+                        reduce=reduce)
+                assert torch.equal(a.view(torch.int16), b.view(torch.int16)), \
+                    (layer, seed, m, grid, reduce)
             check_case(layer, seed, True, m, h=h, W=W, variant=B.PROJ_VARIANT_EXPWIN12)
         # one-hot rows on escaped columns reproduce the column exactly
         K = W.shape[1]
