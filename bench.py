@@ -163,9 +163,10 @@ def _external_events_supported(torch) -> bool:
 
 
 class LoadGraph:
-    """The five layers of one load captured in one CUDA graph, with timing
-    events recorded between the kernels when torch supports external events
-    (otherwise one graph per layer, timed back to back)."""
+    """The five layers of one load captured in one CUDA graph.  A second graph
+    with timing events recorded between the kernels (when torch supports
+    external events) gives the per-layer breakdown; the plain graph, with no
+    event nodes inside, gives the load time."""
 
     def __init__(self, B, torch, shapes, stream):
         self.shapes = shapes
@@ -175,12 +176,16 @@ class LoadGraph:
                 for S in shapes:
                     B.proj_run(S.h, S.x, S.m, S.out, stream)
         torch.cuda.synchronize()
+        self.plain = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.plain, stream=stream):
+            for S in shapes:
+                B.proj_run(S.h, S.x, S.m, S.out, stream)
         self.inner = _external_events_supported(torch)
         n = len(shapes)
         if self.inner:
             self.ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n + 1)]
-            self.graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(self.graph, stream=stream):
+            self.evgraph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.evgraph, stream=stream):
                 self.ev[0].record(stream)
                 for i, S in enumerate(shapes):
                     B.proj_run(S.h, S.x, S.m, S.out, stream)
@@ -194,19 +199,21 @@ class LoadGraph:
                 with torch.cuda.graph(g, stream=stream):
                     B.proj_run(S.h, S.x, S.m, S.out, stream)
                 self.graphs.append(g)
-            self.graph = None
         torch.cuda.synchronize()
 
-    def step(self, B, torch, flush, sink):
-        """flush (untimed) -> events -> replay; returns (outer us, per-layer us)."""
+    def step(self, B, torch, flush, sink, breakdown=False):
+        """flush (untimed) -> event -> replay -> event.  Returns the load's
+        microseconds, and with breakdown=True the per-layer microseconds."""
         s = self.stream
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(s):
             B.proj_read_floor(flush, flush.numel() * 4, sink, 0, 0, s)
             a.record(s)
-            if self.graph is not None:
-                self.graph.replay()
+            if not breakdown:
+                self.plain.replay()
+            elif self.inner:
+                self.evgraph.replay()
             else:
                 self.ev[0].record(s)
                 for i, g in enumerate(self.graphs):
@@ -214,17 +221,19 @@ class LoadGraph:
                     self.ev[i + 1].record(s)
             b.record(s)
         s.synchronize()
-        per = [self.ev[i].elapsed_time(self.ev[i + 1]) * 1e3 for i in range(len(self.shapes))]
+        per = None
+        if breakdown:
+            per = [self.ev[i].elapsed_time(self.ev[i + 1]) * 1e3 for i in range(len(self.shapes))]
         return a.elapsed_time(b) * 1e3, per
 
 
-def time_load(B, torch, lg, flush, sink, steps):
+def time_load(B, torch, lg, flush, sink, steps, breakdown=False):
     outer, per = [], []
     for _ in range(steps):
-        o, p = lg.step(B, torch, flush, sink)
+        o, p = lg.step(B, torch, flush, sink, breakdown)
         outer.append(o)
         per.append(p)
-    return np.array(outer), np.array(per)
+    return np.array(outer), (np.array(per) if breakdown else None)
 
 
 def time_read_floor(B, torch, nbytes_list, flush, sink, stream, reps, mode=0):
@@ -398,12 +407,14 @@ def run_ours(args):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
-    outer, per = time_load(B, torch, lg, flush, sink, args.steps)
+    outer, _ = time_load(B, torch, lg, flush, sink, args.steps)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
+    # per-layer breakdown (graph with event nodes between the kernels)
+    _, per = time_load(B, torch, lg, flush, sink, args.steps, breakdown=True)
 
     mean_us = float(outer.mean())
     if world > 1:
@@ -441,15 +452,15 @@ def run_ours(args):
             "m": m,
             "l2": f"flushed before every step by a {4 * l2 >> 20} MiB read (4x L2), "
                   "outside the events",
-            "timing": "one CUDA graph per load (5 kernels); value = event pair around the "
-                      "replay (includes one graph launch); per-layer = event nodes inside "
-                      "the graph" if lg.inner else
-                      "one CUDA graph per layer replayed back to back; value includes 5 "
-                      "graph launches",
+            "timing": "one CUDA graph per load (5 kernels); value = mean of an event pair "
+                      "around each replay (includes one graph launch); per-layer = a second "
+                      "pass with event nodes between the kernels" + (
+                          "" if lg.inner else " (here: per-layer graphs)"),
             "weights": "dense bf16" if args.dense else "12-bit exponent-window for bf16 "
                                                        "layers at m<=16, dense otherwise",
             "parallelism": f"replicas x{world}",
         },
+        "median_us": round(float(np.median(outer)), 3),
         "kernel_sum_us": round(float(layer_us.sum()), 3),
         "per_layer_us": {S.spec.name: round(float(u), 3) for S, u in zip(lg.shapes, layer_us)},
         "kernels": {S.spec.name: S.desc for S in lg.shapes},
@@ -474,7 +485,9 @@ def run_ours(args):
     if args.all_loads and rank == 0:
         loads_out = {}
         for ld in loads:
-            o, pl = time_load(B, torch, graphs[ld], flush, sink, max(20, min(args.steps, 100)))
+            nrep = max(20, min(args.steps, 100))
+            o, _ = time_load(B, torch, graphs[ld], flush, sink, nrep)
+            _, pl = time_load(B, torch, graphs[ld], flush, sink, nrep, breakdown=True)
             loads_out[ld] = {"us": round(float(o.mean()), 2),
                              "kernel_sum_us": round(float(pl.mean(axis=0).sum()), 2),
                              "per_layer_us": {S.spec.name: round(float(u), 2) for S, u in

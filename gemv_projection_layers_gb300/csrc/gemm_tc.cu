@@ -262,8 +262,9 @@ __global__ void __launch_bounds__(Cfg<BN, EXPWIN>::kThreads, 1)
           }
           int a_idx = e;
           if (EXPWIN) {
-            a_idx = static_cast<int>(j % SA);
-            if (!mbar_wait(decf0 + 8 * a_idx, static_cast<uint32_t>((j / SA) & 1), p.status,
+            constexpr int SAd = SA > 0 ? SA : 1;
+            a_idx = static_cast<int>(j % SAd);
+            if (!mbar_wait(decf0 + 8 * a_idx, static_cast<uint32_t>((j / SAd) & 1), p.status,
                            kStatusTimeoutMma)) {
               ok = false;
               break;
@@ -312,8 +313,8 @@ __global__ void __launch_bounds__(Cfg<BN, EXPWIN>::kThreads, 1)
       if constexpr (kOwnerOk) {
         if (owner) {
           const TileSplit ts = tile_split(sg.tile, p.KB, U, G);
-          ok = spin_until_ge(p.counters + sg.tile, static_cast<uint32_t>(ts.c_last - ts.c_first),
-                             p.status);
+          ok = spin_until_ge(p.counters + sg.tile,
+                             static_cast<uint32_t>(ts.c_last - ts.c_first) * 128u, p.status);
           owner_presum<BN>(p.ws, ts.c_first, ts.c_last, mv, r, pre);
         }
       }
@@ -350,89 +351,127 @@ __global__ void __launch_bounds__(Cfg<BN, EXPWIN>::kThreads, 1)
           named_bar_sync(1, 128);
           if (etid == 0) p.counters[sg.tile] = 0u;
         } else {
-          __threadfence();
-          named_bar_sync(1, 128);
-          if (etid == 0) red_release_gpu_add(p.counters + sg.tile, 1u);
+          // Each thread releases its own partial stores; the reader waits
+          // for 128 arrivals per contributor.
+          red_release_gpu_add(p.counters + sg.tile, 1u);
           if (!owner_mode) pend[npend++] = sg.tile;
         }
       }
       ++segi;
     }
-    // distributed mode: reduce this CTA's share of each split tile it touched
+    // distributed mode: reduce this CTA's share of each split tile it touched.
+    // Shares are runs of 4 consecutive rows (one float4 of a partial slot);
+    // each thread keeps 4 of them and 4 contributors' loads in flight.
     for (int i = 0; ok && i < npend; ++i) {
       const int tile = pend[i];
       const TileSplit ts = tile_split(tile, p.KB, U, G);
       const int64_t S = ts.c_last - ts.c_first + 1;
-      if (!spin_until_ge(p.counters + tile, static_cast<uint32_t>(S), p.status)) break;
+      if (!spin_until_ge(p.counters + tile, static_cast<uint32_t>(S) * 128u, p.status)) break;
       const int t = tile / p.MT;
       const int mt = tile % p.MT;
       const int mv = min(BN, p.m - mt * BN);
-      const int64_t n = static_cast<int64_t>(kTileRows) * mv;
+      const int64_t nq = static_cast<int64_t>(kTileRows / 4) * mv;  // float4 quads
       const int64_t me = cta - ts.c_first;
-      const int64_t o0 = me * n / S, o1 = (me + 1) * n / S;
+      const int64_t q0 = me * nq / S, q1 = (me + 1) * nq / S;
       const int64_t s_first =
           2 * ts.c_first + ((part_begin(ts.c_first, U, G) / p.KB) == tile ? 0 : 1);
-      for (int64_t o = o0 + etid; o < o1; o += 128) {
-        const int j = static_cast<int>(o / kTileRows), rr = static_cast<int>(o % kTileRows);
-        const float* base = p.ws + j * kTileRows + rr;
-        float acc = __ldcg(base + s_first * kSlot);
-        for (int64_t c = ts.c_first + 1; c <= ts.c_last; c += 8) {
-          float v[8];
+      const float4* ws4 = reinterpret_cast<const float4*>(p.ws);
+      constexpr int64_t kSlot4 = kSlot / 4;
+      for (int64_t qb = q0 + etid; qb < q1; qb += 128 * 4) {
+        float4 acc[4];
 #pragma unroll
-          for (int a = 0; a < 8; ++a) v[a] = (c + a <= ts.c_last) ? __ldcg(base + 2 * (c + a) * kSlot) : 0.f;
-#pragma unroll
-          for (int a = 0; a < 8; ++a) acc += v[a];
+        for (int b = 0; b < 4; ++b) {
+          const int64_t q = qb + 128 * b;
+          acc[b] = q < q1 ? __ldcg(ws4 + s_first * kSlot4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        out[(static_cast<size_t>(mt) * BN + j) * p.n_out + static_cast<size_t>(t) * kTileRows + rr] =
-            __float2bfloat16_rn(acc);
+        for (int64_t c = ts.c_first + 1; c <= ts.c_last; c += 4) {
+          float4 v[4][4];
+#pragma unroll
+          for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+              const int64_t q = qb + 128 * b;
+              v[a][b] = (c + a <= ts.c_last && q < q1) ? __ldcg(ws4 + 2 * (c + a) * kSlot4 + q)
+                                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+          for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+              acc[b].x += v[a][b].x;
+              acc[b].y += v[a][b].y;
+              acc[b].z += v[a][b].z;
+              acc[b].w += v[a][b].w;
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const int64_t q = qb + 128 * b;
+          if (q < q1) {
+            const int j = static_cast<int>(q / (kTileRows / 4));
+            const int rr = static_cast<int>(q % (kTileRows / 4)) * 4;
+            __nv_bfloat16* o = out + (static_cast<size_t>(mt) * BN + j) * p.n_out +
+                               static_cast<size_t>(t) * kTileRows + rr;
+            __nv_bfloat162 lo2, hi2;
+            lo2.x = __float2bfloat16_rn(acc[b].x);
+            lo2.y = __float2bfloat16_rn(acc[b].y);
+            hi2.x = __float2bfloat16_rn(acc[b].z);
+            hi2.y = __float2bfloat16_rn(acc[b].w);
+            *reinterpret_cast<__nv_bfloat162*>(o) = lo2;
+            *reinterpret_cast<__nv_bfloat162*>(o + 2) = hi2;
+          }
+        }
       }
       named_bar_sync(1, 128);
       if (etid == 0) {
-        const uint32_t old = atomicAdd(p.counters + tile, 1u);
-        if (old == static_cast<uint32_t>(2 * S - 1)) p.counters[tile] = 0u;
+        const uint32_t old = atomicAdd(p.counters + tile, 128u);
+        if (old == static_cast<uint32_t>(2 * S - 1) * 128u) p.counters[tile] = 0u;
       }
     }
   } else if (EXPWIN) {
     // -------------------------------------------------------------- decode
-    const int dtid = threadIdx.x - 192;  // 0..127
+    // Decode warp d (0..3) owns every unit j with j % 4 == d and the decoded
+    // buffer d, so stages decode in parallel with warp-local syncs only.
+    constexpr int SAd = SA > 0 ? SA : 1;
+    const int d = warp - 6;
     int64_t j = 0;
     int64_t u = u0;
     Seg sg;
     bool ok = true;
     while (ok && next_seg(u, u1, p.KB, sg)) {
       for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++j) {
+        if (static_cast<int>(j % SAd) != d) continue;
         const int e = static_cast<int>(j % SE);
-        const int ai = static_cast<int>(j % (SA > 0 ? SA : 1));
         if (!mbar_wait(full0 + 8 * e, static_cast<uint32_t>((j / SE) & 1), p.status,
                        kStatusTimeoutDecode) ||
-            !mbar_wait(dece0 + 8 * ai, static_cast<uint32_t>(((j / (SA > 0 ? SA : 1)) & 1) ^ 1),
-                       p.status, kStatusTimeoutDecode)) {
+            !mbar_wait(dece0 + 8 * d, static_cast<uint32_t>(((j / SAd) & 1) ^ 1), p.status,
+                       kStatusTimeoutDecode)) {
           ok = false;
           break;
         }
         const uint8_t* rec = sE + e * kRecBytes;
-        uint8_t* a = sA + ai * kTileBytes;
-#pragma unroll 4
-        for (int ch = dtid; ch < 1024; ch += 128) {
+        uint8_t* a = sA + d * kTileBytes;
+#pragma unroll 8
+        for (int ch = lane; ch < 1024; ch += 32) {
           const int rr = ch >> 3, cc = ch & 7;
           const uint2 lo = *reinterpret_cast<const uint2*>(rec + kRecLowOff + ch * 8);
           const uint32_t nb = *reinterpret_cast<const uint32_t*>(rec + kRecNibOff + ch * 4);
           *reinterpret_cast<uint4*>(a + rr * 128 + ((cc ^ (rr & 7)) << 4)) =
               expwin_decode8(lo, nb, p.e0x4);
         }
-        named_bar_sync(2, 128);
+        __syncwarp();
         const uint32_t* esc = reinterpret_cast<const uint32_t*>(rec + kRecEscOff);
         const uint32_t cnt = esc[0];
-        if (dtid < static_cast<int>(cnt) && dtid < kEscCap) {
-          const uint32_t ent = esc[1 + dtid];
+        if (lane < static_cast<int>(cnt) && lane < kEscCap) {
+          const uint32_t ent = esc[1 + lane];
           const uint32_t pos = ent >> 8;
           const int rr = static_cast<int>(pos >> 6), kk = static_cast<int>(pos & 63);
           a[rr * 128 + (((kk >> 3) ^ (rr & 7)) << 4) + (kk & 7) * 2 + 1] =
               static_cast<uint8_t>(ent & 0xFF);
         }
         fence_proxy_async_smem();
-        named_bar_sync(2, 128);
-        if (dtid == 0) mbar_arrive(decf0 + 8 * ai);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(decf0 + 8 * d);
       }
     }
   }

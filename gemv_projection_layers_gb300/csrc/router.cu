@@ -186,8 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     TileSplit ts{0, 0};
     if (owner) {
       ts = tile_split(tile, p.KB, U, G);
-      if (!spin_until_ge(p.counters + tile, static_cast<uint32_t>(ts.c_last - ts.c_first),
-                         p.status))
+      if (!spin_until_ge(p.counters + tile,
+                         static_cast<uint32_t>(ts.c_last - ts.c_first) * kThreads, p.status))
         ok = false;
     }
     float* slot = p.ws + (owner_mode ? cta : 2 * cta + (tile == first_tile ? 0 : 1)) * kSlot;
@@ -219,45 +219,71 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
         if (tid == 0) p.counters[tile] = 0u;
       } else {
-        __threadfence();
-        __syncthreads();
-        if (tid == 0) red_release_gpu_add(p.counters + tile, 1u);
+        // each thread releases its own partial stores (kThreads arrivals per CTA)
+        red_release_gpu_add(p.counters + tile, 1u);
         if (!owner_mode) pend[npend++] = tile;
       }
     }
     __syncthreads();  // sRed reuse
   }
 
-  // distributed mode: this CTA's share of each split tile it touched
+  // distributed mode: this CTA's share of each split tile it touched, as
+  // float4 runs of 4 rows, 4 runs and 4 contributors in flight per thread.
   for (int i = 0; ok && i < npend; ++i) {
     const int tile = pend[i];
     const TileSplit ts = tile_split(tile, p.KB, U, G);
     const int64_t S = ts.c_last - ts.c_first + 1;
-    if (!spin_until_ge(p.counters + tile, static_cast<uint32_t>(S), p.status)) break;
+    if (!spin_until_ge(p.counters + tile, static_cast<uint32_t>(S) * kThreads, p.status)) break;
     const int t = tile / p.MT, mt = tile % p.MT;
     const int mv = min(TM, p.m - mt * TM);
-    const int64_t n = 64 * static_cast<int64_t>(mv);
+    const int64_t nq = 16 * static_cast<int64_t>(mv);
     const int64_t me = cta - ts.c_first;
-    const int64_t o0 = me * n / S, o1 = (me + 1) * n / S;
+    const int64_t q0 = me * nq / S, q1 = (me + 1) * nq / S;
     const int64_t s_first =
         2 * ts.c_first + ((part_begin(ts.c_first, U, G) / p.KB) == tile ? 0 : 1);
-    for (int64_t o = o0 + tid; o < o1; o += kThreads) {
-      const int ii = static_cast<int>(o / 64), r = static_cast<int>(o % 64);
-      const float* base = p.ws + ii * 64 + r;
-      float v = __ldcg(base + s_first * kSlot);
-      for (int64_t c = ts.c_first + 1; c <= ts.c_last; c += 8) {
-        float w8[8];
+    const float4* ws4 = reinterpret_cast<const float4*>(p.ws);
+    constexpr int64_t kSlot4 = kSlot / 4;
+    for (int64_t qb = q0 + tid; qb < q1; qb += kThreads * 4) {
+      float4 acc[4];
 #pragma unroll
-        for (int a = 0; a < 8; ++a) w8[a] = (c + a <= ts.c_last) ? __ldcg(base + 2 * (c + a) * kSlot) : 0.f;
-#pragma unroll
-        for (int a = 0; a < 8; ++a) v += w8[a];
+      for (int b = 0; b < 4; ++b) {
+        const int64_t q = qb + kThreads * b;
+        acc[b] = q < q1 ? __ldcg(ws4 + s_first * kSlot4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      p.out[(static_cast<size_t>(mt) * TM + ii) * 256 + t * 64 + r] = v;
+      for (int64_t c = ts.c_first + 1; c <= ts.c_last; c += 4) {
+        float4 v[4][4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            const int64_t q = qb + kThreads * b;
+            v[a][b] = (c + a <= ts.c_last && q < q1) ? __ldcg(ws4 + 2 * (c + a) * kSlot4 + q)
+                                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            acc[b].x += v[a][b].x;
+            acc[b].y += v[a][b].y;
+            acc[b].z += v[a][b].z;
+            acc[b].w += v[a][b].w;
+          }
+      }
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int64_t q = qb + kThreads * b;
+        if (q < q1) {
+          const int ii = static_cast<int>(q / 16), r = static_cast<int>(q % 16) * 4;
+          *reinterpret_cast<float4*>(p.out + (static_cast<size_t>(mt) * TM + ii) * 256 + t * 64 + r) =
+              acc[b];
+        }
+      }
     }
     __syncthreads();
     if (tid == 0) {
-      const uint32_t old = atomicAdd(p.counters + tile, 1u);
-      if (old == static_cast<uint32_t>(2 * S - 1)) p.counters[tile] = 0u;
+      const uint32_t old = atomicAdd(p.counters + tile, static_cast<uint32_t>(kThreads));
+      if (old == static_cast<uint32_t>(2 * S - 1) * kThreads) p.counters[tile] = 0u;
     }
   }
 
