@@ -25,6 +25,7 @@ PROJ_ENCODE_EXPWIN12 = 1
  PROJ_EDEVICE) = range(7)
 PROJ_VARIANT_AUTO, PROJ_VARIANT_DENSE, PROJ_VARIANT_EXPWIN12 = range(3)
 PROJ_REDUCE_AUTO, PROJ_REDUCE_OWNER, PROJ_REDUCE_DISTRIBUTED = range(3)
+PROJ_KERNEL_AUTO, PROJ_KERNEL_GEMV, PROJ_KERNEL_TILE = range(3)
 
 LAYER_INDEX = {"qkv_gate": 0, "o": 1, "pooler": 2, "unpooler": 3, "router": 4}
 
@@ -42,7 +43,7 @@ class NativeLibraryMissing(ImportError):
 
 class proj_run_opts(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int), ("grid", ctypes.c_int),
-                ("reduce", ctypes.c_int), ("reserved", ctypes.c_int)]
+                ("reduce", ctypes.c_int), ("kernel", ctypes.c_int)]
 
 
 class proj_info_t(ctypes.Structure):
@@ -164,8 +165,9 @@ def proj_run(h: int, x, m: int, out, stream=None) -> None:
 
 
 def proj_run_ex(h: int, x, m: int, out, stream=None, variant: int = PROJ_VARIANT_AUTO,
-                grid: int = 0, reduce: int = PROJ_REDUCE_AUTO) -> None:
-    opts = proj_run_opts(int(variant), int(grid), int(reduce), 0)
+                grid: int = 0, reduce: int = PROJ_REDUCE_AUTO,
+                kernel: int = PROJ_KERNEL_AUTO) -> None:
+    opts = proj_run_opts(int(variant), int(grid), int(reduce), int(kernel))
     _check(load().proj_run_ex(h, _addr(x), int(m), _addr(out), _stream(stream),
                               ctypes.byref(opts)), "proj_run_ex")
 

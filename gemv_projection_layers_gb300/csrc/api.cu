@@ -117,7 +117,12 @@ constexpr int64_t kExpwinMaxM = 32;
 constexpr int64_t kTcOwnerMaxM = 8;
 constexpr int64_t kRouterOwnerMaxM = 4;
 
+constexpr int64_t kGemvMaxM = 2;
+
+int mt_for_gemv(int64_t m) { return m <= 1 ? 1 : 2; }
+
 struct Plan {
+  bool gemv;
   bool router;
   bool expwin;
   int reduce;   // 0 owner, 1 distributed
@@ -135,6 +140,9 @@ struct proj_ctx {
   int device = 0, num_sms = 0;
   uint8_t* w_dense = nullptr;
   size_t w_dense_bytes = 0;
+  void* w_rows = nullptr;          // row-major copy for the streaming GEMV
+  uint32_t* gemv_flags = nullptr;  // [num_sms], zero between calls
+  float* gemv_ws = nullptr;        // [num_sms][2]
   uint8_t* w_exp = nullptr;
   size_t w_exp_bytes = 0;
   int e0 = 0;
@@ -162,6 +170,9 @@ namespace {
 void free_ctx(proj_ctx* h) {
   if (!h) return;
   cudaFree(h->w_dense);
+  cudaFree(h->w_rows);
+  cudaFree(h->gemv_flags);
+  cudaFree(h->gemv_ws);
   cudaFree(h->w_exp);
   cudaFree(h->ws);
   cudaFree(h->counters);
@@ -194,8 +205,25 @@ int64_t out_rows(const proj_ctx* h, int64_t m) {
 
 int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl) {
   const int variant = opts ? opts->variant : PROJ_VARIANT_AUTO;
+  const int kern = opts ? opts->kernel : PROJ_KERNEL_AUTO;
+  if (kern < PROJ_KERNEL_AUTO || kern > PROJ_KERNEL_TILE) return PROJ_EINVAL;
   pl->router = (h->layer == PROJ_ROUTER);
   pl->n_out = out_rows(h, m);
+  // Streaming GEMV: small m, uncompressed weights.
+  const bool gemv_ok = m <= kGemvMaxM && variant != PROJ_VARIANT_EXPWIN12;
+  if (kern == PROJ_KERNEL_GEMV && !gemv_ok) return PROJ_EUNSUPPORTED;
+  if (gemv_ok && kern != PROJ_KERNEL_TILE) {
+    pl->gemv = true;
+    pl->expwin = false;
+    pl->reduce = 0;
+    pl->bn = mt_for_gemv(m);
+    pl->T = pl->KB = pl->MT = 0;
+    int64_t G = h->num_sms;
+    if (opts && opts->grid > 0) G = std::min<int64_t>(opts->grid, h->num_sms);
+    pl->G = static_cast<int>(std::min<int64_t>(G, pl->n_out));
+    return PROJ_OK;
+  }
+  pl->gemv = false;
   if (pl->router) {
     if (variant == PROJ_VARIANT_EXPWIN12) return PROJ_EUNSUPPORTED;
     pl->expwin = false;
@@ -228,7 +256,6 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
   } else {
     return PROJ_EINVAL;
   }
-  if (opts && opts->reserved != 0) return PROJ_EINVAL;
   pl->MT = static_cast<int>((m + pl->bn - 1) / pl->bn);
   const int64_t U = static_cast<int64_t>(pl->MT) * pl->T * pl->KB;
   int64_t G = h->num_sms;
@@ -323,6 +350,7 @@ proj_handle proj_prepare_ex(int layer, const void* W, int64_t N, int64_t K, int 
     return bail_cuda(e, "cudaDeviceGetAttribute");
   if ((e = tc_init_attributes()) != cudaSuccess) return bail_cuda(e, "tc attributes");
   if ((e = router_init_attributes()) != cudaSuccess) return bail_cuda(e, "router attributes");
+  if ((e = gemv_init_attributes()) != cudaSuccess) return bail_cuda(e, "gemv attributes");
   if (!encode_fn()) return bail_cuda(cudaErrorNotSupported, "cuTensorMapEncodeTiled");
 
   cudaStream_t s;
@@ -412,6 +440,15 @@ proj_handle proj_prepare_ex(int layer, const void* W, int64_t N, int64_t K, int 
     h->counters_bytes = static_cast<size_t>(std::max<int64_t>(mt_max, 1) * (N / kTileRows)) * 4;
   }
   const size_t out_elem = (layer == PROJ_ROUTER) ? 4 : 2;
+  const size_t w_bytes = static_cast<size_t>(N) * K * (layer == PROJ_ROUTER ? 4 : 2);
+  if ((e = dmalloc(&h->w_rows, w_bytes)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(h->w_rows, W, w_bytes, cudaMemcpyDeviceToDevice, s)) != cudaSuccess ||
+      (e = dmalloc(&h->gemv_flags, static_cast<size_t>(sms) * 4)) != cudaSuccess ||
+      (e = cudaMemsetAsync(h->gemv_flags, 0, static_cast<size_t>(sms) * 4, s)) != cudaSuccess ||
+      (e = dmalloc(&h->gemv_ws, static_cast<size_t>(sms) * 2 * 4)) != cudaSuccess) {
+    done();
+    return bail_cuda(e, "cudaMalloc(row-major weights)");
+  }
   if ((e = dmalloc(&h->ws, h->ws_bytes)) != cudaSuccess ||
       (e = dmalloc(&h->counters, h->counters_bytes)) != cudaSuccess ||
       (e = dmalloc(&h->status, 16)) != cudaSuccess ||
@@ -452,9 +489,26 @@ int proj_run_ex(proj_handle h, const void* x, int64_t m, void* out, proj_stream 
   int st = make_plan(h, m, opts, &pl);
   if (st != PROJ_OK) return fail(st);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (pl.gemv) {
+    GemvParams g;
+    g.w = h->w_rows;
+    g.x = x;
+    g.out = out;
+    g.ws = h->gemv_ws;
+    g.flags = h->gemv_flags;
+    g.status = h->status;
+    g.m = static_cast<int>(m);
+    g.n_rows = static_cast<int>(pl.n_out);
+    g.K = static_cast<int>(h->K);
+    g.G = pl.G;
+    g.out_f32 = pl.router ? 1 : 0;
+    e = gemv_launch(pl.router, pl.bn, g, s);
+    if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
+    return PROJ_OK;
+  }
   const CUtensorMap* map = get_map(h, x, m, pl.bn, !pl.router);
   if (!map) return fail_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(x)");
-  cudaError_t e;
   if (pl.router) {
     RouterParams p;
     p.w = h->w_dense;
@@ -538,7 +592,10 @@ int proj_describe(proj_handle h, int64_t m, char* buf, size_t cap) {
   Plan pl;
   int st = make_plan(h, m, nullptr, &pl);
   if (st != PROJ_OK) return fail(st);
-  if (pl.router) {
+  if (pl.gemv) {
+    std::snprintf(buf, cap, "gemv_%s MT=%d G=%d n_rows=%lld", pl.router ? "f32w" : "bf16w", pl.bn,
+                  pl.G, static_cast<long long>(pl.n_out));
+  } else if (pl.router) {
     std::snprintf(buf, cap, "router_fma TM=%d stages=8 G=%d T=%d KB=%d MT=%d reduce=%s", pl.bn,
                   pl.G, pl.T, pl.KB, pl.MT, pl.reduce ? "distributed" : "owner");
   } else {

@@ -313,8 +313,8 @@ __global__ void __launch_bounds__(Cfg<BN, EXPWIN>::kThreads, 1)
       if constexpr (kOwnerOk) {
         if (owner) {
           const TileSplit ts = tile_split(sg.tile, p.KB, U, G);
-          ok = spin_until_ge(p.counters + sg.tile,
-                             static_cast<uint32_t>(ts.c_last - ts.c_first) * 128u, p.status);
+          ok = spin_until_ge(p.counters + sg.tile, static_cast<uint32_t>(ts.c_last - ts.c_first),
+                             p.status);
           owner_presum<BN>(p.ws, ts.c_first, ts.c_last, mv, r, pre);
         }
       }
@@ -351,9 +351,13 @@ __global__ void __launch_bounds__(Cfg<BN, EXPWIN>::kThreads, 1)
           named_bar_sync(1, 128);
           if (etid == 0) p.counters[sg.tile] = 0u;
         } else {
-          // Each thread releases its own partial stores; the reader waits
-          // for 128 arrivals per contributor.
-          red_release_gpu_add(p.counters + sg.tile, 1u);
+          // The barrier orders the warps' partial stores before thread 0's
+          // fence and release, which publishes them with one arrival.
+          named_bar_sync(1, 128);
+          if (etid == 0) {
+            __threadfence();
+            red_release_gpu_add(p.counters + sg.tile, 1u);
+          }
           if (!owner_mode) pend[npend++] = sg.tile;
         }
       }
@@ -366,7 +370,7 @@ __global__ void __launch_bounds__(Cfg<BN, EXPWIN>::kThreads, 1)
       const int tile = pend[i];
       const TileSplit ts = tile_split(tile, p.KB, U, G);
       const int64_t S = ts.c_last - ts.c_first + 1;
-      if (!spin_until_ge(p.counters + tile, static_cast<uint32_t>(S) * 128u, p.status)) break;
+      if (!spin_until_ge(p.counters + tile, static_cast<uint32_t>(S), p.status)) break;
       const int t = tile / p.MT;
       const int mt = tile % p.MT;
       const int mv = min(BN, p.m - mt * BN);
@@ -424,8 +428,8 @@ __global__ void __launch_bounds__(Cfg<BN, EXPWIN>::kThreads, 1)
       }
       named_bar_sync(1, 128);
       if (etid == 0) {
-        const uint32_t old = atomicAdd(p.counters + tile, 128u);
-        if (old == static_cast<uint32_t>(2 * S - 1) * 128u) p.counters[tile] = 0u;
+        const uint32_t old = atomicAdd(p.counters + tile, 1u);
+        if (old == static_cast<uint32_t>(2 * S - 1)) p.counters[tile] = 0u;
       }
     }
   } else if (EXPWIN) {

@@ -76,6 +76,23 @@ struct RouterParams {
   int reduce;           // split-K combine: 0 = owner, 1 = distributed
 };
 
+// Streaming GEMV (m <= 2): W row-major, bf16 or fp32; MT in {1, 2}.
+struct GemvParams {
+  const void* w;        // row-major [n_rows (+ more), K]
+  const void* x;        // bf16 [m, K]
+  void* out;            // [m, n_rows], bf16 or fp32
+  float* ws;            // [G][MT] partial rows
+  uint32_t* flags;      // [G], zero between calls
+  uint32_t* status;
+  int m;
+  int n_rows;           // rows computed
+  int K;                // multiple of 1024, <= 8192
+  int G;                // CTAs, <= n_rows
+  int out_f32;
+};
+cudaError_t gemv_init_attributes();
+cudaError_t gemv_launch(bool f32w, int MT, const GemvParams& p, cudaStream_t s);
+
 // Tensor-core path: BN in {16, 32, 64, 128, 256}; expwin12 for BN in {16, 32}.
 bool tc_supported(int BN, bool expwin);
 int tc_threads(bool expwin);

@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (owner) {
       ts = tile_split(tile, p.KB, U, G);
       if (!spin_until_ge(p.counters + tile,
-                         static_cast<uint32_t>(ts.c_last - ts.c_first) * kThreads, p.status))
+                         static_cast<uint32_t>(ts.c_last - ts.c_first), p.status))
         ok = false;
     }
     float* slot = p.ws + (owner_mode ? cta : 2 * cta + (tile == first_tile ? 0 : 1)) * kSlot;
@@ -219,8 +219,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
         if (tid == 0) p.counters[tile] = 0u;
       } else {
-        // each thread releases its own partial stores (kThreads arrivals per CTA)
-        red_release_gpu_add(p.counters + tile, 1u);
+        // the barrier orders every thread's partial stores before thread 0's
+        // fence and release (one arrival per CTA)
+        __syncthreads();
+        if (tid == 0) {
+          __threadfence();
+          red_release_gpu_add(p.counters + tile, 1u);
+        }
         if (!owner_mode) pend[npend++] = tile;
       }
     }
@@ -233,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tile = pend[i];
     const TileSplit ts = tile_split(tile, p.KB, U, G);
     const int64_t S = ts.c_last - ts.c_first + 1;
-    if (!spin_until_ge(p.counters + tile, static_cast<uint32_t>(S) * kThreads, p.status)) break;
+    if (!spin_until_ge(p.counters + tile, static_cast<uint32_t>(S), p.status)) break;
     const int t = tile / p.MT, mt = tile % p.MT;
     const int mv = min(TM, p.m - mt * TM);
     const int64_t nq = 16 * static_cast<int64_t>(mv);
@@ -282,8 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
     if (tid == 0) {
-      const uint32_t old = atomicAdd(p.counters + tile, static_cast<uint32_t>(kThreads));
-      if (old == static_cast<uint32_t>(2 * S - 1) * kThreads) p.counters[tile] = 0u;
+      const uint32_t old = atomicAdd(p.counters + tile, 1u);
+      if (old == static_cast<uint32_t>(2 * S - 1)) p.counters[tile] = 0u;
     }
   }
 

@@ -102,11 +102,18 @@ enum proj_reduce {
     PROJ_REDUCE_DISTRIBUTED = 2  /* every contributor sums 1/S of the tile */
 };
 
+/* Kernel family for proj_run_ex (testing and tuning). */
+enum proj_kernel {
+    PROJ_KERNEL_AUTO = 0,   /* the dispatch table's choice */
+    PROJ_KERNEL_GEMV = 1,   /* row-streaming CUDA-core GEMV, m <= 2 */
+    PROJ_KERNEL_TILE = 2    /* tiled kernels: tensor cores (bf16) / FMA tiles (router) */
+};
+
 typedef struct proj_run_opts {
     int variant;    /* enum proj_variant */
-    int grid;       /* CTAs of the split-K partition (1 .. SMs); 0 = dispatch table */
-    int reduce;     /* enum proj_reduce; owner mode needs m <= 32 on bf16 layers */
-    int reserved;   /* 0 */
+    int grid;       /* CTAs of the partition (1 .. SMs); 0 = dispatch table */
+    int reduce;     /* enum proj_reduce (tiled kernels); owner needs m <= 32 on bf16 */
+    int kernel;     /* enum proj_kernel */
 } proj_run_opts;
 
 typedef struct proj_info_t {

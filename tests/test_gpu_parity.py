@@ -22,7 +22,7 @@ pytestmark = pytest.mark.gpu
 FULL_ORACLE_MAX_M = 33
 SAMPLED_ROWS = 20
 M_SCORED = (1, 8, 16, 32, 128, 256)
-M_AWKWARD = (5, 7, 9, 33, 130, 512, 1000)
+M_AWKWARD = (2, 3, 5, 7, 9, 33, 130, 512, 1000)
 
 
 @pytest.fixture(scope="module")
@@ -117,8 +117,8 @@ def test_parity_all_shapes(dev, layer, m):
                                      ("unpooler", 8), ("qkv_gate", 130), ("pooler", 16),
                                      ("router", 256)])
 def test_split_partitions_and_determinism(dev, layer, m):
-    """Every partition and both split-K combine modes meet the contract and
-    are bitwise reproducible."""
+    """Every partition and both split-K combine modes of the tiled kernels
+    meet the contract and are bitwise reproducible."""
     h, W, _ = prepared(layer, 0)
     sms = B.proj_num_sms()
     modes = [B.PROJ_REDUCE_DISTRIBUTED]
@@ -126,9 +126,26 @@ def test_split_partitions_and_determinism(dev, layer, m):
         modes.append(B.PROJ_REDUCE_OWNER)
     for reduce in modes:
         for grid in (1, 7, 64, sms - 1, sms):
-            a = check_case(layer, 0, True, m, h=h, W=W, grid=grid, reduce=reduce)
-            b = check_case(layer, 0, True, m, h=h, W=W, grid=grid, reduce=reduce)
+            kw = dict(grid=grid, reduce=reduce, kernel=B.PROJ_KERNEL_TILE)
+            a = check_case(layer, 0, True, m, h=h, W=W, **kw)
+            b = check_case(layer, 0, True, m, h=h, W=W, **kw)
             assert np.array_equal(a, b), (layer, m, grid, reduce)
+    assert B.proj_device_status(h) == 0
+
+
+@pytest.mark.parametrize("layer", [s.name for s in wl.LAYERS])
+@pytest.mark.parametrize("m", [1, 2])
+def test_gemv_partitions_and_determinism(dev, layer, m):
+    """The streaming GEMV over several partitions (rows shared by neighbouring
+    CTAs at every boundary) meets the contract and is reproducible."""
+    h, W, _ = prepared(layer, 1)
+    sms = B.proj_num_sms()
+    assert "gemv" in B.proj_describe(h, m)
+    for grid in (1, 3, 37, 100, sms - 1, sms):
+        kw = dict(grid=grid, kernel=B.PROJ_KERNEL_GEMV)
+        a = check_case(layer, 1, True, m, h=h, W=W, **kw)
+        b = check_case(layer, 1, True, m, h=h, W=W, **kw)
+        assert np.array_equal(a, b), (layer, m, grid)
     assert B.proj_device_status(h) == 0
 
 
@@ -138,6 +155,9 @@ def test_owner_mode_rejected_for_wide_token_tiles(dev):
     out = torch.zeros((64, 4096), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(B.ProjError) as e:
         B.proj_run_ex(h, x, 64, out, reduce=B.PROJ_REDUCE_OWNER)
+    assert e.value.status == B.PROJ_EUNSUPPORTED
+    with pytest.raises(B.ProjError) as e:
+        B.proj_run_ex(h, x, 3, out, kernel=B.PROJ_KERNEL_GEMV)
     assert e.value.status == B.PROJ_EUNSUPPORTED
 
 
@@ -206,7 +226,8 @@ def test_expwin12_lossless_and_bit_identical(dev, layer):
             x = to_dev_x(act.x_bits)
             for grid, reduce in ((0, 0), (37, B.PROJ_REDUCE_OWNER),
                                  (0, B.PROJ_REDUCE_DISTRIBUTED)):
-                a = run(layer, h, x, m, variant=B.PROJ_VARIANT_DENSE, grid=grid, reduce=reduce)
+                a = run(layer, h, x, m, variant=B.PROJ_VARIANT_DENSE, grid=grid, reduce=reduce,
+                        kernel=B.PROJ_KERNEL_TILE)
                 b = run(layer, h, x, m, variant=B.PROJ_VARIANT_EXPWIN12, grid=grid,
                         reduce=reduce)
                 assert torch.equal(a.view(torch.int16), b.view(torch.int16)), \
@@ -253,7 +274,8 @@ def test_edge_arguments(dev):
     assert e.value.status == B.PROJ_EALIGN
     assert B.proj_out_features(prepared("unpooler", 0)[0], 8) == 1024
     assert B.proj_out_features(prepared("unpooler", 0)[0], 9) == 8192
-    assert "BN=16" in B.proj_describe(h, 1)
+    assert "gemv" in B.proj_describe(h, 1)
+    assert "BN=16" in B.proj_describe(h, 3)
 
 
 @pytest.mark.parametrize("mode", [0, 1])
