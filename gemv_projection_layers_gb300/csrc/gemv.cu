@@ -39,7 +39,7 @@ namespace {
 constexpr int kComputeWarps = 8;
 constexpr int kGemvThreads = (kComputeWarps + 1) * 32;
 constexpr int kChunkElems = 1024;
-constexpr int kRowRing = 32;    // rows in flight in the reduction ring
+constexpr int kRowRing = 128;   // rows in flight in the reduction ring (>= run-ahead + 1 stage)
 constexpr int kMaxSlices = 8;   // K <= 8192
 
 template <typename WT>
@@ -55,8 +55,9 @@ struct GSmem {
   static constexpr size_t kRing = static_cast<size_t>(GCfg<WT>::S) * GCfg<WT>::kStageBytes;
   static constexpr size_t kRed = static_cast<size_t>(kRowRing) * kMaxSlices * MT * 4;
   static constexpr size_t kEdge = 2 * kMaxSlices * MT * 4;
+  static constexpr size_t kCnt = (kRowRing + 2) * 4;
   static constexpr size_t kBars = 2 * GCfg<WT>::S * 8;
-  static constexpr size_t kTotal = 1024 + kRing + kRed + kEdge + kBars + 64;
+  static constexpr size_t kTotal = 1024 + kRing + kRed + kEdge + kCnt + kBars + 64;
 };
 
 // Stage j of this CTA's processing order: chunks [qs, qs + ns).
@@ -104,7 +105,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
   float* red = reinterpret_cast<float*>(ring + SM::kRing);        // [kRowRing][slices][MT]
   float* head_red = red + kRowRing * kMaxSlices * MT;              // [slices][MT]
   float* tail_red = head_red + kMaxSlices * MT;                    // [slices][MT]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(tail_red + kMaxSlices * MT);
+  // slices deposited per ring row; [kRowRing] = head row, [kRowRing + 1] = tail row
+  uint32_t* cnt = reinterpret_cast<uint32_t*>(tail_red + kMaxSlices * MT);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(cnt + kRowRing + 2);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * S;
 
@@ -133,6 +136,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
     }
     fence_mbar_init();
   }
+  for (int i = threadIdx.x; i < kRowRing + 2; i += blockDim.x) cnt[i] = 0;
   __syncthreads();
 
   if (warp == kComputeWarps) {
@@ -195,103 +199,120 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
     }
   }
 
+  const int head_nsl = has_head ? static_cast<int>(ks - (q0 - head_row * ks)) : 0;
+  const int tail_nsl = has_tail ? static_cast<int>(q1 - tail_row * ks) : 0;
+  auto store_out = [&](int64_t row, int t, float v) {
+    if (p.out_f32)
+      static_cast<float*>(p.out)[static_cast<int64_t>(t) * p.n_rows + row] = v;
+    else
+      static_cast<__nv_bfloat16*>(p.out)[static_cast<int64_t>(t) * p.n_rows + row] =
+          __float2bfloat16_rn(v);
+  };
+
+  // Warps run independently: each waits for its stage, reduces its chunk,
+  // deposits the slice sum, and the warp that deposits a row's last slice
+  // sums the row in slice order.  The copy ring bounds how far one warp can
+  // run ahead of another (S stages), which the row ring covers.
   bool ok = true;
   for (int64_t j = 0; j < n_stages; ++j) {
     const int s = static_cast<int>(j % S);
     int64_t qs;
     int ns;
     plan.stage(j, qs, ns);
-    // this warp's chunk in the stage: q with q % 8 == warp
     const int off = static_cast<int>(((warp - qs) % 8 + 8) % 8);
-    const bool mine = off < ns;
     const bool got = mbar_wait(full0 + 8 * s, static_cast<uint32_t>((j / S) & 1), p.status,
                                kStatusTimeoutMma);
-    if (mine && got) {
+    if (!got) {
+      ok = false;
+      break;
+    }
+    if (off < ns) {
       const uint8_t* chunk = ring + static_cast<size_t>(s) * C::kStageBytes +
                              static_cast<size_t>(off) * C::kChunkBytes;
-      float acc[MT];
+      // 4 independent FMA chains per token (one per group of loads, mod 4)
+      float acc[MT][4];
 #pragma unroll
-      for (int t = 0; t < MT; ++t) acc[t] = 0.f;
+      for (int t = 0; t < MT; ++t)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[t][c] = 0.f;
+      uint4 raw[NI];
+#pragma unroll
+      for (int i = 0; i < NI; ++i)
+        raw[i] = *reinterpret_cast<const uint4*>(chunk + (lane + 32 * i) * 16);
 #pragma unroll
       for (int i = 0; i < NI; ++i) {
-        const uint4 v = *reinterpret_cast<const uint4*>(chunk + (lane + 32 * i) * 16);
         float wv[VEC];
         if constexpr (VEC == 8) {
           float f[8];
-          widen8<__nv_bfloat16>(v, f);
+          widen8<__nv_bfloat16>(raw[i], f);
 #pragma unroll
           for (int e = 0; e < 8; ++e) wv[e] = f[e];
         } else {
-          wv[0] = __uint_as_float(v.x);
-          wv[1] = __uint_as_float(v.y);
-          wv[2] = __uint_as_float(v.z);
-          wv[3] = __uint_as_float(v.w);
+          wv[0] = __uint_as_float(raw[i].x);
+          wv[1] = __uint_as_float(raw[i].y);
+          wv[2] = __uint_as_float(raw[i].z);
+          wv[3] = __uint_as_float(raw[i].w);
         }
 #pragma unroll
         for (int t = 0; t < MT; ++t)
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) acc[t] = fmaf(wv[e], xr[t][i * VEC + e], acc[t]);
+          for (int e = 0; e < VEC; ++e)
+            acc[t][i & 3] = fmaf(wv[e], xr[t][i * VEC + e], acc[t][i & 3]);
       }
+      float sum[MT];
 #pragma unroll
       for (int t = 0; t < MT; ++t) {
+        sum[t] = (acc[t][0] + acc[t][1]) + (acc[t][2] + acc[t][3]);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
+        for (int o = 16; o > 0; o >>= 1) sum[t] += __shfl_xor_sync(0xffffffffu, sum[t], o);
       }
       const int64_t row = (qs + off) / ks;
-      float* dst;
-      if (has_head && row == head_row) {
-        dst = head_red + slice * MT;
-      } else if (has_tail && row == tail_row) {
-        dst = tail_red + slice * MT;
-      } else {
-        dst = red + (static_cast<int>(row % kRowRing) * kMaxSlices + slice) * MT;
-      }
+      const bool is_head = has_head && row == head_row;
+      const bool is_tail = has_tail && row == tail_row;
+      float* dst = is_head ? head_red
+                 : is_tail ? tail_red
+                           : red + static_cast<int>(row % kRowRing) * kMaxSlices * MT;
+      uint32_t* c = is_head ? cnt + kRowRing : is_tail ? cnt + kRowRing + 1
+                                                       : cnt + static_cast<int>(row % kRowRing);
+      const uint32_t need = is_head ? head_nsl : is_tail ? tail_nsl : static_cast<uint32_t>(ks);
+      uint32_t prev = 0;
       if (lane == 0) {
 #pragma unroll
-        for (int t = 0; t < MT; ++t) dst[t] = acc[t];
+        for (int t = 0; t < MT; ++t) dst[slice * MT + t] = sum[t];
+        __threadfence_block();
+        prev = atomicAdd(c, 1u);
+      }
+      prev = __shfl_sync(0xffffffffu, prev, 0);
+      if (prev + 1 == need && !is_head) {
+        // last slice of the row: sum slices in order
+        __threadfence_block();
+        const int sl0 = is_tail ? 0 : 0;
+        const int sl1 = is_tail ? tail_nsl : ks;
+        if (lane < MT) {
+          float v = 0.f;
+          for (int sl = sl0; sl < sl1; ++sl) v += dst[sl * MT + lane];
+          if (is_tail) {
+            p.ws[cta * MT + lane] = v;
+          } else if (lane < p.m) {
+            store_out(row, lane, v);
+          }
+        }
+        if (is_tail) {
+          __syncwarp();
+          if (lane == 0) {
+            __threadfence();
+            red_release_gpu_add(p.flags + cta, 1u);
+          }
+        } else if (lane == 0) {
+          *c = 0u;  // ring slot free for row + kRowRing
+        }
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * s);
-    // one barrier per stage; an abort anywhere stops every compute warp
-    if (named_bar_sync_or(1, kComputeWarps * 32, !got)) {
-      ok = false;
-      break;
-    }
-    if (j < plan.n_tail_stages) {
-      if (j == plan.n_tail_stages - 1) {
-        // lower slices of the last row, in slice order: publish for CTA + 1
-        if (tid < MT) {
-          float v = 0.f;
-          const int nsl = static_cast<int>(q1 - plan.tail_lo);
-          for (int sl = 0; sl < nsl; ++sl) v += tail_red[sl * MT + tid];
-          p.ws[cta * MT + tid] = v;
-        }
-        named_bar_sync(1, kComputeWarps * 32);
-        if (tid == 0) {
-          __threadfence();
-          red_release_gpu_add(p.flags + cta, 1u);
-        }
-      }
-    } else {
-      // rows whose last chunk lies in [qs, qs + ns): [qs / ks, (qs + ns) / ks)
-      const int64_t r_lo = qs / ks;
-      const int64_t r_hi = (qs + ns) / ks;
-      const int idx = tid / MT;
-      const int t = tid % MT;
-      const int64_t row = r_lo + idx;
-      if (row < r_hi && t < p.m && !(has_head && row == head_row)) {
-        const float* rr = red + static_cast<int>(row % kRowRing) * kMaxSlices * MT;
-        float v = 0.f;
-        for (int sl = 0; sl < ks; ++sl) v += rr[sl * MT + t];
-        if (p.out_f32)
-          static_cast<float*>(p.out)[static_cast<int64_t>(t) * p.n_rows + row] = v;
-        else
-          static_cast<__nv_bfloat16*>(p.out)[static_cast<int64_t>(t) * p.n_rows + row] =
-              __float2bfloat16_rn(v);
-      }
-    }
   }
+  // Every compute warp is done: the head row's upper slices are all deposited.
+  if (named_bar_sync_or(1, kComputeWarps * 32, !ok)) ok = false;
   // The first row of the run: its lower slices come from the previous CTA,
   // which published them right after streaming them.
   if (ok && has_head && tid < MT) {
@@ -299,15 +320,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
     if (spin_until_ge(p.flags + cta - 1, 1u, p.status)) {
       const float lo = __ldcg(p.ws + (cta - 1) * MT + t);
       float up = 0.f;
-      for (int sl = static_cast<int>(q0 - head_row * ks); sl < ks; ++sl) up += head_red[sl * MT + t];
-      const float v = lo + up;
-      if (t < p.m) {
-        if (p.out_f32)
-          static_cast<float*>(p.out)[static_cast<int64_t>(t) * p.n_rows + head_row] = v;
-        else
-          static_cast<__nv_bfloat16*>(p.out)[static_cast<int64_t>(t) * p.n_rows + head_row] =
-              __float2bfloat16_rn(v);
-      }
+      for (int sl = ks - head_nsl; sl < ks; ++sl) up += head_red[sl * MT + t];
+      if (t < p.m) store_out(head_row, t, lo + up);
     }
   }
   if (has_head) {
