@@ -8,25 +8,25 @@
 // streaming and about the tail:
 //
 // * W stays row-major.  Each row is cut into chunks of 1024 consecutive
-//   weights (k-slices: K / 1024 per row, 8 for K = 8192), and the chunks of
-//   the whole matrix, in row-major order, are split into G equal contiguous
-//   runs, one per CTA (one CTA per SM).  Every CTA therefore streams the same
-//   number of bytes and, with runs of at least one row, only the first and
-//   the last row of a run can be shared with a neighbour.
+//   weights (K / 1024 "slices" per row), and the chunks of the whole matrix,
+//   in row-major order, are split into G equal contiguous runs, one per CTA
+//   (one CTA per SM).  Every CTA streams the same number of bytes; a run is at
+//   least one row long, so only its first and last row can be shared with a
+//   neighbour.
 // * One producer thread streams 8-chunk stages (16 KB bf16 / 32 KB fp32)
-//   with bulk copies into a 12 / 6 stage ring.  Eight compute warps: warp w
-//   takes the chunk q with q % 8 == w of every stage, so its k-slice is fixed
-//   (q % slices == w % slices) and its part of x lives in registers, widened
-//   to fp32 once.  Each chunk is a 32-lane dot product (32 weights per lane,
-//   16-byte conflict-free shared loads), reduced with a fixed shuffle tree.
-// * Rows are summed over their k-slices in slice order inside the CTA.  The
-//   run's last row, when it continues into the next CTA, is streamed FIRST;
-//   its partial (lower slices) is published with a release flag early, and
-//   the next CTA -- which holds that row's upper slices as the start of its
-//   run -- adds it at its end: row = lower part + upper part, a fixed order.
-//   No tensor memory, no tile-level split-K (muse_bf16_proj notebook, n. 47:
-//   one-token vector reduction; project report, "What did not pay off":
-//   in-CTA reduction beat cross-CTA split-K).
+//   with bulk copies into a ring.  Stage j belongs to compute warp j % 8,
+//   which keeps a lane partial per row across the stage's chunks and reduces
+//   each row segment once with a shuffle tree; x sits in shared memory as
+//   bf16 in the same lane layout as the weights (conflict-free 16-byte loads).
+// * A row is summed in a fixed order: lane partials over its chunks in
+//   column order, the shuffle tree, then lower segment + upper segment when
+//   the row straddles two stages (the warp that deposits second finishes it).
+//   The run's last row, when it continues into the next CTA, is streamed
+//   FIRST and published with a release flag; the next CTA, which holds that
+//   row's upper slices at the start of its run, adds it at its end.
+//   No tensor memory and no tile-level split-K (muse_bf16_proj notebook,
+//   n. 47: a one-token vector reduction; project report, "What did not pay
+//   off": in-CTA reduction beat cross-CTA split-K).
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -39,30 +39,28 @@ namespace {
 constexpr int kComputeWarps = 8;
 constexpr int kGemvThreads = (kComputeWarps + 1) * 32;
 constexpr int kChunkElems = 1024;
-constexpr int kRowRing = 128;   // rows in flight in the reduction ring (>= run-ahead + 1 stage)
-constexpr int kMaxSlices = 8;   // K <= 8192
+constexpr int kSplitRing = 64;  // rows straddling two stages, in flight
 
-template <typename WT>
+template <typename WT, int MT>
 struct GCfg {
   static constexpr int kChunkBytes = kChunkElems * static_cast<int>(sizeof(WT));
   static constexpr int kStageBytes = 8 * kChunkBytes;
-  static constexpr int S = sizeof(WT) == 2 ? 12 : 6;
-  static constexpr int kVec = 16 / static_cast<int>(sizeof(WT));  // elements per 16 B
+  static constexpr int kVec = 16 / static_cast<int>(sizeof(WT));  // weights per 16 B
+  static constexpr int kXBytes = MT * 8192 * 2;                    // bf16 x, K <= 8192
+  static constexpr int kFit = (232448 - 1024 - kXBytes - 2048) / kStageBytes;
+  static constexpr int S = kFit > 12 ? 12 : kFit;
+  static constexpr size_t kSplit = static_cast<size_t>(kSplitRing) * 2 * MT * 4;
+  static constexpr size_t kSmem = 1024 + static_cast<size_t>(S) * kStageBytes + kXBytes + kSplit +
+                                  kSplitRing * 4 + 2 * S * 8 + 64;
+  static_assert(S >= 4, "ring too shallow");
+  static_assert(kSmem <= 232448, "shared memory budget");
 };
 
-template <typename WT, int MT>
-struct GSmem {
-  static constexpr size_t kRing = static_cast<size_t>(GCfg<WT>::S) * GCfg<WT>::kStageBytes;
-  static constexpr size_t kRed = static_cast<size_t>(kRowRing) * kMaxSlices * MT * 4;
-  static constexpr size_t kEdge = 2 * kMaxSlices * MT * 4;
-  static constexpr size_t kCnt = (kRowRing + 2) * 4;
-  static constexpr size_t kBars = 2 * GCfg<WT>::S * 8;
-  static constexpr size_t kTotal = 1024 + kRing + kRed + kEdge + kCnt + kBars + 64;
-};
-
-// Stage j of this CTA's processing order: chunks [qs, qs + ns).
+// Stage j of this CTA's processing order covers chunks [qs, qs + ns): first
+// the tail piece (the run's last row, when it continues in the next CTA),
+// then the run from its start.
 struct StagePlan {
-  int64_t tail_lo;   // first chunk of the streamed-first tail piece (== q1 if none)
+  int64_t tail_lo;   // first chunk of the tail piece (== q1 if none)
   int64_t q0, q1;
   int64_t n_tail_stages;
   __device__ void stage(int64_t j, int64_t& qs, int& ns) const {
@@ -76,67 +74,106 @@ struct StagePlan {
   }
 };
 
-template <typename WT>
-__device__ __forceinline__ void widen8(const uint4 v, float (&f)[8]);
+__device__ __forceinline__ void bf16x2_to_f32(uint32_t w, float& lo, float& hi) {
+  lo = __uint_as_float(w << 16);
+  hi = __uint_as_float(w & 0xFFFF0000u);
+}
 
-template <>
-__device__ __forceinline__ void widen8<__nv_bfloat16>(const uint4 v, float (&f)[8]) {
-  f[0] = __uint_as_float(v.x << 16);
-  f[1] = __uint_as_float(v.x & 0xFFFF0000u);
-  f[2] = __uint_as_float(v.y << 16);
-  f[3] = __uint_as_float(v.y & 0xFFFF0000u);
-  f[4] = __uint_as_float(v.z << 16);
-  f[5] = __uint_as_float(v.z & 0xFFFF0000u);
-  f[6] = __uint_as_float(v.w << 16);
-  f[7] = __uint_as_float(v.w & 0xFFFF0000u);
+// Lane partial of one chunk for MT tokens.  bf16 weights: lane loads 16 B
+// (8 weights) at (lane + 32 i) * 16, i < 4; fp32 weights: 16 B (4 weights),
+// i < 8.  x (bf16, smem) is read with the matching lane layout.
+template <typename WT, int MT>
+__device__ __forceinline__ void chunk_partial(const uint8_t* chunk, const uint16_t* xs, int K,
+                                              int64_t col0, int lane, float (&acc)[MT]) {
+  constexpr int VEC = GCfg<WT, MT>::kVec;
+  constexpr int NI = 32 / VEC;
+  float a4[MT][4];
+#pragma unroll
+  for (int t = 0; t < MT; ++t)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) a4[t][c] = 0.f;
+  uint4 wraw[NI];
+#pragma unroll
+  for (int i = 0; i < NI; ++i) wraw[i] = *reinterpret_cast<const uint4*>(chunk + (lane + 32 * i) * 16);
+#pragma unroll
+  for (int i = 0; i < NI; ++i) {
+    float wv[VEC];
+    if constexpr (VEC == 8) {
+      bf16x2_to_f32(wraw[i].x, wv[0], wv[1]);
+      bf16x2_to_f32(wraw[i].y, wv[2], wv[3]);
+      bf16x2_to_f32(wraw[i].z, wv[4], wv[5]);
+      bf16x2_to_f32(wraw[i].w, wv[6], wv[7]);
+    } else {
+      wv[0] = __uint_as_float(wraw[i].x);
+      wv[1] = __uint_as_float(wraw[i].y);
+      wv[2] = __uint_as_float(wraw[i].z);
+      wv[3] = __uint_as_float(wraw[i].w);
+    }
+    const int64_t col = col0 + static_cast<int64_t>(lane + 32 * i) * VEC;
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+      float xv[VEC];
+      const uint16_t* xp = xs + static_cast<int64_t>(t) * K + col;
+      if constexpr (VEC == 8) {
+        const uint4 xr = *reinterpret_cast<const uint4*>(xp);
+        bf16x2_to_f32(xr.x, xv[0], xv[1]);
+        bf16x2_to_f32(xr.y, xv[2], xv[3]);
+        bf16x2_to_f32(xr.z, xv[4], xv[5]);
+        bf16x2_to_f32(xr.w, xv[6], xv[7]);
+      } else {
+        const uint2 xr = *reinterpret_cast<const uint2*>(xp);
+        bf16x2_to_f32(xr.x, xv[0], xv[1]);
+        bf16x2_to_f32(xr.y, xv[2], xv[3]);
+      }
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) a4[t][i & 3] = fmaf(wv[e], xv[e], a4[t][i & 3]);
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < MT; ++t) acc[t] += (a4[t][0] + a4[t][1]) + (a4[t][2] + a4[t][3]);
 }
 
 template <typename WT, int MT>
 __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams p) {
-  using C = GCfg<WT>;
-  using SM = GSmem<WT, MT>;
+  using C = GCfg<WT, MT>;
   constexpr int S = C::S;
-  constexpr int VEC = C::kVec;
-  constexpr int NI = 32 / VEC;  // 16-byte loads per lane per chunk
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* ring = smem;
-  float* red = reinterpret_cast<float*>(ring + SM::kRing);        // [kRowRing][slices][MT]
-  float* head_red = red + kRowRing * kMaxSlices * MT;              // [slices][MT]
-  float* tail_red = head_red + kMaxSlices * MT;                    // [slices][MT]
-  // slices deposited per ring row; [kRowRing] = head row, [kRowRing + 1] = tail row
-  uint32_t* cnt = reinterpret_cast<uint32_t*>(tail_red + kMaxSlices * MT);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(cnt + kRowRing + 2);
+  uint16_t* xs = reinterpret_cast<uint16_t*>(ring + static_cast<size_t>(S) * C::kStageBytes);
+  float* split = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(xs) + C::kXBytes);
+  uint32_t* split_cnt = reinterpret_cast<uint32_t*>(split + kSplitRing * 2 * MT);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(split_cnt + kSplitRing);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * S;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int ks = p.K / kChunkElems;  // k-slices per row (1..8)
+  const int ks = p.K / kChunkElems;  // slices per row (1..8)
   const int64_t C_total = static_cast<int64_t>(p.n_rows) * ks;
   const int64_t cta = blockIdx.x;
   const int64_t q0 = part_begin(cta, C_total, p.G);
   const int64_t q1 = part_begin(cta + 1, C_total, p.G);
-  const bool has_head = (q0 % ks) != 0;               // row q0/ks began in CTA cta-1
-  const bool has_tail = (q1 % ks) != 0;               // row q1/ks continues in CTA cta+1
+  const bool has_head = (q0 % ks) != 0;  // row q0 / ks began in CTA cta - 1
+  const bool has_tail = (q1 % ks) != 0;  // row q1 / ks continues in CTA cta + 1
   const int64_t head_row = q0 / ks;
   const int64_t tail_row = q1 / ks;
   StagePlan plan;
   plan.q0 = q0;
   plan.q1 = q1;
   plan.tail_lo = has_tail ? tail_row * ks : q1;
-  plan.n_tail_stages = has_tail ? (q1 - plan.tail_lo + 7) / 8 : 0;
+  plan.n_tail_stages = has_tail ? 1 : 0;  // the tail piece is < ks <= 8 chunks
   const int64_t n_stages = plan.n_tail_stages + (plan.tail_lo - q0 + 7) / 8;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, kComputeWarps);
+      mbar_init(empty0 + 8 * s, 1);
     }
     fence_mbar_init();
   }
-  for (int i = threadIdx.x; i < kRowRing + 2; i += blockDim.x) cnt[i] = 0;
+  for (int i = threadIdx.x; i < kSplitRing; i += blockDim.x) split_cnt[i] = 0;
   __syncthreads();
 
   if (warp == kComputeWarps) {
@@ -167,40 +204,18 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
 
   // ----------------------------------------------------------- compute warps
   const int tid = threadIdx.x;  // 0..255
-  const int slice = warp % ks;
-  // x for this warp's k-slice, widened to fp32: element (i, e) of the lane is
-  // column slice*1024 + lane*VEC + 32*VEC*i + e.
-  float xr[MT][32];
   {
-    const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(p.x);
-#pragma unroll
-    for (int t = 0; t < MT; ++t) {
-#pragma unroll
-      for (int i = 0; i < NI; ++i) {
-        const int64_t col = static_cast<int64_t>(slice) * kChunkElems + lane * VEC + 32 * VEC * i;
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) xr[t][i * VEC + e] = 0.f;
-        if (t < p.m) {
-          if (VEC == 8) {
-            const uint4 v = *reinterpret_cast<const uint4*>(xb + t * static_cast<int64_t>(p.K) + col);
-            float f[8];
-            widen8<__nv_bfloat16>(v, f);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) xr[t][i * VEC + e] = f[e];
-          } else {
-            const uint2 v = *reinterpret_cast<const uint2*>(xb + t * static_cast<int64_t>(p.K) + col);
-            xr[t][i * VEC + 0] = __uint_as_float(v.x << 16);
-            xr[t][i * VEC + 1] = __uint_as_float(v.x & 0xFFFF0000u);
-            xr[t][i * VEC + 2] = __uint_as_float(v.y << 16);
-            xr[t][i * VEC + 3] = __uint_as_float(v.y & 0xFFFF0000u);
-          }
-        }
-      }
+    // x -> shared memory (bf16, zero rows beyond m)
+    const uint4* xg = static_cast<const uint4*>(p.x);
+    uint4* xd = reinterpret_cast<uint4*>(xs);
+    const int n16 = MT * p.K / 8;
+    for (int i = tid; i < n16; i += kComputeWarps * 32) {
+      const int t = i / (p.K / 8);
+      xd[i] = t < p.m ? xg[i] : make_uint4(0, 0, 0, 0);
     }
   }
+  named_bar_sync(1, kComputeWarps * 32);
 
-  const int head_nsl = has_head ? static_cast<int>(ks - (q0 - head_row * ks)) : 0;
-  const int tail_nsl = has_tail ? static_cast<int>(q1 - tail_row * ks) : 0;
   auto store_out = [&](int64_t row, int t, float v) {
     if (p.out_f32)
       static_cast<float*>(p.out)[static_cast<int64_t>(t) * p.n_rows + row] = v;
@@ -209,122 +224,101 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
           __float2bfloat16_rn(v);
   };
 
-  // Warps run independently: each waits for its stage, reduces its chunk,
-  // deposits the slice sum, and the warp that deposits a row's last slice
-  // sums the row in slice order.  The copy ring bounds how far one warp can
-  // run ahead of another (S stages), which the row ring covers.
+  float head_val[MT];
+#pragma unroll
+  for (int t = 0; t < MT; ++t) head_val[t] = 0.f;
   bool ok = true;
-  for (int64_t j = 0; j < n_stages; ++j) {
+  for (int64_t j = warp; j < n_stages; j += kComputeWarps) {
     const int s = static_cast<int>(j % S);
     int64_t qs;
     int ns;
     plan.stage(j, qs, ns);
-    const int off = static_cast<int>(((warp - qs) % 8 + 8) % 8);
-    const bool got = mbar_wait(full0 + 8 * s, static_cast<uint32_t>((j / S) & 1), p.status,
-                               kStatusTimeoutMma);
-    if (!got) {
+    if (!mbar_wait(full0 + 8 * s, static_cast<uint32_t>((j / S) & 1), p.status,
+                   kStatusTimeoutMma)) {
       ok = false;
       break;
     }
-    if (off < ns) {
-      const uint8_t* chunk = ring + static_cast<size_t>(s) * C::kStageBytes +
-                             static_cast<size_t>(off) * C::kChunkBytes;
-      // 4 independent FMA chains per token (one per group of loads, mod 4)
-      float acc[MT][4];
+    const uint8_t* stage = ring + static_cast<size_t>(s) * C::kStageBytes;
+    // Walk the stage's chunks, one row segment at a time.
+    int c = 0;
+    while (c < ns) {
+      const int64_t row = (qs + c) / ks;
+      const int64_t seg_lo = qs + c;
+      int64_t seg_hi = (row + 1) * ks;  // exclusive chunk bound of the row
+      if (seg_hi > qs + ns) seg_hi = qs + ns;
+      float acc[MT];
 #pragma unroll
-      for (int t = 0; t < MT; ++t)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) acc[t][c] = 0.f;
-      uint4 raw[NI];
-#pragma unroll
-      for (int i = 0; i < NI; ++i)
-        raw[i] = *reinterpret_cast<const uint4*>(chunk + (lane + 32 * i) * 16);
-#pragma unroll
-      for (int i = 0; i < NI; ++i) {
-        float wv[VEC];
-        if constexpr (VEC == 8) {
-          float f[8];
-          widen8<__nv_bfloat16>(raw[i], f);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) wv[e] = f[e];
-        } else {
-          wv[0] = __uint_as_float(raw[i].x);
-          wv[1] = __uint_as_float(raw[i].y);
-          wv[2] = __uint_as_float(raw[i].z);
-          wv[3] = __uint_as_float(raw[i].w);
-        }
-#pragma unroll
-        for (int t = 0; t < MT; ++t)
-#pragma unroll
-          for (int e = 0; e < VEC; ++e)
-            acc[t][i & 3] = fmaf(wv[e], xr[t][i * VEC + e], acc[t][i & 3]);
+      for (int t = 0; t < MT; ++t) acc[t] = 0.f;
+      for (int64_t q = seg_lo; q < seg_hi; ++q) {
+        const int cc = static_cast<int>(q - qs);
+        chunk_partial<WT, MT>(stage + static_cast<size_t>(cc) * C::kChunkBytes, xs, p.K,
+                              (q - row * ks) * kChunkElems, lane, acc);
       }
-      float sum[MT];
 #pragma unroll
       for (int t = 0; t < MT; ++t) {
-        sum[t] = (acc[t][0] + acc[t][1]) + (acc[t][2] + acc[t][3]);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sum[t] += __shfl_xor_sync(0xffffffffu, sum[t], o);
+        for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
       }
-      const int64_t row = (qs + off) / ks;
-      const bool is_head = has_head && row == head_row;
-      const bool is_tail = has_tail && row == tail_row;
-      float* dst = is_head ? head_red
-                 : is_tail ? tail_red
-                           : red + static_cast<int>(row % kRowRing) * kMaxSlices * MT;
-      uint32_t* c = is_head ? cnt + kRowRing : is_tail ? cnt + kRowRing + 1
-                                                       : cnt + static_cast<int>(row % kRowRing);
-      const uint32_t need = is_head ? head_nsl : is_tail ? tail_nsl : static_cast<uint32_t>(ks);
-      uint32_t prev = 0;
-      if (lane == 0) {
+      const bool whole_here = (seg_lo == row * ks) && (seg_hi == (row + 1) * ks);
+      if (has_head && row == head_row) {
 #pragma unroll
-        for (int t = 0; t < MT; ++t) dst[slice * MT + t] = sum[t];
-        __threadfence_block();
-        prev = atomicAdd(c, 1u);
-      }
-      prev = __shfl_sync(0xffffffffu, prev, 0);
-      if (prev + 1 == need && !is_head) {
-        // last slice of the row: sum slices in order
-        __threadfence_block();
-        const int sl0 = is_tail ? 0 : 0;
-        const int sl1 = is_tail ? tail_nsl : ks;
-        if (lane < MT) {
-          float v = 0.f;
-          for (int sl = sl0; sl < sl1; ++sl) v += dst[sl * MT + lane];
-          if (is_tail) {
-            p.ws[cta * MT + lane] = v;
-          } else if (lane < p.m) {
+        for (int t = 0; t < MT; ++t) head_val[t] = acc[t];  // all of it lies in one stage
+      } else if (has_tail && row == tail_row) {
+#pragma unroll
+        for (int t = 0; t < MT; ++t)
+          if (lane == t) p.ws[cta * MT + t] = acc[t];
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence();
+          red_release_gpu_add(p.flags + cta, 1u);
+        }
+      } else if (whole_here) {
+#pragma unroll
+        for (int t = 0; t < MT; ++t)
+          if (lane == t && t < p.m) store_out(row, t, acc[t]);
+      } else {
+        // the row straddles two stages: lower segment (holds its first
+        // chunk) + upper segment; whichever warp deposits second sums them
+        const int slot = static_cast<int>(row % kSplitRing);
+        const int part = (seg_lo == row * ks) ? 0 : 1;
+        uint32_t prev = 0;
+        if (lane == 0) {
+#pragma unroll
+          for (int t = 0; t < MT; ++t) split[(slot * 2 + part) * MT + t] = acc[t];
+          __threadfence_block();
+          prev = atomicAdd(split_cnt + slot, 1u);
+        }
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        if (prev == 1) {
+          __threadfence_block();
+          if (lane < MT && lane < p.m) {
+            const float v = split[(slot * 2 + 0) * MT + lane] + split[(slot * 2 + 1) * MT + lane];
             store_out(row, lane, v);
           }
-        }
-        if (is_tail) {
-          __syncwarp();
-          if (lane == 0) {
-            __threadfence();
-            red_release_gpu_add(p.flags + cta, 1u);
-          }
-        } else if (lane == 0) {
-          *c = 0u;  // ring slot free for row + kRowRing
+          if (lane == 0) split_cnt[slot] = 0u;
         }
       }
+      c = static_cast<int>(seg_hi - qs);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * s);
   }
-  // Every compute warp is done: the head row's upper slices are all deposited.
-  if (named_bar_sync_or(1, kComputeWarps * 32, !ok)) ok = false;
-  // The first row of the run: its lower slices come from the previous CTA,
-  // which published them right after streaming them.
-  if (ok && has_head && tid < MT) {
-    const int t = tid;
-    if (spin_until_ge(p.flags + cta - 1, 1u, p.status)) {
-      const float lo = __ldcg(p.ws + (cta - 1) * MT + t);
-      float up = 0.f;
-      for (int sl = ks - head_nsl; sl < ks; ++sl) up += head_red[sl * MT + t];
-      if (t < p.m) store_out(head_row, t, lo + up);
-    }
-  }
+  // The head row: its upper slices were reduced by the warp that owns the
+  // first main stage; its lower slices come from the previous CTA, which
+  // published them right after streaming them.
   if (has_head) {
+    const int64_t owner_stage = plan.n_tail_stages;
+    if (warp == static_cast<int>(owner_stage % kComputeWarps) && ok && lane < MT) {
+      if (spin_until_ge(p.flags + cta - 1, 1u, p.status)) {
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+          if (lane == t) {
+            const float lo = __ldcg(p.ws + (cta - 1) * MT + t);
+            if (t < p.m) store_out(head_row, t, lo + head_val[t]);
+          }
+        }
+      }
+    }
     named_bar_sync(1, kComputeWarps * 32);
     if (tid == 0) p.flags[cta - 1] = 0u;
   }
@@ -333,7 +327,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
 template <typename WT, int MT>
 cudaError_t set_attr() {
   return cudaFuncSetAttribute(gemv_kernel<WT, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(GSmem<WT, MT>::kTotal));
+                              static_cast<int>(GCfg<WT, MT>::kSmem));
 }
 
 template <typename WT, int MT>
@@ -341,7 +335,7 @@ cudaError_t launch(const GemvParams& p, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.G);
   cfg.blockDim = dim3(kGemvThreads);
-  cfg.dynamicSmemBytes = GSmem<WT, MT>::kTotal;
+  cfg.dynamicSmemBytes = GCfg<WT, MT>::kSmem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
