@@ -446,7 +446,13 @@ __global__ void __launch_bounds__(Cfg<BN, EXPWIN>::kThreads, 1)
       for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++j) {
         if (static_cast<int>(j % SAd) != d) continue;
         const int e = static_cast<int>(j % SE);
-        if (!mbar_wait(full0 + 8 * e, static_cast<uint32_t>((j / SE) & 1), p.status,
+        // Four warps share the copy ring: before waiting for generation g of
+        // slot e, wait for generation g - 1 to have been released (consumed
+        // by the MMA), since a parity wait cannot tell g from g - 2.
+        const int64_t g = j / SE;
+        if ((g > 0 && !mbar_wait(empty0 + 8 * e, static_cast<uint32_t>((g - 1) & 1), p.status,
+                                 kStatusTimeoutDecode)) ||
+            !mbar_wait(full0 + 8 * e, static_cast<uint32_t>(g & 1), p.status,
                        kStatusTimeoutDecode) ||
             !mbar_wait(dece0 + 8 * d, static_cast<uint32_t>(((j / SAd) & 1) ^ 1), p.status,
                        kStatusTimeoutDecode)) {

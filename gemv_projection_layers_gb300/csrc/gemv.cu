@@ -233,8 +233,17 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
     int64_t qs;
     int ns;
     plan.stage(j, qs, ns);
-    if (!mbar_wait(full0 + 8 * s, static_cast<uint32_t>((j / S) & 1), p.status,
-                   kStatusTimeoutMma)) {
+    // Several warps consume the ring, so a warp may reach slot s before the
+    // slot's previous generation has landed; a parity wait cannot tell
+    // generation g from g - 2, so first wait until generation g - 1 of the
+    // slot has been released, then for generation g to land.
+    const int64_t g = j / S;
+    if (g > 0 && !mbar_wait(empty0 + 8 * s, static_cast<uint32_t>((g - 1) & 1), p.status,
+                            kStatusTimeoutMma)) {
+      ok = false;
+      break;
+    }
+    if (!mbar_wait(full0 + 8 * s, static_cast<uint32_t>(g & 1), p.status, kStatusTimeoutMma)) {
       ok = false;
       break;
     }
