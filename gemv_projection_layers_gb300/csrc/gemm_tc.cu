@@ -47,7 +47,8 @@ struct Cfg {
   static constexpr int SA = EXPWIN ? 4 : 0;  // decoded-tile ring (12-bit only)
   static constexpr int kCopyStage = (EXPWIN ? kRecBytes : kTileBytes) + kXBytes;
   static constexpr int kFit = (kSmemLimit - kSmemReserve - SA * kTileBytes) / kCopyStage;
-  static constexpr int SE = kFit > 12 ? 12 : kFit;  // copy ring
+  // copy ring; with 12-bit decode a multiple of the 4 decode warps
+  static constexpr int SE = EXPWIN ? (kFit >= 8 ? 8 : 4) : (kFit > 12 ? 12 : kFit);
   static constexpr int kThreads = EXPWIN ? 320 : 192;
   static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
   static constexpr int kABytes = (EXPWIN ? SA : SE) * kTileBytes;
@@ -445,14 +446,11 @@ __global__ void __launch_bounds__(Cfg<BN, EXPWIN>::kThreads, 1)
     while (ok && next_seg(u, u1, p.KB, sg)) {
       for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++j) {
         if (static_cast<int>(j % SAd) != d) continue;
+        // SE is a multiple of 4, so slot e only ever belongs to decode warp
+        // e % 4, which consumes its generations in order (a parity wait
+        // cannot tell one lap of the ring from the one two laps earlier).
         const int e = static_cast<int>(j % SE);
-        // Four warps share the copy ring: before waiting for generation g of
-        // slot e, wait for generation g - 1 to have been released (consumed
-        // by the MMA), since a parity wait cannot tell g from g - 2.
-        const int64_t g = j / SE;
-        if ((g > 0 && !mbar_wait(empty0 + 8 * e, static_cast<uint32_t>((g - 1) & 1), p.status,
-                                 kStatusTimeoutDecode)) ||
-            !mbar_wait(full0 + 8 * e, static_cast<uint32_t>(g & 1), p.status,
+        if (!mbar_wait(full0 + 8 * e, static_cast<uint32_t>((j / SE) & 1), p.status,
                        kStatusTimeoutDecode) ||
             !mbar_wait(dece0 + 8 * d, static_cast<uint32_t>(((j / SAd) & 1) ^ 1), p.status,
                        kStatusTimeoutDecode)) {

@@ -14,10 +14,14 @@
 //   least one row long, so only its first and last row can be shared with a
 //   neighbour.
 // * One producer thread streams 8-chunk stages (16 KB bf16 / 32 KB fp32)
-//   with bulk copies into a ring.  Stage j belongs to compute warp j % 8,
-//   which keeps a lane partial per row across the stage's chunks and reduces
-//   each row segment once with a shuffle tree; x sits in shared memory as
-//   bf16 in the same lane layout as the weights (conflict-free 16-byte loads).
+//   with bulk copies into a ring of S slots, and there is one compute warp
+//   per slot: stage j lands in slot j % S and belongs to warp j % S, so every
+//   slot has a single, in-order consumer (a parity wait cannot tell one ring
+//   generation from the one two laps earlier, so no slot may be shared by
+//   warps that can drift apart).  The warp keeps a lane partial per row
+//   across the stage's chunks and reduces each row segment once with a
+//   shuffle tree; x sits in shared memory as bf16 in the same lane layout as
+//   the weights (conflict-free 16-byte loads).
 // * A row is summed in a fixed order: lane partials over its chunks in
 //   column order, the shuffle tree, then lower segment + upper segment when
 //   the row straddles two stages (the warp that deposits second finishes it).
@@ -36,8 +40,6 @@
 namespace proj {
 namespace {
 
-constexpr int kComputeWarps = 8;
-constexpr int kGemvThreads = (kComputeWarps + 1) * 32;
 constexpr int kChunkElems = 1024;
 constexpr int kSplitRing = 64;  // rows straddling two stages, in flight
 
@@ -48,7 +50,8 @@ struct GCfg {
   static constexpr int kVec = 16 / static_cast<int>(sizeof(WT));  // weights per 16 B
   static constexpr int kXBytes = MT * 8192 * 2;                    // bf16 x, K <= 8192
   static constexpr int kFit = (232448 - 1024 - kXBytes - 2048) / kStageBytes;
-  static constexpr int S = kFit > 12 ? 12 : kFit;
+  static constexpr int S = kFit > 12 ? 12 : kFit;  // ring slots == compute warps
+  static constexpr int kThreads = (S + 1) * 32;
   static constexpr size_t kSplit = static_cast<size_t>(kSplitRing) * 2 * MT * 4;
   static constexpr size_t kSmem = 1024 + static_cast<size_t>(S) * kStageBytes + kXBytes + kSplit +
                                   kSplitRing * 4 + 2 * S * 8 + 64;
@@ -134,9 +137,10 @@ __device__ __forceinline__ void chunk_partial(const uint8_t* chunk, const uint16
 }
 
 template <typename WT, int MT>
-__global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams p) {
+__global__ void __launch_bounds__(GCfg<WT, MT>::kThreads, 1) gemv_kernel(const GemvParams p) {
   using C = GCfg<WT, MT>;
   constexpr int S = C::S;
+  constexpr int kComputeWarps = S;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -233,17 +237,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
     int64_t qs;
     int ns;
     plan.stage(j, qs, ns);
-    // Several warps consume the ring, so a warp may reach slot s before the
-    // slot's previous generation has landed; a parity wait cannot tell
-    // generation g from g - 2, so first wait until generation g - 1 of the
-    // slot has been released, then for generation g to land.
-    const int64_t g = j / S;
-    if (g > 0 && !mbar_wait(empty0 + 8 * s, static_cast<uint32_t>((g - 1) & 1), p.status,
-                            kStatusTimeoutMma)) {
-      ok = false;
-      break;
-    }
-    if (!mbar_wait(full0 + 8 * s, static_cast<uint32_t>(g & 1), p.status, kStatusTimeoutMma)) {
+    // slot s == warp: this warp consumed the slot's previous generation itself
+    if (!mbar_wait(full0 + 8 * s, static_cast<uint32_t>((j / S) & 1), p.status,
+                   kStatusTimeoutMma)) {
       ok = false;
       break;
     }
@@ -317,7 +313,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
   // published them right after streaming them.
   if (has_head) {
     const int64_t owner_stage = plan.n_tail_stages;
-    if (warp == static_cast<int>(owner_stage % kComputeWarps) && ok && lane < MT) {
+    if (warp == static_cast<int>(owner_stage % S) && ok && lane < MT) {
       if (spin_until_ge(p.flags + cta - 1, 1u, p.status)) {
 #pragma unroll
         for (int t = 0; t < MT; ++t) {
@@ -343,7 +339,7 @@ template <typename WT, int MT>
 cudaError_t launch(const GemvParams& p, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.G);
-  cfg.blockDim = dim3(kGemvThreads);
+  cfg.blockDim = dim3(GCfg<WT, MT>::kThreads);
   cfg.dynamicSmemBytes = GCfg<WT, MT>::kSmem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
