@@ -526,6 +526,41 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
+def run_shape(args):
+    """Run one layer at one token count a few times, each after the L2 flush
+    (a small, fixed launch sequence for profilers)."""
+    import torch
+    from gemv_projection_layers_gb300 import binding as B
+    layer, m = args.shape.split(":")
+    m = int(m)
+    B.load()
+    spec = wl.LAYER_BY_NAME[layer]
+    W = wl.make_weights(spec, 0)
+    if spec.weight_dtype == "fp32":
+        Wd, dt, odt, flags = torch.from_numpy(W).cuda(), B.PROJ_FP32, torch.float32, 0
+    else:
+        Wd = torch.from_numpy(W.view(np.int16)).cuda().view(torch.bfloat16)
+        dt, odt = B.PROJ_BF16, torch.bfloat16
+        flags = B.PROJ_ENCODE_EXPWIN12 if args.variant == "expwin12" else 0
+    h = B.proj_prepare_ex(spec.index, Wd, spec.N, spec.K, dt, flags, 1024)
+    x = torch.from_numpy(wl.make_activations(spec, m, 0).x_bits.view(np.int16)).cuda().view(
+        torch.bfloat16)
+    out = torch.empty((m, B.proj_out_features(h, m)), dtype=odt, device="cuda")
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    flush = torch.ones(l2 + 4096, dtype=torch.int32, device="cuda")
+    sink = torch.zeros(2 * B.proj_num_sms() + 8, dtype=torch.int32, device="cuda")
+    variant = {"auto": B.PROJ_VARIANT_AUTO, "dense": B.PROJ_VARIANT_DENSE,
+               "expwin12": B.PROJ_VARIANT_EXPWIN12}[args.variant]
+    for _ in range(args.steps):
+        B.proj_read_floor(flush, flush.numel() * 4, sink, 0, 0)
+        B.proj_run_ex(h, x, m, out, variant=variant)
+    torch.cuda.synchronize()
+    status = B.proj_device_status(h)
+    print(json.dumps({"shape": args.shape, "kernel": B.proj_describe(h, m), "launches": args.steps,
+                      "device_status": status}))
+    B.proj_destroy(h)
+
+
 def run_reference(args):
     """The oracle (CPU, FP64) timed on the same load; rank 0 only."""
     rank = int(os.environ.get("RANK", "0"))
@@ -570,10 +605,15 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--all-loads", action=argparse.BooleanOptionalAction, default=True,
                     help="also time the other five loads (reported under 'loads')")
+    ap.add_argument("--shape", default=None,
+                    help="layer:m -- only run that shape --steps times after a flush (profiling)")
+    ap.add_argument("--variant", choices=["auto", "dense", "expwin12"], default="auto")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.shape:
+        run_shape(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -48,7 +48,7 @@ struct GCfg {
   static constexpr int kChunkBytes = kChunkElems * static_cast<int>(sizeof(WT));
   static constexpr int kStageBytes = 8 * kChunkBytes;
   static constexpr int kVec = 16 / static_cast<int>(sizeof(WT));  // weights per 16 B
-  static constexpr int kXBytes = MT * 8192 * 2;                    // bf16 x, K <= 8192
+  static constexpr int kXBytes = MT * 8192 * 4;                    // fp32 x, K <= 8192
   static constexpr int kFit = (232448 - 1024 - kXBytes - 2048) / kStageBytes;
   static constexpr int S = kFit > 12 ? 12 : kFit;  // ring slots == compute warps
   static constexpr int kThreads = (S + 1) * 32;
@@ -82,12 +82,24 @@ __device__ __forceinline__ void bf16x2_to_f32(uint32_t w, float& lo, float& hi) 
   hi = __uint_as_float(w & 0xFFFF0000u);
 }
 
-// Lane partial of one chunk for MT tokens.  bf16 weights: lane loads 16 B
-// (8 weights) at (lane + 32 i) * 16, i < 4; fp32 weights: 16 B (4 weights),
-// i < 8.  x (bf16, smem) is read with the matching lane layout.
+// x in shared memory, fp32.  For bf16 weights a lane's 16-byte load i of a
+// chunk holds columns (lane + 32 i) * 8 + e, e < 8; x is stored permuted
+// inside each 256-column block so that the two matching 16-byte x loads are
+// contiguous across the warp: column k -> (k & ~255) | (e / 4) * 128 |
+// lane * 4 | e % 4.  For fp32 weights (4 columns per lane load) the natural
+// order already lines up.
+template <typename WT>
+__device__ __forceinline__ int x_slot(int k) {
+  if constexpr (sizeof(WT) == 2)
+    return (k & ~255) | ((k & 4) << 5) | (((k >> 3) & 31) << 2) | (k & 3);
+  else
+    return k;
+}
+
+// Lane partial of one chunk for MT tokens (col0: the chunk's first column).
 template <typename WT, int MT>
-__device__ __forceinline__ void chunk_partial(const uint8_t* chunk, const uint16_t* xs, int K,
-                                              int64_t col0, int lane, float (&acc)[MT]) {
+__device__ __forceinline__ void chunk_partial(const uint8_t* chunk, const float* xs, int K,
+                                              int col0, int lane, float (&acc)[MT]) {
   constexpr int VEC = GCfg<WT, MT>::kVec;
   constexpr int NI = 32 / VEC;
   float a4[MT][4];
@@ -112,21 +124,18 @@ __device__ __forceinline__ void chunk_partial(const uint8_t* chunk, const uint16
       wv[2] = __uint_as_float(wraw[i].z);
       wv[3] = __uint_as_float(wraw[i].w);
     }
-    const int64_t col = col0 + static_cast<int64_t>(lane + 32 * i) * VEC;
 #pragma unroll
     for (int t = 0; t < MT; ++t) {
       float xv[VEC];
-      const uint16_t* xp = xs + static_cast<int64_t>(t) * K + col;
       if constexpr (VEC == 8) {
-        const uint4 xr = *reinterpret_cast<const uint4*>(xp);
-        bf16x2_to_f32(xr.x, xv[0], xv[1]);
-        bf16x2_to_f32(xr.y, xv[2], xv[3]);
-        bf16x2_to_f32(xr.z, xv[4], xv[5]);
-        bf16x2_to_f32(xr.w, xv[6], xv[7]);
+        const float* xb = xs + t * K + col0 + i * 256 + lane * 4;
+        const float4 lo = *reinterpret_cast<const float4*>(xb);
+        const float4 hi = *reinterpret_cast<const float4*>(xb + 128);
+        xv[0] = lo.x; xv[1] = lo.y; xv[2] = lo.z; xv[3] = lo.w;
+        xv[4] = hi.x; xv[5] = hi.y; xv[6] = hi.z; xv[7] = hi.w;
       } else {
-        const uint2 xr = *reinterpret_cast<const uint2*>(xp);
-        bf16x2_to_f32(xr.x, xv[0], xv[1]);
-        bf16x2_to_f32(xr.y, xv[2], xv[3]);
+        const float4 v = *reinterpret_cast<const float4*>(xs + t * K + col0 + (lane + 32 * i) * 4);
+        xv[0] = v.x; xv[1] = v.y; xv[2] = v.z; xv[3] = v.w;
       }
 #pragma unroll
       for (int e = 0; e < VEC; ++e) a4[t][i & 3] = fmaf(wv[e], xv[e], a4[t][i & 3]);
@@ -145,7 +154,7 @@ __global__ void __launch_bounds__(GCfg<WT, MT>::kThreads, 1) gemv_kernel(const G
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* ring = smem;
-  uint16_t* xs = reinterpret_cast<uint16_t*>(ring + static_cast<size_t>(S) * C::kStageBytes);
+  float* xs = reinterpret_cast<float*>(ring + static_cast<size_t>(S) * C::kStageBytes);
   float* split = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(xs) + C::kXBytes);
   uint32_t* split_cnt = reinterpret_cast<uint32_t*>(split + kSplitRing * 2 * MT);
   uint64_t* bars = reinterpret_cast<uint64_t*>(split_cnt + kSplitRing);
@@ -209,13 +218,20 @@ __global__ void __launch_bounds__(GCfg<WT, MT>::kThreads, 1) gemv_kernel(const G
   // ----------------------------------------------------------- compute warps
   const int tid = threadIdx.x;  // 0..255
   {
-    // x -> shared memory (bf16, zero rows beyond m)
+    // x -> shared memory as fp32 in the lane layout (zero rows beyond m)
     const uint4* xg = static_cast<const uint4*>(p.x);
-    uint4* xd = reinterpret_cast<uint4*>(xs);
-    const int n16 = MT * p.K / 8;
-    for (int i = tid; i < n16; i += kComputeWarps * 32) {
+    const int n8 = MT * p.K / 8;  // groups of 8 columns
+    for (int i = tid; i < n8; i += kComputeWarps * 32) {
       const int t = i / (p.K / 8);
-      xd[i] = t < p.m ? xg[i] : make_uint4(0, 0, 0, 0);
+      const int k = (i % (p.K / 8)) * 8;
+      uint4 v = t < p.m ? xg[i] : make_uint4(0, 0, 0, 0);
+      float f[8];
+      bf16x2_to_f32(v.x, f[0], f[1]);
+      bf16x2_to_f32(v.y, f[2], f[3]);
+      bf16x2_to_f32(v.z, f[4], f[5]);
+      bf16x2_to_f32(v.w, f[6], f[7]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) xs[t * p.K + x_slot<WT>(k + e)] = f[e];
     }
   }
   named_bar_sync(1, kComputeWarps * 32);
@@ -254,10 +270,13 @@ __global__ void __launch_bounds__(GCfg<WT, MT>::kThreads, 1) gemv_kernel(const G
       float acc[MT];
 #pragma unroll
       for (int t = 0; t < MT; ++t) acc[t] = 0.f;
-      for (int64_t q = seg_lo; q < seg_hi; ++q) {
-        const int cc = static_cast<int>(q - qs);
-        chunk_partial<WT, MT>(stage + static_cast<size_t>(cc) * C::kChunkBytes, xs, p.K,
-                              (q - row * ks) * kChunkElems, lane, acc);
+      const int cc0 = static_cast<int>(seg_lo - qs);
+      const int cc1 = static_cast<int>(seg_hi - qs);
+      const int col_base = static_cast<int>(seg_lo - row * ks) * kChunkElems - cc0 * kChunkElems;
+#pragma unroll 2
+      for (int cc = cc0; cc < cc1; ++cc) {
+        chunk_partial<WT, MT>(stage + cc * C::kChunkBytes, xs, p.K, col_base + cc * kChunkElems,
+                              lane, acc);
       }
 #pragma unroll
       for (int t = 0; t < MT; ++t) {
