@@ -33,6 +33,8 @@
 //   off": in-CTA reduction beat cross-CTA split-K).
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "kernels.h"
 #include "ptx.cuh"
 #include "splitk.cuh"
@@ -48,7 +50,7 @@ struct GCfg {
   static constexpr int kChunkBytes = kChunkElems * static_cast<int>(sizeof(WT));
   static constexpr int kStageBytes = 8 * kChunkBytes;
   static constexpr int kVec = 16 / static_cast<int>(sizeof(WT));  // weights per 16 B
-  static constexpr int kXBytes = MT * 8192 * 4;                    // fp32 x, K <= 8192
+  static constexpr int kXBytes = MT * 8192 * static_cast<int>(sizeof(WT));  // x, K <= 8192
   static constexpr int kFit = (232448 - 1024 - kXBytes - 2048) / kStageBytes;
   static constexpr int S = kFit > 12 ? 12 : kFit;  // ring slots == compute warps
   static constexpr int kThreads = (S + 1) * 32;
@@ -82,67 +84,75 @@ __device__ __forceinline__ void bf16x2_to_f32(uint32_t w, float& lo, float& hi) 
   hi = __uint_as_float(w & 0xFFFF0000u);
 }
 
-// x in shared memory, fp32.  For bf16 weights a lane's 16-byte load i of a
-// chunk holds columns (lane + 32 i) * 8 + e, e < 8; x is stored permuted
-// inside each 256-column block so that the two matching 16-byte x loads are
-// contiguous across the warp: column k -> (k & ~255) | (e / 4) * 128 |
-// lane * 4 | e % 4.  For fp32 weights (4 columns per lane load) the natural
-// order already lines up.
-template <typename WT>
-__device__ __forceinline__ int x_slot(int k) {
-  if constexpr (sizeof(WT) == 2)
-    return (k & ~255) | ((k & 4) << 5) | (((k >> 3) & 31) << 2) | (k & 3);
-  else
-    return k;
+// x in shared memory, in the same lane layout as the weights: bf16 for bf16
+// weights (16-byte loads of 8 columns), fp32 for fp32 weights (16-byte loads
+// of 4 columns); a warp's loads are contiguous 512-byte runs (conflict-free).
+
+// acc += lo(w) * lo(x) and acc2 += hi(w) * hi(x): fp32 = bf16 * bf16 + fp32
+// (the product of two bf16 values is exact in fp32, so this equals widening
+// both operands and a single-precision FMA), one instruction per weight.
+__device__ __forceinline__ void fma_bf16x2(float& acc, float& acc2, uint32_t w, uint32_t x) {
+  asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\t"
+      "mov.b32 {wl, wh}, %2;\n\t"
+      "mov.b32 {xl, xh}, %3;\n\t"
+      "fma.rn.f32.bf16 %0, wl, xl, %0;\n\t"
+      "fma.rn.f32.bf16 %1, wh, xh, %1;\n\t}"
+      : "+f"(acc), "+f"(acc2)
+      : "r"(w), "r"(x));
 }
 
+// (acc, acc2) += (w0, w1) * (x0, x1), two fp32 FMAs in one instruction.
+__device__ __forceinline__ void fma_f32x2(float& acc, float& acc2, uint32_t w0, uint32_t w1,
+                                          float x0, float x1) {
+  uint64_t a = (static_cast<uint64_t>(__float_as_uint(acc2)) << 32) | __float_as_uint(acc);
+  const uint64_t w = (static_cast<uint64_t>(w1) << 32) | w0;
+  const uint64_t x = (static_cast<uint64_t>(__float_as_uint(x1)) << 32) | __float_as_uint(x0);
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a) : "l"(w), "l"(x));
+  acc = __uint_as_float(static_cast<uint32_t>(a));
+  acc2 = __uint_as_float(static_cast<uint32_t>(a >> 32));
+}
+
+template <typename WT>
+using XT = typename std::conditional<sizeof(WT) == 2, uint16_t, float>::type;
+
 // Lane partial of one chunk for MT tokens (col0: the chunk's first column).
+// Eight independent accumulation chains; combined in a fixed order.
 template <typename WT, int MT>
-__device__ __forceinline__ void chunk_partial(const uint8_t* chunk, const float* xs, int K,
+__device__ __forceinline__ void chunk_partial(const uint8_t* chunk, const XT<WT>* xs, int K,
                                               int col0, int lane, float (&acc)[MT]) {
   constexpr int VEC = GCfg<WT, MT>::kVec;
   constexpr int NI = 32 / VEC;
-  float a4[MT][4];
+  float a8[MT][8];
 #pragma unroll
   for (int t = 0; t < MT; ++t)
 #pragma unroll
-    for (int c = 0; c < 4; ++c) a4[t][c] = 0.f;
+    for (int c = 0; c < 8; ++c) a8[t][c] = 0.f;
   uint4 wraw[NI];
 #pragma unroll
   for (int i = 0; i < NI; ++i) wraw[i] = *reinterpret_cast<const uint4*>(chunk + (lane + 32 * i) * 16);
 #pragma unroll
   for (int i = 0; i < NI; ++i) {
-    float wv[VEC];
-    if constexpr (VEC == 8) {
-      bf16x2_to_f32(wraw[i].x, wv[0], wv[1]);
-      bf16x2_to_f32(wraw[i].y, wv[2], wv[3]);
-      bf16x2_to_f32(wraw[i].z, wv[4], wv[5]);
-      bf16x2_to_f32(wraw[i].w, wv[6], wv[7]);
-    } else {
-      wv[0] = __uint_as_float(wraw[i].x);
-      wv[1] = __uint_as_float(wraw[i].y);
-      wv[2] = __uint_as_float(wraw[i].z);
-      wv[3] = __uint_as_float(wraw[i].w);
-    }
 #pragma unroll
     for (int t = 0; t < MT; ++t) {
-      float xv[VEC];
+      const uint4 xv = *reinterpret_cast<const uint4*>(xs + t * K + col0 + (lane + 32 * i) * VEC);
+      float* a = a8[t];
       if constexpr (VEC == 8) {
-        const float* xb = xs + t * K + col0 + i * 256 + lane * 4;
-        const float4 lo = *reinterpret_cast<const float4*>(xb);
-        const float4 hi = *reinterpret_cast<const float4*>(xb + 128);
-        xv[0] = lo.x; xv[1] = lo.y; xv[2] = lo.z; xv[3] = lo.w;
-        xv[4] = hi.x; xv[5] = hi.y; xv[6] = hi.z; xv[7] = hi.w;
+        fma_bf16x2(a[(i & 1) * 4 + 0], a[(i & 1) * 4 + 1], wraw[i].x, xv.x);
+        fma_bf16x2(a[(i & 1) * 4 + 2], a[(i & 1) * 4 + 3], wraw[i].y, xv.y);
+        fma_bf16x2(a[(i & 1) * 4 + 0], a[(i & 1) * 4 + 1], wraw[i].z, xv.z);
+        fma_bf16x2(a[(i & 1) * 4 + 2], a[(i & 1) * 4 + 3], wraw[i].w, xv.w);
       } else {
-        const float4 v = *reinterpret_cast<const float4*>(xs + t * K + col0 + (lane + 32 * i) * 4);
-        xv[0] = v.x; xv[1] = v.y; xv[2] = v.z; xv[3] = v.w;
+        fma_f32x2(a[(i & 3) * 2 + 0], a[(i & 3) * 2 + 1], wraw[i].x, wraw[i].y,
+                  __uint_as_float(xv.x), __uint_as_float(xv.y));
+        fma_f32x2(a[(i & 3) * 2 + 0], a[(i & 3) * 2 + 1], wraw[i].z, wraw[i].w,
+                  __uint_as_float(xv.z), __uint_as_float(xv.w));
       }
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) a4[t][i & 3] = fmaf(wv[e], xv[e], a4[t][i & 3]);
     }
   }
 #pragma unroll
-  for (int t = 0; t < MT; ++t) acc[t] += (a4[t][0] + a4[t][1]) + (a4[t][2] + a4[t][3]);
+  for (int t = 0; t < MT; ++t)
+    acc[t] += ((a8[t][0] + a8[t][1]) + (a8[t][2] + a8[t][3])) +
+              ((a8[t][4] + a8[t][5]) + (a8[t][6] + a8[t][7]));
 }
 
 template <typename WT, int MT>
@@ -154,7 +164,7 @@ __global__ void __launch_bounds__(GCfg<WT, MT>::kThreads, 1) gemv_kernel(const G
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* ring = smem;
-  float* xs = reinterpret_cast<float*>(ring + static_cast<size_t>(S) * C::kStageBytes);
+  XT<WT>* xs = reinterpret_cast<XT<WT>*>(ring + static_cast<size_t>(S) * C::kStageBytes);
   float* split = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(xs) + C::kXBytes);
   uint32_t* split_cnt = reinterpret_cast<uint32_t*>(split + kSplitRing * 2 * MT);
   uint64_t* bars = reinterpret_cast<uint64_t*>(split_cnt + kSplitRing);
@@ -218,20 +228,24 @@ __global__ void __launch_bounds__(GCfg<WT, MT>::kThreads, 1) gemv_kernel(const G
   // ----------------------------------------------------------- compute warps
   const int tid = threadIdx.x;  // 0..255
   {
-    // x -> shared memory as fp32 in the lane layout (zero rows beyond m)
+    // x -> shared memory (bf16 as is, or widened to fp32 for fp32 weights;
+    // zero rows beyond m)
     const uint4* xg = static_cast<const uint4*>(p.x);
     const int n8 = MT * p.K / 8;  // groups of 8 columns
     for (int i = tid; i < n8; i += kComputeWarps * 32) {
       const int t = i / (p.K / 8);
-      const int k = (i % (p.K / 8)) * 8;
-      uint4 v = t < p.m ? xg[i] : make_uint4(0, 0, 0, 0);
-      float f[8];
-      bf16x2_to_f32(v.x, f[0], f[1]);
-      bf16x2_to_f32(v.y, f[2], f[3]);
-      bf16x2_to_f32(v.z, f[4], f[5]);
-      bf16x2_to_f32(v.w, f[6], f[7]);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) xs[t * p.K + x_slot<WT>(k + e)] = f[e];
+      const uint4 v = t < p.m ? xg[i] : make_uint4(0, 0, 0, 0);
+      if constexpr (sizeof(WT) == 2) {
+        reinterpret_cast<uint4*>(xs)[i] = v;
+      } else {
+        float4 a, b;
+        bf16x2_to_f32(v.x, a.x, a.y);
+        bf16x2_to_f32(v.y, a.z, a.w);
+        bf16x2_to_f32(v.z, b.x, b.y);
+        bf16x2_to_f32(v.w, b.z, b.w);
+        reinterpret_cast<float4*>(xs)[2 * i] = a;
+        reinterpret_cast<float4*>(xs)[2 * i + 1] = b;
+      }
     }
   }
   named_bar_sync(1, kComputeWarps * 32);
@@ -254,8 +268,8 @@ __global__ void __launch_bounds__(GCfg<WT, MT>::kThreads, 1) gemv_kernel(const G
     int ns;
     plan.stage(j, qs, ns);
     // slot s == warp: this warp consumed the slot's previous generation itself
-    if (!mbar_wait(full0 + 8 * s, static_cast<uint32_t>((j / S) & 1), p.status,
-                   kStatusTimeoutMma)) {
+    if (!mbar_wait_sleep(full0 + 8 * s, static_cast<uint32_t>((j / S) & 1), p.status,
+                         kStatusTimeoutMma)) {
       ok = false;
       break;
     }
