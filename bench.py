@@ -180,6 +180,12 @@ class LoadGraph:
         with torch.cuda.graph(self.plain, stream=stream):
             for S in shapes:
                 B.proj_run(S.h, S.x, S.m, S.out, stream)
+        self.single = []
+        for S in shapes:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                B.proj_run(S.h, S.x, S.m, S.out, stream)
+            self.single.append(g)
         self.inner = _external_events_supported(torch)
         n = len(shapes)
         if self.inner:
@@ -225,6 +231,25 @@ class LoadGraph:
         if breakdown:
             per = [self.ev[i].elapsed_time(self.ev[i + 1]) * 1e3 for i in range(len(self.shapes))]
         return a.elapsed_time(b) * 1e3, per
+
+
+def time_single_layers(B, torch, lg, flush, sink, reps):
+    """Each layer's one-kernel graph, timed like the read floor (flush, event,
+    replay, event); mean microseconds per layer."""
+    s = lg.stream
+    res = []
+    for g in lg.single:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(reps)]
+        with torch.cuda.stream(s):
+            for a, b in evs:
+                B.proj_read_floor(flush, flush.numel() * 4, sink, 0, 0, s)
+                a.record(s)
+                g.replay()
+                b.record(s)
+        s.synchronize()
+        res.append(float(np.mean([a.elapsed_time(b) * 1e3 for a, b in evs])))
+    return res
 
 
 def time_load(B, torch, lg, flush, sink, steps, breakdown=False):
@@ -507,10 +532,14 @@ def run_ours(args):
         ov = time_empty_graph(B, torch, flush, sink, stream, 50)
         result["read_floor_us"] = {k: round(floors[v], 3) for k, v in wb.items()}
         result["empty_graph_us"] = round(ov, 3)
-        if lg.inner:
-            # kernel-only layer times vs the read kernel net of its replay cost
-            result["floor_fraction"] = {k: round(max(floors[wb[k]] - ov, 0.0) / float(u), 3)
-                                        for k, u in zip(wb, layer_us)}
+        single = time_single_layers(B, torch, lg, flush, sink, max(20, min(args.steps, 100)))
+        result["single_layer_graph_us"] = {S.spec.name: round(u, 3)
+                                           for S, u in zip(lg.shapes, single)}
+        # same method for both (one-kernel graph, cold L2), net of the replay
+        # cost of a graph holding one empty-ish kernel
+        result["floor_fraction_net"] = {
+            S.spec.name: round(max(floors[wb[S.spec.name]] - ov, 0.0) / max(u - ov, 1e-3), 3)
+            for S, u in zip(lg.shapes, single)}
         result["direct_launch_us"] = {S.spec.name: round(time_direct_kernel(
             B, torch, S, flush, sink, stream, 20), 3) for S in lg.shapes}
         cb_us, cores, n = cpu_baseline(m, budget_s=args.cpu_seconds)

@@ -353,12 +353,9 @@ __global__ void __launch_bounds__(Cfg<BN, EXPWIN>::kThreads, 1)
           if (etid == 0) p.counters[sg.tile] = 0u;
         } else {
           // The barrier orders the warps' partial stores before thread 0's
-          // fence and release, which publishes them with one arrival.
+          // release (cumulative), which publishes them with one arrival.
           named_bar_sync(1, 128);
-          if (etid == 0) {
-            __threadfence();
-            red_release_gpu_add(p.counters + sg.tile, 1u);
-          }
+          if (etid == 0) red_release_gpu_add(p.counters + sg.tile, 1u);
           if (!owner_mode) pend[npend++] = sg.tile;
         }
       }

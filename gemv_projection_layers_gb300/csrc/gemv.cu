@@ -262,6 +262,7 @@ __global__ void __launch_bounds__(GCfg<WT, MT>::kThreads, 1) gemv_kernel(const G
 #pragma unroll
   for (int t = 0; t < MT; ++t) head_val[t] = 0.f;
   bool ok = true;
+  bool publish_tail = false;
   for (int64_t j = warp; j < n_stages; j += kComputeWarps) {
     const int s = static_cast<int>(j % S);
     int64_t qs;
@@ -302,14 +303,11 @@ __global__ void __launch_bounds__(GCfg<WT, MT>::kThreads, 1) gemv_kernel(const G
 #pragma unroll
         for (int t = 0; t < MT; ++t) head_val[t] = acc[t];  // all of it lies in one stage
       } else if (has_tail && row == tail_row) {
+        // published below, after the stage is released
 #pragma unroll
         for (int t = 0; t < MT; ++t)
           if (lane == t) p.ws[cta * MT + t] = acc[t];
-        __syncwarp();
-        if (lane == 0) {
-          __threadfence();
-          red_release_gpu_add(p.flags + cta, 1u);
-        }
+        publish_tail = true;
       } else if (whole_here) {
 #pragma unroll
         for (int t = 0; t < MT; ++t)
@@ -340,6 +338,12 @@ __global__ void __launch_bounds__(GCfg<WT, MT>::kThreads, 1) gemv_kernel(const G
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * s);
+    if (publish_tail) {
+      // the lanes' partial stores, ordered by the warp barrier above, are
+      // published by one release (cumulative)
+      if (lane == 0) red_release_gpu_add(p.flags + cta, 1u);
+      publish_tail = false;
+    }
   }
   // The head row: its upper slices were reduced by the warp that owns the
   // first main stage; its lower slices come from the previous CTA, which

@@ -220,12 +220,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0) p.counters[tile] = 0u;
       } else {
         // the barrier orders every thread's partial stores before thread 0's
-        // fence and release (one arrival per CTA)
+        // release (cumulative; one arrival per CTA)
         __syncthreads();
-        if (tid == 0) {
-          __threadfence();
-          red_release_gpu_add(p.counters + tile, 1u);
-        }
+        if (tid == 0) red_release_gpu_add(p.counters + tile, 1u);
         if (!owner_mode) pend[npend++] = tile;
       }
     }
