@@ -118,11 +118,29 @@ constexpr int64_t kTcOwnerMaxM = 8;
 constexpr int64_t kRouterOwnerMaxM = 4;
 
 constexpr int64_t kGemvMaxM = 2;
+// Wide token tiles go to the cluster split-K kernel.
+constexpr int64_t kClusterMinM = 33;
+
+int bn_for_cluster(int64_t m) { return m <= 64 ? 64 : (m <= 128 ? 128 : 256); }
+
+// Largest cluster size (K split) that keeps every cluster of the grid
+// resident in one wave on no more CTAs than SMs.  max_active[cs - 1] is the
+// occupancy query's count of co-resident clusters of cs CTAs.
+int pick_cluster(int64_t tiles, int KB, int sms, const int max_active[8]) {
+  int best = 1;
+  for (int cs = 2; cs <= 8; ++cs) {
+    if (cs > KB || tiles * cs > sms) break;
+    if (max_active[cs - 1] > 0 && tiles > max_active[cs - 1]) continue;
+    best = cs;
+  }
+  return best;
+}
 
 int mt_for_gemv(int64_t m) { return m <= 1 ? 1 : 2; }
 
 struct Plan {
   bool gemv;
+  bool cluster;
   bool router;
   bool expwin;
   int reduce;   // 0 owner, 1 distributed
@@ -143,6 +161,7 @@ struct proj_ctx {
   void* w_rows = nullptr;          // row-major copy for the streaming GEMV
   uint32_t* gemv_flags = nullptr;  // [num_sms], zero between calls
   float* gemv_ws = nullptr;        // [num_sms][2]
+  int cluster_active[3][8] = {};   // co-resident clusters: BN 64/128/256 x size 1..8
   uint8_t* w_exp = nullptr;
   size_t w_exp_bytes = 0;
   int e0 = 0;
@@ -206,7 +225,8 @@ int64_t out_rows(const proj_ctx* h, int64_t m) {
 int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl) {
   const int variant = opts ? opts->variant : PROJ_VARIANT_AUTO;
   const int kern = opts ? opts->kernel : PROJ_KERNEL_AUTO;
-  if (kern < PROJ_KERNEL_AUTO || kern > PROJ_KERNEL_TILE) return PROJ_EINVAL;
+  if (kern < PROJ_KERNEL_AUTO || kern > PROJ_KERNEL_CLUSTER) return PROJ_EINVAL;
+  if (variant < PROJ_VARIANT_AUTO || variant > PROJ_VARIANT_EXPWIN12) return PROJ_EINVAL;
   pl->router = (h->layer == PROJ_ROUTER);
   pl->n_out = out_rows(h, m);
   // Streaming GEMV: small m, uncompressed weights.
@@ -224,6 +244,33 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
     return PROJ_OK;
   }
   pl->gemv = false;
+  pl->cluster = false;
+  // The dispatch table sends wide token tiles to the cluster kernel; an
+  // explicit grid or reduction mode names the global-memory split-K kernel.
+  const bool auto_cluster = kern == PROJ_KERNEL_AUTO && m >= kClusterMinM &&
+                            (!opts || (opts->grid == 0 && opts->reduce == PROJ_REDUCE_AUTO));
+  if (kern == PROJ_KERNEL_CLUSTER && (pl->router || variant == PROJ_VARIANT_EXPWIN12))
+    return PROJ_EUNSUPPORTED;
+  if (!pl->router && variant != PROJ_VARIANT_EXPWIN12 &&
+      (kern == PROJ_KERNEL_CLUSTER || auto_cluster)) {
+    pl->cluster = true;
+    pl->expwin = false;
+    pl->reduce = 0;
+    pl->bn = bn_for_cluster(m);
+    pl->T = static_cast<int>(pl->n_out / kTileRows);
+    pl->KB = static_cast<int>(h->K / kTileK);
+    pl->MT = static_cast<int>((m + pl->bn - 1) / pl->bn);
+    const int bi = pl->bn == 64 ? 0 : (pl->bn == 128 ? 1 : 2);
+    int cs = pick_cluster(static_cast<int64_t>(pl->MT) * pl->T, pl->KB, h->num_sms,
+                          h->cluster_active[bi]);
+    if (opts && opts->grid > 0) {
+      cs = opts->grid;
+      if (cs > 8) return PROJ_EINVAL;
+      if (cs > pl->KB) return PROJ_EUNSUPPORTED;
+    }
+    pl->G = cs;  // cluster size
+    return PROJ_OK;
+  }
   if (pl->router) {
     if (variant == PROJ_VARIANT_EXPWIN12) return PROJ_EUNSUPPORTED;
     pl->expwin = false;
@@ -351,6 +398,12 @@ proj_handle proj_prepare_ex(int layer, const void* W, int64_t N, int64_t K, int 
   if ((e = tc_init_attributes()) != cudaSuccess) return bail_cuda(e, "tc attributes");
   if ((e = router_init_attributes()) != cudaSuccess) return bail_cuda(e, "router attributes");
   if ((e = gemv_init_attributes()) != cudaSuccess) return bail_cuda(e, "gemv attributes");
+  if ((e = cluster_init_attributes()) != cudaSuccess) return bail_cuda(e, "cluster attributes");
+  {
+    const int bns[3] = {64, 128, 256};
+    for (int b = 0; b < 3; ++b)
+      for (int c = 0; c < 8; ++c) h->cluster_active[b][c] = cluster_max_active(bns[b], c + 1);
+  }
   if (!encode_fn()) return bail_cuda(cudaErrorNotSupported, "cuTensorMapEncodeTiled");
 
   cudaStream_t s;
@@ -509,6 +562,21 @@ int proj_run_ex(proj_handle h, const void* x, int64_t m, void* out, proj_stream 
   }
   const CUtensorMap* map = get_map(h, x, m, pl.bn, !pl.router);
   if (!map) return fail_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(x)");
+  if (pl.cluster) {
+    ClusterParams c;
+    c.w = h->w_dense;
+    c.out = out;
+    c.status = h->status;
+    c.m = static_cast<int>(m);
+    c.n_out = static_cast<int>(pl.n_out);
+    c.T = pl.T;
+    c.KB = pl.KB;
+    c.MT = pl.MT;
+    c.CS = pl.G;
+    e = cluster_launch(pl.bn, *map, c, s);
+    if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
+    return PROJ_OK;
+  }
   if (pl.router) {
     RouterParams p;
     p.w = h->w_dense;
@@ -595,6 +663,10 @@ int proj_describe(proj_handle h, int64_t m, char* buf, size_t cap) {
   if (pl.gemv) {
     std::snprintf(buf, cap, "gemv_%s MT=%d G=%d n_rows=%lld", pl.router ? "f32w" : "bf16w", pl.bn,
                   pl.G, static_cast<long long>(pl.n_out));
+  } else if (pl.cluster) {
+    std::snprintf(buf, cap, "tc_cluster BN=%d stages=%d CS=%d CTAs=%d T=%d KB=%d MT=%d n_out=%lld",
+                  pl.bn, cluster_stages(pl.bn), pl.G, pl.MT * pl.T * pl.G, pl.T, pl.KB, pl.MT,
+                  static_cast<long long>(pl.n_out));
   } else if (pl.router) {
     std::snprintf(buf, cap, "router_fma TM=%d stages=8 G=%d T=%d KB=%d MT=%d reduce=%s", pl.bn,
                   pl.G, pl.T, pl.KB, pl.MT, pl.reduce ? "distributed" : "owner");

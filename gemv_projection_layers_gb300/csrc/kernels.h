@@ -102,6 +102,25 @@ cudaError_t tc_init_attributes();
 cudaError_t tc_launch(int BN, bool expwin, const CUtensorMap& tmap_x, const TcParams& p,
                       cudaStream_t s);
 
+// Cluster split-K tensor-core path (wide token tiles): BN in {64, 128, 256}.
+struct ClusterParams {
+  const uint8_t* w;     // packed tiles (same layout as TcParams::w)
+  void* out;            // bf16 [m, n_out]
+  uint32_t* status;
+  int m;
+  int n_out;
+  int T;                // n_out / 128
+  int KB;               // K / 64
+  int MT;               // ceil(m / BN)
+  int CS;               // cluster size = K split
+};
+bool cluster_supported(int BN);
+cudaError_t cluster_init_attributes();
+int cluster_max_active(int BN, int cs);
+int cluster_stages(int BN);
+cudaError_t cluster_launch(int BN, const CUtensorMap& tmap_x, const ClusterParams& p,
+                           cudaStream_t s);
+
 // Router FP32-FMA path: TM in {4, 8, 16, 32, 64}.
 bool router_supported(int TM);
 size_t router_smem_bytes(int TM);

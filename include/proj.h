@@ -106,12 +106,17 @@ enum proj_reduce {
 enum proj_kernel {
     PROJ_KERNEL_AUTO = 0,   /* the dispatch table's choice */
     PROJ_KERNEL_GEMV = 1,   /* row-streaming CUDA-core GEMV, m <= 2 */
-    PROJ_KERNEL_TILE = 2    /* tiled kernels: tensor cores (bf16) / FMA tiles (router) */
+    PROJ_KERNEL_TILE = 2,   /* tiled kernels: tensor cores (bf16) / FMA tiles (router),
+                               split-K across CTAs through global memory */
+    PROJ_KERNEL_CLUSTER = 3 /* bf16 layers, dense weights: tensor cores, split-K inside a
+                               thread-block cluster combined through distributed shared
+                               memory; proj_run_opts.grid then sets the cluster size (1..8) */
 };
 
 typedef struct proj_run_opts {
     int variant;    /* enum proj_variant */
-    int grid;       /* CTAs of the partition (1 .. SMs); 0 = dispatch table */
+    int grid;       /* CTAs of the partition (1 .. SMs), or the cluster size for
+                       PROJ_KERNEL_CLUSTER; 0 = dispatch table */
     int reduce;     /* enum proj_reduce (tiled kernels); owner needs m <= 32 on bf16 */
     int kernel;     /* enum proj_kernel */
 } proj_run_opts;

@@ -133,6 +133,38 @@ def test_split_partitions_and_determinism(dev, layer, m):
     assert B.proj_device_status(h) == 0
 
 
+@pytest.mark.parametrize("layer,m", [("o", 1), ("pooler", 16), ("o", 33), ("unpooler", 64),
+                                     ("qkv_gate", 130), ("pooler", 256), ("qkv_gate", 512),
+                                     ("o", 1000)])
+def test_cluster_sizes_and_determinism(dev, layer, m):
+    """The cluster split-K kernel at every cluster size (1..8 CTAs sharing K)
+    meets the contract and is bitwise reproducible."""
+    h, W, _ = prepared(layer, 0)
+    if m >= 33:
+        assert "tc_cluster" in B.proj_describe(h, m)
+    for cs in range(1, 9):
+        kw = dict(grid=cs, kernel=B.PROJ_KERNEL_CLUSTER)
+        a = check_case(layer, 0, True, m, h=h, W=W, **kw)
+        b = check_case(layer, 0, True, m, h=h, W=W, **kw)
+        assert np.array_equal(a, b), (layer, m, cs)
+    assert B.proj_device_status(h) == 0
+
+
+def test_cluster_kernel_rejections(dev):
+    h, _, _ = prepared("router", 0)
+    x = torch.zeros((64, 8192), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros((64, 256), dtype=torch.float32, device="cuda")
+    with pytest.raises(B.ProjError) as e:
+        B.proj_run_ex(h, x, 64, out, kernel=B.PROJ_KERNEL_CLUSTER)
+    assert e.value.status == B.PROJ_EUNSUPPORTED
+    h, _, _ = prepared("o", 0)
+    x = torch.zeros((64, 1024), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros((64, 8192), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(B.ProjError) as e:
+        B.proj_run_ex(h, x, 64, out, kernel=B.PROJ_KERNEL_CLUSTER, grid=9)
+    assert e.value.status == B.PROJ_EINVAL
+
+
 @pytest.mark.parametrize("layer", [s.name for s in wl.LAYERS])
 @pytest.mark.parametrize("m", [1, 2])
 def test_gemv_partitions_and_determinism(dev, layer, m):
