@@ -101,6 +101,8 @@ def load() -> ctypes.CDLL:
     lib.proj_read_floor.argtypes = [vp, i64, vp, i32, i32, vp]
     lib.proj_num_sms.restype = i32
     lib.proj_num_sms.argtypes = []
+    lib.proj_gemv_static.argtypes = [vp, i32, i64, i64, vp, i64, vp, vp]
+    lib.proj_gemv_static.restype = i32
     _lib = lib
     return lib
 
@@ -236,3 +238,12 @@ def proj_read_floor(buf, nbytes: int, sink, grid: int = 0, mode: int = 0, stream
 
 def proj_num_sms() -> int:
     return int(load().proj_num_sms())
+
+
+def proj_gemv_static(W, w_dtype: int, N: int, K: int, x, m: int, out, stream=None) -> None:
+    """Allocation-free GEMV (m <= 2) on caller-owned row-major weights; see
+    proj.h for the limits and for the shared static scratch."""
+    st = load().proj_gemv_static(_addr(W), int(w_dtype), int(N), int(K), _addr(x), int(m),
+                                 _addr(out), _stream(stream))
+    if st != PROJ_OK:
+        raise ProjError(st, f"proj_gemv_static ({last_cuda_error()})")

@@ -38,6 +38,18 @@ int fail_cuda(cudaError_t e, const char* what) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+}  // namespace
+
+// Error recording for entry points defined in other translation units.
+int proj::record_status(int status, const char* text) {
+  std::snprintf(g_last_cuda, sizeof g_last_cuda, "%s", text);
+  return fail(status);
+}
+
+int proj::record_cuda(cudaError_t e, const char* what) { return fail_cuda(e, what); }
+
+namespace {
+
 // ------------------------------------------------------------ layer table --
 struct LayerShape {
   int64_t N, K;

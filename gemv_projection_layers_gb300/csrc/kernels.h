@@ -91,6 +91,10 @@ struct GemvParams {
   int out_f32;
 };
 cudaError_t gemv_init_attributes();
+// Record a failing status (and its text) for proj_last_status /
+// proj_last_cuda_error; both return the status.
+int record_status(int status, const char* text);
+int record_cuda(cudaError_t e, const char* what);
 cudaError_t gemv_launch(bool f32w, int MT, const GemvParams& p, cudaStream_t s);
 
 // Tensor-core path: BN in {16, 32, 64, 128, 256}; expwin12 for BN in {16, 32}.

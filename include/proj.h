@@ -218,7 +218,8 @@ void proj_destroy(proj_handle h);
 /* Status of the last failing call on this thread, and its text. */
 int proj_last_status(void);
 const char *proj_status_string(int status);
-/* Last CUDA error string recorded on this thread ("" if none). */
+/* Last error text recorded on this thread: a CUDA error, or the reason an
+ * argument was rejected ("" if none). */
 const char *proj_last_cuda_error(void);
 
 /*
@@ -235,6 +236,49 @@ int proj_read_floor(const void *buf, int64_t bytes, void *sink, int grid, int mo
 
 /* Number of SMs of the current device (0 on error). */
 int proj_num_sms(void);
+
+/*
+ * Allocation-free GEMV for one or two tokens on caller-owned weights.
+ * The method's pages have no counterpart of this call: it exists for callers
+ * that may not allocate device memory -- a plugin or custom operator that a
+ * host framework hands only its input and output buffers while that
+ * framework's allocator owns the device memory, or latency-critical code
+ * that must not call cudaMalloc/cudaFree (they can stall the whole device and
+ * can fail at run time).  Such callers cannot use proj_prepare, which
+ * allocates repacked weights and a workspace.
+ *
+ *   out[i, n] = sum over k of x[i, k] * W[n, k],  0 <= i < m,  0 <= n < N
+ *
+ *   W       : device, row-major [N, K], contiguous, 16-byte aligned; any N >= 1.
+ *   w_dtype : PROJ_BF16 (out is bf16, fp32 sum rounded to nearest even) or
+ *             PROJ_FP32 (out is fp32).
+ *   K       : a multiple of 1024 in [1024, 8192].
+ *   x       : device, bf16 row-major [m, K], 16-byte aligned.
+ *   m       : 0, 1 or 2 (0 returns PROJ_OK and launches nothing).
+ *   out     : device, row-major [m, N], 16-byte aligned; every element written.
+ *
+ * The kernel is the streaming GEMV of proj_run at m <= 2 (same partition of
+ * W over min(SMs, N, 256) CTAs, same summation order).  Its scratch is a
+ * 4 KB static device array inside the library (hand-off flags, partial row
+ * sums and a status word for at most 256 CTAs); each device that loads the
+ * library holds it until the process exits.  Nothing is allocated by any
+ * call: the first call on a device (the current device when it is made) looks
+ * up the array's device address and sets the kernels' shared-memory limit, so
+ * make that first call before capturing any stream.  Every call then clears
+ * the flags and status word with an asynchronous memset on `stream` and
+ * launches one kernel.  All calls on a device share the one array, so calls
+ * that overlap on the GPU (different streams, or threads without ordering)
+ * race and give wrong results; serialise them.  A stall of the kernel's
+ * bounded waits is recorded only in that internal status word, which this
+ * call does not report.
+ *
+ * Returns PROJ_OK; PROJ_EINVAL for NULL pointers, N < 1, m < 0 or a bad
+ * w_dtype; PROJ_EUNSUPPORTED for m > 2 or K outside the rule above (the
+ * static scratch is sized for those limits); PROJ_EALIGN; PROJ_ECUDA.  The
+ * reason for a rejection is readable through proj_last_cuda_error().
+ */
+int proj_gemv_static(const void *W, int w_dtype, int64_t N, int64_t K, const void *x,
+                     int64_t m, void *out, proj_stream stream);
 
 #ifdef __cplusplus
 }

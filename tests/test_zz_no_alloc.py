@@ -1,0 +1,81 @@
+"""proj_gemv_static -- the entry point that allocates no device memory.
+
+It serves callers that may not allocate: a plugin or custom operator that a
+host framework hands only its input and output buffers (the framework's
+allocator owns the device memory), or latency-critical code that cannot
+afford cudaMalloc/cudaFree (they can stall the whole device and can fail at
+run time).  Its scratch is a small static array inside the library, shared
+by every call on a device.
+
+Each case calls it twice in a row on fresh inputs -- so the second call
+runs on the scratch the first one left behind -- and compares both outputs
+with proj_run's on the same inputs, under the same tolerance contract as the
+parity tests (relative L2, per-row bound, probe rows).  This file is named
+to be collected last; it passes alone in a fresh process and after the rest
+of the suite.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from gemv_projection_layers_gb300 import binding as B
+from gemv_projection_layers_gb300 import workloads as wl
+from oracle import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def _device_weights(spec, seed):
+    W = wl.make_weights(spec, seed)
+    if spec.weight_dtype == "fp32":
+        return torch.from_numpy(W).cuda(), B.PROJ_FP32, torch.float32
+    return (torch.from_numpy(W.view(np.int16)).cuda().view(torch.bfloat16), B.PROJ_BF16,
+            torch.bfloat16)
+
+
+@pytest.mark.parametrize("m", [1, 2])
+@pytest.mark.parametrize("layer", [s.name for s in wl.LAYERS])
+def test_static_scratch_gemv_matches_proj_run(layer, m):
+    assert torch.cuda.is_available()
+    B.load()
+    spec = wl.LAYER_BY_NAME[layer]
+    Wd, dt, odt = _device_weights(spec, 3)
+    h = B.proj_prepare_ex(spec.index, Wd, spec.N, spec.K, dt, 0, 16)
+    try:
+        n_out = B.proj_out_features(h, m)  # the unpooler computes its first 1024 rows
+        acts = [wl.make_activations(spec, m, seed, outliers=bool(seed % 2)) for seed in (5, 6)]
+        xs = [torch.from_numpy(a.x_bits.view(np.int16)).cuda().view(torch.bfloat16)
+              for a in acts]
+        got = [torch.full((m, n_out), float("nan"), dtype=odt, device="cuda") for _ in xs]
+        for x, o in zip(xs, got):  # two calls in a row
+            B.proj_gemv_static(Wd, dt, n_out, spec.K, x, m, o)
+        ref = [torch.full((m, n_out), float("nan"), dtype=odt, device="cuda") for _ in xs]
+        for x, o in zip(xs, ref):
+            B.proj_run(h, x, m, o)
+        torch.cuda.synchronize()
+        assert B.proj_device_status(h) == 0
+        for call, (a, g, r) in enumerate(zip(acts, got, ref)):
+            g64 = g.float().cpu().numpy().astype(np.float64)
+            r64 = r.float().cpu().numpy().astype(np.float64)
+            res = oracle.check(layer, g64, r64, a.probe_rows)
+            assert res["ok"], (layer, m, call, res)
+    finally:
+        B.proj_destroy(h)
+
+
+def test_static_scratch_gemv_rejects_sizes_beyond_its_limits():
+    assert torch.cuda.is_available()
+    B.load()
+    W = torch.zeros((64, 1024), dtype=torch.bfloat16, device="cuda")
+    x = torch.zeros((3, 1024), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros((3, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(B.ProjError) as e:
+        B.proj_gemv_static(W, B.PROJ_BF16, 64, 1024, x, 3, out)
+    assert e.value.status == B.PROJ_EUNSUPPORTED
+    assert "m > 2" in B.last_cuda_error()
+    for K in (1536, 16384):  # not a multiple of 1024; beyond the 8192 columns x staging holds
+        with pytest.raises(B.ProjError) as e:
+            B.proj_gemv_static(W, B.PROJ_BF16, 4, K, x, 1, out)
+        assert e.value.status == B.PROJ_EUNSUPPORTED
+        assert "K must be" in B.last_cuda_error()
