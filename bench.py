@@ -415,7 +415,7 @@ def run_ours(args):
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
     flush = torch.ones(l2 + 4096, dtype=torch.int32, device="cuda")  # 4x L2 bytes
     sink = torch.zeros(2 * B.proj_num_sms() + 8, dtype=torch.int32, device="cuda")
-    layers = setup_layers(B, torch, expwin=not args.dense)
+    layers = setup_layers(B, torch, expwin=False)
 
     loads = [args.load] + ([n for n, _ in wl.LOADS if n != args.load] if args.all_loads else [])
     graphs = {}
@@ -481,8 +481,7 @@ def run_ours(args):
                       "around each replay (includes one graph launch); per-layer = a second "
                       "pass with event nodes between the kernels" + (
                           "" if lg.inner else " (here: per-layer graphs)"),
-            "weights": "dense bf16" if args.dense else "12-bit exponent-window for bf16 "
-                                                       "layers at m<=16, dense otherwise",
+            "weights": "dense bf16; router fp32 (from m = 3 read as three exact bf16 planes)",
             "parallelism": f"replicas x{world}",
         },
         "median_us": round(float(np.median(outer)), 3),
@@ -629,7 +628,6 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--load", choices=[n for n, _ in wl.LOADS], default=HEADLINE_LOAD)
-    ap.add_argument("--dense", action="store_true", help="no 12-bit weights")
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--all-loads", action=argparse.BooleanOptionalAction, default=True,

@@ -23,7 +23,7 @@ PROJ_BF16, PROJ_FP32 = 0, 1
 PROJ_ENCODE_EXPWIN12 = 1
 (PROJ_OK, PROJ_EINVAL, PROJ_EUNSUPPORTED, PROJ_EALIGN, PROJ_ENOMEM, PROJ_ECUDA,
  PROJ_EDEVICE) = range(7)
-PROJ_VARIANT_AUTO, PROJ_VARIANT_DENSE, PROJ_VARIANT_EXPWIN12 = range(3)
+PROJ_VARIANT_AUTO, PROJ_VARIANT_DENSE, PROJ_VARIANT_EXPWIN12, PROJ_VARIANT_PLANES3 = range(4)
 PROJ_REDUCE_AUTO, PROJ_REDUCE_OWNER, PROJ_REDUCE_DISTRIBUTED = range(3)
 PROJ_KERNEL_AUTO, PROJ_KERNEL_GEMV, PROJ_KERNEL_TILE, PROJ_KERNEL_CLUSTER = range(4)
 

@@ -130,17 +130,25 @@ constexpr int64_t kTcOwnerMaxM = 8;
 constexpr int64_t kRouterOwnerMaxM = 4;
 
 constexpr int64_t kGemvMaxM = 2;
-// Wide token tiles go to the cluster split-K kernel.
-constexpr int64_t kClusterMinM = 33;
+// From three tokens on every layer goes to the cluster split-K kernel (the
+// router as three bf16 planes of its fp32 weights); below that, the GEMV.
+constexpr int64_t kClusterMinM = 3;
+constexpr int64_t kRouterClusterMinM = 3;
 
-int bn_for_cluster(int64_t m) { return m <= 64 ? 64 : (m <= 128 ? 128 : 256); }
+int bn_for_cluster(int64_t m) {
+  if (m <= 16) return 16;
+  if (m <= 32) return 32;
+  if (m <= 64) return 64;
+  return m <= 128 ? 128 : 256;
+}
+int bn_index(int bn) { return bn == 16 ? 0 : bn == 32 ? 1 : bn == 64 ? 2 : bn == 128 ? 3 : 4; }
 
 // Largest cluster size (K split) that keeps every cluster of the grid
 // resident in one wave on no more CTAs than SMs.  max_active[cs - 1] is the
 // occupancy query's count of co-resident clusters of cs CTAs.
-int pick_cluster(int64_t tiles, int KB, int sms, const int max_active[8]) {
+int pick_cluster(int64_t tiles, int KB, int sms, const int max_active[kClusterMaxCS]) {
   int best = 1;
-  for (int cs = 2; cs <= 8; ++cs) {
+  for (int cs = 2; cs <= kClusterMaxCS; ++cs) {
     if (cs > KB || tiles * cs > sms) break;
     if (max_active[cs - 1] > 0 && tiles > max_active[cs - 1]) continue;
     best = cs;
@@ -173,7 +181,8 @@ struct proj_ctx {
   void* w_rows = nullptr;          // row-major copy for the streaming GEMV
   uint32_t* gemv_flags = nullptr;  // [num_sms], zero between calls
   float* gemv_ws = nullptr;        // [num_sms][2]
-  int cluster_active[3][8] = {};   // co-resident clusters: BN 64/128/256 x size 1..8
+  uint8_t* w_planes = nullptr;     // router: bf16 planes hi/mid/lo as [N, 3K] tiles
+  int cluster_active[5][kClusterMaxCS] = {};  // co-resident clusters: BN 16..256 x size 1..16
   uint8_t* w_exp = nullptr;
   size_t w_exp_bytes = 0;
   int e0 = 0;
@@ -201,6 +210,7 @@ namespace {
 void free_ctx(proj_ctx* h) {
   if (!h) return;
   cudaFree(h->w_dense);
+  cudaFree(h->w_planes);
   cudaFree(h->w_rows);
   cudaFree(h->gemv_flags);
   cudaFree(h->gemv_ws);
@@ -238,11 +248,12 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
   const int variant = opts ? opts->variant : PROJ_VARIANT_AUTO;
   const int kern = opts ? opts->kernel : PROJ_KERNEL_AUTO;
   if (kern < PROJ_KERNEL_AUTO || kern > PROJ_KERNEL_CLUSTER) return PROJ_EINVAL;
-  if (variant < PROJ_VARIANT_AUTO || variant > PROJ_VARIANT_EXPWIN12) return PROJ_EINVAL;
+  if (variant < PROJ_VARIANT_AUTO || variant > PROJ_VARIANT_PLANES3) return PROJ_EINVAL;
   pl->router = (h->layer == PROJ_ROUTER);
   pl->n_out = out_rows(h, m);
   // Streaming GEMV: small m, uncompressed weights.
-  const bool gemv_ok = m <= kGemvMaxM && variant != PROJ_VARIANT_EXPWIN12;
+  const bool gemv_ok =
+      m <= kGemvMaxM && (variant == PROJ_VARIANT_AUTO || variant == PROJ_VARIANT_DENSE);
   if (kern == PROJ_KERNEL_GEMV && !gemv_ok) return PROJ_EUNSUPPORTED;
   if (gemv_ok && kern != PROJ_KERNEL_TILE) {
     pl->gemv = true;
@@ -259,32 +270,48 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
   pl->cluster = false;
   // The dispatch table sends wide token tiles to the cluster kernel; an
   // explicit grid or reduction mode names the global-memory split-K kernel.
-  const bool auto_cluster = kern == PROJ_KERNEL_AUTO && m >= kClusterMinM &&
+  const bool auto_cluster = kern == PROJ_KERNEL_AUTO &&
+                            m >= (pl->router ? kRouterClusterMinM : kClusterMinM) &&
                             (!opts || (opts->grid == 0 && opts->reduce == PROJ_REDUCE_AUTO));
-  if (kern == PROJ_KERNEL_CLUSTER && (pl->router || variant == PROJ_VARIANT_EXPWIN12))
-    return PROJ_EUNSUPPORTED;
-  if (!pl->router && variant != PROJ_VARIANT_EXPWIN12 &&
-      (kern == PROJ_KERNEL_CLUSTER || auto_cluster)) {
+  bool want_cluster;
+  if (pl->router) {
+    // The cluster kernel runs the router on its bf16 planes only.
+    if (variant == PROJ_VARIANT_PLANES3) {
+      if (kern != PROJ_KERNEL_AUTO && kern != PROJ_KERNEL_CLUSTER) return PROJ_EUNSUPPORTED;
+      want_cluster = true;
+    } else if (kern == PROJ_KERNEL_CLUSTER) {
+      if (variant != PROJ_VARIANT_AUTO) return PROJ_EUNSUPPORTED;
+      want_cluster = true;
+    } else {
+      want_cluster = auto_cluster && variant == PROJ_VARIANT_AUTO;
+    }
+  } else {
+    if (variant == PROJ_VARIANT_PLANES3) return PROJ_EUNSUPPORTED;
+    if (kern == PROJ_KERNEL_CLUSTER && variant == PROJ_VARIANT_EXPWIN12) return PROJ_EUNSUPPORTED;
+    want_cluster =
+        variant != PROJ_VARIANT_EXPWIN12 && (kern == PROJ_KERNEL_CLUSTER || auto_cluster);
+  }
+  if (want_cluster) {
     pl->cluster = true;
     pl->expwin = false;
     pl->reduce = 0;
     pl->bn = bn_for_cluster(m);
     pl->T = static_cast<int>(pl->n_out / kTileRows);
-    pl->KB = static_cast<int>(h->K / kTileK);
+    pl->KB = static_cast<int>(h->K / kTileK) * (pl->router ? 3 : 1);
     pl->MT = static_cast<int>((m + pl->bn - 1) / pl->bn);
-    const int bi = pl->bn == 64 ? 0 : (pl->bn == 128 ? 1 : 2);
     int cs = pick_cluster(static_cast<int64_t>(pl->MT) * pl->T, pl->KB, h->num_sms,
-                          h->cluster_active[bi]);
+                          h->cluster_active[bn_index(pl->bn)]);
     if (opts && opts->grid > 0) {
       cs = opts->grid;
-      if (cs > 8) return PROJ_EINVAL;
+      if (cs > kClusterMaxCS) return PROJ_EINVAL;
       if (cs > pl->KB) return PROJ_EUNSUPPORTED;
     }
     pl->G = cs;  // cluster size
     return PROJ_OK;
   }
   if (pl->router) {
-    if (variant == PROJ_VARIANT_EXPWIN12) return PROJ_EUNSUPPORTED;
+    if (variant == PROJ_VARIANT_EXPWIN12 || variant == PROJ_VARIANT_PLANES3)
+      return PROJ_EUNSUPPORTED;
     pl->expwin = false;
     pl->bn = tm_for_m(m);
     pl->T = static_cast<int>(h->N / kRtRows);
@@ -412,9 +439,10 @@ proj_handle proj_prepare_ex(int layer, const void* W, int64_t N, int64_t K, int 
   if ((e = gemv_init_attributes()) != cudaSuccess) return bail_cuda(e, "gemv attributes");
   if ((e = cluster_init_attributes()) != cudaSuccess) return bail_cuda(e, "cluster attributes");
   {
-    const int bns[3] = {64, 128, 256};
-    for (int b = 0; b < 3; ++b)
-      for (int c = 0; c < 8; ++c) h->cluster_active[b][c] = cluster_max_active(bns[b], c + 1);
+    const int bns[5] = {16, 32, 64, 128, 256};
+    for (int b = 0; b < 5; ++b)
+      for (int c = 0; c < kClusterMaxCS; ++c)
+        h->cluster_active[b][c] = cluster_max_active(bns[b], c + 1);
   }
   if (!encode_fn()) return bail_cuda(cudaErrorNotSupported, "cuTensorMapEncodeTiled");
 
@@ -434,6 +462,15 @@ proj_handle proj_prepare_ex(int layer, const void* W, int64_t N, int64_t K, int 
                                static_cast<int>(K), h->w_dense, s)) != cudaSuccess) {
       done();
       return bail_cuda(e, "pack router");
+    }
+    if ((e = dmalloc(&h->w_planes, static_cast<size_t>(N) * K * 6)) != cudaSuccess) {
+      done();
+      return bail_cuda(e, "cudaMalloc(weight planes)");
+    }
+    if ((e = pack_router_planes(static_cast<const float*>(W), static_cast<int>(N),
+                                static_cast<int>(K), h->w_planes, s)) != cudaSuccess) {
+      done();
+      return bail_cuda(e, "pack router planes");
     }
     const int tm_max = tm_for_m(std::min<int64_t>(m_max, 64));
     h->ws_bytes = static_cast<size_t>(2 * sms) * 64 * tm_max * 4;
@@ -572,11 +609,13 @@ int proj_run_ex(proj_handle h, const void* x, int64_t m, void* out, proj_stream 
     if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
     return PROJ_OK;
   }
-  const CUtensorMap* map = get_map(h, x, m, pl.bn, !pl.router);
+  const CUtensorMap* map = get_map(h, x, m, pl.bn, pl.cluster || !pl.router);
   if (!map) return fail_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(x)");
   if (pl.cluster) {
     ClusterParams c;
-    c.w = h->w_dense;
+    c.w = pl.router ? h->w_planes : h->w_dense;
+    c.KBx = static_cast<int>(h->K / kTileK);
+    c.out_f32 = pl.router ? 1 : 0;
     c.out = out;
     c.status = h->status;
     c.m = static_cast<int>(m);
@@ -676,9 +715,12 @@ int proj_describe(proj_handle h, int64_t m, char* buf, size_t cap) {
     std::snprintf(buf, cap, "gemv_%s MT=%d G=%d n_rows=%lld", pl.router ? "f32w" : "bf16w", pl.bn,
                   pl.G, static_cast<long long>(pl.n_out));
   } else if (pl.cluster) {
-    std::snprintf(buf, cap, "tc_cluster BN=%d stages=%d CS=%d CTAs=%d T=%d KB=%d MT=%d n_out=%lld",
-                  pl.bn, cluster_stages(pl.bn), pl.G, pl.MT * pl.T * pl.G, pl.T, pl.KB, pl.MT,
-                  static_cast<long long>(pl.n_out));
+    std::snprintf(buf, cap,
+                  "tc_cluster%s BN=%d stages=%d CS=%d CTAs=%d T=%d KB=%d MT=%d n_out=%lld "
+                  "resident_clusters=%d",
+                  pl.router ? "_planes3" : "", pl.bn, cluster_stages(pl.bn), pl.G,
+                  pl.MT * pl.T * pl.G, pl.T, pl.KB, pl.MT, static_cast<long long>(pl.n_out),
+                  h->cluster_active[bn_index(pl.bn)][pl.G - 1]);
   } else if (pl.router) {
     std::snprintf(buf, cap, "router_fma TM=%d stages=8 G=%d T=%d KB=%d MT=%d reduce=%s", pl.bn,
                   pl.G, pl.T, pl.KB, pl.MT, pl.reduce ? "distributed" : "owner");
@@ -698,8 +740,14 @@ int proj_unpack_weights(proj_handle h, int variant, void* W_out, proj_stream str
   cudaError_t e;
   if (h->layer == PROJ_ROUTER) {
     if (variant == PROJ_VARIANT_EXPWIN12) return fail(PROJ_EUNSUPPORTED);
-    e = unpack_router_tiles(h->w_dense, static_cast<int>(h->N), static_cast<int>(h->K),
-                            static_cast<float*>(W_out), s);
+    if (variant == PROJ_VARIANT_PLANES3)
+      e = unpack_router_planes(h->w_planes, static_cast<int>(h->N), static_cast<int>(h->K),
+                               static_cast<float*>(W_out), s);
+    else
+      e = unpack_router_tiles(h->w_dense, static_cast<int>(h->N), static_cast<int>(h->K),
+                              static_cast<float*>(W_out), s);
+  } else if (variant == PROJ_VARIANT_PLANES3) {
+    return fail(PROJ_EUNSUPPORTED);
   } else if (variant == PROJ_VARIANT_EXPWIN12 ||
              (variant == PROJ_VARIANT_AUTO && h->w_exp != nullptr)) {
     if (!h->w_exp) return fail(PROJ_EUNSUPPORTED);

@@ -1,6 +1,6 @@
-// gemm_cluster.cu -- tensor-core GEMM for wide token tiles (m >= 33):
-// split-K inside a thread-block cluster, combined through distributed
-// shared memory.
+// gemm_cluster.cu -- tensor-core GEMM, split-K inside a thread-block
+// cluster, combined through distributed shared memory: the bf16 layers at
+// wide token tiles and the router (fp32 weights as three exact bf16 planes).
 //
 // out[i, n] = sum_k x[i, k] W[n, k]            (muse_bf16_proj guide, ch. 1, §1.1)
 //
@@ -8,18 +8,25 @@
 // partial sums, so splitting K across CTAs that meet in global memory moves
 // as many partial bytes as weight bytes and serialises a long epilogue
 // behind the MMAs.  Here every output tile (128 weight rows x BN tokens) is
-// one cluster of CS CTAs (CS = 1 .. 8); CTA rank r computes the r-th 1/CS of
+// one cluster of CS CTAs (CS = 1 .. 16); CTA rank r computes the r-th 1/CS of
 // K with the same swapped-operand tcgen05 pipeline as the narrow kernel
 // (bulk copies of prepacked swizzled weight tiles, 2-D TMA for x, fp32
 // accumulation in tensor memory).  After its last MMA the accumulator goes
 // to the CTA's own shared memory, a cluster barrier publishes it, and rank r
 // sums tokens [r BN / CS, (r + 1) BN / CS) over the cluster's CTAs in rank
-// order (distributed shared memory loads), rounds to bf16 and stores.  No
+// order (distributed shared memory loads), rounds to bf16 (the router keeps
+// fp32) and stores.  No
 // global partials, no atomics, no waits on other clusters; the sum order is
 // fixed, so results are deterministic.  The pages' nearest design is the
 // cluster/DSMEM split-K of a small-token QKV kernel (muse_bf16_proj notebook,
 // n. 20 "Hopper pipelines and block clusters", distributed shared-memory
 // reduction), here on tcgen05 and for the wide token tiles.
+//
+// Router: W (fp32) was split at prepare into bf16 planes hi + mid + lo == W
+// exactly, stored as the tiles of a [N, 3K] bf16 matrix.  Weight k-block kb
+// meets x k-block kb % KBx, so x @ [hi | mid | lo].T accumulates the three
+// exact bf16 x bf16 products of every weight in fp32 -- the same sum as
+// fp32 weights, without TF32 truncation -- and the result is stored as fp32.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -133,7 +140,8 @@ __global__ void __launch_bounds__(192, 1)
         mbar_arrive_expect_tx(fb, kTileBytes + C::kXBytes);
         bulk_g2s(smem_u32(sA + s * kTileBytes),
                  p.w + (static_cast<size_t>(t) * p.KB + kb) * kTileBytes, kTileBytes, fb, pol);
-        tma_load_2d(smem_u32(sB + s * C::kXBytes), &tmap_x, kb * kTileK, mt * BN, fb);
+        tma_load_2d(smem_u32(sB + s * C::kXBytes), &tmap_x, (kb % p.KBx) * kTileK, mt * BN,
+                    fb);
         ++issued;
       }
       // Wait (bounded) for the copies still in flight before the ring is
@@ -198,22 +206,32 @@ __global__ void __launch_bounds__(192, 1)
       const int j = j0 + idx / 32;
       const int quad = idx % 32;
       const uint32_t off = static_cast<uint32_t>((j * kTileRows + quad * 4) * 4);
-      float4 v[8];
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int rr = 0; rr < 8; ++rr)
-        if (rr < p.CS) v[rr] = ld_dsmem_v4(map_to_rank(red_base + off, static_cast<uint32_t>(rr)));
-      float4 acc = v[0];
+      for (int r0 = 0; r0 < kClusterMaxCS; r0 += 8) {
+        if (r0 >= p.CS) break;
+        float4 v[8];
 #pragma unroll
-      for (int rr = 1; rr < 8; ++rr) {
-        if (rr < p.CS) {
-          acc.x += v[rr].x;
-          acc.y += v[rr].y;
-          acc.z += v[rr].z;
-          acc.w += v[rr].w;
+        for (int rr = 0; rr < 8; ++rr)
+          if (r0 + rr < p.CS)
+            v[rr] = ld_dsmem_v4(map_to_rank(red_base + off, static_cast<uint32_t>(r0 + rr)));
+#pragma unroll
+        for (int rr = 0; rr < 8; ++rr) {
+          if (r0 + rr < p.CS) {
+            acc.x += v[rr].x;
+            acc.y += v[rr].y;
+            acc.z += v[rr].z;
+            acc.w += v[rr].w;
+          }
         }
       }
-      __nv_bfloat16* o = out + (static_cast<size_t>(mt) * BN + j) * p.n_out +
-                         static_cast<size_t>(t) * kTileRows + quad * 4;
+      const size_t o_idx = (static_cast<size_t>(mt) * BN + j) * p.n_out +
+                           static_cast<size_t>(t) * kTileRows + quad * 4;
+      if (p.out_f32) {
+        *reinterpret_cast<float4*>(static_cast<float*>(p.out) + o_idx) = acc;
+        continue;
+      }
+      __nv_bfloat16* o = out + o_idx;
       __nv_bfloat162 lo2, hi2;
       lo2.x = __float2bfloat16_rn(acc.x);
       lo2.y = __float2bfloat16_rn(acc.y);
@@ -282,10 +300,14 @@ int max_clusters(int cs) {
 
 }  // namespace
 
-bool cluster_supported(int BN) { return BN == 64 || BN == 128 || BN == 256; }
+bool cluster_supported(int BN) {
+  return BN == 16 || BN == 32 || BN == 64 || BN == 128 || BN == 256;
+}
 
 cudaError_t cluster_init_attributes() {
   cudaError_t e;
+  if ((e = set_attr<16>()) != cudaSuccess) return e;
+  if ((e = set_attr<32>()) != cudaSuccess) return e;
   if ((e = set_attr<64>()) != cudaSuccess) return e;
   if ((e = set_attr<128>()) != cudaSuccess) return e;
   if ((e = set_attr<256>()) != cudaSuccess) return e;
@@ -294,6 +316,8 @@ cudaError_t cluster_init_attributes() {
 
 int cluster_max_active(int BN, int cs) {
   switch (BN) {
+    case 16: return max_clusters<16>(cs);
+    case 32: return max_clusters<32>(cs);
     case 64: return max_clusters<64>(cs);
     case 128: return max_clusters<128>(cs);
     case 256: return max_clusters<256>(cs);
@@ -303,6 +327,8 @@ int cluster_max_active(int BN, int cs) {
 
 int cluster_stages(int BN) {
   switch (BN) {
+    case 16: return CCfg<16>::S;
+    case 32: return CCfg<32>::S;
     case 64: return CCfg<64>::S;
     case 128: return CCfg<128>::S;
     case 256: return CCfg<256>::S;
@@ -313,6 +339,8 @@ int cluster_stages(int BN) {
 cudaError_t cluster_launch(int BN, const CUtensorMap& tmap, const ClusterParams& p,
                            cudaStream_t s) {
   switch (BN) {
+    case 16: return launch<16>(tmap, p, s);
+    case 32: return launch<32>(tmap, p, s);
     case 64: return launch<64>(tmap, p, s);
     case 128: return launch<128>(tmap, p, s);
     case 256: return launch<256>(tmap, p, s);

@@ -106,18 +106,23 @@ cudaError_t tc_init_attributes();
 cudaError_t tc_launch(int BN, bool expwin, const CUtensorMap& tmap_x, const TcParams& p,
                       cudaStream_t s);
 
-// Cluster split-K tensor-core path (wide token tiles): BN in {64, 128, 256}.
+// Cluster split-K tensor-core path: BN in {16, 32, 64, 128, 256}, cluster
+// size 1..16.  Weight k-block kb multiplies x k-block kb % KBx, so the
+// router's three bf16 planes (KB = 3 KBx) run as one bf16 GEMM.
 struct ClusterParams {
-  const uint8_t* w;     // packed tiles (same layout as TcParams::w)
-  void* out;            // bf16 [m, n_out]
+  const uint8_t* w;     // packed bf16 tiles (same layout as TcParams::w), KB per tile row
+  void* out;            // [m, n_out], bf16 or fp32 (out_f32)
   uint32_t* status;
   int m;
   int n_out;
   int T;                // n_out / 128
-  int KB;               // K / 64
+  int KB;               // weight k-blocks per tile row
+  int KBx;              // x k-blocks (K / 64)
   int MT;               // ceil(m / BN)
   int CS;               // cluster size = K split
+  int out_f32;
 };
+constexpr int kClusterMaxCS = 16;
 bool cluster_supported(int BN);
 cudaError_t cluster_init_attributes();
 int cluster_max_active(int BN, int cs);
@@ -142,6 +147,10 @@ cudaError_t decode_expwin12(const uint8_t* src, int N, int K, int e0, uint16_t* 
                             cudaStream_t s);
 cudaError_t pack_router_tiles(const float* W, int N, int K, uint8_t* dst, cudaStream_t s);
 cudaError_t unpack_router_tiles(const uint8_t* src, int N, int K, float* W, cudaStream_t s);
+// Router W -> bf16 planes hi, mid, lo (hi + mid + lo == W) packed as the bf16
+// tiles of a [N, 3K] matrix: tile (t, p KB + kb) holds plane p.
+cudaError_t pack_router_planes(const float* W, int N, int K, uint8_t* dst, cudaStream_t s);
+cudaError_t unpack_router_planes(const uint8_t* src, int N, int K, float* W, cudaStream_t s);
 
 // Streaming read (read.cu).
 cudaError_t read_floor_launch(const void* buf, int64_t bytes, uint32_t* sink, int grid, int mode,

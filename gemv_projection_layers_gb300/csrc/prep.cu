@@ -3,8 +3,13 @@
 //   * histogram of the 7 high exponent bits, and the 12-bit exponent-window
 //     encoder/decoder (muse_bf16_proj project report, "Round 5 -- lossless
 //     12-bit compressed weights", "Format");
-//   * router fp32 W -> 64 x 64 swizzled tiles (and back).
+//   * router fp32 W -> 64 x 64 swizzled tiles (and back);
+//   * router fp32 W -> three bf16 planes hi + mid + lo == W (exact), packed as
+//     bf16 tiles of a [N, 3K] matrix whose column p K + k holds plane p of
+//     W[:, k] (and back, summing the planes).
 // The tile and record layouts are defined in kernels.h.
+#include <cuda_bf16.h>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -200,6 +205,85 @@ __global__ void unpack_router_kernel(const uint8_t* __restrict__ src, int N, int
   }
 }
 
+// Exact three-way split of an fp32 value into bf16 planes: each plane is the
+// round-to-nearest bf16 of what the previous ones left.  A normal fp32 value
+// has 24 significant bits; each rounding to 8 bits leaves a remainder that is
+// exact in fp32 and at least 8 bits shorter, so the third plane is the last
+// remainder exactly (for |w| >= 2^-100; subnormal remainders are not met by
+// the weights here and are still split as closely as bf16 allows).
+__device__ __forceinline__ void split3(float w, uint16_t& hi, uint16_t& mid, uint16_t& lo) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(w);
+  const float r1 = w - __bfloat162float(h);
+  const __nv_bfloat16 m = __float2bfloat16_rn(r1);
+  const float r2 = r1 - __bfloat162float(m);
+  const __nv_bfloat16 l = __float2bfloat16_rn(r2);
+  hi = __bfloat16_as_ushort(h);
+  mid = __bfloat16_as_ushort(m);
+  lo = __bfloat16_as_ushort(l);
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// One thread per 8 consecutive weights of a row.
+__global__ void pack_planes_kernel(const float* __restrict__ W, int N, int K,
+                                   uint8_t* __restrict__ dst) {
+  const int64_t chunks = static_cast<int64_t>(N) * (K / 8);
+  const int KB = K / kTileK;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < chunks;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int n = static_cast<int>(i / (K / 8));
+    const int k8 = static_cast<int>(i % (K / 8));
+    const int t = n / kTileRows, r = n % kTileRows;
+    const int kb = k8 / 8, c = k8 % 8;
+    const float* src = W + static_cast<size_t>(n) * K + k8 * 8;
+    uint16_t pl[3][8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) split3(src[j], pl[0][j], pl[1][j], pl[2][j]);
+#pragma unroll
+    for (int p = 0; p < 3; ++p) {
+      uint4 v;
+      v.x = pl[p][0] | (static_cast<uint32_t>(pl[p][1]) << 16);
+      v.y = pl[p][2] | (static_cast<uint32_t>(pl[p][3]) << 16);
+      v.z = pl[p][4] | (static_cast<uint32_t>(pl[p][5]) << 16);
+      v.w = pl[p][6] | (static_cast<uint32_t>(pl[p][7]) << 16);
+      uint8_t* tile = dst + (static_cast<size_t>(t) * 3 * KB + p * KB + kb) * kTileBytes;
+      *reinterpret_cast<uint4*>(tile + tile_chunk_offset(r, c)) = v;
+    }
+  }
+}
+
+__global__ void unpack_planes_kernel(const uint8_t* __restrict__ src, int N, int K,
+                                     float* __restrict__ W) {
+  const int64_t chunks = static_cast<int64_t>(N) * (K / 8);
+  const int KB = K / kTileK;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < chunks;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int n = static_cast<int>(i / (K / 8));
+    const int k8 = static_cast<int>(i % (K / 8));
+    const int t = n / kTileRows, r = n % kTileRows;
+    const int kb = k8 / 8, c = k8 % 8;
+    uint4 v[3];
+#pragma unroll
+    for (int p = 0; p < 3; ++p)
+      v[p] = *reinterpret_cast<const uint4*>(
+          src + (static_cast<size_t>(t) * 3 * KB + p * KB + kb) * kTileBytes +
+          tile_chunk_offset(r, c));
+    float* o = W + static_cast<size_t>(n) * K + k8 * 8;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t wd = j / 2, sh = (j % 2) * 16;
+      auto pick = [&](const uint4& q) -> uint16_t {
+        const uint32_t word = wd == 0 ? q.x : (wd == 1 ? q.y : (wd == 2 ? q.z : q.w));
+        return static_cast<uint16_t>(word >> sh);
+      };
+      o[j] = (bf16_bits_to_float(pick(v[0])) + bf16_bits_to_float(pick(v[1]))) +
+             bf16_bits_to_float(pick(v[2]));
+    }
+  }
+}
+
 constexpr int kPrepBlock = 256;
 constexpr int kPrepGrid = 152 * 8;
 
@@ -235,6 +319,16 @@ cudaError_t decode_expwin12(const uint8_t* src, int N, int K, int e0, uint16_t* 
 
 cudaError_t pack_router_tiles(const float* W, int N, int K, uint8_t* dst, cudaStream_t s) {
   pack_router_kernel<<<kPrepGrid, kPrepBlock, 0, s>>>(W, N, K, dst);
+  return cudaGetLastError();
+}
+
+cudaError_t pack_router_planes(const float* W, int N, int K, uint8_t* dst, cudaStream_t s) {
+  pack_planes_kernel<<<kPrepGrid, kPrepBlock, 0, s>>>(W, N, K, dst);
+  return cudaGetLastError();
+}
+
+cudaError_t unpack_router_planes(const uint8_t* src, int N, int K, float* W, cudaStream_t s) {
+  unpack_planes_kernel<<<kPrepGrid, kPrepBlock, 0, s>>>(src, N, K, W);
   return cudaGetLastError();
 }
 

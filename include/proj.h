@@ -16,9 +16,12 @@
  *     router      256 x 8192   fp32      fp32
  *
  * Accumulation is in fp32; the dense layers round the fp32 sum to bf16
- * (round-to-nearest-even) on output.  The router multiplies the bf16 input
- * (widened exactly to fp32) by its fp32 weights with fp32 fused multiply-adds
- * (no TF32, no bf16 split of the weights).
+ * (round-to-nearest-even) on output.  The router keeps fp32 weights and an
+ * fp32 sum: at m <= 2 the bf16 input (widened exactly) meets the fp32
+ * weights in fp32 fused multiply-adds; from m = 3 on the weights run on the
+ * tensor cores as three bf16 planes with hi + mid + lo == W exactly, so
+ * every product x * plane is exact and only the fp32 accumulation rounds
+ * (no TF32 truncation anywhere).
  *
  * Interface shape (guide ch. 1, §1.6 "Rules that shaped the code"):
  * prepare(weights) runs once, untimed, and may repack or losslessly recode
@@ -90,7 +93,9 @@ enum proj_status {
 enum proj_variant {
     PROJ_VARIANT_AUTO = 0,      /* the dispatch table's choice */
     PROJ_VARIANT_DENSE = 1,     /* uncompressed weights */
-    PROJ_VARIANT_EXPWIN12 = 2   /* 12-bit weights (handle must hold them) */
+    PROJ_VARIANT_EXPWIN12 = 2,  /* 12-bit weights (handle must hold them) */
+    PROJ_VARIANT_PLANES3 = 3    /* router only: the fp32 weights as three bf16 planes,
+                                   hi + mid + lo == W exactly, on the tensor cores */
 };
 
 /* How CTAs sharing a tile combine their fp32 partials (both deterministic:
@@ -204,7 +209,9 @@ int proj_describe(proj_handle h, int64_t m, char *buf, size_t cap);
  * Decode the handle's packed weights back to row-major [N, K] at W_out
  * (device, same dtype as prepared).  With the 12-bit copy present it
  * decodes that copy, so a bitwise comparison with the original W checks
- * that the recode is lossless.  Enqueued on `stream`.
+ * that the recode is lossless.  For the router, PROJ_VARIANT_PLANES3 sums
+ * the three bf16 planes back to fp32 (the same check for the plane split).
+ * Enqueued on `stream`.
  */
 int proj_unpack_weights(proj_handle h, int variant, void *W_out, proj_stream stream);
 

@@ -133,16 +133,19 @@ def test_split_partitions_and_determinism(dev, layer, m):
     assert B.proj_device_status(h) == 0
 
 
-@pytest.mark.parametrize("layer,m", [("o", 1), ("pooler", 16), ("o", 33), ("unpooler", 64),
-                                     ("qkv_gate", 130), ("pooler", 256), ("qkv_gate", 512),
-                                     ("o", 1000)])
+@pytest.mark.parametrize("layer,m", [("o", 1), ("pooler", 16), ("qkv_gate", 32), ("o", 33),
+                                     ("unpooler", 64), ("qkv_gate", 130), ("pooler", 256),
+                                     ("qkv_gate", 512), ("o", 1000), ("router", 1),
+                                     ("router", 3), ("router", 16), ("router", 130),
+                                     ("router", 256), ("router", 1000)])
 def test_cluster_sizes_and_determinism(dev, layer, m):
-    """The cluster split-K kernel at every cluster size (1..8 CTAs sharing K)
-    meets the contract and is bitwise reproducible."""
+    """The cluster split-K kernel at every cluster size (1..16 CTAs sharing K)
+    meets the contract and is bitwise reproducible; for the router it runs the
+    three bf16 planes of the fp32 weights."""
     h, W, _ = prepared(layer, 0)
-    if m >= 33:
+    if m >= (3 if layer == "router" else 33):
         assert "tc_cluster" in B.proj_describe(h, m)
-    for cs in range(1, 9):
+    for cs in range(1, 17):
         kw = dict(grid=cs, kernel=B.PROJ_KERNEL_CLUSTER)
         a = check_case(layer, 0, True, m, h=h, W=W, **kw)
         b = check_case(layer, 0, True, m, h=h, W=W, **kw)
@@ -154,15 +157,21 @@ def test_cluster_kernel_rejections(dev):
     h, _, _ = prepared("router", 0)
     x = torch.zeros((64, 8192), dtype=torch.bfloat16, device="cuda")
     out = torch.zeros((64, 256), dtype=torch.float32, device="cuda")
-    with pytest.raises(B.ProjError) as e:
-        B.proj_run_ex(h, x, 64, out, kernel=B.PROJ_KERNEL_CLUSTER)
-    assert e.value.status == B.PROJ_EUNSUPPORTED
+    for kw in (dict(kernel=B.PROJ_KERNEL_CLUSTER, variant=B.PROJ_VARIANT_DENSE),
+               dict(kernel=B.PROJ_KERNEL_TILE, variant=B.PROJ_VARIANT_PLANES3),
+               dict(kernel=B.PROJ_KERNEL_GEMV, variant=B.PROJ_VARIANT_PLANES3)):
+        with pytest.raises(B.ProjError) as e:
+            B.proj_run_ex(h, x, 2 if kw["kernel"] == B.PROJ_KERNEL_GEMV else 64, out, **kw)
+        assert e.value.status == B.PROJ_EUNSUPPORTED, kw
     h, _, _ = prepared("o", 0)
     x = torch.zeros((64, 1024), dtype=torch.bfloat16, device="cuda")
     out = torch.zeros((64, 8192), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(B.ProjError) as e:
-        B.proj_run_ex(h, x, 64, out, kernel=B.PROJ_KERNEL_CLUSTER, grid=9)
+        B.proj_run_ex(h, x, 64, out, kernel=B.PROJ_KERNEL_CLUSTER, grid=17)
     assert e.value.status == B.PROJ_EINVAL
+    with pytest.raises(B.ProjError) as e:
+        B.proj_run_ex(h, x, 64, out, variant=B.PROJ_VARIANT_PLANES3)
+    assert e.value.status == B.PROJ_EUNSUPPORTED
 
 
 @pytest.mark.parametrize("layer", [s.name for s in wl.LAYERS])
@@ -234,6 +243,11 @@ def test_unpack_is_lossless(dev, layer):
     torch.cuda.synchronize()
     assert torch.equal(back.view(torch.int16) if back.dtype == torch.bfloat16 else back,
                        Wd.view(torch.int16) if Wd.dtype == torch.bfloat16 else Wd)
+    if layer == "router":
+        # the three bf16 planes sum back to the fp32 weights bit for bit
+        B.proj_unpack_weights(h, B.PROJ_VARIANT_PLANES3, back)
+        torch.cuda.synchronize()
+        assert torch.equal(back.view(torch.int32), Wd.view(torch.int32))
 
 
 @pytest.mark.parametrize("layer", ["qkv_gate", "o", "pooler", "unpooler"])
