@@ -43,7 +43,8 @@ class NativeLibraryMissing(ImportError):
 
 class proj_run_opts(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int), ("grid", ctypes.c_int),
-                ("reduce", ctypes.c_int), ("kernel", ctypes.c_int)]
+                ("reduce", ctypes.c_int), ("kernel", ctypes.c_int), ("groups", ctypes.c_int),
+                ("tile_n", ctypes.c_int)]
 
 
 class proj_info_t(ctypes.Structure):
@@ -168,8 +169,9 @@ def proj_run(h: int, x, m: int, out, stream=None) -> None:
 
 def proj_run_ex(h: int, x, m: int, out, stream=None, variant: int = PROJ_VARIANT_AUTO,
                 grid: int = 0, reduce: int = PROJ_REDUCE_AUTO,
-                kernel: int = PROJ_KERNEL_AUTO) -> None:
-    opts = proj_run_opts(int(variant), int(grid), int(reduce), int(kernel))
+                kernel: int = PROJ_KERNEL_AUTO, groups: int = 0, tile_n: int = 0) -> None:
+    opts = proj_run_opts(int(variant), int(grid), int(reduce), int(kernel), int(groups),
+                         int(tile_n))
     _check(load().proj_run_ex(h, _addr(x), int(m), _addr(out), _stream(stream),
                               ctypes.byref(opts)), "proj_run_ex")
 

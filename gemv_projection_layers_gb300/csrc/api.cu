@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -143,24 +144,67 @@ int bn_for_cluster(int64_t m) {
 }
 int bn_index(int bn) { return bn == 16 ? 0 : bn == 32 ? 1 : bn == 64 ? 2 : bn == 128 ? 3 : 4; }
 
-// Largest cluster size (K split) that keeps every cluster of the grid
-// resident in one wave on no more CTAs than SMs.  max_active[cs - 1] is the
-// occupancy query's count of co-resident clusters of cs CTAs.
-int pick_cluster(int64_t tiles, int KB, int sms, const int max_active[kClusterMaxCS]) {
-  int best = 1;
-  for (int cs = 2; cs <= kClusterMaxCS; ++cs) {
-    if (cs > KB || tiles * cs > sms) break;
-    if (max_active[cs - 1] > 0 && tiles > max_active[cs - 1]) continue;
-    best = cs;
+// Launch shape of the cluster kernel: token tile bn (the smallest covering m,
+// or one or two halvings of it), cluster size cs and clusters per tile kg,
+// chosen by a cost model calibrated on GB300 (in-kernel timestamps and a
+// bulk-copy probe):
+//   stream  = max(k-blocks per CTA x per-k-block time, weight bytes / HBM);
+//             an SM's copy engine takes max(~160 ns, bytes / 135 GB/s) per
+//             request, and a k-block is two requests (16 KB of weights, then
+//             bn x 128 B of x);
+//   combine = remote part of the cluster's partials through distributed
+//             shared memory (~30 GB/s per SM, less in large clusters);
+//   groups  = kg > 1 adds a fence, an atomic and an L2 round trip (~2 us)
+//             plus the last cluster's reads of the kg partials.
+// Candidates keep every cluster resident in one wave (max_active), at most
+// one CTA per SM and at least kMinKbPerCta k-blocks per CTA.
+constexpr int kMinKbPerCta = 4;
+struct ClusterShape {
+  int bn, cs, kg;
+};
+ClusterShape pick_cluster(int64_t m, int T, int KB, int64_t weight_bytes, int sms, int bn0,
+                          int bn_lo, const int (*max_active)[kClusterMaxCS]) {
+  constexpr double kReqFloor = 160e-9;  // s per copy request, small copies
+  constexpr double kReqRate = 135e9;    // bytes/s per SM, large copies
+  constexpr double kHbm = 6.4e12;       // bytes/s, streaming reads
+  constexpr double kDsmem = 30e9;       // bytes/s per SM for clusters of <= 4
+  constexpr double kL2 = 100e9;         // bytes/s per SM, group partial reads
+  constexpr double kGroupFixed = 2e-6;  // s
+  ClusterShape best{bn0, 1, 1};
+  double best_t = 1e30;
+  for (int bn = bn0; bn >= 16 && bn >= bn_lo; bn /= 2) {
+    const int64_t tiles = static_cast<int64_t>(T) * ((m + bn - 1) / bn);
+    const double part = 128.0 * bn * 4;  // one CTA's partial, bytes
+    for (int kg = 1; kg <= kClusterMaxGroups; ++kg) {
+      for (int cs = 1; cs <= kClusterMaxCS; ++cs) {
+        if (cs * kg > 1 && KB / (cs * kg) < kMinKbPerCta) continue;
+        const int64_t ctas = tiles * cs * kg;
+        if (ctas > sms && !(cs == 1 && kg == 1)) continue;
+        const int act = max_active[bn_index(bn)][cs - 1];
+        if (act > 0 && tiles * kg > act && !(cs == 1 && kg == 1)) continue;
+        const double nk = static_cast<double>(KB) / (cs * kg);
+        const double waves = static_cast<double>((ctas + sms - 1) / sms);
+        const double t_kb = std::max(kReqFloor, 16384.0 / kReqRate) +
+                            std::max(kReqFloor, 128.0 * bn / kReqRate);
+        double t = std::max(nk * t_kb * waves, static_cast<double>(weight_bytes) / kHbm);
+        if (cs > 1)
+          t += (cs - 1.0) / cs * part / (kDsmem * std::min(1.0, std::sqrt(4.0 / cs)));
+        if (kg > 1) t += kGroupFixed + kg * (part / cs) / kL2;
+        if (t < best_t * 0.999 || (t < best_t * 1.001 && kg < best.kg)) {
+          best_t = t;
+          best = ClusterShape{bn, cs, kg};
+        }
+      }
+    }
   }
   return best;
 }
-
 int mt_for_gemv(int64_t m) { return m <= 1 ? 1 : 2; }
 
 struct Plan {
   bool gemv;
   bool cluster;
+  int KG = 1;  // cluster kernel: clusters per output tile
   bool router;
   bool expwin;
   int reduce;   // 0 owner, 1 distributed
@@ -182,6 +226,7 @@ struct proj_ctx {
   uint32_t* gemv_flags = nullptr;  // [num_sms], zero between calls
   float* gemv_ws = nullptr;        // [num_sms][2]
   uint8_t* w_planes = nullptr;     // router: bf16 planes hi/mid/lo as [N, 3K] tiles
+  uint32_t* cl_counters = nullptr; // cluster groups: [SMs][16], zero between calls
   int cluster_active[5][kClusterMaxCS] = {};  // co-resident clusters: BN 16..256 x size 1..16
   uint8_t* w_exp = nullptr;
   size_t w_exp_bytes = 0;
@@ -211,6 +256,7 @@ void free_ctx(proj_ctx* h) {
   if (!h) return;
   cudaFree(h->w_dense);
   cudaFree(h->w_planes);
+  cudaFree(h->cl_counters);
   cudaFree(h->w_rows);
   cudaFree(h->gemv_flags);
   cudaFree(h->gemv_ws);
@@ -249,13 +295,17 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
   const int kern = opts ? opts->kernel : PROJ_KERNEL_AUTO;
   if (kern < PROJ_KERNEL_AUTO || kern > PROJ_KERNEL_CLUSTER) return PROJ_EINVAL;
   if (variant < PROJ_VARIANT_AUTO || variant > PROJ_VARIANT_PLANES3) return PROJ_EINVAL;
+  const int tile_n = opts ? opts->tile_n : 0;
+  if (tile_n != 0 && tile_n != 16 && tile_n != 32 && tile_n != 64 && tile_n != 128 &&
+      tile_n != 256)
+    return PROJ_EINVAL;
   pl->router = (h->layer == PROJ_ROUTER);
   pl->n_out = out_rows(h, m);
   // Streaming GEMV: small m, uncompressed weights.
   const bool gemv_ok =
       m <= kGemvMaxM && (variant == PROJ_VARIANT_AUTO || variant == PROJ_VARIANT_DENSE);
   if (kern == PROJ_KERNEL_GEMV && !gemv_ok) return PROJ_EUNSUPPORTED;
-  if (gemv_ok && kern != PROJ_KERNEL_TILE) {
+  if (gemv_ok && (kern == PROJ_KERNEL_GEMV || (kern == PROJ_KERNEL_AUTO && tile_n == 0))) {
     pl->gemv = true;
     pl->expwin = false;
     pl->reduce = 0;
@@ -272,7 +322,8 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
   // explicit grid or reduction mode names the global-memory split-K kernel.
   const bool auto_cluster = kern == PROJ_KERNEL_AUTO &&
                             m >= (pl->router ? kRouterClusterMinM : kClusterMinM) &&
-                            (!opts || (opts->grid == 0 && opts->reduce == PROJ_REDUCE_AUTO));
+                            (!opts || (opts->grid == 0 && opts->reduce == PROJ_REDUCE_AUTO &&
+                                       opts->tile_n == 0));
   bool want_cluster;
   if (pl->router) {
     // The cluster kernel runs the router on its bf16 planes only.
@@ -295,24 +346,36 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
     pl->cluster = true;
     pl->expwin = false;
     pl->reduce = 0;
-    pl->bn = bn_for_cluster(m);
     pl->T = static_cast<int>(pl->n_out / kTileRows);
     pl->KB = static_cast<int>(h->K / kTileK) * (pl->router ? 3 : 1);
+    const int64_t wbytes = pl->n_out * h->K * (pl->router ? 6 : 2);
+    // A forced tile width, cluster size or group count keeps the token tile
+    // the smallest covering m (or the forced one).
+    const bool forced = opts && (opts->grid > 0 || opts->groups > 0);
+    const int bn0 = tile_n ? tile_n : bn_for_cluster(m);
+    const ClusterShape shp = pick_cluster(m, pl->T, pl->KB, wbytes, h->num_sms, bn0,
+                                          (tile_n || forced) ? bn0 : bn0 / 4, h->cluster_active);
+    pl->bn = shp.bn;
     pl->MT = static_cast<int>((m + pl->bn - 1) / pl->bn);
-    int cs = pick_cluster(static_cast<int64_t>(pl->MT) * pl->T, pl->KB, h->num_sms,
-                          h->cluster_active[bn_index(pl->bn)]);
-    if (opts && opts->grid > 0) {
-      cs = opts->grid;
-      if (cs > kClusterMaxCS) return PROJ_EINVAL;
-      if (cs > pl->KB) return PROJ_EUNSUPPORTED;
+    int cs = shp.cs, kg = shp.kg;
+    if (opts && (opts->grid > 0 || opts->groups > 0)) {
+      cs = opts->grid > 0 ? opts->grid : 1;
+      kg = opts->groups > 0 ? opts->groups : 1;
+      if (cs > kClusterMaxCS || kg > kClusterMaxGroups) return PROJ_EINVAL;
+      if (cs * kg > pl->KB) return PROJ_EUNSUPPORTED;
+      // the group partials and counters are sized for one CTA per SM
+      if (kg > 1 && static_cast<int64_t>(pl->MT) * pl->T * kg * cs > h->num_sms)
+        return PROJ_EUNSUPPORTED;
     }
     pl->G = cs;  // cluster size
+    pl->KG = kg;
     return PROJ_OK;
   }
   if (pl->router) {
     if (variant == PROJ_VARIANT_EXPWIN12 || variant == PROJ_VARIANT_PLANES3)
       return PROJ_EUNSUPPORTED;
     pl->expwin = false;
+    if (tile_n) return PROJ_EUNSUPPORTED;  // the FMA tiles pick their own width
     pl->bn = tm_for_m(m);
     pl->T = static_cast<int>(h->N / kRtRows);
     pl->KB = static_cast<int>(h->K / kRtK);
@@ -327,7 +390,8 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
       return PROJ_EINVAL;
     }
     pl->expwin = use_exp;
-    pl->bn = bn_for_m(m);
+    pl->bn = tile_n ? tile_n : bn_for_m(m);
+    if (use_exp && pl->bn > 32) return PROJ_EUNSUPPORTED;
     pl->T = static_cast<int>(pl->n_out / kTileRows);
     pl->KB = static_cast<int>(h->K / kTileK);
   }
@@ -551,6 +615,14 @@ proj_handle proj_prepare_ex(int layer, const void* W, int64_t N, int64_t K, int 
     done();
     return bail_cuda(e, "cudaMalloc(row-major weights)");
   }
+  // cluster groups: one [256][128] fp32 partial per cluster, at most one per SM
+  h->ws_bytes = std::max(h->ws_bytes, static_cast<size_t>(sms) * 256 * kTileRows * 4);
+  const size_t cl_counter_bytes = static_cast<size_t>(sms) * kClusterMaxCS * 4;
+  if ((e = dmalloc(&h->cl_counters, cl_counter_bytes)) != cudaSuccess ||
+      (e = cudaMemsetAsync(h->cl_counters, 0, cl_counter_bytes, s)) != cudaSuccess) {
+    done();
+    return bail_cuda(e, "cudaMalloc(cluster counters)");
+  }
   if ((e = dmalloc(&h->ws, h->ws_bytes)) != cudaSuccess ||
       (e = dmalloc(&h->counters, h->counters_bytes)) != cudaSuccess ||
       (e = dmalloc(&h->status, 16)) != cudaSuccess ||
@@ -624,6 +696,9 @@ int proj_run_ex(proj_handle h, const void* x, int64_t m, void* out, proj_stream 
     c.KB = pl.KB;
     c.MT = pl.MT;
     c.CS = pl.G;
+    c.KG = pl.KG;
+    c.ws = reinterpret_cast<float*>(h->ws);
+    c.counters = h->cl_counters;
     e = cluster_launch(pl.bn, *map, c, s);
     if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
     return PROJ_OK;
@@ -716,10 +791,11 @@ int proj_describe(proj_handle h, int64_t m, char* buf, size_t cap) {
                   pl.G, static_cast<long long>(pl.n_out));
   } else if (pl.cluster) {
     std::snprintf(buf, cap,
-                  "tc_cluster%s BN=%d stages=%d CS=%d CTAs=%d T=%d KB=%d MT=%d n_out=%lld "
-                  "resident_clusters=%d",
-                  pl.router ? "_planes3" : "", pl.bn, cluster_stages(pl.bn), pl.G,
-                  pl.MT * pl.T * pl.G, pl.T, pl.KB, pl.MT, static_cast<long long>(pl.n_out),
+                  "tc_cluster%s BN=%d stages=%d CS=%d KG=%d CTAs=%d T=%d KB=%d MT=%d "
+                  "n_out=%lld resident_clusters=%d",
+                  pl.router ? "_planes3" : "", pl.bn, cluster_stages(pl.bn), pl.G, pl.KG,
+                  pl.MT * pl.T * pl.KG * pl.G, pl.T, pl.KB, pl.MT,
+                  static_cast<long long>(pl.n_out),
                   h->cluster_active[bn_index(pl.bn)][pl.G - 1]);
   } else if (pl.router) {
     std::snprintf(buf, cap, "router_fma TM=%d stages=8 G=%d T=%d KB=%d MT=%d reduce=%s", pl.bn,

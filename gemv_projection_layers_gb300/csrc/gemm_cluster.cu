@@ -43,7 +43,10 @@ struct CCfg {
   static constexpr int kStage = kTileBytes + kXBytes;
   static constexpr int kFit = (kSmemLimit - 1024 - 1024) / kStage;
   static constexpr int S = kFit > 12 ? 12 : kFit;
-  static constexpr int kThreads = 192;
+  // warp 0 copies, warp 1 issues MMAs, warps 2..9 drain the accumulator
+  // (two per tensor-memory lane quarter, one column half each), all twelve
+  // warps combine the cluster's partials.
+  static constexpr int kThreads = 384;
   static constexpr int kTmemCols = BN < 32 ? 32 : BN;
   static constexpr size_t kRing = static_cast<size_t>(S) * kStage;
   static constexpr size_t kRed = static_cast<size_t>(BN) * kTileRows * 4;  // [BN][128] fp32
@@ -71,18 +74,54 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
   return r;
 }
 
-// Peer partials are stable between the two cluster barriers, so these loads
-// carry no memory clobber and can be issued back to back.
-__device__ __forceinline__ float4 ld_dsmem_v4(uint32_t addr) {
+// The staging buffer is addressed through 32-bit shared-window addresses:
+// the 1 KB alignment arithmetic on the dynamic shared-memory pointer hides
+// its address space from the compiler, and generic accesses are slower.
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ float4 ld_shared_v4(uint32_t addr) {
   float4 v;
-  asm("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
-      : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-      : "r"(addr));
+  asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
   return v;
 }
 
+// Peer partials are stable between the two cluster barriers: these loads
+// carry no memory clobber, so they issue back to back; volatile keeps them
+// after the barrier (volatile asm too).
+__device__ __forceinline__ float4 ld_dsmem_v4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+// Token j, rows row0..row0 + 3 of output tile (t, mt): fp32 as is, or
+// rounded to bf16 (round-to-nearest-even).
 template <int BN>
-__global__ void __launch_bounds__(192, 1)
+__device__ __forceinline__ void store_out(const ClusterParams& p, int mt, int t, int j, int row0,
+                                          float4 v) {
+  const size_t o_idx = (static_cast<size_t>(mt) * BN + j) * p.n_out +
+                       static_cast<size_t>(t) * kTileRows + row0;
+  if (p.out_f32) {
+    *reinterpret_cast<float4*>(static_cast<float*>(p.out) + o_idx) = v;
+  } else {
+    __nv_bfloat162 lo2, hi2;
+    lo2.x = __float2bfloat16_rn(v.x);
+    lo2.y = __float2bfloat16_rn(v.y);
+    hi2.x = __float2bfloat16_rn(v.z);
+    hi2.y = __float2bfloat16_rn(v.w);
+    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + o_idx;
+    *reinterpret_cast<__nv_bfloat162*>(o) = lo2;
+    *reinterpret_cast<__nv_bfloat162*>(o + 2) = hi2;
+  }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(384, 1)
     tc_cluster_kernel(const __grid_constant__ CUtensorMap tmap_x, const ClusterParams p) {
   using C = CCfg<BN>;
   constexpr int S = C::S;
@@ -91,7 +130,8 @@ __global__ void __launch_bounds__(192, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = sA + static_cast<size_t>(S) * kTileBytes;
-  float* red = reinterpret_cast<float*>(smem);  // reuses the ring after the last MMA
+  // [BN][128] fp32 accumulator staging; reuses the ring after the last MMA
+  const uint32_t red_base = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kData);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 2);
   const uint32_t full0 = smem_u32(bars);
@@ -101,11 +141,15 @@ __global__ void __launch_bounds__(192, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
-  const int tile = static_cast<int>(blockIdx.x) / p.CS;  // cluster index
+  const int cluster = static_cast<int>(blockIdx.x) / p.CS;
+  const int tile = cluster / p.KG;   // output tile (t, mt)
+  const int grp = cluster % p.KG;    // which of the tile's KG clusters
   const int t = tile / p.MT;
   const int mt = tile % p.MT;
-  const int kb0 = static_cast<int>((static_cast<int64_t>(rank) * p.KB) / p.CS);
-  const int kb1 = static_cast<int>((static_cast<int64_t>(rank + 1) * p.KB) / p.CS);
+  const int64_t split = static_cast<int64_t>(grp) * p.CS + rank;  // K slice of this CTA
+  const int64_t nsplit = static_cast<int64_t>(p.KG) * p.CS;
+  const int kb0 = static_cast<int>(split * p.KB / nsplit);
+  const int kb1 = static_cast<int>((split + 1) * p.KB / nsplit);
   const int mv = min(BN, p.m - mt * BN);
 
   if (threadIdx.x == 0) {
@@ -117,21 +161,43 @@ __global__ void __launch_bounds__(192, 1)
     fence_mbar_init();
     prefetch_tmap(&tmap_x);
   }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
+  griddep_launch_dependents();
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  // The producer starts streaming at once; the tensor-memory allocation runs
+  // meanwhile and is published to the MMA and epilogue warps (1..5) only.
+  uint32_t tmem = 0;
+  if (warp >= 1) {
+    if (warp == 1) {
+      tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+      tmem_relinquish();
+    }
+    tc_fence_before();
+    named_bar_sync(1, C::kThreads - 32);
+    tc_fence_after();
+    tmem = *tmem_slot;
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      int64_t issued = 0;
-      for (int kb = kb0; kb < kb1; ++kb) {
+      // The weights of the first ring's worth of stages stream before the
+      // wait on the previous kernel of the stream (they are constant); x and
+      // every global write come after it.
+      const int pre = min(kb1 - kb0, S);
+      for (int j = 0; j < pre; ++j) {
+        const uint32_t fb = full0 + 8 * j;
+        mbar_arrive_expect_tx(fb, kTileBytes + C::kXBytes);
+        bulk_g2s(smem_u32(sA + j * kTileBytes),
+                 p.w + (static_cast<size_t>(t) * p.KB + kb0 + j) * kTileBytes, kTileBytes, fb,
+                 pol);
+      }
+      griddep_wait();
+      for (int j = 0; j < pre; ++j)
+        tma_load_2d(smem_u32(sB + j * C::kXBytes), &tmap_x, ((kb0 + j) % p.KBx) * kTileK,
+                    mt * BN, full0 + 8 * j);
+      int64_t issued = pre;
+      for (int kb = kb0 + pre; kb < kb1; ++kb) {
         const int s = static_cast<int>(issued % S);
         if (!mbar_wait(empty0 + 8 * s, static_cast<uint32_t>(((issued / S) & 1) ^ 1), p.status,
                        kStatusTimeoutProducer))
@@ -174,20 +240,43 @@ __global__ void __launch_bounds__(192, 1)
       }
       tc_commit(accf);  // also covers an aborted loop: arrives once prior MMAs finish
     }
-  } else {
+  } else if (warp < 10) {
     // ------------------------------------- epilogue: accumulator -> smem
-    const int q = warp & 3;
+    const int q = warp & 3;         // lane quarter this warp may access
+    const int half = (warp - 2) >> 2;  // column half
     const int r = q * 32 + lane;
     if (mbar_wait(accf, 0, p.status, kStatusTimeoutEpilogue)) {
       tc_fence_after();
       const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
-#pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 16) {
-        float v[16];
-        tmem_ld16(taddr + c0, v);
-        tmem_ld_wait();
+      constexpr int kHalf = BN / 2;
+      if constexpr (kHalf <= 16) {
+        if (half == 0) {
+          float v[16];
+          tmem_ld16(taddr, v);
+          tmem_ld_wait();
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) red[(c0 + jj) * kTileRows + r] = v[jj];
+          for (int jj = 0; jj < 16; ++jj)
+            if (jj < BN) st_shared_f32(red_base + static_cast<uint32_t>((jj * kTileRows + r) * 4), v[jj]);
+        } else if (BN == 32) {
+          float v[16];
+          tmem_ld16(taddr + 16, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) st_shared_f32(red_base + static_cast<uint32_t>(((16 + jj) * kTileRows + r) * 4), v[jj]);
+        }
+      } else {
+        // two loads in flight per wait
+#pragma unroll 1
+        for (int c0 = half * kHalf; c0 < (half + 1) * kHalf; c0 += 32) {
+          float v[16], u[16];
+          tmem_ld16(taddr + c0, v);
+          tmem_ld16(taddr + c0 + 16, u);
+          tmem_ld_wait();
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) st_shared_f32(red_base + static_cast<uint32_t>(((c0 + jj) * kTileRows + r) * 4), v[jj]);
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) st_shared_f32(red_base + static_cast<uint32_t>(((c0 + 16 + jj) * kTileRows + r) * 4), u[jj]);
+        }
       }
       tc_fence_before();
     }
@@ -195,50 +284,101 @@ __global__ void __launch_bounds__(192, 1)
   __syncwarp();
   // Every CTA of the cluster has its partial in shared memory.
   cluster_sync_all();
+  griddep_wait();  // before the first global write of this thread
   // Rank r sums tokens [r BN / CS, (r + 1) BN / CS) over the cluster, in rank
-  // order; a thread handles 4 consecutive rows of one token (float4).
+  // order; an item is 4 consecutive rows of one token (float4).  A thread
+  // keeps kItems items x 4 ranks of loads in flight; its own rank's partial
+  // comes from local shared memory, the others' through distributed shared
+  // memory.  (Pushing the slices with bulk shared-to-shared copies instead
+  // measured slower: the extra mbarrier round trip outweighs the copy.)
+  const int j0 = static_cast<int>(rank) * BN / p.CS;
+  const int j1 = min(static_cast<int>(rank + 1) * BN / p.CS, mv);
+  const int n_items = max(j1 - j0, 0) * 32;
   {
-    const int j0 = static_cast<int>(rank) * BN / p.CS;
-    const int j1 = min(static_cast<int>(rank + 1) * BN / p.CS, mv);
-    const uint32_t red_base = smem_u32(red);
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
-    for (int idx = threadIdx.x; idx < (j1 - j0) * 32; idx += C::kThreads) {
-      const int j = j0 + idx / 32;
-      const int quad = idx % 32;
-      const uint32_t off = static_cast<uint32_t>((j * kTileRows + quad * 4) * 4);
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    constexpr int kItems = 4;
+    for (int base = threadIdx.x; base < n_items; base += kItems * C::kThreads) {
+      float4 acc[kItems];
+      uint32_t off[kItems];
 #pragma unroll
-      for (int r0 = 0; r0 < kClusterMaxCS; r0 += 8) {
-        if (r0 >= p.CS) break;
-        float4 v[8];
+      for (int u = 0; u < kItems; ++u) {
+        acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int idx = min(base + u * C::kThreads, n_items - 1);
+        off[u] = static_cast<uint32_t>(((j0 + idx / 32) * kTileRows + (idx % 32) * 4) * 4);
+      }
+      for (int r0 = 0; r0 < p.CS; r0 += 4) {
+        float4 v[kItems][4];
 #pragma unroll
-        for (int rr = 0; rr < 8; ++rr)
-          if (r0 + rr < p.CS)
-            v[rr] = ld_dsmem_v4(map_to_rank(red_base + off, static_cast<uint32_t>(r0 + rr)));
+        for (int u = 0; u < kItems; ++u)
 #pragma unroll
-        for (int rr = 0; rr < 8; ++rr) {
-          if (r0 + rr < p.CS) {
-            acc.x += v[rr].x;
-            acc.y += v[rr].y;
-            acc.z += v[rr].z;
-            acc.w += v[rr].w;
+          for (int rr = 0; rr < 4; ++rr) {
+            const uint32_t src = static_cast<uint32_t>(r0 + rr);
+            if (src == rank)
+              v[u][rr] = ld_shared_v4(red_base + off[u]);
+            else if (r0 + rr < p.CS)
+              v[u][rr] = ld_dsmem_v4(map_to_rank(red_base + off[u], src));
           }
+#pragma unroll
+        for (int u = 0; u < kItems; ++u)
+#pragma unroll
+          for (int rr = 0; rr < 4; ++rr)
+            if (r0 + rr < p.CS) {
+              acc[u].x += v[u][rr].x;
+              acc[u].y += v[u][rr].y;
+              acc[u].z += v[u][rr].z;
+              acc[u].w += v[u][rr].w;
+            }
+      }
+#pragma unroll
+      for (int u = 0; u < kItems; ++u) {
+        const int idx = base + u * C::kThreads;
+        if (idx >= n_items) break;
+        if (p.KG > 1) {
+          // this cluster's partial of the tile, summed with the others below
+          *reinterpret_cast<float4*>(p.ws + static_cast<size_t>(cluster) * BN * kTileRows +
+                                     off[u] / 4) = acc[u];
+        } else {
+          store_out<BN>(p, mt, t, j0 + idx / 32, (idx % 32) * 4, acc[u]);
         }
       }
-      const size_t o_idx = (static_cast<size_t>(mt) * BN + j) * p.n_out +
-                           static_cast<size_t>(t) * kTileRows + quad * 4;
-      if (p.out_f32) {
-        *reinterpret_cast<float4*>(static_cast<float*>(p.out) + o_idx) = acc;
-        continue;
+    }
+  }
+  if (p.KG > 1) {
+    // The last of the tile's KG clusters to finish sums their partials in
+    // cluster order -- the same order whichever finishes last -- and
+    // stores the tile.  Nothing waits: earlier clusters just leave.
+    // One release per CTA after the barrier (it orders the CTA's partial
+    // stores before the count); its acquire, through the second barrier,
+    // orders the last CTA's loads after every other cluster's stores.
+    __shared__ uint32_t s_last;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const uint32_t old = atom_add_acq_rel_gpu(p.counters + tile * p.CS + rank, 1u);
+      s_last = old == static_cast<uint32_t>(p.KG - 1) ? 1u : 0u;
+    }
+    __syncthreads();
+    if (s_last) {
+      const float* slab0 = p.ws + static_cast<size_t>(tile) * p.KG * BN * kTileRows;
+      for (int idx = threadIdx.x; idx < n_items; idx += C::kThreads) {
+        const uint32_t o4 = static_cast<uint32_t>((j0 + idx / 32) * kTileRows + (idx % 32) * 4);
+        // every group's partial in one round trip, summed in group order
+        float4 v[kClusterMaxGroups];
+#pragma unroll
+        for (int gg = 0; gg < kClusterMaxGroups; ++gg)
+          if (gg < p.KG)
+            v[gg] = __ldcg(reinterpret_cast<const float4*>(
+                slab0 + static_cast<size_t>(gg) * BN * kTileRows + o4));
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int gg = 0; gg < kClusterMaxGroups; ++gg)
+          if (gg < p.KG) {
+            acc.x += v[gg].x;
+            acc.y += v[gg].y;
+            acc.z += v[gg].z;
+            acc.w += v[gg].w;
+          }
+        store_out<BN>(p, mt, t, j0 + idx / 32, (idx % 32) * 4, acc);
       }
-      __nv_bfloat16* o = out + o_idx;
-      __nv_bfloat162 lo2, hi2;
-      lo2.x = __float2bfloat16_rn(acc.x);
-      lo2.y = __float2bfloat16_rn(acc.y);
-      hi2.x = __float2bfloat16_rn(acc.z);
-      hi2.y = __float2bfloat16_rn(acc.w);
-      *reinterpret_cast<__nv_bfloat162*>(o) = lo2;
-      *reinterpret_cast<__nv_bfloat162*>(o + 2) = hi2;
+      if (threadIdx.x == 0) p.counters[tile * p.CS + rank] = 0u;  // ready for the next call
     }
   }
   // No CTA may leave while a peer still reads its shared memory.
@@ -262,7 +402,7 @@ cudaError_t set_attr() {
 template <int BN>
 cudaLaunchConfig_t make_cfg(const ClusterParams& p, cudaStream_t s, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.MT * p.T * p.CS);
+  cfg.gridDim = dim3(p.MT * p.T * p.KG * p.CS);
   cfg.blockDim = dim3(CCfg<BN>::kThreads);
   cfg.dynamicSmemBytes = CCfg<BN>::kSmem;
   cfg.stream = s;
@@ -277,8 +417,11 @@ cudaLaunchConfig_t make_cfg(const ClusterParams& p, cudaStream_t s, cudaLaunchAt
 
 template <int BN>
 cudaError_t launch(const CUtensorMap& tmap, const ClusterParams& p, cudaStream_t s) {
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = make_cfg<BN>(p, s, attr);
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, tc_cluster_kernel<BN>, tmap, p);
 }
 
@@ -287,6 +430,7 @@ int max_clusters(int cs) {
   ClusterParams p = {};
   p.MT = 1;
   p.T = 1;
+  p.KG = 1;
   p.CS = cs;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_cfg<BN>(p, nullptr, attr);

@@ -118,8 +118,8 @@ using XT = typename std::conditional<sizeof(WT) == 2, uint16_t, float>::type;
 // Lane partial of one chunk for MT tokens (col0: the chunk's first column).
 // Eight independent accumulation chains; combined in a fixed order.
 template <typename WT, int MT>
-__device__ __forceinline__ void chunk_partial(const uint8_t* chunk, const XT<WT>* xs, int K,
-                                              int col0, int lane, float (&acc)[MT]) {
+__device__ __forceinline__ void chunk_partial(uint32_t chunk, uint32_t xs, int K, int col0,
+                                              int lane, float (&acc)[MT]) {
   constexpr int VEC = GCfg<WT, MT>::kVec;
   constexpr int NI = 32 / VEC;
   float a8[MT][8];
@@ -129,12 +129,13 @@ __device__ __forceinline__ void chunk_partial(const uint8_t* chunk, const XT<WT>
     for (int c = 0; c < 8; ++c) a8[t][c] = 0.f;
   uint4 wraw[NI];
 #pragma unroll
-  for (int i = 0; i < NI; ++i) wraw[i] = *reinterpret_cast<const uint4*>(chunk + (lane + 32 * i) * 16);
+  for (int i = 0; i < NI; ++i) wraw[i] = ld_shared_u4(chunk + (lane + 32 * i) * 16);
 #pragma unroll
   for (int i = 0; i < NI; ++i) {
 #pragma unroll
     for (int t = 0; t < MT; ++t) {
-      const uint4 xv = *reinterpret_cast<const uint4*>(xs + t * K + col0 + (lane + 32 * i) * VEC);
+      const uint4 xv = ld_shared_u4(
+          xs + static_cast<uint32_t>((t * K + col0 + (lane + 32 * i) * VEC) * sizeof(XT<WT>)));
       float* a = a8[t];
       if constexpr (VEC == 8) {
         fma_bf16x2(a[(i & 1) * 4 + 0], a[(i & 1) * 4 + 1], wraw[i].x, xv.x);
@@ -197,6 +198,7 @@ __global__ void __launch_bounds__(GCfg<WT, MT>::kThreads, 1) gemv_kernel(const G
     fence_mbar_init();
   }
   for (int i = threadIdx.x; i < kSplitRing; i += blockDim.x) split_cnt[i] = 0;
+  griddep_launch_dependents();
   __syncthreads();
 
   if (warp == kComputeWarps) {
@@ -227,6 +229,9 @@ __global__ void __launch_bounds__(GCfg<WT, MT>::kThreads, 1) gemv_kernel(const G
 
   // ----------------------------------------------------------- compute warps
   const int tid = threadIdx.x;  // 0..255
+  // The producer streams W (constant) at once; x and every global write wait
+  // for the previous kernel of the stream.
+  griddep_wait();
   {
     // x -> shared memory (bf16 as is, or widened to fp32 for fp32 weights;
     // zero rows beyond m)
@@ -290,7 +295,8 @@ __global__ void __launch_bounds__(GCfg<WT, MT>::kThreads, 1) gemv_kernel(const G
       const int col_base = static_cast<int>(seg_lo - row * ks) * kChunkElems - cc0 * kChunkElems;
 #pragma unroll 2
       for (int cc = cc0; cc < cc1; ++cc) {
-        chunk_partial<WT, MT>(stage + cc * C::kChunkBytes, xs, p.K, col_base + cc * kChunkElems,
+        chunk_partial<WT, MT>(smem_u32(stage + cc * C::kChunkBytes), smem_u32(xs), p.K,
+                              col_base + cc * kChunkElems,
                               lane, acc);
       }
 #pragma unroll
@@ -379,9 +385,14 @@ cudaError_t launch(const GemvParams& p, cudaStream_t s) {
   cfg.blockDim = dim3(GCfg<WT, MT>::kThreads);
   cfg.dynamicSmemBytes = GCfg<WT, MT>::kSmem;
   cfg.stream = s;
+  // No cooperative launch: a CTA waits only on its predecessor (blockIdx - 1),
+  // which is dispatched no later than it, and G <= SMs at one CTA per SM,
+  // so every wait ends even while the previous kernel still holds SMs.
+  // Programmatic stream serialization lets this grid start under the
+  // previous kernel's tail (see griddep_wait above).
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, gemv_kernel<WT, MT>, p);

@@ -119,10 +119,14 @@ struct ClusterParams {
   int KB;               // weight k-blocks per tile row
   int KBx;              // x k-blocks (K / 64)
   int MT;               // ceil(m / BN)
-  int CS;               // cluster size = K split
+  int CS;               // cluster size
+  int KG;               // clusters per output tile (K split = KG x CS)
   int out_f32;
+  float* ws;            // KG > 1: [T MT][KG][BN][128] fp32 cluster partials
+  uint32_t* counters;   // KG > 1: [T MT][CS], zero between calls
 };
-constexpr int kClusterMaxCS = 16;
+constexpr int kClusterMaxCS = 16;      // CTAs per cluster, at most
+constexpr int kClusterMaxGroups = 16;  // clusters per output tile, at most
 bool cluster_supported(int BN);
 cudaError_t cluster_init_attributes();
 int cluster_max_active(int BN, int cs);

@@ -265,6 +265,29 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
   return v;
 }
 
+// Shared-memory loads through 32-bit shared-window addresses (ld.shared).
+// Buffers carved out of the dynamic shared-memory block by pointer
+// arithmetic lose their address space, and generic loads from them are much
+// slower.  volatile: the loads stay after the barrier and mbarrier waits that
+// publish the data (those are volatile asm as well).
+__device__ __forceinline__ uint4 ld_shared_u4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+// Programmatic dependent launch.  launch_dependents lets the next kernel of
+// the stream (launched with programmatic stream serialization) start once
+// every CTA of this grid has issued it or exited; wait blocks until the
+// grids this one depends on have completed and their memory is visible
+// (it returns at once when there is no such dependency).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
   uint32_t old;
   asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)

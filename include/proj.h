@@ -113,9 +113,12 @@ enum proj_kernel {
     PROJ_KERNEL_GEMV = 1,   /* row-streaming CUDA-core GEMV, m <= 2 */
     PROJ_KERNEL_TILE = 2,   /* tiled kernels: tensor cores (bf16) / FMA tiles (router),
                                split-K across CTAs through global memory */
-    PROJ_KERNEL_CLUSTER = 3 /* bf16 layers, dense weights: tensor cores, split-K inside a
-                               thread-block cluster combined through distributed shared
-                               memory; proj_run_opts.grid then sets the cluster size (1..8) */
+    PROJ_KERNEL_CLUSTER = 3 /* tensor cores (dense bf16 weights; the router's bf16 planes),
+                               split-K inside a thread-block cluster combined through
+                               distributed shared memory, and optionally across several
+                               clusters per tile through global memory:
+                               proj_run_opts.grid = cluster size (1..16),
+                               proj_run_opts.groups = clusters per tile (1..8) */
 };
 
 typedef struct proj_run_opts {
@@ -124,6 +127,10 @@ typedef struct proj_run_opts {
                        PROJ_KERNEL_CLUSTER; 0 = dispatch table */
     int reduce;     /* enum proj_reduce (tiled kernels); owner needs m <= 32 on bf16 */
     int kernel;     /* enum proj_kernel */
+    int groups;     /* PROJ_KERNEL_CLUSTER: clusters sharing one output tile's K
+                       (1..16); 0 = dispatch table */
+    int tile_n;     /* token tile width of the tensor-core kernels (16, 32, 64, 128
+                       or 256; the 12-bit kernel 16 or 32); 0 = dispatch table */
 } proj_run_opts;
 
 typedef struct proj_info_t {

@@ -153,6 +153,33 @@ def test_cluster_sizes_and_determinism(dev, layer, m):
     assert B.proj_device_status(h) == 0
 
 
+@pytest.mark.parametrize("layer,m", [("router", 3), ("router", 256), ("qkv_gate", 16),
+                                     ("unpooler", 8), ("o", 130), ("pooler", 64)])
+def test_cluster_groups_and_determinism(dev, layer, m):
+    """Several clusters per output tile, their partials summed through global
+    memory by whichever finishes last, in a fixed order: meets the contract,
+    is bitwise reproducible, and leaves its counters at zero (a second call
+    would go wrong otherwise)."""
+    h, W, _ = prepared(layer, 1)
+    sms = B.proj_num_sms()
+    # a forced cluster shape keeps the smallest token tile covering m
+    spec = wl.LAYER_BY_NAME[layer]
+    bn = next(b for b in (16, 32, 64, 128, 256) if m <= b or b == 256)
+    tiles = B.proj_out_features(h, m) // 128 * -(-m // bn)
+    kb = spec.K // 64 * (3 if layer == "router" else 1)
+    ran = 0
+    for cs, kg in ((1, 2), (2, 3), (4, 2), (8, 4), (16, 2), (3, 5), (1, 16), (5, 7)):
+        if tiles * cs * kg > sms or cs * kg > kb:
+            continue
+        kw = dict(grid=cs, groups=kg, kernel=B.PROJ_KERNEL_CLUSTER)
+        a = check_case(layer, 1, True, m, h=h, W=W, **kw)
+        b = check_case(layer, 1, True, m, h=h, W=W, **kw)
+        assert np.array_equal(a, b), (layer, m, cs, kg)
+        ran += 1
+    assert ran >= 1
+    assert B.proj_device_status(h) == 0
+
+
 def test_cluster_kernel_rejections(dev):
     h, _, _ = prepared("router", 0)
     x = torch.zeros((64, 8192), dtype=torch.bfloat16, device="cuda")
@@ -344,3 +371,38 @@ def test_read_floor_checksums(dev, mode):
             expect = np.bitwise_xor.reduce(seg[::4096]) if seg.size else 0
         assert int(sink[c].item()) & 0xFFFFFFFF == int(expect), c
     assert int(sink[grid].item()) == 0
+
+
+@pytest.mark.parametrize("m", [1, 2, 3, 16, 128, 256])
+def test_dependent_chain_back_to_back(dev, m):
+    """o -> pooler -> unpooler -> router with each layer's input the previous
+    layer's output, launched back to back on one stream with no host sync
+    (the kernels let their successor start early and wait for their
+    predecessor before reading x): every stage meets the contract against the
+    oracle applied to the GPU's own input for that stage."""
+    chain = ["o", "pooler", "unpooler"] + (["router"] if m > 8 else [])
+    hs = {name: prepared(name, 2) for name in chain}
+    x0 = to_dev_x(wl.make_activations("o", m, 9).x_bits)
+    rows = np.unique(np.linspace(0, m - 1, min(m, 12)).astype(np.int64))
+    for rep in range(3):
+        outs = []
+        for name in chain:
+            spec = wl.LAYER_BY_NAME[name]
+            dt = torch.float32 if spec.out_dtype == "fp32" else torch.bfloat16
+            outs.append(torch.full((m, B.proj_out_features(hs[name][0], m)), float("nan"),
+                                   dtype=dt, device="cuda"))
+        torch.cuda.synchronize()
+        x = x0
+        for name, o in zip(chain, outs):
+            B.proj_run(hs[name][0], x, m, o)
+            x = o
+        torch.cuda.synchronize()
+        xin = x0
+        for name, o in zip(chain, outs):
+            h, W, _ = hs[name]
+            x_bits = xin.view(torch.int16).cpu().numpy().view(np.uint16)
+            ref = oracle.reference(name, x_bits[rows], W)
+            res = oracle.check(name, out_f64(o)[rows], ref)
+            assert res["ok"], (m, rep, name, res)
+            assert B.proj_device_status(h) == 0
+            xin = o
