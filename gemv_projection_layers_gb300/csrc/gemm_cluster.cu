@@ -41,12 +41,20 @@ template <int BN>
 struct CCfg {
   static constexpr int kXBytes = BN * 128;
   static constexpr int kStage = kTileBytes + kXBytes;
-  static constexpr int kFit = (kSmemLimit - 1024 - 1024) / kStage;
+  // Narrow token tiles (the weight-streaming regime) take half an SM's
+  // shared memory, so that the next kernel of the stream -- launched early
+  // by programmatic dependent launch -- can sit beside this one and stream
+  // its first weights during this kernel's tail; wide tiles keep the SM.
+  static constexpr bool kHalfSm = BN <= 64;
+  static constexpr int kBlocksPerSm = kHalfSm ? 2 : 1;
+  static constexpr int kBudget = kHalfSm ? 113 * 1024 : kSmemLimit;
+  static constexpr int kFit = (kBudget - 1024 - 1024) / kStage;
   static constexpr int S = kFit > 12 ? 12 : kFit;
-  // warp 0 copies, warp 1 issues MMAs, warps 2..9 drain the accumulator
-  // (two per tensor-memory lane quarter, one column half each), all twelve
-  // warps combine the cluster's partials.
-  static constexpr int kThreads = 384;
+  // warp 0 copies, warp 1 issues MMAs, the next kDrainWarps drain the
+  // accumulator (one or two per tensor-memory lane quarter), and every warp
+  // combines the cluster's partials.
+  static constexpr int kThreads = kHalfSm ? 192 : 384;
+  static constexpr int kDrainWarps = kHalfSm ? 4 : 8;
   static constexpr int kTmemCols = BN < 32 ? 32 : BN;
   static constexpr size_t kRing = static_cast<size_t>(S) * kStage;
   static constexpr size_t kRed = static_cast<size_t>(BN) * kTileRows * 4;  // [BN][128] fp32
@@ -121,7 +129,7 @@ __device__ __forceinline__ void store_out(const ClusterParams& p, int mt, int t,
 }
 
 template <int BN>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(CCfg<BN>::kThreads, CCfg<BN>::kBlocksPerSm)
     tc_cluster_kernel(const __grid_constant__ CUtensorMap tmap_x, const ClusterParams p) {
   using C = CCfg<BN>;
   constexpr int S = C::S;
@@ -240,42 +248,38 @@ __global__ void __launch_bounds__(384, 1)
       }
       tc_commit(accf);  // also covers an aborted loop: arrives once prior MMAs finish
     }
-  } else if (warp < 10) {
+  } else if (warp < 2 + C::kDrainWarps) {
     // ------------------------------------- epilogue: accumulator -> smem
-    const int q = warp & 3;         // lane quarter this warp may access
-    const int half = (warp - 2) >> 2;  // column half
+    const int q = warp & 3;            // lane quarter this warp may access
+    const int part = (warp - 2) >> 2;  // column part
+    constexpr int kParts = (C::kDrainWarps == 8 && BN >= 32) ? 2 : 1;
+    constexpr int kCols = BN / kParts;
     const int r = q * 32 + lane;
-    if (mbar_wait(accf, 0, p.status, kStatusTimeoutEpilogue)) {
+    if (part < kParts && mbar_wait(accf, 0, p.status, kStatusTimeoutEpilogue)) {
       tc_fence_after();
       const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
-      constexpr int kHalf = BN / 2;
-      if constexpr (kHalf <= 16) {
-        if (half == 0) {
-          float v[16];
-          tmem_ld16(taddr, v);
-          tmem_ld_wait();
+      const int c_beg = part * kCols;
+      auto put = [&](int c, float val) {
+        st_shared_f32(red_base + static_cast<uint32_t>((c * kTileRows + r) * 4), val);
+      };
+      if constexpr (kCols == 16) {
+        float v[16];
+        tmem_ld16(taddr + c_beg, v);
+        tmem_ld_wait();
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj)
-            if (jj < BN) st_shared_f32(red_base + static_cast<uint32_t>((jj * kTileRows + r) * 4), v[jj]);
-        } else if (BN == 32) {
-          float v[16];
-          tmem_ld16(taddr + 16, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int jj = 0; jj < 16; ++jj) st_shared_f32(red_base + static_cast<uint32_t>(((16 + jj) * kTileRows + r) * 4), v[jj]);
-        }
+        for (int jj = 0; jj < 16; ++jj) put(c_beg + jj, v[jj]);
       } else {
         // two loads in flight per wait
 #pragma unroll 1
-        for (int c0 = half * kHalf; c0 < (half + 1) * kHalf; c0 += 32) {
+        for (int c0 = c_beg; c0 < c_beg + kCols; c0 += 32) {
           float v[16], u[16];
           tmem_ld16(taddr + c0, v);
           tmem_ld16(taddr + c0 + 16, u);
           tmem_ld_wait();
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) st_shared_f32(red_base + static_cast<uint32_t>(((c0 + jj) * kTileRows + r) * 4), v[jj]);
+          for (int jj = 0; jj < 16; ++jj) put(c0 + jj, v[jj]);
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) st_shared_f32(red_base + static_cast<uint32_t>(((c0 + 16 + jj) * kTileRows + r) * 4), u[jj]);
+          for (int jj = 0; jj < 16; ++jj) put(c0 + 16 + jj, u[jj]);
         }
       }
       tc_fence_before();
