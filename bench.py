@@ -252,6 +252,32 @@ def time_single_layers(B, torch, lg, flush, sink, reps):
     return res
 
 
+def time_router_forms(B, torch, S, flush, sink, stream, reps):
+    """The router at this load's token count in both of its forms, each as a
+    one-kernel graph timed like the read floor: the FP32-FMA kernels (the
+    default) and the tensor-core form on three exact bf16 planes (opt-in)."""
+    res = {}
+    for name, variant in (("fp32_fma", B.PROJ_VARIANT_AUTO), ("bf16x3_planes", B.PROJ_VARIANT_PLANES3)):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                B.proj_run_ex(S.h, S.x, S.m, S.out, stream, variant=variant)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            B.proj_run_ex(S.h, S.x, S.m, S.out, stream, variant=variant)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(reps)]
+        with torch.cuda.stream(stream):
+            for a, b in evs:
+                B.proj_read_floor(flush, flush.numel() * 4, sink, 0, 0, stream)
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+        stream.synchronize()
+        res[name] = round(float(np.mean([a.elapsed_time(b) * 1e3 for a, b in evs])), 2)
+    return res
+
+
 def time_load(B, torch, lg, flush, sink, steps, breakdown=False):
     outer, per = [], []
     for _ in range(steps):
@@ -516,6 +542,10 @@ def run_ours(args):
                              "kernel_sum_us": round(float(pl.mean(axis=0).sum()), 2),
                              "per_layer_us": {S.spec.name: round(float(u), 2) for S, u in
                                               zip(graphs[ld].shapes, pl.mean(axis=0))}}
+            rs = graphs[ld].shapes[-1]
+            if rs.spec.weight_dtype == "fp32" and rs.m >= 3:
+                loads_out[ld]["router_forms_single_graph_us"] = time_router_forms(
+                    B, torch, rs, flush, sink, stream, nrep)
         result["loads"] = loads_out
 
     if not args.no_extras and rank == 0:

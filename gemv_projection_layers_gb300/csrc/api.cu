@@ -112,14 +112,6 @@ int bn_for_m(int64_t m) {
   return 256;
 }
 
-int tm_for_m(int64_t m) {
-  if (m <= 4) return 4;
-  if (m <= 8) return 8;
-  if (m <= 16) return 16;
-  if (m <= 32) return 32;
-  return 64;
-}
-
 // Token counts up to which the 12-bit copy is used by the dispatch table.
 constexpr int64_t kExpwinAutoMaxM = 16;
 constexpr int64_t kExpwinMaxM = 32;
@@ -128,13 +120,13 @@ constexpr int64_t kExpwinMaxM = 32;
 // its last segment streams (short tail, but one CTA reads S - 1 partials);
 // the distributed form spreads that reading over the contributors.
 constexpr int64_t kTcOwnerMaxM = 8;
-constexpr int64_t kRouterOwnerMaxM = 4;
 
 constexpr int64_t kGemvMaxM = 2;
-// From three tokens on every layer goes to the cluster split-K kernel (the
-// router as three bf16 planes of its fp32 weights); below that, the GEMV.
+// From three tokens on every layer goes to a cluster split-K kernel (the
+// router to its FP32-FMA one); below that, the GEMV.
 constexpr int64_t kClusterMinM = 3;
 constexpr int64_t kRouterClusterMinM = 3;
+constexpr int kRouterMaxBN = 64;  // widest token tile of the FP32-FMA router kernel
 
 int bn_for_cluster(int64_t m) {
   if (m <= 16) return 16;
@@ -144,7 +136,7 @@ int bn_for_cluster(int64_t m) {
 }
 int bn_index(int bn) { return bn == 16 ? 0 : bn == 32 ? 1 : bn == 64 ? 2 : bn == 128 ? 3 : 4; }
 
-// Launch shape of the cluster kernel: token tile bn (the smallest covering m,
+// Launch shape of the cluster kernels: token tile bn (the smallest covering m,
 // or one or two halvings of it), cluster size cs and clusters per tile kg,
 // chosen by a cost model calibrated on GB300 (in-kernel timestamps and a
 // bulk-copy probe):
@@ -155,14 +147,20 @@ int bn_index(int bn) { return bn == 16 ? 0 : bn == 32 ? 1 : bn == 64 ? 2 : bn ==
 //   combine = remote part of the cluster's partials through distributed
 //             shared memory (~30 GB/s per SM, less in large clusters);
 //   groups  = kg > 1 adds a fence, an atomic and an L2 round trip (~2 us)
-//             plus the last cluster's reads of the kg partials.
+//             plus the last cluster's reads of the kg partials;
+//   FP32 FMA router: the stream cannot beat the CUDA cores' FMA rate.
 // Candidates keep every cluster resident in one wave (max_active), at most
 // one CTA per SM and at least kMinKbPerCta k-blocks per CTA.
 constexpr int kMinKbPerCta = 4;
 struct ClusterShape {
   int bn, cs, kg;
 };
-ClusterShape pick_cluster(int64_t m, int T, int KB, int64_t weight_bytes, int sms, int bn0,
+struct ClusterCost {
+  int64_t weight_bytes = 0;  // bytes of weights one call streams
+  int w_request = 16384;     // bytes of one weight-tile copy (one per k-block)
+  bool fma = false;          // CUDA-core FP32 FMAs instead of the tensor cores
+};
+ClusterShape pick_cluster(int64_t m, int T, int KB, const ClusterCost& cost, int sms, int bn0,
                           int bn_lo, const int (*max_active)[kClusterMaxCS]) {
   constexpr double kReqFloor = 160e-9;  // s per copy request, small copies
   constexpr double kReqRate = 135e9;    // bytes/s per SM, large copies
@@ -170,6 +168,9 @@ ClusterShape pick_cluster(int64_t m, int T, int KB, int64_t weight_bytes, int sm
   constexpr double kDsmem = 30e9;       // bytes/s per SM for clusters of <= 4
   constexpr double kL2 = 100e9;         // bytes/s per SM, group partial reads
   constexpr double kGroupFixed = 2e-6;  // s
+  constexpr double kFmaRate = 150e9;    // FP32 FMAs/s per SM, fma.rn.f32x2 register tiles
+  constexpr double kStageSync = 0.15e-6;  // s per stage of the FMA kernel (barriers)
+  const int64_t weight_bytes = cost.weight_bytes;
   ClusterShape best{bn0, 1, 1};
   double best_t = 1e30;
   for (int bn = bn0; bn >= 16 && bn >= bn_lo; bn /= 2) {
@@ -184,9 +185,11 @@ ClusterShape pick_cluster(int64_t m, int T, int KB, int64_t weight_bytes, int sm
         if (act > 0 && tiles * kg > act && !(cs == 1 && kg == 1)) continue;
         const double nk = static_cast<double>(KB) / (cs * kg);
         const double waves = static_cast<double>((ctas + sms - 1) / sms);
-        const double t_kb = std::max(kReqFloor, 16384.0 / kReqRate) +
+        const double t_kb = std::max(kReqFloor, cost.w_request / kReqRate) +
                             std::max(kReqFloor, 128.0 * bn / kReqRate);
         double t = std::max(nk * t_kb * waves, static_cast<double>(weight_bytes) / kHbm);
+        if (cost.fma)
+          t = std::max(t, nk * (128.0 * bn * kTileK / kFmaRate + kStageSync) * waves);
         if (cs > 1)
           t += (cs - 1.0) / cs * part / (kDsmem * std::min(1.0, std::sqrt(4.0 / cs)));
         if (kg > 1) t += kGroupFixed + kg * (part / cs) / kL2;
@@ -204,6 +207,7 @@ int mt_for_gemv(int64_t m) { return m <= 1 ? 1 : 2; }
 struct Plan {
   bool gemv;
   bool cluster;
+  bool planes = false;  // router on the tensor cores (three bf16 planes)
   int KG = 1;  // cluster kernel: clusters per output tile
   bool router;
   bool expwin;
@@ -227,7 +231,8 @@ struct proj_ctx {
   float* gemv_ws = nullptr;        // [num_sms][2]
   uint8_t* w_planes = nullptr;     // router: bf16 planes hi/mid/lo as [N, 3K] tiles
   uint32_t* cl_counters = nullptr; // cluster groups: [SMs][16], zero between calls
-  int cluster_active[5][kClusterMaxCS] = {};  // co-resident clusters: BN 16..256 x size 1..16
+  int cluster_active[5][kClusterMaxCS] = {};   // co-resident clusters: BN 16..256 x size 1..16
+  int rcluster_active[5][kClusterMaxCS] = {};  // the same for the FP32-FMA router kernel
   uint8_t* w_exp = nullptr;
   size_t w_exp_bytes = 0;
   int e0 = 0;
@@ -325,17 +330,14 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
                             (!opts || (opts->grid == 0 && opts->reduce == PROJ_REDUCE_AUTO &&
                                        opts->tile_n == 0));
   bool want_cluster;
+  pl->planes = false;
   if (pl->router) {
-    // The cluster kernel runs the router on its bf16 planes only.
-    if (variant == PROJ_VARIANT_PLANES3) {
-      if (kern != PROJ_KERNEL_AUTO && kern != PROJ_KERNEL_CLUSTER) return PROJ_EUNSUPPORTED;
-      want_cluster = true;
-    } else if (kern == PROJ_KERNEL_CLUSTER) {
-      if (variant != PROJ_VARIANT_AUTO) return PROJ_EUNSUPPORTED;
-      want_cluster = true;
-    } else {
-      want_cluster = auto_cluster && variant == PROJ_VARIANT_AUTO;
-    }
+    // From three tokens on (or when asked for) the router runs on the
+    // cluster kernels: FP32 FMAs on its fp32 weights, or -- on request --
+    // the tensor cores on its three exact bf16 planes.
+    if (variant == PROJ_VARIANT_EXPWIN12 || kern == PROJ_KERNEL_TILE) return PROJ_EUNSUPPORTED;
+    pl->planes = variant == PROJ_VARIANT_PLANES3;
+    want_cluster = true;
   } else {
     if (variant == PROJ_VARIANT_PLANES3) return PROJ_EUNSUPPORTED;
     if (kern == PROJ_KERNEL_CLUSTER && variant == PROJ_VARIANT_EXPWIN12) return PROJ_EUNSUPPORTED;
@@ -346,15 +348,22 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
     pl->cluster = true;
     pl->expwin = false;
     pl->reduce = 0;
+    const bool fma = pl->router && !pl->planes;
+    if (fma && tile_n > kRouterMaxBN) return PROJ_EUNSUPPORTED;
     pl->T = static_cast<int>(pl->n_out / kTileRows);
-    pl->KB = static_cast<int>(h->K / kTileK) * (pl->router ? 3 : 1);
-    const int64_t wbytes = pl->n_out * h->K * (pl->router ? 6 : 2);
+    pl->KB = static_cast<int>(h->K / kTileK) * (pl->planes ? 3 : 1);
+    ClusterCost cost;
+    cost.weight_bytes = pl->n_out * h->K * (pl->planes ? 6 : (pl->router ? 4 : 2));
+    cost.w_request = fma ? kRfBytes : kTileBytes;
+    cost.fma = fma;
     // A forced tile width, cluster size or group count keeps the token tile
     // the smallest covering m (or the forced one).
     const bool forced = opts && (opts->grid > 0 || opts->groups > 0);
-    const int bn0 = tile_n ? tile_n : bn_for_cluster(m);
-    const ClusterShape shp = pick_cluster(m, pl->T, pl->KB, wbytes, h->num_sms, bn0,
-                                          (tile_n || forced) ? bn0 : bn0 / 4, h->cluster_active);
+    int bn0 = tile_n ? tile_n : bn_for_cluster(m);
+    if (fma && bn0 > kRouterMaxBN) bn0 = kRouterMaxBN;
+    const ClusterShape shp =
+        pick_cluster(m, pl->T, pl->KB, cost, h->num_sms, bn0, (tile_n || forced) ? bn0 : bn0 / 4,
+                     fma ? h->rcluster_active : h->cluster_active);
     pl->bn = shp.bn;
     pl->MT = static_cast<int>((m + pl->bn - 1) / pl->bn);
     int cs = shp.cs, kg = shp.kg;
@@ -371,15 +380,7 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
     pl->KG = kg;
     return PROJ_OK;
   }
-  if (pl->router) {
-    if (variant == PROJ_VARIANT_EXPWIN12 || variant == PROJ_VARIANT_PLANES3)
-      return PROJ_EUNSUPPORTED;
-    pl->expwin = false;
-    if (tile_n) return PROJ_EUNSUPPORTED;  // the FMA tiles pick their own width
-    pl->bn = tm_for_m(m);
-    pl->T = static_cast<int>(h->N / kRtRows);
-    pl->KB = static_cast<int>(h->K / kRtK);
-  } else {
+  {
     bool use_exp = false;
     if (variant == PROJ_VARIANT_EXPWIN12) {
       if (!h->w_exp || m > kExpwinMaxM) return PROJ_EUNSUPPORTED;
@@ -397,9 +398,9 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
   }
   const int rq = opts ? opts->reduce : PROJ_REDUCE_AUTO;
   if (rq == PROJ_REDUCE_AUTO) {
-    pl->reduce = (m <= (pl->router ? kRouterOwnerMaxM : kTcOwnerMaxM)) ? 0 : 1;
+    pl->reduce = (m <= kTcOwnerMaxM) ? 0 : 1;
   } else if (rq == PROJ_REDUCE_OWNER) {
-    if (!pl->router && pl->bn > 32) return PROJ_EUNSUPPORTED;
+    if (pl->bn > 32) return PROJ_EUNSUPPORTED;
     pl->reduce = 0;
   } else if (rq == PROJ_REDUCE_DISTRIBUTED) {
     pl->reduce = 1;
@@ -499,14 +500,17 @@ proj_handle proj_prepare_ex(int layer, const void* W, int64_t N, int64_t K, int 
       cudaSuccess)
     return bail_cuda(e, "cudaDeviceGetAttribute");
   if ((e = tc_init_attributes()) != cudaSuccess) return bail_cuda(e, "tc attributes");
-  if ((e = router_init_attributes()) != cudaSuccess) return bail_cuda(e, "router attributes");
+  if ((e = router_cluster_init_attributes()) != cudaSuccess)
+    return bail_cuda(e, "router attributes");
   if ((e = gemv_init_attributes()) != cudaSuccess) return bail_cuda(e, "gemv attributes");
   if ((e = cluster_init_attributes()) != cudaSuccess) return bail_cuda(e, "cluster attributes");
   {
     const int bns[5] = {16, 32, 64, 128, 256};
     for (int b = 0; b < 5; ++b)
-      for (int c = 0; c < kClusterMaxCS; ++c)
+      for (int c = 0; c < kClusterMaxCS; ++c) {
         h->cluster_active[b][c] = cluster_max_active(bns[b], c + 1);
+        h->rcluster_active[b][c] = router_cluster_max_active(bns[b], c + 1);
+      }
   }
   if (!encode_fn()) return bail_cuda(cudaErrorNotSupported, "cuTensorMapEncodeTiled");
 
@@ -522,8 +526,8 @@ proj_handle proj_prepare_ex(int layer, const void* W, int64_t N, int64_t K, int 
       done();
       return bail_cuda(e, "cudaMalloc(weights)");
     }
-    if ((e = pack_router_tiles(static_cast<const float*>(W), static_cast<int>(N),
-                               static_cast<int>(K), h->w_dense, s)) != cudaSuccess) {
+    if ((e = pack_router_fma_tiles(static_cast<const float*>(W), static_cast<int>(N),
+                                   static_cast<int>(K), h->w_dense, s)) != cudaSuccess) {
       done();
       return bail_cuda(e, "pack router");
     }
@@ -536,10 +540,8 @@ proj_handle proj_prepare_ex(int layer, const void* W, int64_t N, int64_t K, int 
       done();
       return bail_cuda(e, "pack router planes");
     }
-    const int tm_max = tm_for_m(std::min<int64_t>(m_max, 64));
-    h->ws_bytes = static_cast<size_t>(2 * sms) * 64 * tm_max * 4;
-    const int64_t mt_max = (m_max + 63) / 64;
-    h->counters_bytes = static_cast<size_t>(std::max<int64_t>(mt_max, 1) * (N / kRtRows)) * 4;
+    h->ws_bytes = 16;  // sized below for the cluster groups
+    h->counters_bytes = 16;
   } else {
     h->w_dense_bytes = static_cast<size_t>(N) * K * 2;
     if ((e = dmalloc(&h->w_dense, h->w_dense_bytes)) != cudaSuccess) {
@@ -681,11 +683,11 @@ int proj_run_ex(proj_handle h, const void* x, int64_t m, void* out, proj_stream 
     if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
     return PROJ_OK;
   }
-  const CUtensorMap* map = get_map(h, x, m, pl.bn, pl.cluster || !pl.router);
+  const CUtensorMap* map = get_map(h, x, m, pl.bn, true);
   if (!map) return fail_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(x)");
   if (pl.cluster) {
     ClusterParams c;
-    c.w = pl.router ? h->w_planes : h->w_dense;
+    c.w = pl.planes ? h->w_planes : h->w_dense;
     c.KBx = static_cast<int>(h->K / kTileK);
     c.out_f32 = pl.router ? 1 : 0;
     c.out = out;
@@ -699,25 +701,12 @@ int proj_run_ex(proj_handle h, const void* x, int64_t m, void* out, proj_stream 
     c.KG = pl.KG;
     c.ws = reinterpret_cast<float*>(h->ws);
     c.counters = h->cl_counters;
-    e = cluster_launch(pl.bn, *map, c, s);
+    e = (pl.router && !pl.planes) ? router_cluster_launch(pl.bn, *map, c, s)
+                                   : cluster_launch(pl.bn, *map, c, s);
     if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
     return PROJ_OK;
   }
-  if (pl.router) {
-    RouterParams p;
-    p.w = h->w_dense;
-    p.out = static_cast<float*>(out);
-    p.ws = h->ws;
-    p.counters = h->counters;
-    p.status = h->status;
-    p.m = static_cast<int>(m);
-    p.T = pl.T;
-    p.KB = pl.KB;
-    p.MT = pl.MT;
-    p.G = pl.G;
-    p.reduce = pl.reduce;
-    e = router_launch(pl.bn, *map, p, s);
-  } else {
+  {
     TcParams p;
     p.w = pl.expwin ? h->w_exp : h->w_dense;
     p.out = out;
@@ -790,16 +779,15 @@ int proj_describe(proj_handle h, int64_t m, char* buf, size_t cap) {
     std::snprintf(buf, cap, "gemv_%s MT=%d G=%d n_rows=%lld", pl.router ? "f32w" : "bf16w", pl.bn,
                   pl.G, static_cast<long long>(pl.n_out));
   } else if (pl.cluster) {
+    const bool fma = pl.router && !pl.planes;
     std::snprintf(buf, cap,
-                  "tc_cluster%s BN=%d stages=%d CS=%d KG=%d CTAs=%d T=%d KB=%d MT=%d "
+                  "%s BN=%d stages=%d CS=%d KG=%d CTAs=%d T=%d KB=%d MT=%d "
                   "n_out=%lld resident_clusters=%d",
-                  pl.router ? "_planes3" : "", pl.bn, cluster_stages(pl.bn), pl.G, pl.KG,
+                  fma ? "fma_cluster" : (pl.planes ? "tc_cluster_planes3" : "tc_cluster"), pl.bn,
+                  fma ? router_cluster_stages(pl.bn) : cluster_stages(pl.bn), pl.G, pl.KG,
                   pl.MT * pl.T * pl.KG * pl.G, pl.T, pl.KB, pl.MT,
                   static_cast<long long>(pl.n_out),
-                  h->cluster_active[bn_index(pl.bn)][pl.G - 1]);
-  } else if (pl.router) {
-    std::snprintf(buf, cap, "router_fma TM=%d stages=8 G=%d T=%d KB=%d MT=%d reduce=%s", pl.bn,
-                  pl.G, pl.T, pl.KB, pl.MT, pl.reduce ? "distributed" : "owner");
+                  (fma ? h->rcluster_active : h->cluster_active)[bn_index(pl.bn)][pl.G - 1]);
   } else {
     std::snprintf(buf, cap, "tc_%s BN=%d stages=%d G=%d T=%d KB=%d MT=%d n_out=%lld reduce=%s",
                   pl.expwin ? "expwin12" : "dense", pl.bn, tc_stages(pl.bn, pl.expwin), pl.G,
@@ -820,8 +808,8 @@ int proj_unpack_weights(proj_handle h, int variant, void* W_out, proj_stream str
       e = unpack_router_planes(h->w_planes, static_cast<int>(h->N), static_cast<int>(h->K),
                                static_cast<float*>(W_out), s);
     else
-      e = unpack_router_tiles(h->w_dense, static_cast<int>(h->N), static_cast<int>(h->K),
-                              static_cast<float*>(W_out), s);
+      e = unpack_router_fma_tiles(h->w_dense, static_cast<int>(h->N), static_cast<int>(h->K),
+                                  static_cast<float*>(W_out), s);
   } else if (variant == PROJ_VARIANT_PLANES3) {
     return fail(PROJ_EUNSUPPORTED);
   } else if (variant == PROJ_VARIANT_EXPWIN12 ||

@@ -38,12 +38,12 @@ constexpr int kRecNibOff = 8192;
 constexpr int kRecEscOff = 12288;
 constexpr int kEscCap = 15;
 
-// Router (fp32) tiles: 64 rows x 64 columns, 16384 bytes, tile (t, kb) at
-// (t * 128 + kb) * 16384; row r at r * 256, its float4 q (columns 4q .. 4q+3)
-// at slot q ^ (r & 7).
-constexpr int kRtRows = 64;
-constexpr int kRtK = 64;
-constexpr int kRtBytes = kRtRows * kRtK * 4;
+// Router (fp32) tiles for the FMA kernel: 128 rows x 64 columns, 32768
+// bytes, tile (t, kb) at (t * K / 64 + kb) * 32768; row r at r * 256, its
+// 16-byte chunk c (columns 4c .. 4c+3) at slot c ^ (r & 15).
+constexpr int kRfRows = 128;
+constexpr int kRfK = 64;
+constexpr int kRfBytes = kRfRows * kRfK * 4;
 
 struct TcParams {
   const uint8_t* w;     // packed tiles or 12-bit records
@@ -62,19 +62,6 @@ struct TcParams {
   int reduce;           // split-K combine: 0 = owner, 1 = distributed
 };
 
-struct RouterParams {
-  const uint8_t* w;     // packed router tiles
-  float* out;           // fp32 [m, 256]
-  float* ws;            // [2 G][64 * TM] fp32
-  uint32_t* counters;   // [MT * 4]
-  uint32_t* status;
-  int m;
-  int T;                // 4
-  int KB;               // 128
-  int MT;               // ceil(m / TM)
-  int G;
-  int reduce;           // split-K combine: 0 = owner, 1 = distributed
-};
 
 // Streaming GEMV (m <= 2): W row-major, bf16 or fp32; MT in {1, 2}.
 struct GemvParams {
@@ -134,12 +121,12 @@ int cluster_stages(int BN);
 cudaError_t cluster_launch(int BN, const CUtensorMap& tmap_x, const ClusterParams& p,
                            cudaStream_t s);
 
-// Router FP32-FMA path: TM in {4, 8, 16, 32, 64}.
-bool router_supported(int TM);
-size_t router_smem_bytes(int TM);
-cudaError_t router_init_attributes();
-cudaError_t router_launch(int TM, const CUtensorMap& tmap_x, const RouterParams& p,
-                          cudaStream_t s);
+// FP32-FMA router on the cluster split-K skeleton: BN in {16, 32, 64}.
+cudaError_t router_cluster_init_attributes();
+int router_cluster_max_active(int BN, int cs);
+int router_cluster_stages(int BN);
+cudaError_t router_cluster_launch(int BN, const CUtensorMap& tmap_x, const ClusterParams& p,
+                                  cudaStream_t s);
 
 // Prepare-time kernels (prep.cu).
 cudaError_t pack_bf16_tiles(const uint16_t* W, int N, int K, uint8_t* dst, cudaStream_t s);
@@ -149,8 +136,8 @@ cudaError_t encode_expwin12(const uint16_t* W, int N, int K, int e0, uint8_t* ds
                             uint32_t* overflow, unsigned long long* n_esc, cudaStream_t s);
 cudaError_t decode_expwin12(const uint8_t* src, int N, int K, int e0, uint16_t* W,
                             cudaStream_t s);
-cudaError_t pack_router_tiles(const float* W, int N, int K, uint8_t* dst, cudaStream_t s);
-cudaError_t unpack_router_tiles(const uint8_t* src, int N, int K, float* W, cudaStream_t s);
+cudaError_t pack_router_fma_tiles(const float* W, int N, int K, uint8_t* dst, cudaStream_t s);
+cudaError_t unpack_router_fma_tiles(const uint8_t* src, int N, int K, float* W, cudaStream_t s);
 // Router W -> bf16 planes hi, mid, lo (hi + mid + lo == W) packed as the bf16
 // tiles of a [N, 3K] matrix: tile (t, p KB + kb) holds plane p.
 cudaError_t pack_router_planes(const float* W, int N, int K, uint8_t* dst, cudaStream_t s);

@@ -3,7 +3,7 @@
 //   * histogram of the 7 high exponent bits, and the 12-bit exponent-window
 //     encoder/decoder (muse_bf16_proj project report, "Round 5 -- lossless
 //     12-bit compressed weights", "Format");
-//   * router fp32 W -> 64 x 64 swizzled tiles (and back);
+//   * router fp32 W -> 128 x 64 swizzled tiles for the FMA kernel (and back);
 //   * router fp32 W -> three bf16 planes hi + mid + lo == W (exact), packed as
 //     bf16 tiles of a [N, 3K] matrix whose column p K + k holds plane p of
 //     W[:, k] (and back, summing the planes).
@@ -172,36 +172,36 @@ __global__ void decode_expwin12_kernel(const uint8_t* __restrict__ src, int N, i
   }
 }
 
-// Router: one thread per float4 of W.
-__global__ void pack_router_kernel(const float* __restrict__ W, int N, int K,
-                                   uint8_t* __restrict__ dst) {
+// Router (FMA tiles): one thread per float4 of W.
+__global__ void pack_router_fma_kernel(const float* __restrict__ W, int N, int K,
+                                       uint8_t* __restrict__ dst) {
   const int64_t quads = static_cast<int64_t>(N) * (K / 4);
-  const int KB = K / kRtK;
+  const int KB = K / kRfK;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < quads;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int n = static_cast<int>(i / (K / 4));
     const int k4 = static_cast<int>(i % (K / 4));
-    const int t = n / kRtRows, r = n % kRtRows;
-    const int kb = k4 / 16, q = k4 % 16;
+    const int t = n / kRfRows, r = n % kRfRows;
+    const int kb = k4 / 16, c = k4 % 16;
     const float4 v = *reinterpret_cast<const float4*>(W + static_cast<size_t>(n) * K + k4 * 4);
-    uint8_t* tile = dst + (static_cast<size_t>(t) * KB + kb) * kRtBytes;
-    *reinterpret_cast<float4*>(tile + r * 256 + ((q ^ (r & 7)) << 4)) = v;
+    uint8_t* tile = dst + (static_cast<size_t>(t) * KB + kb) * kRfBytes;
+    *reinterpret_cast<float4*>(tile + r * 256 + ((c ^ (r & 15)) << 4)) = v;
   }
 }
 
-__global__ void unpack_router_kernel(const uint8_t* __restrict__ src, int N, int K,
-                                     float* __restrict__ W) {
+__global__ void unpack_router_fma_kernel(const uint8_t* __restrict__ src, int N, int K,
+                                         float* __restrict__ W) {
   const int64_t quads = static_cast<int64_t>(N) * (K / 4);
-  const int KB = K / kRtK;
+  const int KB = K / kRfK;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < quads;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int n = static_cast<int>(i / (K / 4));
     const int k4 = static_cast<int>(i % (K / 4));
-    const int t = n / kRtRows, r = n % kRtRows;
-    const int kb = k4 / 16, q = k4 % 16;
-    const uint8_t* tile = src + (static_cast<size_t>(t) * KB + kb) * kRtBytes;
+    const int t = n / kRfRows, r = n % kRfRows;
+    const int kb = k4 / 16, c = k4 % 16;
+    const uint8_t* tile = src + (static_cast<size_t>(t) * KB + kb) * kRfBytes;
     *reinterpret_cast<float4*>(W + static_cast<size_t>(n) * K + k4 * 4) =
-        *reinterpret_cast<const float4*>(tile + r * 256 + ((q ^ (r & 7)) << 4));
+        *reinterpret_cast<const float4*>(tile + r * 256 + ((c ^ (r & 15)) << 4));
   }
 }
 
@@ -317,8 +317,8 @@ cudaError_t decode_expwin12(const uint8_t* src, int N, int K, int e0, uint16_t* 
   return cudaGetLastError();
 }
 
-cudaError_t pack_router_tiles(const float* W, int N, int K, uint8_t* dst, cudaStream_t s) {
-  pack_router_kernel<<<kPrepGrid, kPrepBlock, 0, s>>>(W, N, K, dst);
+cudaError_t pack_router_fma_tiles(const float* W, int N, int K, uint8_t* dst, cudaStream_t s) {
+  pack_router_fma_kernel<<<kPrepGrid, kPrepBlock, 0, s>>>(W, N, K, dst);
   return cudaGetLastError();
 }
 
@@ -332,8 +332,9 @@ cudaError_t unpack_router_planes(const uint8_t* src, int N, int K, float* W, cud
   return cudaGetLastError();
 }
 
-cudaError_t unpack_router_tiles(const uint8_t* src, int N, int K, float* W, cudaStream_t s) {
-  unpack_router_kernel<<<kPrepGrid, kPrepBlock, 0, s>>>(src, N, K, W);
+cudaError_t unpack_router_fma_tiles(const uint8_t* src, int N, int K, float* W,
+                                    cudaStream_t s) {
+  unpack_router_fma_kernel<<<kPrepGrid, kPrepBlock, 0, s>>>(src, N, K, W);
   return cudaGetLastError();
 }
 

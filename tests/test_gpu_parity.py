@@ -113,16 +113,15 @@ def test_parity_all_shapes(dev, layer, m):
         check_case(layer, seed, outl, m)
 
 
-@pytest.mark.parametrize("layer,m", [("o", 1), ("o", 33), ("router", 1), ("router", 33),
-                                     ("unpooler", 8), ("qkv_gate", 130), ("pooler", 16),
-                                     ("router", 256)])
+@pytest.mark.parametrize("layer,m", [("o", 1), ("o", 33), ("unpooler", 8), ("qkv_gate", 130),
+                                     ("pooler", 16)])
 def test_split_partitions_and_determinism(dev, layer, m):
-    """Every partition and both split-K combine modes of the tiled kernels
-    meet the contract and are bitwise reproducible."""
+    """Every partition and both split-K combine modes of the stream-K
+    tensor-core kernel meet the contract and are bitwise reproducible."""
     h, W, _ = prepared(layer, 0)
     sms = B.proj_num_sms()
     modes = [B.PROJ_REDUCE_DISTRIBUTED]
-    if layer == "router" or m <= 32:
+    if m <= 32:
         modes.append(B.PROJ_REDUCE_OWNER)
     for reduce in modes:
         for grid in (1, 7, 64, sms - 1, sms):
@@ -140,11 +139,11 @@ def test_split_partitions_and_determinism(dev, layer, m):
                                      ("router", 256), ("router", 1000)])
 def test_cluster_sizes_and_determinism(dev, layer, m):
     """The cluster split-K kernel at every cluster size (1..16 CTAs sharing K)
-    meets the contract and is bitwise reproducible; for the router it runs the
-    three bf16 planes of the fp32 weights."""
+    meets the contract and is bitwise reproducible; for the router this is the
+    FP32-FMA cluster kernel (fp32 weights as they are)."""
     h, W, _ = prepared(layer, 0)
     if m >= (3 if layer == "router" else 33):
-        assert "tc_cluster" in B.proj_describe(h, m)
+        assert "cluster" in B.proj_describe(h, m)
     for cs in range(1, 17):
         kw = dict(grid=cs, kernel=B.PROJ_KERNEL_CLUSTER)
         a = check_case(layer, 0, True, m, h=h, W=W, **kw)
@@ -164,9 +163,12 @@ def test_cluster_groups_and_determinism(dev, layer, m):
     sms = B.proj_num_sms()
     # a forced cluster shape keeps the smallest token tile covering m
     spec = wl.LAYER_BY_NAME[layer]
+    # (the router's FP32-FMA kernel takes token tiles of at most 64)
     bn = next(b for b in (16, 32, 64, 128, 256) if m <= b or b == 256)
+    if layer == "router":
+        bn = min(bn, 64)
     tiles = B.proj_out_features(h, m) // 128 * -(-m // bn)
-    kb = spec.K // 64 * (3 if layer == "router" else 1)
+    kb = spec.K // 64
     ran = 0
     for cs, kg in ((1, 2), (2, 3), (4, 2), (8, 4), (16, 2), (3, 5), (1, 16), (5, 7)):
         if tiles * cs * kg > sms or cs * kg > kb:
@@ -180,15 +182,33 @@ def test_cluster_groups_and_determinism(dev, layer, m):
     assert B.proj_device_status(h) == 0
 
 
+@pytest.mark.parametrize("m", [1, 3, 16, 130, 256])
+def test_router_planes_variant(dev, m):
+    """The router's opt-in tensor-core form -- its fp32 weights as three exact
+    bf16 planes -- meets the router's 1e-4 contract (probe rows exactly) at
+    several cluster shapes, reproducibly."""
+    h, W, _ = prepared("router", 1)
+    for kw in (dict(), dict(grid=4), dict(grid=2, groups=4), dict(grid=16)):
+        kw = dict(kw, variant=B.PROJ_VARIANT_PLANES3)
+        if kw.get("grid") or kw.get("groups"):
+            kw["kernel"] = B.PROJ_KERNEL_CLUSTER
+        a = check_case("router", 1, True, m, h=h, W=W, **kw)
+        b = check_case("router", 1, True, m, h=h, W=W, **kw)
+        assert np.array_equal(a, b), (m, kw)
+    assert B.proj_device_status(h) == 0
+
+
 def test_cluster_kernel_rejections(dev):
     h, _, _ = prepared("router", 0)
     x = torch.zeros((64, 8192), dtype=torch.bfloat16, device="cuda")
     out = torch.zeros((64, 256), dtype=torch.float32, device="cuda")
-    for kw in (dict(kernel=B.PROJ_KERNEL_CLUSTER, variant=B.PROJ_VARIANT_DENSE),
+    for kw in (dict(kernel=B.PROJ_KERNEL_TILE),
                dict(kernel=B.PROJ_KERNEL_TILE, variant=B.PROJ_VARIANT_PLANES3),
-               dict(kernel=B.PROJ_KERNEL_GEMV, variant=B.PROJ_VARIANT_PLANES3)):
+               dict(kernel=B.PROJ_KERNEL_GEMV, variant=B.PROJ_VARIANT_PLANES3),
+               dict(kernel=B.PROJ_KERNEL_CLUSTER, tile_n=256),
+               dict(variant=B.PROJ_VARIANT_EXPWIN12)):
         with pytest.raises(B.ProjError) as e:
-            B.proj_run_ex(h, x, 2 if kw["kernel"] == B.PROJ_KERNEL_GEMV else 64, out, **kw)
+            B.proj_run_ex(h, x, 2 if kw.get("kernel") == B.PROJ_KERNEL_GEMV else 64, out, **kw)
         assert e.value.status == B.PROJ_EUNSUPPORTED, kw
     h, _, _ = prepared("o", 0)
     x = torch.zeros((64, 1024), dtype=torch.bfloat16, device="cuda")
