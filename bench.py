@@ -407,6 +407,11 @@ def cpu_baseline(load_m: int, budget_s: float = 10.0, seed: int = 0):
     return dt / n * 1e6, oracle.threads(), n
 
 
+# GB300's maximum SM clock (nvidia-smi clocks.max.sm), for the derived FP32
+# FMA peak of the router's CUDA-core path.
+FP32_PEAK_CLOCK_GHZ = 2.07
+
+
 def traffic_from_profiles(kernel_key: str):
     """DRAM bytes per launch recorded from an ncu capture, if still current."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.json")
@@ -416,8 +421,10 @@ def traffic_from_profiles(kernel_key: str):
         if not e:
             return None
         import hashlib
-        src = os.path.join(ROOT, e["source"])
-        if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != e["source_sha"]:
+        h = hashlib.sha256()
+        for src in e["sources"]:
+            h.update(open(os.path.join(ROOT, src), "rb").read())
+        if h.hexdigest()[:16] != e["source_sha"]:
             return None
         return float(e["bytes_per_launch"])
     except Exception:
@@ -482,6 +489,23 @@ def run_ours(args):
     dom_us = float(layer_us[di])
     achieved = dom_bytes / (dom_us * 1e-6) / 1e9
     kernel_key = f"{D.spec.name}_m{m}_{'expwin12' if wbpe == 1.5 else 'dense'}"
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_gbs, "unit": "GB/s",
+            "frac": round(achieved / hbm_gbs, 4),
+            "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                           if peak_src == "measured" else "fallback 6.8 TB/s"}
+    if D.spec.weight_dtype == "fp32" and m >= 3:
+        # The FP32-FMA router: bound by the CUDA cores' FP32 FMA rate when its
+        # FLOPs take longer at that peak than its bytes at the HBM peak.
+        sms = B.proj_num_sms()
+        alu_tflops = sms * 128 * 2 * FP32_PEAK_CLOCK_GHZ / 1e3
+        flops = 2.0 * m * D.n_out * D.spec.K
+        if flops / (alu_tflops * 1e12) > dom_bytes / (hbm_gbs * 1e9):
+            ach = flops / (dom_us * 1e-6) / 1e12
+            roof = {"bound": "alu", "achieved": round(ach, 2), "peak": round(alu_tflops, 1),
+                    "unit": "TFLOP/s", "frac": round(ach / alu_tflops, 4),
+                    "peak_source": f"derived: {sms} SMs x 128 FP32 lanes x 2 FLOP x "
+                                   f"{FP32_PEAK_CLOCK_GHZ} GHz (maximum SM clock)",
+                    "flops": flops}
     slice_rows = lg.shapes[3].n_out
 
     result = {
@@ -507,7 +531,8 @@ def run_ours(args):
                       "around each replay (includes one graph launch); per-layer = a second "
                       "pass with event nodes between the kernels" + (
                           "" if lg.inner else " (here: per-layer graphs)"),
-            "weights": "dense bf16; router fp32 (from m = 3 read as three exact bf16 planes)",
+            "weights": "dense bf16; router fp32 on FP32 FMAs (its opt-in bf16x3-planes tensor-core "
+                       "form is timed per load under loads.*.router_forms_single_graph_us)",
             "parallelism": f"replicas x{world}",
         },
         "median_us": round(float(np.median(outer)), 3),
@@ -515,14 +540,8 @@ def run_ours(args):
         "per_layer_us": {S.spec.name: round(float(u), 3) for S, u in zip(lg.shapes, layer_us)},
         "kernels": {S.spec.name: S.desc for S in lg.shapes},
         "roofline": {
-            "bound": "hbm",
+            **roof,
             "kernel": f"{D.spec.name} ({D.desc})",
-            "achieved": round(achieved, 1),
-            "peak": hbm_gbs,
-            "unit": "GB/s",
-            "frac": round(achieved / hbm_gbs, 4),
-            "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
-                           if peak_src == "measured" else "fallback 6.8 TB/s",
             "algorithmic_bytes": int(dom_bytes),
             "duration_us": round(dom_us, 3),
             "traffic": traffic_from_profiles(kernel_key),
