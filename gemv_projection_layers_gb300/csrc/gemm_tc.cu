@@ -482,6 +482,9 @@ __global__ void __launch_bounds__(Cfg<BN, EXPWIN>::kThreads, 1)
   }
 
   tc_fence_before();
+  // __syncthreads is an aligned barrier: the producer and MMA warps, whose
+  // lane 0 ran their loops alone, reconverge first.
+  __syncwarp();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();

@@ -198,26 +198,33 @@ __global__ void __launch_bounds__(RCfg<BN>::kThreads, 1)
           const int r = rg + 16 * i;
           ld_shared_2x64(wst + r * 256 + ((c ^ (r & 15)) << 4), w01[i], w23[i]);
         }
+        uint64_t x01[4], x23[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int jt = 8 * tt + 4 * tg + u;
           const uint2 xv = ld_shared_u2(xst + jt * 128 + ((((k0 >> 3) ^ (jt & 7))) << 4) +
                                         ((k0 >> 2) & 1) * 8);
-          const uint64_t x01 = bf16x2_to_f32x2(xv.x);
-          const uint64_t x23 = bf16x2_to_f32x2(xv.y);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            ffma2(acc[i][u], w01[i], x01);
-            ffma2(acc[i][u], w23[i], x23);
-          }
+          x01[u] = bf16x2_to_f32x2(xv.x);
+          x23[u] = bf16x2_to_f32x2(xv.y);
         }
+        // 32 independent pair-FMAs, then the 32 that depend on them
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+          for (int u = 0; u < 4; ++u) ffma2(acc[i][u], w01[i], x01[u]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+          for (int u = 0; u < 4; ++u) ffma2(acc[i][u], w23[i], x23[u]);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * s);
     }
   }
   // Every copy has landed and every stage has been read: the ring becomes
-  // the partial-tile area.
+  // the partial-tile area.  (__syncthreads is an aligned barrier: warp 0,
+  // whose lane 0 ran the producer loop alone, reconverges first.)
+  __syncwarp();
   __syncthreads();
   if (warp > 0) {
 #pragma unroll
