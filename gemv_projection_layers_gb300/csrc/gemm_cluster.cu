@@ -98,6 +98,12 @@ __global__ void __launch_bounds__(CCfg<BN>::kThreads, CCfg<BN>::kBlocksPerSm)
   const int kb1 = static_cast<int>((split + 1) * p.KB / nsplit);
   const int mv = min(BN, p.m - mt * BN);
 
+  // Thread 0 (the producer) sets up the barriers and issues the weights of
+  // the first ring's worth of stages before the CTA barrier: they are
+  // constant, so they stream before the wait on the previous kernel of the
+  // stream; x and every global write come after that wait.
+  const int pre = min(kb1 - kb0, S);
+  uint64_t pol = 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full0 + 8 * s, 1);
@@ -105,9 +111,18 @@ __global__ void __launch_bounds__(CCfg<BN>::kThreads, CCfg<BN>::kBlocksPerSm)
     }
     mbar_init(accf, 1);
     fence_mbar_init();
+    pol = policy_evict_first();
+    for (int j = 0; j < pre; ++j) {
+      const uint32_t fb = full0 + 8 * j;
+      mbar_arrive_expect_tx(fb, kTileBytes + C::kXBytes);
+      bulk_g2s(smem_u32(sA + j * kTileBytes),
+               p.w + (static_cast<size_t>(t) * p.KB + kb0 + j) * kTileBytes, kTileBytes, fb,
+               pol);
+    }
     prefetch_tmap(&tmap_x);
   }
   griddep_launch_dependents();
+  __syncwarp();
   __syncthreads();
   // The producer starts streaming at once; the tensor-memory allocation runs
   // meanwhile and is published to the MMA and epilogue warps (1..5) only.
@@ -126,18 +141,6 @@ __global__ void __launch_bounds__(CCfg<BN>::kThreads, CCfg<BN>::kBlocksPerSm)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
-      // The weights of the first ring's worth of stages stream before the
-      // wait on the previous kernel of the stream (they are constant); x and
-      // every global write come after it.
-      const int pre = min(kb1 - kb0, S);
-      for (int j = 0; j < pre; ++j) {
-        const uint32_t fb = full0 + 8 * j;
-        mbar_arrive_expect_tx(fb, kTileBytes + C::kXBytes);
-        bulk_g2s(smem_u32(sA + j * kTileBytes),
-                 p.w + (static_cast<size_t>(t) * p.KB + kb0 + j) * kTileBytes, kTileBytes, fb,
-                 pol);
-      }
       griddep_wait();
       for (int j = 0; j < pre; ++j)
         tma_load_2d(smem_u32(sB + j * C::kXBytes), &tmap_x, ((kb0 + j) % p.KBx) * kTileK,

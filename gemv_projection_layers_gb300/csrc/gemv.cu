@@ -177,8 +177,17 @@ __global__ void __launch_bounds__(GCfg<WT, MT>::kThreads, 1) gemv_kernel(const G
   const int ks = p.K / kChunkElems;  // slices per row (1..8)
   const int64_t C_total = static_cast<int64_t>(p.n_rows) * ks;
   const int64_t cta = blockIdx.x;
-  const int64_t q0 = part_begin(cta, C_total, p.G);
-  const int64_t q1 = part_begin(cta + 1, C_total, p.G);
+  // The partition in 32-bit arithmetic when it fits (every fixed layer):
+  // 64-bit divisions are software routines and delay the first copy.
+  int64_t q0, q1;
+  if (C_total < (int64_t{1} << 22)) {
+    const uint32_t ct = static_cast<uint32_t>(C_total), g = static_cast<uint32_t>(p.G);
+    q0 = static_cast<uint32_t>(blockIdx.x) * ct / g;
+    q1 = (static_cast<uint32_t>(blockIdx.x) + 1u) * ct / g;
+  } else {
+    q0 = part_begin(cta, C_total, p.G);
+    q1 = part_begin(cta + 1, C_total, p.G);
+  }
   const bool has_head = (q0 % ks) != 0;  // row q0 / ks began in CTA cta - 1
   const bool has_tail = (q1 % ks) != 0;  // row q1 / ks continues in CTA cta + 1
   const int64_t head_row = q0 / ks;
@@ -190,35 +199,46 @@ __global__ void __launch_bounds__(GCfg<WT, MT>::kThreads, 1) gemv_kernel(const G
   plan.n_tail_stages = has_tail ? 1 : 0;  // the tail piece is < ks <= 8 chunks
   const int64_t n_stages = plan.n_tail_stages + (plan.tail_lo - q0 + 7) / 8;
 
-  if (threadIdx.x == 0) {
+  // The producer thread sets up the ring.  Its copies go out after the CTA
+  // barrier: a bulk-copy issue blocks while the SM's copy queue is full, and
+  // issuing a ring's worth first held the compute warps (and the x staging)
+  // back by microseconds.
+  const bool producer = warp == kComputeWarps && lane == 0;
+  uint64_t pol = 0;
+  int64_t issued = 0;
+  auto issue = [&](int64_t j) {
+    const int s = static_cast<int>(j % S);
+    int64_t qs;
+    int ns;
+    plan.stage(j, qs, ns);
+    const uint32_t bytes = static_cast<uint32_t>(ns) * C::kChunkBytes;
+    mbar_arrive_expect_tx(full0 + 8 * s, bytes);
+    bulk_g2s(smem_u32(ring + static_cast<size_t>(s) * C::kStageBytes),
+             static_cast<const uint8_t*>(p.w) + qs * C::kChunkBytes, bytes, full0 + 8 * s, pol);
+  };
+  if (producer) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
     }
     fence_mbar_init();
+    pol = policy_evict_first();
   }
   for (int i = threadIdx.x; i < kSplitRing; i += blockDim.x) split_cnt[i] = 0;
   griddep_launch_dependents();
+  __syncwarp();
   __syncthreads();
 
   if (warp == kComputeWarps) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
-      const uint8_t* w = static_cast<const uint8_t*>(p.w);
-      int64_t j = 0;
+      int64_t j = issued;
       for (; j < n_stages; ++j) {
         const int s = static_cast<int>(j % S);
         if (!mbar_wait(empty0 + 8 * s, static_cast<uint32_t>(((j / S) & 1) ^ 1), p.status,
                        kStatusTimeoutProducer))
           break;
-        int64_t qs;
-        int ns;
-        plan.stage(j, qs, ns);
-        const uint32_t bytes = static_cast<uint32_t>(ns) * C::kChunkBytes;
-        mbar_arrive_expect_tx(full0 + 8 * s, bytes);
-        bulk_g2s(smem_u32(ring + static_cast<size_t>(s) * C::kStageBytes),
-                 w + qs * C::kChunkBytes, bytes, full0 + 8 * s, pol);
+        issue(j);
       }
       for (int64_t d = (j > S ? j - S : 0); d < j; ++d)
         mbar_wait(full0 + 8 * static_cast<int>(d % S), static_cast<uint32_t>((d / S) & 1),

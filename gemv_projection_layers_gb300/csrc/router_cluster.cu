@@ -112,31 +112,35 @@ __global__ void __launch_bounds__(RCfg<BN>::kThreads, 1)
   const int kb1 = static_cast<int>((split + 1) * p.KB / nsplit);
   const int mv = min(BN, p.m - mt * BN);
 
+  // Thread 0 (the producer) sets up the barriers and issues the weights of
+  // the first ring's worth of stages before the CTA barrier: they are
+  // constant, so they stream before the wait on the previous kernel of the
+  // stream; x comes after that wait.
+  const int pre = min(kb1 - kb0, S);
+  uint64_t pol = 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, C::kComputeWarps);
     }
     fence_mbar_init();
+    pol = policy_evict_first();
+    for (int j = 0; j < pre; ++j) {
+      const uint32_t fb = full0 + 8 * j;
+      mbar_arrive_expect_tx(fb, kRfBytes + C::kXBytes);
+      bulk_g2s(sW + j * kRfBytes, p.w + (static_cast<size_t>(t) * p.KB + kb0 + j) * kRfBytes,
+               kRfBytes, fb, pol);
+    }
     prefetch_tmap(&tmap_x);
   }
   griddep_launch_dependents();
+  __syncwarp();
   __syncthreads();
 
   bool ok = true;
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
-      // The weights of the first ring's worth of stages stream before the
-      // wait on the previous kernel of the stream; x comes after it.
-      const int pre = min(kb1 - kb0, S);
-      for (int j = 0; j < pre; ++j) {
-        const uint32_t fb = full0 + 8 * j;
-        mbar_arrive_expect_tx(fb, kRfBytes + C::kXBytes);
-        bulk_g2s(sW + j * kRfBytes, p.w + (static_cast<size_t>(t) * p.KB + kb0 + j) * kRfBytes,
-                 kRfBytes, fb, pol);
-      }
       griddep_wait();
       for (int j = 0; j < pre; ++j)
         tma_load_2d(sX + j * C::kXBytes, &tmap_x, (kb0 + j) * kRfK, mt * BN, full0 + 8 * j);
