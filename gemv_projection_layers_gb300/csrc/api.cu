@@ -122,6 +122,8 @@ constexpr int64_t kExpwinMaxM = 32;
 constexpr int64_t kTcOwnerMaxM = 8;
 
 constexpr int64_t kGemvMaxM = 2;
+// Weight streams up to this many bytes take the register-streaming GEMV.
+constexpr int64_t kGemvRegMaxBytes = 20ll << 20;
 // From three tokens on every layer goes to a cluster split-K kernel (the
 // router to its FP32-FMA one); below that, the GEMV.
 constexpr int64_t kClusterMinM = 3;
@@ -206,6 +208,7 @@ int mt_for_gemv(int64_t m) { return m <= 1 ? 1 : 2; }
 
 struct Plan {
   bool gemv;
+  bool gemv_reg = false;  // m <= 2: register-streaming form
   bool cluster;
   bool planes = false;  // router on the tensor cores (three bf16 planes)
   int KG = 1;  // cluster kernel: clusters per output tile
@@ -298,7 +301,7 @@ int64_t out_rows(const proj_ctx* h, int64_t m) {
 int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl) {
   const int variant = opts ? opts->variant : PROJ_VARIANT_AUTO;
   const int kern = opts ? opts->kernel : PROJ_KERNEL_AUTO;
-  if (kern < PROJ_KERNEL_AUTO || kern > PROJ_KERNEL_CLUSTER) return PROJ_EINVAL;
+  if (kern < PROJ_KERNEL_AUTO || kern > PROJ_KERNEL_GEMV_REG) return PROJ_EINVAL;
   if (variant < PROJ_VARIANT_AUTO || variant > PROJ_VARIANT_PLANES3) return PROJ_EINVAL;
   const int tile_n = opts ? opts->tile_n : 0;
   if (tile_n != 0 && tile_n != 16 && tile_n != 32 && tile_n != 64 && tile_n != 128 &&
@@ -309,8 +312,10 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
   // Streaming GEMV: small m, uncompressed weights.
   const bool gemv_ok =
       m <= kGemvMaxM && (variant == PROJ_VARIANT_AUTO || variant == PROJ_VARIANT_DENSE);
-  if (kern == PROJ_KERNEL_GEMV && !gemv_ok) return PROJ_EUNSUPPORTED;
-  if (gemv_ok && (kern == PROJ_KERNEL_GEMV || (kern == PROJ_KERNEL_AUTO && tile_n == 0))) {
+  if ((kern == PROJ_KERNEL_GEMV || kern == PROJ_KERNEL_GEMV_REG) && !gemv_ok)
+    return PROJ_EUNSUPPORTED;
+  if (gemv_ok && (kern == PROJ_KERNEL_GEMV || kern == PROJ_KERNEL_GEMV_REG ||
+                  (kern == PROJ_KERNEL_AUTO && tile_n == 0))) {
     pl->gemv = true;
     pl->expwin = false;
     pl->reduce = 0;
@@ -319,6 +324,18 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
     int64_t G = h->num_sms;
     if (opts && opts->grid > 0) G = std::min<int64_t>(opts->grid, h->num_sms);
     pl->G = static_cast<int>(std::min<int64_t>(G, pl->n_out));
+    // The register form keeps a CTA's chunk partials in shared memory.  It
+    // wins on the shorter weight streams (its loads start at once, with no
+    // ring set-up); the ring, with more bytes in flight per SM, wins on the
+    // long ones (measured on GB300: o, the unpooler slice and the router at
+    // m = 1; also qkv_gate at m = 2).
+    const int64_t chunks = pl->n_out * (h->K / 1024);
+    const bool reg_ok = (chunks + pl->G - 1) / pl->G <= kGemvRegMaxChunks;
+    if (kern == PROJ_KERNEL_GEMV_REG && !reg_ok) return PROJ_EUNSUPPORTED;
+    const int64_t wbytes = pl->n_out * h->K * (pl->router ? 4 : 2);
+    const bool reg_better = wbytes <= kGemvRegMaxBytes || (m == 2 && wbytes <= 2 * kGemvRegMaxBytes);
+    pl->gemv_reg =
+        kern == PROJ_KERNEL_GEMV_REG || (kern == PROJ_KERNEL_AUTO && reg_ok && reg_better);
     return PROJ_OK;
   }
   pl->gemv = false;
@@ -503,6 +520,7 @@ proj_handle proj_prepare_ex(int layer, const void* W, int64_t N, int64_t K, int 
   if ((e = router_cluster_init_attributes()) != cudaSuccess)
     return bail_cuda(e, "router attributes");
   if ((e = gemv_init_attributes()) != cudaSuccess) return bail_cuda(e, "gemv attributes");
+  if ((e = gemv_reg_init_attributes()) != cudaSuccess) return bail_cuda(e, "gemv attributes");
   if ((e = cluster_init_attributes()) != cudaSuccess) return bail_cuda(e, "cluster attributes");
   {
     const int bns[5] = {16, 32, 64, 128, 256};
@@ -679,7 +697,7 @@ int proj_run_ex(proj_handle h, const void* x, int64_t m, void* out, proj_stream 
     g.K = static_cast<int>(h->K);
     g.G = pl.G;
     g.out_f32 = pl.router ? 1 : 0;
-    e = gemv_launch(pl.router, pl.bn, g, s);
+    e = pl.gemv_reg ? gemv_reg_launch(pl.router, pl.bn, g, s) : gemv_launch(pl.router, pl.bn, g, s);
     if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
     return PROJ_OK;
   }
@@ -776,8 +794,8 @@ int proj_describe(proj_handle h, int64_t m, char* buf, size_t cap) {
   int st = make_plan(h, m, nullptr, &pl);
   if (st != PROJ_OK) return fail(st);
   if (pl.gemv) {
-    std::snprintf(buf, cap, "gemv_%s MT=%d G=%d n_rows=%lld", pl.router ? "f32w" : "bf16w", pl.bn,
-                  pl.G, static_cast<long long>(pl.n_out));
+    std::snprintf(buf, cap, "gemv%s_%s MT=%d G=%d n_rows=%lld", pl.gemv_reg ? "_reg" : "",
+                  pl.router ? "f32w" : "bf16w", pl.bn, pl.G, static_cast<long long>(pl.n_out));
   } else if (pl.cluster) {
     const bool fma = pl.router && !pl.planes;
     std::snprintf(buf, cap,

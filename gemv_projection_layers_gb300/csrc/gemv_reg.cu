@@ -1,0 +1,306 @@
+// gemv_reg.cu -- streaming GEMV for m <= 2 with the weights loaded straight
+// into registers (no shared-memory ring, no producer, no mbarriers).
+//
+// out[i, n] = sum_k x[i, k] W[n, k]            (muse_bf16_proj guide, ch. 1, §1.1)
+//
+// The partition is the ring GEMV's (gemv.cu): W row-major in 1024-element
+// chunks, the chunk sequence cut into G equal contiguous runs, one CTA each.
+// Here sixteen warps take the run's chunks round-robin, each chunk being 16
+// (bf16) or 32 (fp32) 16-byte loads across the warp, coalesced.  A warp keeps
+// two batches of chunks in flight (double-buffered registers: the next
+// batch's loads go out before the current batch is multiplied), so an SM has
+// ~128 KB of loads outstanding with no set-up beyond the launch.  x sits in
+// shared memory in the lanes' layout.  Each chunk's lane partials are reduced
+// by a shuffle tree and parked in shared memory; after a CTA barrier the rows
+// are summed over their chunks in chunk order (deterministic).  A row shared
+// with the previous CTA is finished as in the ring GEMV: the previous CTA
+// publishes its part with a release flag, this CTA adds it.  This follows the
+// pages' "weights straight to registers" GEMV (project report, "What was
+// built"; notebook n. 47), on a row-chunk partition instead of 16-row blocks.
+#include <cuda_bf16.h>
+
+#include <type_traits>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "splitk.cuh"
+
+namespace proj {
+namespace {
+
+constexpr int kChunk = 1024;
+constexpr int kWarps = 16;
+constexpr int kThreads = kWarps * 32;
+
+template <typename WT, int MT>
+struct RCfgG {
+  using XT = typename std::conditional<sizeof(WT) == 2, uint16_t, float>::type;
+  static constexpr int kVec = 16 / static_cast<int>(sizeof(WT));       // weights per 16 B
+  static constexpr int kLd = kChunk / kVec / 32;                        // 16-B loads per lane
+  static constexpr int U = sizeof(WT) == 2 ? 2 : 1;                      // chunks per batch
+  static constexpr int kXBytes = MT * 8192 * static_cast<int>(sizeof(XT));  // K <= 8192
+  static constexpr size_t kSmem = 64 + kXBytes + static_cast<size_t>(kGemvRegMaxChunks) * MT * 4;
+};
+
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void bf16x2_to_f32(uint32_t w, float& lo, float& hi) {
+  lo = __uint_as_float(w << 16);
+  hi = __uint_as_float(w & 0xFFFF0000u);
+}
+
+// acc += lo(w) * lo(x), acc2 += hi(w) * hi(x): bf16 x bf16 + fp32 with the
+// exact product, one instruction per weight.
+__device__ __forceinline__ void fma_bf16x2(float& acc, float& acc2, uint32_t w, uint32_t x) {
+  asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\t"
+      "mov.b32 {wl, wh}, %2;\n\t"
+      "mov.b32 {xl, xh}, %3;\n\t"
+      "fma.rn.f32.bf16 %0, wl, xl, %0;\n\t"
+      "fma.rn.f32.bf16 %1, wh, xh, %1;\n\t}"
+      : "+f"(acc), "+f"(acc2)
+      : "r"(w), "r"(x));
+}
+
+// (acc, acc2) += (w0, w1) * (x0, x1) in one instruction.
+__device__ __forceinline__ void fma_f32x2(float& acc, float& acc2, uint32_t w0, uint32_t w1,
+                                          float x0, float x1) {
+  uint64_t a = (static_cast<uint64_t>(__float_as_uint(acc2)) << 32) | __float_as_uint(acc);
+  const uint64_t w = (static_cast<uint64_t>(w1) << 32) | w0;
+  const uint64_t x = (static_cast<uint64_t>(__float_as_uint(x1)) << 32) | __float_as_uint(x0);
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a) : "l"(w), "l"(x));
+  acc = __uint_as_float(static_cast<uint32_t>(a));
+  acc2 = __uint_as_float(static_cast<uint32_t>(a >> 32));
+}
+
+template <typename WT, int MT>
+__global__ void __launch_bounds__(kThreads, 1) gemv_reg_kernel(const GemvParams p) {
+  using C = RCfgG<WT, MT>;
+  using XT = typename C::XT;
+  constexpr int U = C::U;
+  constexpr int L = C::kLd;
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  XT* xs = reinterpret_cast<XT*>(smem_raw);
+  float* cp = reinterpret_cast<float*>(smem_raw + C::kXBytes);  // [chunk][MT]
+  const uint32_t xs_a = smem_u32(xs);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int ks = p.K / kChunk;
+  const int64_t C_total = static_cast<int64_t>(p.n_rows) * ks;
+  const int64_t cta = blockIdx.x;
+  int64_t q0, q1;
+  if (C_total < (int64_t{1} << 22)) {
+    const uint32_t ct = static_cast<uint32_t>(C_total), g = static_cast<uint32_t>(p.G);
+    q0 = static_cast<uint32_t>(blockIdx.x) * ct / g;
+    q1 = (static_cast<uint32_t>(blockIdx.x) + 1u) * ct / g;
+  } else {
+    q0 = part_begin(cta, C_total, p.G);
+    q1 = part_begin(cta + 1, C_total, p.G);
+  }
+  const int nq = static_cast<int>(q1 - q0);  // <= kGemvRegMaxChunks (host-checked)
+  const WT* W = static_cast<const WT*>(p.w);
+
+  // Chunk q of the run: row (q0 + q) / ks, columns ((q0 + q) % ks) * 1024 + ...
+  auto load_batch = [&](int base, uint4 (&w)[U][L]) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int q = base + u * kWarps;
+      if (q < nq) {
+        const WT* src = W + (q0 + q) * static_cast<int64_t>(kChunk);  // chunks are contiguous
+#pragma unroll
+        for (int i = 0; i < L; ++i) w[u][i] = ldg_stream(src + (lane + 32 * i) * C::kVec);
+      }
+    }
+  };
+  auto compute_batch = [&](int base, const uint4 (&w)[U][L]) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int q = base + u * kWarps;
+      if (q >= nq) break;
+      const int col0 = static_cast<int>((q0 + q) % ks) * kChunk;
+      float a8[MT][8];
+#pragma unroll
+      for (int t = 0; t < MT; ++t)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) a8[t][c] = 0.f;
+#pragma unroll
+      for (int i = 0; i < L; ++i) {
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+          const uint4 xv = ld_shared_u4(
+              xs_a + static_cast<uint32_t>((t * p.K + col0 + (lane + 32 * i) * C::kVec) *
+                                           static_cast<int>(sizeof(XT))));
+          float* a = a8[t];
+          if constexpr (sizeof(WT) == 2) {
+            fma_bf16x2(a[(i & 1) * 4 + 0], a[(i & 1) * 4 + 1], w[u][i].x, xv.x);
+            fma_bf16x2(a[(i & 1) * 4 + 2], a[(i & 1) * 4 + 3], w[u][i].y, xv.y);
+            fma_bf16x2(a[(i & 1) * 4 + 0], a[(i & 1) * 4 + 1], w[u][i].z, xv.z);
+            fma_bf16x2(a[(i & 1) * 4 + 2], a[(i & 1) * 4 + 3], w[u][i].w, xv.w);
+          } else {
+            fma_f32x2(a[(i & 3) * 2 + 0], a[(i & 3) * 2 + 1], w[u][i].x, w[u][i].y,
+                      __uint_as_float(xv.x), __uint_as_float(xv.y));
+            fma_f32x2(a[(i & 3) * 2 + 0], a[(i & 3) * 2 + 1], w[u][i].z, w[u][i].w,
+                      __uint_as_float(xv.z), __uint_as_float(xv.w));
+          }
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < MT; ++t) {
+        float v = ((a8[t][0] + a8[t][1]) + (a8[t][2] + a8[t][3])) +
+                  ((a8[t][4] + a8[t][5]) + (a8[t][6] + a8[t][7]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == t) cp[q * MT + t] = v;
+      }
+    }
+  };
+
+  // The first batch of weights streams before the wait on the previous
+  // kernel of the stream (weights are constant); x and every global write
+  // come after it.
+  uint4 wa[U][L], wb[U][L];
+  int base = warp;
+  load_batch(base, wa);
+  griddep_launch_dependents();
+  griddep_wait();
+  {
+    // x -> shared memory (bf16 as is, fp32 widened for fp32 weights; rows
+    // beyond m are zero)
+    const uint4* xg = static_cast<const uint4*>(p.x);
+    const int n8 = MT * p.K / 8;
+    for (int i = threadIdx.x; i < n8; i += kThreads) {
+      const int t = i / (p.K / 8);
+      const uint4 v = t < p.m ? xg[i] : make_uint4(0, 0, 0, 0);
+      if constexpr (sizeof(WT) == 2) {
+        reinterpret_cast<uint4*>(xs)[i] = v;
+      } else {
+        float4 a, b;
+        bf16x2_to_f32(v.x, a.x, a.y);
+        bf16x2_to_f32(v.y, a.z, a.w);
+        bf16x2_to_f32(v.z, b.x, b.y);
+        bf16x2_to_f32(v.w, b.z, b.w);
+        reinterpret_cast<float4*>(xs)[2 * i] = a;
+        reinterpret_cast<float4*>(xs)[2 * i + 1] = b;
+      }
+    }
+  }
+  __syncthreads();
+  constexpr int kStride = kWarps * U;
+  // two batches in flight: the next batch's loads go out before this one is
+  // multiplied
+  while (base < nq) {
+    if (base + kStride < nq) load_batch(base + kStride, wb);
+    compute_batch(base, wa);
+    base += kStride;
+    if (base >= nq) break;
+    if (base + kStride < nq) load_batch(base + kStride, wa);
+    compute_batch(base, wb);
+    base += kStride;
+  }
+  __syncthreads();
+
+  // Rows of the run, summed over their chunks in chunk order.
+  const bool has_head = (q0 % ks) != 0;
+  const bool has_tail = (q1 % ks) != 0;
+  const int64_t r_first = q0 / ks;
+  const int64_t r_last = (q1 - 1) / ks;
+  const int n_run_rows = static_cast<int>(r_last - r_first + 1);
+  auto row_part = [&](int64_t r, int t) {
+    const int64_t c0 = (r * ks > q0 ? r * ks : q0) - q0;
+    const int64_t c1 = ((r + 1) * ks < q1 ? (r + 1) * ks : q1) - q0;
+    float v = 0.f;
+    for (int64_t c = c0; c < c1; ++c) v += cp[c * MT + t];
+    return v;
+  };
+  auto store_out = [&](int64_t row, int t, float v) {
+    if (p.out_f32)
+      static_cast<float*>(p.out)[static_cast<int64_t>(t) * p.n_rows + row] = v;
+    else
+      static_cast<__nv_bfloat16*>(p.out)[static_cast<int64_t>(t) * p.n_rows + row] =
+          __float2bfloat16_rn(v);
+  };
+  for (int idx = threadIdx.x; idx < n_run_rows * MT; idx += kThreads) {
+    const int64_t r = r_first + idx / MT;
+    const int t = idx % MT;
+    const float v = row_part(r, t);
+    if (has_tail && r == r_last) {
+      p.ws[cta * MT + t] = v;  // published below
+    } else if (has_head && r == r_first) {
+      // finished below, with the previous CTA's part
+    } else if (t < p.m) {
+      store_out(r, t, v);
+    }
+  }
+  __syncthreads();
+  if (has_tail && threadIdx.x == 0) red_release_gpu_add(p.flags + cta, 1u);
+  if (has_head && threadIdx.x < MT) {
+    const int t = threadIdx.x;
+    const float mine = row_part(r_first, t);
+    if (spin_until_ge(p.flags + cta - 1, 1u, p.status)) {
+      const float lo = __ldcg(p.ws + (cta - 1) * MT + t);
+      if (t < p.m) store_out(r_first, t, lo + mine);
+    }
+  }
+  if (has_head) {
+    __syncwarp();
+    if (threadIdx.x == 0) p.flags[cta - 1] = 0u;  // ready for the next call
+  }
+}
+
+template <typename WT, int MT>
+cudaError_t set_attr() {
+  return cudaFuncSetAttribute(gemv_reg_kernel<WT, MT>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(RCfgG<WT, MT>::kSmem));
+}
+
+template <typename WT, int MT>
+cudaError_t launch(const GemvParams& p, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.G);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = RCfgG<WT, MT>::kSmem;
+  cfg.stream = s;
+  // A CTA waits only on its predecessor (blockIdx - 1), dispatched no later
+  // than it, and G <= SMs at one CTA per SM: every wait ends.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemv_reg_kernel<WT, MT>, p);
+}
+
+}  // namespace
+
+cudaError_t gemv_reg_init_attributes() {
+  cudaError_t e;
+  if ((e = set_attr<__nv_bfloat16, 1>()) != cudaSuccess) return e;
+  if ((e = set_attr<__nv_bfloat16, 2>()) != cudaSuccess) return e;
+  if ((e = set_attr<float, 1>()) != cudaSuccess) return e;
+  if ((e = set_attr<float, 2>()) != cudaSuccess) return e;
+  return cudaSuccess;
+}
+
+cudaError_t gemv_reg_launch(bool f32w, int MT, const GemvParams& p, cudaStream_t s) {
+  if (f32w) {
+    switch (MT) {
+      case 1: return launch<float, 1>(p, s);
+      case 2: return launch<float, 2>(p, s);
+    }
+  } else {
+    switch (MT) {
+      case 1: return launch<__nv_bfloat16, 1>(p, s);
+      case 2: return launch<__nv_bfloat16, 2>(p, s);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace proj

@@ -78,6 +78,11 @@ struct GemvParams {
   int out_f32;
 };
 cudaError_t gemv_init_attributes();
+// Register-streaming GEMV (m <= 2), same parameters; a CTA keeps at most
+// kGemvRegMaxChunks chunk partials (its run of the chunk sequence).
+constexpr int kGemvRegMaxChunks = 2048;
+cudaError_t gemv_reg_init_attributes();
+cudaError_t gemv_reg_launch(bool f32w, int MT, const GemvParams& p, cudaStream_t s);
 // Record a failing status (and its text) for proj_last_status /
 // proj_last_cuda_error; both return the status.
 int record_status(int status, const char* text);

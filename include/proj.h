@@ -113,6 +113,9 @@ enum proj_kernel {
     PROJ_KERNEL_GEMV = 1,   /* row-streaming CUDA-core GEMV, m <= 2 */
     PROJ_KERNEL_TILE = 2,   /* tiled kernels: tensor cores (bf16) / FMA tiles (router),
                                split-K across CTAs through global memory */
+    PROJ_KERNEL_GEMV_REG = 4, /* m <= 2: CUDA-core GEMV with the weights loaded straight
+                                 into registers (PROJ_KERNEL_GEMV: through a shared-
+                                 memory ring fed by bulk copies) */
     PROJ_KERNEL_CLUSTER = 3 /* tensor cores (dense bf16 weights; the router's bf16 planes),
                                split-K inside a thread-block cluster combined through
                                distributed shared memory, and optionally across several

@@ -237,6 +237,22 @@ def test_gemv_partitions_and_determinism(dev, layer, m):
     assert B.proj_device_status(h) == 0
 
 
+@pytest.mark.parametrize("layer", [s.name for s in wl.LAYERS])
+@pytest.mark.parametrize("m", [1, 2])
+def test_register_gemv_partitions_and_determinism(dev, layer, m):
+    """The register-streaming GEMV (the dispatch table's m <= 2 form for the
+    shorter weight streams) over
+    several partitions meets the contract and is reproducible."""
+    h, W, _ = prepared(layer, 1)
+    sms = B.proj_num_sms()
+    for grid in (16, 37, 100, sms - 1, sms):
+        kw = dict(grid=grid, kernel=B.PROJ_KERNEL_GEMV_REG)
+        a = check_case(layer, 1, True, m, h=h, W=W, **kw)
+        b = check_case(layer, 1, True, m, h=h, W=W, **kw)
+        assert np.array_equal(a, b), (layer, m, grid)
+    assert B.proj_device_status(h) == 0
+
+
 def test_owner_mode_rejected_for_wide_token_tiles(dev):
     h, W, _ = prepared("pooler", 0)
     x = torch.zeros((64, 8192), dtype=torch.bfloat16, device="cuda")
@@ -369,6 +385,9 @@ def test_edge_arguments(dev):
     assert B.proj_out_features(prepared("unpooler", 0)[0], 9) == 8192
     assert "gemv" in B.proj_describe(h, 1)
     assert "BN=16" in B.proj_describe(h, 3)
+    with pytest.raises(B.ProjError) as e:  # a run longer than the register form keeps
+        B.proj_run_ex(h, x, 1, out, grid=1, kernel=B.PROJ_KERNEL_GEMV_REG)
+    assert e.value.status == B.PROJ_EUNSUPPORTED
 
 
 @pytest.mark.parametrize("mode", [0, 1])
