@@ -6,12 +6,14 @@ graph replay) and achieved HBM bandwidth against the measured peak.
 
 One step = one load: the five layers (qkv_gate, o, pooler, unpooler, router)
 at the load's token count, each a captured single-kernel CUDA graph replayed
-back to back on one stream.  Before every step a read of 4x the L2 size
-(the library's own streaming-read kernel) evicts the weights, outside the
-timed events (muse_bf16_proj guide, ch. 10, §10.1 "How we measure": graph
-capture after 3 warm-ups, a read larger than L2 before each replay).  Events
-bracket each layer, so every layer's cold-L2 duration is measured inside the
-timed region.
+back to back on one stream.  Before every step an L2 flush (a write of 2x
+and a read of 4x the L2 size, the read by the library's own streaming-read
+kernel) evicts the weights, outside the timed events (muse_bf16_proj guide,
+ch. 10, §10.1 "How we measure": graph capture after 3 warm-ups, a read
+larger than L2 before each replay).  Each kernel's device duration and the
+read floor's for the same bytes are measured differentially (n x (flush,
+kernel) against n x flush, one event pair each) for the roofline and the
+per-shape targets.
 
 --impl reference times the CPU FP64 oracle (the only other program that
 computes this result here) on the same load.
@@ -118,6 +120,29 @@ class ClockSampler:
 
 # --------------------------------------------------------------- our path --
 
+class L2Flush:
+    """Makes the next kernel's weights cold: a write of 2x the L2 size (it
+    displaces every line, whatever the replacement policy protects) and then
+    a read of 4x (the library's streaming-read kernel, which evicts the dirty
+    lines, so the next kernel pays no write-back).  Measured with ncu on
+    GB300: after a read-only flush a re-read buffer still hit L2 for 20-25 %
+    of its sectors; after this one, DRAM bytes read = the buffer's size."""
+
+    def __init__(self, B, torch, l2_bytes: int):
+        self.B, self.torch = B, torch
+        self.w = torch.ones((2 * l2_bytes) // 4 + 1024, dtype=torch.int32, device="cuda")
+        self.r = torch.ones(l2_bytes + 4096, dtype=torch.int32, device="cuda")
+        self.sink = torch.zeros(2 * B.proj_num_sms() + 8, dtype=torch.int32, device="cuda")
+        self.desc = (f"{2 * l2_bytes >> 20} MiB written, then {4 * l2_bytes >> 20} MiB read "
+                     "(2x and 4x L2)")
+
+    def __call__(self, stream=None):
+        s = stream if stream is not None else self.torch.cuda.current_stream()
+        with self.torch.cuda.stream(s):
+            self.w.fill_(1)
+        self.B.proj_read_floor(self.r, self.r.numel() * 4, self.sink, 0, 0, s)
+
+
 class Layer:
     def __init__(self, spec, h, info):
         self.spec, self.h, self.info = spec, h, info
@@ -214,7 +239,7 @@ class LoadGraph:
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(s):
-            B.proj_read_floor(flush, flush.numel() * 4, sink, 0, 0, s)
+            flush(s)
             a.record(s)
             if not breakdown:
                 self.plain.replay()
@@ -243,7 +268,7 @@ def time_single_layers(B, torch, lg, flush, sink, reps):
                for _ in range(reps)]
         with torch.cuda.stream(s):
             for a, b in evs:
-                B.proj_read_floor(flush, flush.numel() * 4, sink, 0, 0, s)
+                flush(s)
                 a.record(s)
                 g.replay()
                 b.record(s)
@@ -269,7 +294,7 @@ def time_router_forms(B, torch, S, flush, sink, stream, reps):
                for _ in range(reps)]
         with torch.cuda.stream(stream):
             for a, b in evs:
-                B.proj_read_floor(flush, flush.numel() * 4, sink, 0, 0, stream)
+                flush(stream)
                 a.record(stream)
                 g.replay()
                 b.record(stream)
@@ -307,7 +332,7 @@ def time_read_floor(B, torch, nbytes_list, flush, sink, stream, reps, mode=0):
             evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(reps)]
             for a, b in evs:
-                B.proj_read_floor(flush, flush.numel() * 4, sink, 0, 0, stream)
+                flush(stream)
                 a.record(stream)
                 g.replay()
                 b.record(stream)
@@ -331,7 +356,7 @@ def time_empty_graph(B, torch, flush, sink, stream, reps):
            for _ in range(reps)]
     with torch.cuda.stream(stream):
         for a, b in evs:
-            B.proj_read_floor(flush, flush.numel() * 4, sink, 0, 0, stream)
+            flush(stream)
             a.record(stream)
             g.replay()
             b.record(stream)
@@ -357,7 +382,7 @@ def time_e2e(B, torch, shapes, flush, sink, stream, steps):
            for _ in range(steps)]
     with torch.cuda.stream(stream):
         for a, b in evs:
-            B.proj_read_floor(flush, flush.numel() * 4, sink, 0, 0, stream)
+            flush(stream)
             a.record(stream)
             for S, (xh, oh) in zip(shapes, hosts):
                 B.proj_run_host(S.h, xh, S.m, oh, stream)
@@ -367,18 +392,70 @@ def time_e2e(B, torch, shapes, flush, sink, stream, steps):
     return float(np.mean(ts)), h2d, d2h
 
 
-def time_direct_kernel(B, torch, S, flush, sink, stream, reps):
-    """Event-bracketed direct launch after a flush (kernel duration, cold)."""
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(reps)]
-    with torch.cuda.stream(stream):
-        for a, b in evs:
-            B.proj_read_floor(flush, flush.numel() * 4, sink, 0, 0, stream)
+def time_device_us(torch, launch, flush_fn, stream, n=25, reps=5):
+    """A kernel's device duration on the launching stream, cold L2: one event
+    pair around n x (flush, kernel), one around n x flush, the difference / n;
+    median over reps.  The launches queue behind the flushes, so the host's
+    launch latency is not in it; the kernel's ramp-up, tail and the gap after
+    the flush are."""
+    def block(with_kernel):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
             a.record(stream)
-            B.proj_run(S.h, S.x, S.m, S.out, stream)
+            for _ in range(n):
+                flush_fn()
+                if with_kernel:
+                    launch()
             b.record(stream)
-    stream.synchronize()
-    return float(np.mean([a.elapsed_time(b) * 1e3 for a, b in evs]))
+        stream.synchronize()
+        return a.elapsed_time(b) * 1e3 / n
+    block(True)
+    block(False)
+    d = []
+    for _ in range(reps):
+        d.append(block(True) - block(False))
+    return float(np.median(d))
+
+
+def device_times(B, torch, shapes, flush, sink, stream):
+    """Per layer: the kernel's device duration (time_device_us) and the read
+    floor's for the same weight bytes (the faster of the floor kernel's two
+    forms, launched the way the projection kernels are)."""
+    flush_fn = lambda: flush(stream)
+    dev = {}
+    for S in shapes:
+        dev[S.spec.name] = time_device_us(
+            torch, lambda S=S: B.proj_run(S.h, S.x, S.m, S.out, stream), flush_fn, stream)
+    floor = {}
+    buf = None
+    sink2 = torch.zeros(2 * B.proj_num_sms() + 8, dtype=torch.int32, device="cuda")
+    cache = {}
+    for S in shapes:
+        bpe, ne = weight_bytes(S)
+        nb = int(S.n_out * S.spec.K * bpe + ne * 4)
+        nb -= nb % 16
+        if nb not in cache:
+            if buf is None or buf.numel() * 4 < nb:
+                buf = torch.ones(nb // 4 + 16, dtype=torch.int32, device="cuda")
+            cache[nb] = min(time_device_us(
+                torch, lambda md=md: B.proj_read_floor(buf, nb, sink2, 0, md | B.PROJ_READ_PDL,
+                                                       stream), flush_fn, stream)
+                for md in (0, 1))
+        floor[S.spec.name] = cache[nb]
+    return dev, floor
+
+
+def shape_targets(S, m, dev_us, floor_us, hbm_gbs, bf16_tf):
+    """The shape's score against its target: m <= 32 -> read floor / kernel;
+    m >= 128 -> max(weight bytes / HBM peak, FLOPs / bf16 tensor peak) / kernel."""
+    if m <= 32:
+        return {"kind": "read_floor", "fraction": round(floor_us / dev_us, 3)}
+    bpe, ne = weight_bytes(S)
+    nbytes = S.n_out * S.spec.K * bpe + ne * 4
+    t = max(nbytes / (hbm_gbs * 1e9), 2.0 * m * S.n_out * S.spec.K / (bf16_tf * 1e12)) * 1e6
+    return {"kind": "max(bytes/HBM, FLOPs/bf16 peak)", "bound_us": round(t, 3),
+            "fraction": round(t / dev_us, 3)}
 
 
 def weight_bytes(S) -> tuple[float, int]:
@@ -460,7 +537,7 @@ def run_ours(args):
 
     stream = torch.cuda.Stream()
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
-    flush = torch.ones(l2 + 4096, dtype=torch.int32, device="cuda")  # 4x L2 bytes
+    flush = L2Flush(B, torch, l2)
     sink = torch.zeros(2 * B.proj_num_sms() + 8, dtype=torch.int32, device="cuda")
     layers = setup_layers(B, torch, expwin=False)
 
@@ -494,11 +571,14 @@ def run_ours(args):
     layer_us = per.mean(axis=0)
 
     hbm_gbs, bf16_tf, peak_src = load_peaks()
-    di = int(np.argmax(layer_us))  # dominant kernel: largest share of the load
+    # each layer's device duration (cold L2) and the read floor's for its bytes
+    dev_us, floor_us = device_times(B, torch, lg.shapes, flush, sink, stream)
+    names = [S.spec.name for S in lg.shapes]
+    di = int(np.argmax([dev_us[n] for n in names]))  # dominant kernel: largest share
     D = lg.shapes[di]
     wbpe, nesc = weight_bytes(D)
     dom_bytes = algorithmic_bytes(D.spec, m, D.n_out, wbpe, nesc)
-    dom_us = float(layer_us[di])
+    dom_us = float(dev_us[D.spec.name])
     achieved = dom_bytes / (dom_us * 1e-6) / 1e9
     kernel_key = f"{D.spec.name}_m{m}_{'expwin12' if wbpe == 1.5 else 'dense'}"
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_gbs, "unit": "GB/s",
@@ -537,8 +617,7 @@ def run_ours(args):
             "workload": f"{args.load} load: m={m} through qkv_gate 2304x8192, o 8192x1024, "
                         f"pooler 4096x8192, unpooler {slice_rows}x4096, router fp32 256x8192",
             "m": m,
-            "l2": f"flushed before every step by a {4 * l2 >> 20} MiB read (4x L2), "
-                  "outside the events",
+            "l2": f"flushed before every step ({flush.desc}), outside the events",
             "timing": "one CUDA graph per load (5 kernels); value = mean of an event pair "
                       "around each replay (includes one graph launch); per-layer = a second "
                       "pass with event nodes between the kernels" + (
@@ -550,12 +629,20 @@ def run_ours(args):
         "median_us": round(float(np.median(outer)), 3),
         "kernel_sum_us": round(float(layer_us.sum()), 3),
         "per_layer_us": {S.spec.name: round(float(u), 3) for S, u in zip(lg.shapes, layer_us)},
+        "per_layer_device_us": {n: round(dev_us[n], 3) for n in names},
+        "read_floor_device_us": {n: round(floor_us[n], 3) for n in names},
+        "shape_targets": {S.spec.name: shape_targets(S, m, dev_us[S.spec.name],
+                                                     floor_us[S.spec.name], hbm_gbs, bf16_tf)
+                          for S in lg.shapes},
         "kernels": {S.spec.name: S.desc for S in lg.shapes},
         "roofline": {
             **roof,
             "kernel": f"{D.spec.name} ({D.desc})",
             "algorithmic_bytes": int(dom_bytes),
             "duration_us": round(dom_us, 3),
+            "duration_method": "device duration on the launching stream: one event pair around "
+                               "25 x (L2 flush, kernel), one around 25 x flush, difference / 25, "
+                               "median of 5",
             "traffic": traffic_from_profiles(kernel_key),
         },
         "clocks": clk,
@@ -569,10 +656,18 @@ def run_ours(args):
             nrep = max(20, min(args.steps, 100))
             o, _ = time_load(B, torch, graphs[ld], flush, sink, nrep)
             _, pl = time_load(B, torch, graphs[ld], flush, sink, nrep, breakdown=True)
+            dv, fl = device_times(B, torch, graphs[ld].shapes, flush, sink, stream)
+            mm = wl.LOAD_M[ld]
             loads_out[ld] = {"us": round(float(o.mean()), 2),
                              "kernel_sum_us": round(float(pl.mean(axis=0).sum()), 2),
                              "per_layer_us": {S.spec.name: round(float(u), 2) for S, u in
-                                              zip(graphs[ld].shapes, pl.mean(axis=0))}}
+                                              zip(graphs[ld].shapes, pl.mean(axis=0))},
+                             "per_layer_device_us": {k: round(v, 2) for k, v in dv.items()},
+                             "read_floor_device_us": {k: round(v, 2) for k, v in fl.items()},
+                             "shape_targets": {S.spec.name: shape_targets(
+                                 S, mm, dv[S.spec.name], fl[S.spec.name], hbm_gbs, bf16_tf)
+                                 for S in graphs[ld].shapes},
+                             "kernels": {S.spec.name: S.desc for S in graphs[ld].shapes}}
             rs = graphs[ld].shapes[-1]
             if rs.spec.weight_dtype == "fp32" and rs.m >= 3:
                 loads_out[ld]["router_forms_single_graph_us"] = time_router_forms(
@@ -595,13 +690,6 @@ def run_ours(args):
         single = time_single_layers(B, torch, lg, flush, sink, max(20, min(args.steps, 100)))
         result["single_layer_graph_us"] = {S.spec.name: round(u, 3)
                                            for S, u in zip(lg.shapes, single)}
-        # same method for both (one-kernel graph, cold L2), net of the replay
-        # cost of a graph holding one empty-ish kernel
-        result["floor_fraction_net"] = {
-            S.spec.name: round(max(floors[wb[S.spec.name]] - ov, 0.0) / max(u - ov, 1e-3), 3)
-            for S, u in zip(lg.shapes, single)}
-        result["direct_launch_us"] = {S.spec.name: round(time_direct_kernel(
-            B, torch, S, flush, sink, stream, 20), 3) for S in lg.shapes}
         cb_us, cores, n = cpu_baseline(m, budget_s=args.cpu_seconds)
         result["cpu_baseline"] = {"value": round(cb_us, 1), "unit": UNIT, "cores": cores,
                                   "kind": "oracle",
@@ -635,13 +723,11 @@ def run_shape(args):
     x = torch.from_numpy(wl.make_activations(spec, m, 0).x_bits.view(np.int16)).cuda().view(
         torch.bfloat16)
     out = torch.empty((m, B.proj_out_features(h, m)), dtype=odt, device="cuda")
-    l2 = torch.cuda.get_device_properties(0).L2_cache_size
-    flush = torch.ones(l2 + 4096, dtype=torch.int32, device="cuda")
-    sink = torch.zeros(2 * B.proj_num_sms() + 8, dtype=torch.int32, device="cuda")
+    flush = L2Flush(B, torch, torch.cuda.get_device_properties(0).L2_cache_size)
     variant = {"auto": B.PROJ_VARIANT_AUTO, "dense": B.PROJ_VARIANT_DENSE,
                "expwin12": B.PROJ_VARIANT_EXPWIN12}[args.variant]
     for _ in range(args.steps):
-        B.proj_read_floor(flush, flush.numel() * 4, sink, 0, 0)
+        flush()
         B.proj_run_ex(h, x, m, out, variant=variant)
     torch.cuda.synchronize()
     status = B.proj_device_status(h)

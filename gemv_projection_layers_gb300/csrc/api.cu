@@ -152,8 +152,12 @@ int bn_index(int bn) { return bn == 16 ? 0 : bn == 32 ? 1 : bn == 64 ? 2 : bn ==
 //             plus the last cluster's reads of the kg partials;
 //   FP32 FMA router: the stream cannot beat the CUDA cores' FMA rate.
 // Candidates keep every cluster resident in one wave (max_active), at most
-// one CTA per SM and at least kMinKbPerCta k-blocks per CTA.
+// one CTA per SM and at least kMinKbPerCta k-blocks per CTA (the FP32-FMA
+// router, whose k-blocks each carry ~1 us of FMAs at m = 16, only
+// kMinKbPerCtaFma: spreading its FMAs over every SM outweighs the pipeline
+// fill).
 constexpr int kMinKbPerCta = 4;
+constexpr int kMinKbPerCtaFma = 2;
 struct ClusterShape {
   int bn, cs, kg;
 };
@@ -180,7 +184,8 @@ ClusterShape pick_cluster(int64_t m, int T, int KB, const ClusterCost& cost, int
     const double part = 128.0 * bn * 4;  // one CTA's partial, bytes
     for (int kg = 1; kg <= kClusterMaxGroups; ++kg) {
       for (int cs = 1; cs <= kClusterMaxCS; ++cs) {
-        if (cs * kg > 1 && KB / (cs * kg) < kMinKbPerCta) continue;
+        if (cs * kg > 1 && KB / (cs * kg) < (cost.fma ? kMinKbPerCtaFma : kMinKbPerCta))
+          continue;
         const int64_t ctas = tiles * cs * kg;
         if (ctas > sms && !(cs == 1 && kg == 1)) continue;
         const int act = max_active[bn_index(bn)][cs - 1];
@@ -190,8 +195,11 @@ ClusterShape pick_cluster(int64_t m, int T, int KB, const ClusterCost& cost, int
         const double t_kb = std::max(kReqFloor, cost.w_request / kReqRate) +
                             std::max(kReqFloor, 128.0 * bn / kReqRate);
         double t = std::max(nk * t_kb * waves, static_cast<double>(weight_bytes) / kHbm);
-        if (cost.fma)
-          t = std::max(t, nk * (128.0 * bn * kTileK / kFmaRate + kStageSync) * waves);
+        if (cost.fma) {
+          // the CTAs with the most k-blocks set the time
+          const double nk_max = static_cast<double>((KB + cs * kg - 1) / (cs * kg));
+          t = std::max(t, nk_max * (128.0 * bn * kTileK / kFmaRate + kStageSync) * waves);
+        }
         if (cs > 1)
           t += (cs - 1.0) / cs * part / (kDsmem * std::min(1.0, std::sqrt(4.0 / cs)));
         if (kg > 1) t += kGroupFixed + kg * (part / cs) / kL2;
@@ -327,13 +335,13 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
     // The register form keeps a CTA's chunk partials in shared memory.  It
     // wins on the shorter weight streams (its loads start at once, with no
     // ring set-up); the ring, with more bytes in flight per SM, wins on the
-    // long ones (measured on GB300: o, the unpooler slice and the router at
-    // m = 1; also qkv_gate at m = 2).
+    // long ones (measured on GB300: the register form is faster for o and
+    // the router, the ring for qkv_gate and the pooler at m = 1 and 2).
     const int64_t chunks = pl->n_out * (h->K / 1024);
     const bool reg_ok = (chunks + pl->G - 1) / pl->G <= kGemvRegMaxChunks;
     if (kern == PROJ_KERNEL_GEMV_REG && !reg_ok) return PROJ_EUNSUPPORTED;
     const int64_t wbytes = pl->n_out * h->K * (pl->router ? 4 : 2);
-    const bool reg_better = wbytes <= kGemvRegMaxBytes || (m == 2 && wbytes <= 2 * kGemvRegMaxBytes);
+    const bool reg_better = wbytes <= kGemvRegMaxBytes;
     pl->gemv_reg =
         kern == PROJ_KERNEL_GEMV_REG || (kern == PROJ_KERNEL_AUTO && reg_ok && reg_better);
     return PROJ_OK;
@@ -864,13 +872,13 @@ void proj_destroy(proj_handle h) {
 
 int proj_read_floor(const void* buf, int64_t bytes, void* sink, int grid, int mode,
                     proj_stream stream) {
-  if (!buf || !sink || bytes <= 0 || (bytes % 16) != 0 || grid < 0 || mode < 0 || mode > 1)
+  if (!buf || !sink || bytes <= 0 || (bytes % 16) != 0 || grid < 0 || (mode & ~5) != 0)
     return fail(PROJ_EINVAL);
   if (!aligned16(buf) || (reinterpret_cast<uintptr_t>(sink) & 3u)) return fail(PROJ_EALIGN);
   if (grid == 0) {
     const int sms = proj_num_sms();
     if (sms <= 0) return fail_cuda(cudaErrorNoDevice, "proj_num_sms");
-    grid = (mode == 0) ? 2 * sms : sms;
+    grid = ((mode & 1) == 0) ? 2 * sms : sms;
   }
   cudaError_t e = read_floor_launch(buf, bytes, static_cast<uint32_t*>(sink), grid, mode,
                                     reinterpret_cast<cudaStream_t>(stream));

@@ -254,12 +254,22 @@ __global__ void __launch_bounds__(GCfg<WT, MT>::kThreads, 1) gemv_kernel(const G
   griddep_wait();
   {
     // x -> shared memory (bf16 as is, or widened to fp32 for fp32 weights;
-    // zero rows beyond m)
+    // zero rows beyond m).  Every load is issued before the first store, so
+    // staging costs one memory round trip (x is cold after a flush).
     const uint4* xg = static_cast<const uint4*>(p.x);
     const int n8 = MT * p.K / 8;  // groups of 8 columns
-    for (int i = tid; i < n8; i += kComputeWarps * 32) {
-      const int t = i / (p.K / 8);
-      const uint4 v = t < p.m ? xg[i] : make_uint4(0, 0, 0, 0);
+    constexpr int kXLd = (MT * 8192 / 8 + kComputeWarps * 32 - 1) / (kComputeWarps * 32);
+    uint4 xv[kXLd];
+#pragma unroll
+    for (int u = 0; u < kXLd; ++u) {
+      const int i = tid + u * kComputeWarps * 32;
+      xv[u] = (i < n8 && i / (p.K / 8) < p.m) ? xg[i] : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kXLd; ++u) {
+      const int i = tid + u * kComputeWarps * 32;
+      if (i >= n8) break;
+      const uint4 v = xv[u];
       if constexpr (sizeof(WT) == 2) {
         reinterpret_cast<uint4*>(xs)[i] = v;
       } else {

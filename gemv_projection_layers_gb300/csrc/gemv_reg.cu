@@ -171,12 +171,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_reg_kernel(const GemvParams 
   griddep_wait();
   {
     // x -> shared memory (bf16 as is, fp32 widened for fp32 weights; rows
-    // beyond m are zero)
+    // beyond m are zero).  Every load is issued before the first store, so
+    // staging costs one memory round trip (x is cold after a flush).
     const uint4* xg = static_cast<const uint4*>(p.x);
     const int n8 = MT * p.K / 8;
-    for (int i = threadIdx.x; i < n8; i += kThreads) {
-      const int t = i / (p.K / 8);
-      const uint4 v = t < p.m ? xg[i] : make_uint4(0, 0, 0, 0);
+    constexpr int kXLd = (MT * 8192 / 8 + kThreads - 1) / kThreads;
+    uint4 xv[kXLd];
+#pragma unroll
+    for (int u = 0; u < kXLd; ++u) {
+      const int i = threadIdx.x + u * kThreads;
+      xv[u] = (i < n8 && i / (p.K / 8) < p.m) ? xg[i] : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kXLd; ++u) {
+      const int i = threadIdx.x + u * kThreads;
+      if (i >= n8) break;
+      const uint4 v = xv[u];
       if constexpr (sizeof(WT) == 2) {
         reinterpret_cast<uint4*>(xs)[i] = v;
       } else {

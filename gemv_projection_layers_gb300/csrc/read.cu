@@ -94,9 +94,21 @@ __global__ void __launch_bounds__(32)
 cudaError_t read_floor_launch(const void* buf, int64_t bytes, uint32_t* sink, int grid, int mode,
                               cudaStream_t s) {
   const int64_t n16 = bytes / 16;
-  if (mode == 0) {
-    read_regs_kernel<<<grid, kRegThreads, 0, s>>>(static_cast<const uint4*>(buf), n16, sink);
-    return cudaGetLastError();
+  // mode bit 2: launched like the projection kernels, as a programmatic
+  // dependent launch (it may start as the previous kernel's CTAs exit; it
+  // reads nothing that kernel writes)
+  const bool pdl = (mode & 4) != 0;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  if ((mode & 3) == 0) {
+    cfg.blockDim = dim3(kRegThreads);
+    return cudaLaunchKernelEx(&cfg, read_regs_kernel, static_cast<const uint4*>(buf), n16, sink);
   }
   static bool attr_done = false;
   if (!attr_done) {
@@ -107,9 +119,10 @@ cudaError_t read_floor_launch(const void* buf, int64_t bytes, uint32_t* sink, in
     attr_done = true;
   }
   // The status word for the bulk form lives in the tail of the sink buffer.
-  read_bulk_kernel<<<grid, 32, kBulkSmem, s>>>(static_cast<const uint8_t*>(buf), n16, sink,
-                                               sink + grid);
-  return cudaGetLastError();
+  cfg.blockDim = dim3(32);
+  cfg.dynamicSmemBytes = kBulkSmem;
+  return cudaLaunchKernelEx(&cfg, read_bulk_kernel, static_cast<const uint8_t*>(buf), n16, sink,
+                            sink + grid);
 }
 
 }  // namespace proj

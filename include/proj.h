@@ -246,8 +246,13 @@ const char *proj_last_cuda_error(void);
  * that makes the next call cold.  Writes one 32-bit checksum per CTA to
  * `sink` (device, >= grid + 1 words; the last one is a status word).
  * grid = 0 picks two CTAs per SM for mode 0 and one for mode 1.
- * mode 0 = 128-bit register loads, mode 1 = bulk copies into shared memory.
+ * mode 0 = 128-bit register loads, mode 1 = bulk copies into shared memory;
+ * adding PROJ_READ_PDL (4) launches it the way proj_run launches the
+ * projection kernels, as a programmatic dependent launch (it may start as
+ * the previous kernel's CTAs exit; it reads nothing that kernel writes).
+ * Any other mode is PROJ_EINVAL.
  */
+#define PROJ_READ_PDL 4
 int proj_read_floor(const void *buf, int64_t bytes, void *sink, int grid, int mode,
                     proj_stream stream);
 

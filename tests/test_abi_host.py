@@ -52,6 +52,8 @@ def test_argument_errors_before_any_device_call(lib):
     assert lib.proj_read_floor(None, 16, 16, 0, 0, None) == B.PROJ_EINVAL
     assert lib.proj_read_floor(16, 15, 16, 0, 0, None) == B.PROJ_EINVAL
     assert lib.proj_read_floor(16, 16, 16, 0, 2, None) == B.PROJ_EINVAL
+    assert lib.proj_read_floor(16, 16, 16, 0, 8, None) == B.PROJ_EINVAL
+    assert lib.proj_read_floor(16, 16, 16, 0, -1, None) == B.PROJ_EINVAL
     assert lib.proj_read_floor(8, 16, 16, 0, 0, None) == B.PROJ_EALIGN
 
 

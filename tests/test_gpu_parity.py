@@ -390,7 +390,7 @@ def test_edge_arguments(dev):
     assert e.value.status == B.PROJ_EUNSUPPORTED
 
 
-@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("mode", [0, 1, 0 | 4, 1 | 4])
 def test_read_floor_checksums(dev, mode):
     nbytes = 48 * 1024 * 1024 + 4096
     g = torch.Generator().manual_seed(5)
@@ -404,7 +404,7 @@ def test_read_floor_checksums(dev, mode):
     for c in range(grid):
         b, e = c * n16 // grid, (c + 1) * n16 // grid
         seg = words[4 * b:4 * e]
-        if mode == 0:
+        if mode & 1 == 0:
             expect = np.bitwise_xor.reduce(seg) if seg.size else 0
         else:
             expect = np.bitwise_xor.reduce(seg[::4096]) if seg.size else 0
