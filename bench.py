@@ -420,8 +420,9 @@ def time_device_us(torch, launch, flush_fn, stream, n=25, reps=5):
 
 def device_times(B, torch, shapes, flush, sink, stream):
     """Per layer: the kernel's device duration (time_device_us) and the read
-    floor's for the same weight bytes (the faster of the floor kernel's two
-    forms, launched the way the projection kernels are)."""
+    floor's for the same weight bytes: the fastest of the streaming-read
+    kernel's launch shapes (register loads at 2, 3 and 4 CTAs per SM, bulk
+    copies at 1), each launched the way the projection kernels are."""
     flush_fn = lambda: flush(stream)
     dev = {}
     for S in shapes:
@@ -429,7 +430,8 @@ def device_times(B, torch, shapes, flush, sink, stream):
             torch, lambda S=S: B.proj_run(S.h, S.x, S.m, S.out, stream), flush_fn, stream)
     floor = {}
     buf = None
-    sink2 = torch.zeros(2 * B.proj_num_sms() + 8, dtype=torch.int32, device="cuda")
+    sms = B.proj_num_sms()
+    sink2 = torch.zeros(4 * sms + 8, dtype=torch.int32, device="cuda")
     cache = {}
     for S in shapes:
         bpe, ne = weight_bytes(S)
@@ -439,9 +441,9 @@ def device_times(B, torch, shapes, flush, sink, stream):
             if buf is None or buf.numel() * 4 < nb:
                 buf = torch.ones(nb // 4 + 16, dtype=torch.int32, device="cuda")
             cache[nb] = min(time_device_us(
-                torch, lambda md=md: B.proj_read_floor(buf, nb, sink2, 0, md | B.PROJ_READ_PDL,
-                                                       stream), flush_fn, stream)
-                for md in (0, 1))
+                torch, lambda md=md, g=g: B.proj_read_floor(buf, nb, sink2, g, md | B.PROJ_READ_PDL,
+                                                            stream), flush_fn, stream)
+                for md, g in ((0, 2 * sms), (0, 3 * sms), (0, 4 * sms), (1, sms)))
         floor[S.spec.name] = cache[nb]
     return dev, floor
 

@@ -122,8 +122,6 @@ constexpr int64_t kExpwinMaxM = 32;
 constexpr int64_t kTcOwnerMaxM = 8;
 
 constexpr int64_t kGemvMaxM = 2;
-// Weight streams up to this many bytes take the register-streaming GEMV.
-constexpr int64_t kGemvRegMaxBytes = 20ll << 20;
 // From three tokens on every layer goes to a cluster split-K kernel (the
 // router to its FP32-FMA one); below that, the GEMV.
 constexpr int64_t kClusterMinM = 3;
@@ -332,18 +330,14 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
     int64_t G = h->num_sms;
     if (opts && opts->grid > 0) G = std::min<int64_t>(opts->grid, h->num_sms);
     pl->G = static_cast<int>(std::min<int64_t>(G, pl->n_out));
-    // The register form keeps a CTA's chunk partials in shared memory.  It
-    // wins on the shorter weight streams (its loads start at once, with no
-    // ring set-up); the ring, with more bytes in flight per SM, wins on the
-    // long ones (measured on GB300: the register form is faster for o and
-    // the router, the ring for qkv_gate and the pooler at m = 1 and 2).
-    const int64_t chunks = pl->n_out * (h->K / 1024);
-    const bool reg_ok = (chunks + pl->G - 1) / pl->G <= kGemvRegMaxChunks;
+    // The register form (whole rows per CTA, weights straight to registers,
+    // no cross-CTA step) measured faster than the ring form on every layer
+    // at m = 1 and 2 on GB300; the ring form remains for the allocation-free
+    // entry point and on request, and for runs longer than the register
+    // form's chunk-partial buffer.
+    const bool reg_ok = (pl->n_out + pl->G - 1) / pl->G * (h->K / 1024) <= kGemvRegMaxChunks;
     if (kern == PROJ_KERNEL_GEMV_REG && !reg_ok) return PROJ_EUNSUPPORTED;
-    const int64_t wbytes = pl->n_out * h->K * (pl->router ? 4 : 2);
-    const bool reg_better = wbytes <= kGemvRegMaxBytes;
-    pl->gemv_reg =
-        kern == PROJ_KERNEL_GEMV_REG || (kern == PROJ_KERNEL_AUTO && reg_ok && reg_better);
+    pl->gemv_reg = kern == PROJ_KERNEL_GEMV_REG || (kern == PROJ_KERNEL_AUTO && reg_ok);
     return PROJ_OK;
   }
   pl->gemv = false;

@@ -3,32 +3,34 @@
 //
 // out[i, n] = sum_k x[i, k] W[n, k]            (muse_bf16_proj guide, ch. 1, §1.1)
 //
-// The partition is the ring GEMV's (gemv.cu): W row-major in 1024-element
-// chunks, the chunk sequence cut into G equal contiguous runs, one CTA each.
-// Here sixteen warps take the run's chunks round-robin, each chunk being 16
-// (bf16) or 32 (fp32) 16-byte loads across the warp, coalesced.  A warp keeps
-// two batches of chunks in flight (double-buffered registers: the next
-// batch's loads go out before the current batch is multiplied), so an SM has
-// ~128 KB of loads outstanding with no set-up beyond the launch.  x sits in
-// shared memory in the lanes' layout.  Each chunk's lane partials are reduced
-// by a shuffle tree and parked in shared memory; after a CTA barrier the rows
-// are summed over their chunks in chunk order (deterministic).  A row shared
-// with the previous CTA is finished as in the ring GEMV: the previous CTA
-// publishes its part with a release flag, this CTA adds it.  This follows the
-// pages' "weights straight to registers" GEMV (project report, "What was
-// built"; notebook n. 47), on a row-chunk partition instead of 16-row blocks.
+// Partition: CTA c of G owns whole rows [c N / G, (c + 1) N / G) of W
+// (row-major, each row cut into 1024-element chunks), so no row is shared
+// between CTAs and nothing crosses CTAs: no flags, no second pass.  (The
+// register form serves the short weight streams, where a CTA's rows fit in
+// one or two batches of loads, so whole-row runs cost no balance.)  Sixteen
+// warps take the CTA's chunks round-robin, each chunk being 16 (bf16) or 32
+// (fp32) 16-byte loads across the warp, coalesced.  A warp keeps two batches
+// of chunks in flight (double-buffered registers: the next batch's loads go
+// out before the current batch is multiplied), so an SM has ~128 KB of loads
+// outstanding with no set-up beyond the launch.  x sits in shared memory in
+// the lanes' layout.  Each chunk's lane partials are reduced by a shuffle
+// tree and parked in shared memory; after a CTA barrier one thread per
+// (row, token) sums the row's chunks in chunk order (deterministic) and
+// stores the output.  This follows the pages' "weights straight to
+// registers" GEMV (project report, "What was built"; notebook n. 47), on a
+// row-chunk layout instead of 16-row blocks.
 #include <cuda_bf16.h>
 
 #include <type_traits>
 
 #include "kernels.h"
 #include "ptx.cuh"
-#include "splitk.cuh"
 
 namespace proj {
 namespace {
 
 constexpr int kChunk = 1024;
+constexpr int kMaxKs = 8;  // chunks per row: K <= 8192
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 
@@ -47,6 +49,12 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
   return v;
 }
 
@@ -92,21 +100,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_reg_kernel(const GemvParams 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int ks = p.K / kChunk;
-  const int64_t C_total = static_cast<int64_t>(p.n_rows) * ks;
-  const int64_t cta = blockIdx.x;
-  int64_t q0, q1;
-  if (C_total < (int64_t{1} << 22)) {
-    const uint32_t ct = static_cast<uint32_t>(C_total), g = static_cast<uint32_t>(p.G);
-    q0 = static_cast<uint32_t>(blockIdx.x) * ct / g;
-    q1 = (static_cast<uint32_t>(blockIdx.x) + 1u) * ct / g;
-  } else {
-    q0 = part_begin(cta, C_total, p.G);
-    q1 = part_begin(cta + 1, C_total, p.G);
-  }
-  const int nq = static_cast<int>(q1 - q0);  // <= kGemvRegMaxChunks (host-checked)
+  // rows [r0, r1): n_rows * G < 2^31 (n_rows <= 65536, G <= SMs)
+  const int r0 = static_cast<int>(static_cast<uint32_t>(blockIdx.x) *
+                                  static_cast<uint32_t>(p.n_rows) / static_cast<uint32_t>(p.G));
+  const int r1 = static_cast<int>((static_cast<uint32_t>(blockIdx.x) + 1u) *
+                                  static_cast<uint32_t>(p.n_rows) / static_cast<uint32_t>(p.G));
+  const int64_t q0 = static_cast<int64_t>(r0) * ks;  // first chunk of the run
+  const int nq = (r1 - r0) * ks;  // <= kGemvRegMaxChunks (host-checked)
   const WT* W = static_cast<const WT*>(p.w);
 
-  // Chunk q of the run: row (q0 + q) / ks, columns ((q0 + q) % ks) * 1024 + ...
+  // Chunk q of the run: row r0 + q / ks, columns (q % ks) * 1024 + ...
   auto load_batch = [&](int base, uint4 (&w)[U][L]) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -123,7 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_reg_kernel(const GemvParams 
     for (int u = 0; u < U; ++u) {
       const int q = base + u * kWarps;
       if (q >= nq) break;
-      const int col0 = static_cast<int>((q0 + q) % ks) * kChunk;
+      const int col0 = (q % ks) * kChunk;
       float a8[MT][8];
 #pragma unroll
       for (int t = 0; t < MT; ++t)
@@ -215,51 +218,27 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_reg_kernel(const GemvParams 
   }
   __syncthreads();
 
-  // Rows of the run, summed over their chunks in chunk order.
-  const bool has_head = (q0 % ks) != 0;
-  const bool has_tail = (q1 % ks) != 0;
-  const int64_t r_first = q0 / ks;
-  const int64_t r_last = (q1 - 1) / ks;
-  const int n_run_rows = static_cast<int>(r_last - r_first + 1);
-  auto row_part = [&](int64_t r, int t) {
-    const int64_t c0 = (r * ks > q0 ? r * ks : q0) - q0;
-    const int64_t c1 = ((r + 1) * ks < q1 ? (r + 1) * ks : q1) - q0;
-    float v = 0.f;
-    for (int64_t c = c0; c < c1; ++c) v += cp[c * MT + t];
-    return v;
-  };
-  auto store_out = [&](int64_t row, int t, float v) {
-    if (p.out_f32)
-      static_cast<float*>(p.out)[static_cast<int64_t>(t) * p.n_rows + row] = v;
-    else
-      static_cast<__nv_bfloat16*>(p.out)[static_cast<int64_t>(t) * p.n_rows + row] =
-          __float2bfloat16_rn(v);
-  };
-  for (int idx = threadIdx.x; idx < n_run_rows * MT; idx += kThreads) {
-    const int64_t r = r_first + idx / MT;
-    const int t = idx % MT;
-    const float v = row_part(r, t);
-    if (has_tail && r == r_last) {
-      p.ws[cta * MT + t] = v;  // published below
-    } else if (has_head && r == r_first) {
-      // finished below, with the previous CTA's part
-    } else if (t < p.m) {
-      store_out(r, t, v);
+  // Rows of the run, each summed over its chunks in chunk order.
+  const uint32_t cp_a = smem_u32(cp);
+  for (int idx = threadIdx.x; idx < (r1 - r0) * MT; idx += kThreads) {
+    const int rr = idx / MT;
+    const int t = idx - rr * MT;
+    float part[kMaxKs];
+#pragma unroll
+    for (int c = 0; c < kMaxKs; ++c)
+      part[c] = c < ks ? ld_shared_f32(cp_a + static_cast<uint32_t>(((rr * ks + c) * MT + t) * 4))
+                       : 0.f;
+    float v = part[0];
+#pragma unroll
+    for (int c = 1; c < kMaxKs; ++c)
+      if (c < ks) v += part[c];
+    if (t < p.m) {
+      const int64_t o = static_cast<int64_t>(t) * p.n_rows + r0 + rr;
+      if (p.out_f32)
+        static_cast<float*>(p.out)[o] = v;
+      else
+        static_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(v);
     }
-  }
-  __syncthreads();
-  if (has_tail && threadIdx.x == 0) red_release_gpu_add(p.flags + cta, 1u);
-  if (has_head && threadIdx.x < MT) {
-    const int t = threadIdx.x;
-    const float mine = row_part(r_first, t);
-    if (spin_until_ge(p.flags + cta - 1, 1u, p.status)) {
-      const float lo = __ldcg(p.ws + (cta - 1) * MT + t);
-      if (t < p.m) store_out(r_first, t, lo + mine);
-    }
-  }
-  if (has_head) {
-    __syncwarp();
-    if (threadIdx.x == 0) p.flags[cta - 1] = 0u;  // ready for the next call
   }
 }
 
@@ -277,8 +256,6 @@ cudaError_t launch(const GemvParams& p, cudaStream_t s) {
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = RCfgG<WT, MT>::kSmem;
   cfg.stream = s;
-  // A CTA waits only on its predecessor (blockIdx - 1), dispatched no later
-  // than it, and G <= SMs at one CTA per SM: every wait ends.
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;

@@ -78,8 +78,9 @@ struct GemvParams {
   int out_f32;
 };
 cudaError_t gemv_init_attributes();
-// Register-streaming GEMV (m <= 2), same parameters; a CTA keeps at most
-// kGemvRegMaxChunks chunk partials (its run of the chunk sequence).
+// Register-streaming GEMV (m <= 2), same parameters (ws and flags unused);
+// CTA c computes rows [c n_rows / G, (c + 1) n_rows / G) and keeps at most
+// kGemvRegMaxChunks chunk partials (its rows x K / 1024).
 constexpr int kGemvRegMaxChunks = 2048;
 cudaError_t gemv_reg_init_attributes();
 cudaError_t gemv_reg_launch(bool f32w, int MT, const GemvParams& p, cudaStream_t s);
