@@ -240,6 +240,7 @@ struct proj_ctx {
   float* gemv_ws = nullptr;        // [num_sms][2]
   uint8_t* w_planes = nullptr;     // router: bf16 planes hi/mid/lo as [N, 3K] tiles
   uint32_t* cl_counters = nullptr; // cluster groups: [SMs][16], zero between calls
+  float* xch = nullptr;            // cluster partials' exchange: [SMs][256][128] fp32
   int cluster_active[5][kClusterMaxCS] = {};   // co-resident clusters: BN 16..256 x size 1..16
   int rcluster_active[5][kClusterMaxCS] = {};  // the same for the FP32-FMA router kernel
   uint8_t* w_exp = nullptr;
@@ -271,6 +272,7 @@ void free_ctx(proj_ctx* h) {
   cudaFree(h->w_dense);
   cudaFree(h->w_planes);
   cudaFree(h->cl_counters);
+  cudaFree(h->xch);
   cudaFree(h->w_rows);
   cudaFree(h->gemv_flags);
   cudaFree(h->gemv_ws);
@@ -640,7 +642,8 @@ proj_handle proj_prepare_ex(int layer, const void* W, int64_t N, int64_t K, int 
   // cluster groups: one [256][128] fp32 partial per cluster, at most one per SM
   h->ws_bytes = std::max(h->ws_bytes, static_cast<size_t>(sms) * 256 * kTileRows * 4);
   const size_t cl_counter_bytes = static_cast<size_t>(sms) * kClusterMaxCS * 4;
-  if ((e = dmalloc(&h->cl_counters, cl_counter_bytes)) != cudaSuccess ||
+  if ((e = dmalloc(&h->xch, static_cast<size_t>(sms) * 256 * kTileRows * 4)) != cudaSuccess ||
+      (e = dmalloc(&h->cl_counters, cl_counter_bytes)) != cudaSuccess ||
       (e = cudaMemsetAsync(h->cl_counters, 0, cl_counter_bytes, s)) != cudaSuccess) {
     done();
     return bail_cuda(e, "cudaMalloc(cluster counters)");
@@ -721,6 +724,14 @@ int proj_run_ex(proj_handle h, const void* x, int64_t m, void* out, proj_stream 
     c.KG = pl.KG;
     c.ws = reinterpret_cast<float*>(h->ws);
     c.counters = h->cl_counters;
+    // The tensor-core kernel exchanges its partials through L2 when three or
+    // more CTAs share a tile and every CTA has a slot (one wave: at most one
+    // CTA per SM); otherwise, and in the FP32-FMA router kernel, through
+    // distributed shared memory (~33 GB/s per SM on GB300; at two CTAs per
+    // tile the remote half is small and the L2 round trip measured no
+    // faster).
+    const int64_t ctas = static_cast<int64_t>(pl.MT) * pl.T * pl.KG * pl.G;
+    c.xch = (!(pl.router && !pl.planes) && pl.G >= 3 && ctas <= h->num_sms) ? h->xch : nullptr;
     e = (pl.router && !pl.planes) ? router_cluster_launch(pl.bn, *map, c, s)
                                    : cluster_launch(pl.bn, *map, c, s);
     if (e != cudaSuccess) return fail_cuda(e, "kernel launch");

@@ -200,39 +200,65 @@ __global__ void __launch_bounds__(CCfg<BN>::kThreads, CCfg<BN>::kBlocksPerSm)
       tc_fence_after();
       const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
       const int c_beg = part * kCols;
-      auto put = [&](int c, float val) {
-        st_shared_f32(red_base + static_cast<uint32_t>((c * kTileRows + r) * 4), val);
-      };
-      if constexpr (kCols == 16) {
-        float v[16];
-        tmem_ld16(taddr + c_beg, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj) put(c_beg + jj, v[jj]);
-      } else {
-        // two loads in flight per wait
-#pragma unroll 1
-        for (int c0 = c_beg; c0 < c_beg + kCols; c0 += 32) {
-          float v[16], u[16];
-          tmem_ld16(taddr + c0, v);
-          tmem_ld16(taddr + c0 + 16, u);
+      // Tokens this rank owns stay in shared memory; with the L2 exchange the
+      // others go to this CTA's exchange slot (32 rows of a token: 128
+      // contiguous bytes per warp store).
+      float* slot = p.xch ? p.xch + static_cast<size_t>(blockIdx.x) * BN * kTileRows : nullptr;
+      // (the previous kernel of the stream may be this handle's previous
+      // call, still reading the exchange: wait for it before storing)
+      if (slot) griddep_wait();
+      const int jo0 = static_cast<int>(rank) * BN / p.CS;
+      const int jo1 = static_cast<int>(rank + 1) * BN / p.CS;
+      auto drain = [&](auto put) {
+        if constexpr (kCols == 16) {
+          float v[16];
+          tmem_ld16(taddr + c_beg, v);
           tmem_ld_wait();
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) put(c0 + jj, v[jj]);
+          for (int jj = 0; jj < 16; ++jj) put(c_beg + jj, v[jj]);
+        } else {
+          // two loads in flight per wait
+#pragma unroll 1
+          for (int c0 = c_beg; c0 < c_beg + kCols; c0 += 32) {
+            float v[16], u[16];
+            tmem_ld16(taddr + c0, v);
+            tmem_ld16(taddr + c0 + 16, u);
+            tmem_ld_wait();
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) put(c0 + 16 + jj, u[jj]);
+            for (int jj = 0; jj < 16; ++jj) put(c0 + jj, v[jj]);
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) put(c0 + 16 + jj, u[jj]);
+          }
         }
+      };
+      if (slot) {
+        drain([&](int c, float val) {
+          if (c < jo0 || c >= jo1)
+            slot[c * kTileRows + r] = val;
+          else
+            st_shared_f32(red_base + static_cast<uint32_t>((c * kTileRows + r) * 4), val);
+        });
+      } else {
+        drain([&](int c, float val) {
+          st_shared_f32(red_base + static_cast<uint32_t>((c * kTileRows + r) * 4), val);
+        });
       }
       tc_fence_before();
     }
   }
   __syncwarp();
-  // Every CTA of the cluster has its partial in shared memory.
+  // Every CTA of the cluster has its partial in shared memory (and, with the
+  // L2 exchange, in its exchange slot; the barrier's release/acquire orders
+  // those global stores too).
   cluster_sync_all();
   griddep_wait();  // before the first global write of this thread
-  cluster_combine<BN, C::kThreads>(p, red_base, cluster, tile, t, mt, rank, mv);
-  // No CTA may leave while a peer still reads its shared memory.
-  cluster_sync_all();
+  if (p.xch) {
+    cluster_combine_l2<BN, C::kThreads>(p, red_base, cluster, tile, t, mt, rank, mv);
+  } else {
+    cluster_combine<BN, C::kThreads>(p, red_base, cluster, tile, t, mt, rank, mv);
+    // No CTA may leave while a peer still reads its shared memory.
+    cluster_sync_all();
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);

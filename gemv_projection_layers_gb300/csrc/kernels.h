@@ -117,6 +117,9 @@ struct ClusterParams {
   int out_f32;
   float* ws;            // KG > 1: [T MT][KG][BN][128] fp32 cluster partials
   uint32_t* counters;   // KG > 1: [T MT][CS], zero between calls
+  float* xch;           // CS > 1 and every CTA resident: [CTA][BN][128] fp32, the
+                        // partials' exchange through L2; null: through distributed
+                        // shared memory
 };
 constexpr int kClusterMaxCS = 16;      // CTAs per cluster, at most
 constexpr int kClusterMaxGroups = 16;  // clusters per output tile, at most
