@@ -724,14 +724,13 @@ int proj_run_ex(proj_handle h, const void* x, int64_t m, void* out, proj_stream 
     c.KG = pl.KG;
     c.ws = reinterpret_cast<float*>(h->ws);
     c.counters = h->cl_counters;
-    // The tensor-core kernel exchanges its partials through L2 when three or
+    // The cluster kernels exchange their partials through L2 when three or
     // more CTAs share a tile and every CTA has a slot (one wave: at most one
-    // CTA per SM); otherwise, and in the FP32-FMA router kernel, through
-    // distributed shared memory (~33 GB/s per SM on GB300; at two CTAs per
-    // tile the remote half is small and the L2 round trip measured no
-    // faster).
+    // CTA per SM); otherwise through distributed shared memory (~33 GB/s per
+    // SM on GB300; at two CTAs per tile the remote half is small and the L2
+    // round trip measured no faster).
     const int64_t ctas = static_cast<int64_t>(pl.MT) * pl.T * pl.KG * pl.G;
-    c.xch = (!(pl.router && !pl.planes) && pl.G >= 3 && ctas <= h->num_sms) ? h->xch : nullptr;
+    c.xch = (pl.G >= 3 && ctas <= h->num_sms) ? h->xch : nullptr;
     e = (pl.router && !pl.planes) ? router_cluster_launch(pl.bn, *map, c, s)
                                    : cluster_launch(pl.bn, *map, c, s);
     if (e != cudaSuccess) return fail_cuda(e, "kernel launch");

@@ -66,7 +66,10 @@ struct CCfg {
   static_assert(kSmem <= kSmemLimit, "shared memory budget");
 };
 
-template <int BN>
+// kXch: the partials are exchanged through L2 (p.xch), else through
+// distributed shared memory (two instantiations, so that neither carries
+// the other's code).
+template <int BN, bool kXch>
 __global__ void __launch_bounds__(CCfg<BN>::kThreads, CCfg<BN>::kBlocksPerSm)
     tc_cluster_kernel(const __grid_constant__ CUtensorMap tmap_x, const ClusterParams p) {
   using C = CCfg<BN>;
@@ -203,10 +206,10 @@ __global__ void __launch_bounds__(CCfg<BN>::kThreads, CCfg<BN>::kBlocksPerSm)
       // Tokens this rank owns stay in shared memory; with the L2 exchange the
       // others go to this CTA's exchange slot (32 rows of a token: 128
       // contiguous bytes per warp store).
-      float* slot = p.xch ? p.xch + static_cast<size_t>(blockIdx.x) * BN * kTileRows : nullptr;
+      float* slot = kXch ? p.xch + static_cast<size_t>(blockIdx.x) * BN * kTileRows : nullptr;
       // (the previous kernel of the stream may be this handle's previous
       // call, still reading the exchange: wait for it before storing)
-      if (slot) griddep_wait();
+      if constexpr (kXch) griddep_wait();
       const int jo0 = static_cast<int>(rank) * BN / p.CS;
       const int jo1 = static_cast<int>(rank + 1) * BN / p.CS;
       auto drain = [&](auto put) {
@@ -231,7 +234,7 @@ __global__ void __launch_bounds__(CCfg<BN>::kThreads, CCfg<BN>::kBlocksPerSm)
           }
         }
       };
-      if (slot) {
+      if constexpr (kXch) {
         drain([&](int c, float val) {
           if (c < jo0 || c >= jo1)
             slot[c * kTileRows + r] = val;
@@ -252,7 +255,7 @@ __global__ void __launch_bounds__(CCfg<BN>::kThreads, CCfg<BN>::kBlocksPerSm)
   // those global stores too).
   cluster_sync_all();
   griddep_wait();  // before the first global write of this thread
-  if (p.xch) {
+  if constexpr (kXch) {
     cluster_combine_l2<BN, C::kThreads>(p, red_base, cluster, tile, t, mt, rank, mv);
   } else {
     cluster_combine<BN, C::kThreads>(p, red_base, cluster, tile, t, mt, rank, mv);
@@ -265,14 +268,21 @@ __global__ void __launch_bounds__(CCfg<BN>::kThreads, CCfg<BN>::kBlocksPerSm)
   }
 }
 
-template <int BN>
-cudaError_t set_attr() {
-  cudaError_t e = cudaFuncSetAttribute(tc_cluster_kernel<BN>,
+template <int BN, bool kXch>
+cudaError_t set_attr_one() {
+  cudaError_t e = cudaFuncSetAttribute(tc_cluster_kernel<BN, kXch>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(CCfg<BN>::kSmem));
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(tc_cluster_kernel<BN>, cudaFuncAttributeNonPortableClusterSizeAllowed,
+  return cudaFuncSetAttribute(tc_cluster_kernel<BN, kXch>, cudaFuncAttributeNonPortableClusterSizeAllowed,
                               1);
+}
+
+template <int BN>
+cudaError_t set_attr() {
+  cudaError_t e = set_attr_one<BN, false>();
+  if (e != cudaSuccess) return e;
+  return set_attr_one<BN, true>();
 }
 
 template <int BN>
@@ -298,7 +308,8 @@ cudaError_t launch(const CUtensorMap& tmap, const ClusterParams& p, cudaStream_t
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, tc_cluster_kernel<BN>, tmap, p);
+  return p.xch ? cudaLaunchKernelEx(&cfg, tc_cluster_kernel<BN, true>, tmap, p)
+                : cudaLaunchKernelEx(&cfg, tc_cluster_kernel<BN, false>, tmap, p);
 }
 
 template <int BN>
@@ -311,7 +322,7 @@ int max_clusters(int cs) {
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_cfg<BN>(p, nullptr, attr);
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, tc_cluster_kernel<BN>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, tc_cluster_kernel<BN, false>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }

@@ -80,7 +80,10 @@ __device__ __forceinline__ void ffma2(uint64_t& acc, uint64_t w, uint64_t x) {
   asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(w), "l"(x));
 }
 
-template <int BN>
+// kXch: the partials are exchanged through L2 (p.xch), else through
+// distributed shared memory (two instantiations, so that neither carries
+// the other's code).
+template <int BN, bool kXch>
 __global__ void __launch_bounds__(RCfg<BN>::kThreads, 1)
     router_cluster_kernel(const __grid_constant__ CUtensorMap tmap_x, const ClusterParams p) {
   using C = RCfg<BN>;
@@ -262,24 +265,51 @@ __global__ void __launch_bounds__(RCfg<BN>::kThreads, 1)
                    : "memory");
     }
   }
+  if constexpr (kXch) {
+    // L2 exchange: the tokens this rank does not own go to the CTA's
+    // exchange slot (after the wait: the previous kernel of the stream may
+    // be this handle's previous call, still reading it).
+    __syncthreads();
+    griddep_wait();
+    const int jo0 = static_cast<int>(rank) * BN / p.CS;
+    const int jo1 = static_cast<int>(rank + 1) * BN / p.CS;
+    float* slot = p.xch + static_cast<size_t>(blockIdx.x) * BN * kTileRows;
+    for (int idx = threadIdx.x; idx < BN * kTileRows / 4; idx += C::kThreads) {
+      const int j = idx / (kTileRows / 4);
+      if (j >= jo0 && j < jo1) continue;
+      *reinterpret_cast<float4*>(slot + idx * 4) = ld_shared_v4(red_base + idx * 16);
+    }
+  }
   __syncwarp();
-  // Every CTA of the cluster has its partial in shared memory.
+  // Every CTA of the cluster has its partial in shared memory (and, with the
+  // L2 exchange, in its exchange slot).
   cluster_sync_all();
   griddep_wait();  // before the first global write of this thread
-  cluster_combine<BN, C::kThreads, 1>(p, red_base, cluster, tile, t, mt, rank, mv);
-  // No CTA may leave while a peer still reads its shared memory.
-  cluster_sync_all();
+  if constexpr (kXch) {
+    cluster_combine_l2<BN, C::kThreads, 1>(p, red_base, cluster, tile, t, mt, rank, mv);
+  } else {
+    cluster_combine<BN, C::kThreads, 1>(p, red_base, cluster, tile, t, mt, rank, mv);
+    // No CTA may leave while a peer still reads its shared memory.
+    cluster_sync_all();
+  }
   (void)ok;
+}
+
+template <int BN, bool kXch>
+cudaError_t set_attr_one() {
+  cudaError_t e = cudaFuncSetAttribute(router_cluster_kernel<BN, kXch>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(RCfg<BN>::kSmem));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(router_cluster_kernel<BN, kXch>,
+                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
 }
 
 template <int BN>
 cudaError_t set_attr() {
-  cudaError_t e = cudaFuncSetAttribute(router_cluster_kernel<BN>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(RCfg<BN>::kSmem));
+  cudaError_t e = set_attr_one<BN, false>();
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(router_cluster_kernel<BN>,
-                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return set_attr_one<BN, true>();
 }
 
 template <int BN>
@@ -305,7 +335,8 @@ cudaError_t launch(const CUtensorMap& tmap, const ClusterParams& p, cudaStream_t
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, router_cluster_kernel<BN>, tmap, p);
+  return p.xch ? cudaLaunchKernelEx(&cfg, router_cluster_kernel<BN, true>, tmap, p)
+                : cudaLaunchKernelEx(&cfg, router_cluster_kernel<BN, false>, tmap, p);
 }
 
 template <int BN>
@@ -318,7 +349,7 @@ int max_clusters(int cs) {
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_cfg<BN>(p, nullptr, attr);
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, router_cluster_kernel<BN>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, router_cluster_kernel<BN, false>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
