@@ -144,8 +144,10 @@ int bn_index(int bn) { return bn == 16 ? 0 : bn == 32 ? 1 : bn == 64 ? 2 : bn ==
 //             an SM's copy engine takes max(~160 ns, bytes / 135 GB/s) per
 //             request, and a k-block is two requests (16 KB of weights, then
 //             bn x 128 B of x);
-//   combine = remote part of the cluster's partials through distributed
-//             shared memory (~30 GB/s per SM, less in large clusters);
+//   combine = the remote part of the cluster's partials: at cs >= 3 stored
+//             to and loaded from L2 (~100 GB/s per SM each way), at cs = 2
+//             through distributed shared memory (~30 GB/s per SM) plus a
+//             second cluster barrier;
 //   groups  = kg > 1 adds a fence, an atomic and an L2 round trip (~2 us)
 //             plus the last cluster's reads of the kg partials;
 //   FP32 FMA router: the stream cannot beat the CUDA cores' FMA rate.
@@ -169,8 +171,9 @@ ClusterShape pick_cluster(int64_t m, int T, int KB, const ClusterCost& cost, int
   constexpr double kReqFloor = 160e-9;  // s per copy request, small copies
   constexpr double kReqRate = 135e9;    // bytes/s per SM, large copies
   constexpr double kHbm = 6.4e12;       // bytes/s, streaming reads
-  constexpr double kDsmem = 30e9;       // bytes/s per SM for clusters of <= 4
-  constexpr double kL2 = 100e9;         // bytes/s per SM, group partial reads
+  constexpr double kDsmem = 30e9;       // bytes/s per SM, distributed shared memory
+  constexpr double kL2 = 100e9;         // bytes/s per SM, partials through L2
+  constexpr double kBarrier = 0.4e-6;   // s, a cluster barrier
   constexpr double kGroupFixed = 2e-6;  // s
   constexpr double kFmaRate = 150e9;    // FP32 FMAs/s per SM, fma.rn.f32x2 register tiles
   constexpr double kStageSync = 0.15e-6;  // s per stage of the FMA kernel (barriers)
@@ -198,10 +201,15 @@ ClusterShape pick_cluster(int64_t m, int T, int KB, const ClusterCost& cost, int
           const double nk_max = static_cast<double>((KB + cs * kg - 1) / (cs * kg));
           t = std::max(t, nk_max * (128.0 * bn * kTileK / kFmaRate + kStageSync) * waves);
         }
-        if (cs > 1)
-          t += (cs - 1.0) / cs * part / (kDsmem * std::min(1.0, std::sqrt(4.0 / cs)));
+        if (cs >= 3)  // exchanged through L2: stored and loaded once each
+          t += 2.0 * (cs - 1.0) / cs * part / kL2;
+        else if (cs == 2)  // through distributed shared memory, and a second barrier
+          t += 0.5 * part / kDsmem + kBarrier;
         if (kg > 1) t += kGroupFixed + kg * (part / cs) / kL2;
-        if (t < best_t * 0.999 || (t < best_t * 1.001 && kg < best.kg)) {
+        // ties (the weight stream at the HBM rate): fewer groups, then more
+        // CTAs per cluster (more streams in flight measured faster)
+        if (t < best_t * 0.999 ||
+            (t < best_t * 1.001 && (kg < best.kg || (kg == best.kg && cs > best.cs)))) {
           best_t = t;
           best = ClusterShape{bn, cs, kg};
         }
@@ -530,7 +538,10 @@ proj_handle proj_prepare_ex(int layer, const void* W, int64_t N, int64_t K, int 
     const int bns[5] = {16, 32, 64, 128, 256};
     for (int b = 0; b < 5; ++b)
       for (int c = 0; c < kClusterMaxCS; ++c) {
-        h->cluster_active[b][c] = cluster_max_active(bns[b], c + 1);
+        // The occupancy query counts one CTA per SM for a cluster launch;
+        // the narrow-tile kernel holds two per SM (measured: 18 clusters of
+        // 8 such CTAs run in one wave where the query says 15).
+        h->cluster_active[b][c] = cluster_max_active(bns[b], c + 1) * cluster_blocks_per_sm(bns[b]);
         h->rcluster_active[b][c] = router_cluster_max_active(bns[b], c + 1);
       }
   }

@@ -356,6 +356,17 @@ int cluster_max_active(int BN, int cs) {
   return 0;
 }
 
+int cluster_blocks_per_sm(int BN) {
+  switch (BN) {
+    case 16: return CCfg<16>::kBlocksPerSm;
+    case 32: return CCfg<32>::kBlocksPerSm;
+    case 64: return CCfg<64>::kBlocksPerSm;
+    case 128: return CCfg<128>::kBlocksPerSm;
+    case 256: return CCfg<256>::kBlocksPerSm;
+  }
+  return 1;
+}
+
 int cluster_stages(int BN) {
   switch (BN) {
     case 16: return CCfg<16>::S;

@@ -126,6 +126,7 @@ constexpr int kClusterMaxGroups = 16;  // clusters per output tile, at most
 bool cluster_supported(int BN);
 cudaError_t cluster_init_attributes();
 int cluster_max_active(int BN, int cs);
+int cluster_blocks_per_sm(int BN);  // CTAs one SM holds (2 for the narrow tiles)
 int cluster_stages(int BN);
 cudaError_t cluster_launch(int BN, const CUtensorMap& tmap_x, const ClusterParams& p,
                            cudaStream_t s);
