@@ -122,6 +122,9 @@ constexpr int64_t kExpwinMaxM = 32;
 constexpr int64_t kTcOwnerMaxM = 8;
 
 constexpr int64_t kGemvMaxM = 2;
+// From three tokens to kGemvMmaMaxM the bf16 layers take the warp-MMA
+// weight stream (measured faster than the tcgen05 cluster kernel there).
+constexpr int64_t kGemvMmaMinM = 3;
 // From three tokens on every layer goes to a cluster split-K kernel (the
 // router to its FP32-FMA one); below that, the GEMV.
 constexpr int64_t kClusterMinM = 3;
@@ -223,6 +226,7 @@ int mt_for_gemv(int64_t m) { return m <= 1 ? 1 : 2; }
 struct Plan {
   bool gemv;
   bool gemv_reg = false;  // m <= 2: register-streaming form
+  bool gemv_mma = false;  // bf16, m <= 8: warp-MMA weight stream
   bool cluster;
   bool planes = false;  // router on the tensor cores (three bf16 planes)
   int KG = 1;  // cluster kernel: clusters per output tile
@@ -249,6 +253,7 @@ struct proj_ctx {
   uint8_t* w_planes = nullptr;     // router: bf16 planes hi/mid/lo as [N, 3K] tiles
   uint32_t* cl_counters = nullptr; // cluster groups: [SMs][16], zero between calls
   float* xch = nullptr;            // cluster partials' exchange: [SMs][256][128] fp32
+  uint32_t* w_frag = nullptr;      // bf16 layers: 16 x 16 MMA-fragment tiles (few tokens)
   int cluster_active[5][kClusterMaxCS] = {};   // co-resident clusters: BN 16..256 x size 1..16
   int rcluster_active[5][kClusterMaxCS] = {};  // the same for the FP32-FMA router kernel
   uint8_t* w_exp = nullptr;
@@ -281,6 +286,7 @@ void free_ctx(proj_ctx* h) {
   cudaFree(h->w_planes);
   cudaFree(h->cl_counters);
   cudaFree(h->xch);
+  cudaFree(h->w_frag);
   cudaFree(h->w_rows);
   cudaFree(h->gemv_flags);
   cudaFree(h->gemv_ws);
@@ -317,7 +323,7 @@ int64_t out_rows(const proj_ctx* h, int64_t m) {
 int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl) {
   const int variant = opts ? opts->variant : PROJ_VARIANT_AUTO;
   const int kern = opts ? opts->kernel : PROJ_KERNEL_AUTO;
-  if (kern < PROJ_KERNEL_AUTO || kern > PROJ_KERNEL_GEMV_REG) return PROJ_EINVAL;
+  if (kern < PROJ_KERNEL_AUTO || kern > PROJ_KERNEL_MMA) return PROJ_EINVAL;
   if (variant < PROJ_VARIANT_AUTO || variant > PROJ_VARIANT_PLANES3) return PROJ_EINVAL;
   const int tile_n = opts ? opts->tile_n : 0;
   if (tile_n != 0 && tile_n != 16 && tile_n != 32 && tile_n != 64 && tile_n != 128 &&
@@ -352,6 +358,32 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
   }
   pl->gemv = false;
   pl->cluster = false;
+  // A few tokens on the bf16 layers: the warp-MMA weight stream.
+  {
+    const int64_t nb = pl->n_out / 16;
+    int64_t G = std::min<int64_t>(nb, h->num_sms);
+    if (opts && opts->grid > 0) G = std::min<int64_t>(opts->grid, nb);
+    const bool mma_ok = !pl->router && h->w_frag && m <= kGemvMmaMaxM &&
+                        (variant == PROJ_VARIANT_AUTO || variant == PROJ_VARIANT_DENSE) &&
+                        pl->n_out % 16 == 0 && G > 0 && (nb + G - 1) / G <= kGemvMmaMaxBlocks;
+    // (measured: faster than the cluster kernel at 3..8 tokens on qkv_gate,
+    // o and the unpooler slice; the pooler's 256 blocks over 152 CTAs leave
+    // it behind -- whole blocks per CTA, two for most)
+    const bool mma_auto = kern == PROJ_KERNEL_AUTO && m >= kGemvMmaMinM &&
+                          (nb % G == 0 || (nb + G - 1) / G == 1 || h->K <= 4096) &&
+                          (!opts || (opts->grid == 0 && opts->groups == 0 &&
+                                     opts->tile_n == 0 && opts->reduce == PROJ_REDUCE_AUTO));
+    if (kern == PROJ_KERNEL_MMA && !mma_ok) return PROJ_EUNSUPPORTED;
+    if (mma_ok && (kern == PROJ_KERNEL_MMA || mma_auto)) {
+      pl->gemv_mma = true;
+      pl->expwin = false;
+      pl->reduce = 0;
+      pl->bn = kGemvMmaMaxM;
+      pl->T = pl->KB = pl->MT = 0;
+      pl->G = static_cast<int>(G);
+      return PROJ_OK;
+    }
+  }
   // The dispatch table sends wide token tiles to the cluster kernel; an
   // explicit grid or reduction mode names the global-memory split-K kernel.
   const bool auto_cluster = kern == PROJ_KERNEL_AUTO &&
@@ -533,6 +565,7 @@ proj_handle proj_prepare_ex(int layer, const void* W, int64_t N, int64_t K, int 
     return bail_cuda(e, "router attributes");
   if ((e = gemv_init_attributes()) != cudaSuccess) return bail_cuda(e, "gemv attributes");
   if ((e = gemv_reg_init_attributes()) != cudaSuccess) return bail_cuda(e, "gemv attributes");
+  if ((e = gemv_mma_init_attributes()) != cudaSuccess) return bail_cuda(e, "gemv attributes");
   if ((e = cluster_init_attributes()) != cudaSuccess) return bail_cuda(e, "cluster attributes");
   {
     const int bns[5] = {16, 32, 64, 128, 256};
@@ -585,6 +618,14 @@ proj_handle proj_prepare_ex(int layer, const void* W, int64_t N, int64_t K, int 
                              static_cast<int>(K), h->w_dense, s)) != cudaSuccess) {
       done();
       return bail_cuda(e, "pack bf16");
+    }
+    if (N % 16 == 0 && K % 256 == 0 && K <= 8192) {
+      if ((e = dmalloc(&h->w_frag, static_cast<size_t>(N) * K * 2)) != cudaSuccess ||
+          (e = pack_frag16(static_cast<const uint16_t*>(W), static_cast<int>(N),
+                           static_cast<int>(K), h->w_frag, s)) != cudaSuccess) {
+        done();
+        return bail_cuda(e, "pack fragment tiles");
+      }
     }
     if (flags & PROJ_ENCODE_EXPWIN12) {
       uint32_t* dev_hist = nullptr;
@@ -717,6 +758,20 @@ int proj_run_ex(proj_handle h, const void* x, int64_t m, void* out, proj_stream 
     if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
     return PROJ_OK;
   }
+  if (pl.gemv_mma) {
+    GemvMmaParams g;
+    g.w = reinterpret_cast<const uint4*>(h->w_frag);
+    g.x = x;
+    g.out = out;
+    g.status = h->status;
+    g.m = static_cast<int>(m);
+    g.n_rows = static_cast<int>(pl.n_out);
+    g.K = static_cast<int>(h->K);
+    g.G = pl.G;
+    e = gemv_mma_launch(g, s);
+    if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
+    return PROJ_OK;
+  }
   const CUtensorMap* map = get_map(h, x, m, pl.bn, true);
   if (!map) return fail_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(x)");
   if (pl.cluster) {
@@ -819,6 +874,10 @@ int proj_describe(proj_handle h, int64_t m, char* buf, size_t cap) {
   if (pl.gemv) {
     std::snprintf(buf, cap, "gemv%s_%s MT=%d G=%d n_rows=%lld", pl.gemv_reg ? "_reg" : "",
                   pl.router ? "f32w" : "bf16w", pl.bn, pl.G, static_cast<long long>(pl.n_out));
+  } else if (pl.gemv_mma) {
+    std::snprintf(buf, cap, "gemv_mma16x8 G=%d blocks_per_cta<=%lld n_rows=%lld", pl.G,
+                  static_cast<long long>((pl.n_out / 16 + pl.G - 1) / pl.G),
+                  static_cast<long long>(pl.n_out));
   } else if (pl.cluster) {
     const bool fma = pl.router && !pl.planes;
     std::snprintf(buf, cap,
@@ -841,10 +900,14 @@ int proj_describe(proj_handle h, int64_t m, char* buf, size_t cap) {
 int proj_unpack_weights(proj_handle h, int variant, void* W_out, proj_stream stream) {
   if (!h || !W_out) return fail(PROJ_EINVAL);
   if (!aligned16(W_out)) return fail(PROJ_EALIGN);
+  if ((variant < PROJ_VARIANT_AUTO || variant > PROJ_VARIANT_PLANES3) &&
+      variant != PROJ_UNPACK_FRAG16)
+    return fail(PROJ_EINVAL);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (h->layer == PROJ_ROUTER) {
-    if (variant == PROJ_VARIANT_EXPWIN12) return fail(PROJ_EUNSUPPORTED);
+    if (variant == PROJ_VARIANT_EXPWIN12 || variant == PROJ_UNPACK_FRAG16)
+      return fail(PROJ_EUNSUPPORTED);
     if (variant == PROJ_VARIANT_PLANES3)
       e = unpack_router_planes(h->w_planes, static_cast<int>(h->N), static_cast<int>(h->K),
                                static_cast<float*>(W_out), s);
@@ -853,6 +916,10 @@ int proj_unpack_weights(proj_handle h, int variant, void* W_out, proj_stream str
                                   static_cast<float*>(W_out), s);
   } else if (variant == PROJ_VARIANT_PLANES3) {
     return fail(PROJ_EUNSUPPORTED);
+  } else if (variant == PROJ_UNPACK_FRAG16) {
+    if (!h->w_frag) return fail(PROJ_EUNSUPPORTED);
+    e = unpack_frag16(h->w_frag, static_cast<int>(h->N), static_cast<int>(h->K),
+                      static_cast<uint16_t*>(W_out), s);
   } else if (variant == PROJ_VARIANT_EXPWIN12 ||
              (variant == PROJ_VARIANT_AUTO && h->w_exp != nullptr)) {
     if (!h->w_exp) return fail(PROJ_EUNSUPPORTED);

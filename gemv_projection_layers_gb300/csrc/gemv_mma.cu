@@ -1,0 +1,234 @@
+// gemv_mma.cu -- the bf16 layers at 3..8 tokens: a weight-streaming GEMV
+// whose multiply-adds run on the warp-level tensor-core MMA.
+//
+// out[i, n] = sum_k x[i, k] W[n, k]            (muse_bf16_proj guide, ch. 1, §1.1)
+//
+// At a few tokens the layer is still a weight stream; what it adds over the
+// one-token GEMV is m products per weight, too many for the CUDA cores'
+// mixed-precision FMA at the stream's rate (the pooler at m = 8 would need
+// half their peak) and too few to fill a tcgen05 tile.  This is the pages'
+// GEMV design (muse_bf16_proj project report, "What was built": 16-row
+// blocks, warps splitting K, mma.sync, weights straight to registers) on
+// GB300:
+//
+// * W is prepacked (lossless) into 16 x 16 tiles in the A-fragment order of
+//   mma.sync m16n8k16, so one 16-byte load per lane -- 512 contiguous bytes
+//   per warp -- is one tile's fragment, straight into registers.
+// * CTA c owns the 16-row blocks [c NB / G, (c + 1) NB / G) (whole blocks:
+//   nothing crosses CTAs).  Its sixteen warps split the blocks' k-tiles into
+//   contiguous runs (a warp changes block at most once, so one accumulator
+//   tile suffices), two batches of eight fragments in flight per warp.
+// * x (up to 8 tokens) is staged once into shared memory in B-fragment
+//   order (8 bytes per lane per k-tile), after the dependency wait, while
+//   the first batch of weights is in flight.
+// * Each warp accumulates a 16 x 8 fp32 tile per row block in registers;
+//   the sixteen warps' tiles are summed in warp order (deterministic) and
+//   rounded to bf16.
+// Products are exact and accumulate in fp32 on the tensor cores.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace proj {
+namespace {
+
+constexpr int kWarps = 16;
+constexpr int kThreads = kWarps * 32;
+constexpr int kU = 8;  // fragments per batch per warp
+constexpr int kXBytes = 8192 / 16 * 256;                          // K <= 8192
+constexpr int kRedBytes = kWarps * kGemvMmaMaxBlocks * 32 * 4 * 4;  // [warp][block][lane][4]
+constexpr int kSmem = kXBytes + kRedBytes;
+
+__device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint2 ld_shared_u2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_shared_f32x4(uint32_t addr, float a, float b, float c,
+                                                float d) {
+  asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+
+// Shared-memory slot of B-fragment word w of lane l for k-tile kt: each
+// k-tile's 32 lanes x 8 bytes form one 256-byte block, lanes permuted by
+// l ^ 2 (kt % 16) so that the staging stores (consecutive k-tiles per warp)
+// spread over the banks; the MMA loads (one k-tile per warp) stay
+// conflict-free.
+__device__ __forceinline__ uint32_t xfrag_off(int kt, int l, int w) {
+  return static_cast<uint32_t>(kt * 256 + ((l ^ ((kt & 15) << 1)) << 3) + w * 4);
+}
+
+// d += A (16 x 16, bf16, row) * B (16 x 8, bf16, col), fp32 accumulate.
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint4& a, const uint2& b) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y));
+}
+
+__global__ void __launch_bounds__(kThreads, 1) gemv_mma_kernel(const GemvMmaParams p) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  const uint32_t sX = smem_u32(smem_raw);       // [K/16 k-tiles][32 lanes][2 words], xfrag_off
+  const uint32_t sRed = sX + kXBytes;           // [warp][block][lane][4] fp32
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int KT = p.K / 16;
+  const int NB = p.n_rows / 16;
+  const int b0 = static_cast<int>(static_cast<uint32_t>(blockIdx.x) * NB / p.G);
+  const int b1 = static_cast<int>((static_cast<uint32_t>(blockIdx.x) + 1u) * NB / p.G);
+  const int nu = (b1 - b0) * KT;  // units (block, k-tile) of this CTA, block-major
+  // Warp w takes the contiguous units [u0, u1): consecutive k-tiles (4 KB
+  // contiguous per batch), at most one block change on the way.
+  const int u0 = static_cast<int>(static_cast<uint32_t>(warp) * nu / kWarps);
+  const int u1 = static_cast<int>(static_cast<uint32_t>(warp + 1) * nu / kWarps);
+  // unit u: block b0 + u / KT, k-tile u % KT; its fragment for this lane
+  const uint4* W = p.w + static_cast<size_t>(b0) * KT * 32 + lane;
+
+  auto load_batch = [&](int base, uint4 (&a)[kU]) {
+#pragma unroll
+    for (int j = 0; j < kU; ++j) {
+      const int u = base + j;
+      if (u < u1) a[j] = ldg_stream(W + static_cast<size_t>(u) * 32);
+    }
+  };
+  // Partial tiles, zero where a warp has no unit of a block.
+#pragma unroll
+  for (int q = 0; q < kGemvMmaMaxBlocks; ++q)
+    st_shared_f32x4(sRed + static_cast<uint32_t>(((warp * kGemvMmaMaxBlocks + q) * 32 + lane) * 16),
+                    0.f, 0.f, 0.f, 0.f);
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  int cur = u0 / KT;  // block of the accumulator (local index)
+  auto flush = [&]() {
+    st_shared_f32x4(sRed + static_cast<uint32_t>(((warp * kGemvMmaMaxBlocks + cur) * 32 + lane) * 16),
+                    acc[0], acc[1], acc[2], acc[3]);
+  };
+  auto compute_batch = [&](int base, const uint4 (&a)[kU]) {
+#pragma unroll
+    for (int j = 0; j < kU; ++j) {
+      const int u = base + j;
+      if (u >= u1) break;
+      const int bl = u / KT;
+      const int kt = u - bl * KT;
+      if (bl != cur) {  // warp-uniform; at most once per warp
+        flush();
+        cur = bl;
+        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+      }
+      const uint2 b = ld_shared_u2(sX + xfrag_off(kt, lane, 0));
+      mma16816(acc, a[j], b);
+    }
+  };
+
+  // The first batch of weights streams before the wait on the previous
+  // kernel of the stream (weights are constant); x comes after it.
+  uint4 wa[kU], wb[kU];
+  int base = u0;
+  load_batch(base, wa);
+  griddep_launch_dependents();
+  griddep_wait();
+  {
+    // x -> B fragments: 16-byte chunk (token n < m, k 8 h .. 8 h + 7) of
+    // k-tile kt = h / 2 feeds lanes 4 n + q (q < 4), word h % 2 (k pairs 2 q,
+    // 2 q + 1 of the tile's low or high eight).  Tokens n >= m are not staged:
+    // their B columns only reach output columns that are never stored.
+    // Eight loads in flight per thread per round.
+    const int n8 = p.m * (p.K / 8);
+    for (int r0 = 0; r0 < n8; r0 += 8 * kThreads) {
+      uint4 xv[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = r0 + threadIdx.x + j * kThreads;
+        if (i < n8)
+          xv[j] = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x) +
+                                                  static_cast<size_t>(i) * 8);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = r0 + threadIdx.x + j * kThreads;
+        if (i >= n8) break;
+        const int n = i / (p.K / 8);
+        const int h = i - n * (p.K / 8);  // 16-byte chunk within the row
+        const int kt = h >> 1;
+        st_shared_u32(sX + xfrag_off(kt, 4 * n + 0, h & 1), xv[j].x);
+        st_shared_u32(sX + xfrag_off(kt, 4 * n + 1, h & 1), xv[j].y);
+        st_shared_u32(sX + xfrag_off(kt, 4 * n + 2, h & 1), xv[j].z);
+        st_shared_u32(sX + xfrag_off(kt, 4 * n + 3, h & 1), xv[j].w);
+      }
+    }
+  }
+  __syncthreads();
+  // two batches in flight: the next batch's loads go out before this one
+  // is multiplied
+  while (base < u1) {
+    if (base + kU < u1) load_batch(base + kU, wb);
+    compute_batch(base, wa);
+    base += kU;
+    if (base >= u1) break;
+    if (base + kU < u1) load_batch(base + kU, wa);
+    compute_batch(base, wb);
+    base += kU;
+  }
+  if (u0 < u1) flush();
+  __syncthreads();
+  // Each (block, row, token) summed over the warps' partial tiles in warp
+  // order.
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+  for (int idx = threadIdx.x; idx < (b1 - b0) * 128; idx += kThreads) {
+    const int q = idx / 128;          // block
+    const int l = (idx / 4) % 32;     // fragment lane
+    const int e = idx % 4;            // fragment element
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w)
+      s += ld_shared_f32(sRed + static_cast<uint32_t>(((w * kGemvMmaMaxBlocks + q) * 32 + l) * 16 +
+                                                      e * 4));
+    // element e of lane l: row l / 4 (+ 8 for e >= 2), token 2 (l % 4) + e % 2
+    const int row = (l >> 2) + (e >= 2 ? 8 : 0);
+    const int tok = 2 * (l & 3) + (e & 1);
+    if (tok < p.m)
+      out[static_cast<size_t>(tok) * p.n_rows + (b0 + q) * 16 + row] = __float2bfloat16_rn(s);
+  }
+}
+
+}  // namespace
+
+cudaError_t gemv_mma_init_attributes() {
+  return cudaFuncSetAttribute(gemv_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kSmem);
+}
+
+cudaError_t gemv_mma_launch(const GemvMmaParams& p, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.G);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemv_mma_kernel, p);
+}
+
+}  // namespace proj

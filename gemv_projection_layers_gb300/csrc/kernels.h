@@ -146,6 +146,27 @@ cudaError_t encode_expwin12(const uint16_t* W, int N, int K, int e0, uint8_t* ds
                             uint32_t* overflow, unsigned long long* n_esc, cudaStream_t s);
 cudaError_t decode_expwin12(const uint8_t* src, int N, int K, int e0, uint16_t* W,
                             cudaStream_t s);
+// Few-token GEMV layout: bf16 W [N, K] as 16 x 16 tiles in the A-fragment
+// order of mma.sync m16n8k16 (row-major A): tile (rb, kb) at
+// (rb K/16 + kb) x 512 bytes, lane l's 16 bytes at l x 16 holding the pairs
+// (row g, k c..c+1), (row g+8, k c..c+1), (row g, k c+8..c+9),
+// (row g+8, k c+8..c+9) with g = l / 4, c = 2 (l % 4).  N % 16 == K % 16 == 0.
+cudaError_t pack_frag16(const uint16_t* W, int N, int K, uint32_t* dst, cudaStream_t s);
+cudaError_t unpack_frag16(const uint32_t* src, int N, int K, uint16_t* W, cudaStream_t s);
+struct GemvMmaParams {
+  const uint4* w;   // frag16 layout of the rows computed (and more)
+  const void* x;    // bf16 [m, K]
+  void* out;        // bf16 [m, n_rows]
+  uint32_t* status;
+  int m;            // <= 8
+  int n_rows;       // rows computed, multiple of 16
+  int K;            // multiple of 256, <= 8192
+  int G;            // CTAs: CTA c computes 16-row blocks [c NB / G, (c + 1) NB / G)
+};
+constexpr int kGemvMmaMaxM = 8;
+constexpr int kGemvMmaMaxBlocks = 4;  // 16-row blocks per CTA, at most
+cudaError_t gemv_mma_init_attributes();
+cudaError_t gemv_mma_launch(const GemvMmaParams& p, cudaStream_t s);
 cudaError_t pack_router_fma_tiles(const float* W, int N, int K, uint8_t* dst, cudaStream_t s);
 cudaError_t unpack_router_fma_tiles(const uint8_t* src, int N, int K, float* W, cudaStream_t s);
 // Router W -> bf16 planes hi, mid, lo (hi + mid + lo == W) packed as the bf16

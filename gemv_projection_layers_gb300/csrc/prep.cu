@@ -7,6 +7,8 @@
 //   * router fp32 W -> three bf16 planes hi + mid + lo == W (exact), packed as
 //     bf16 tiles of a [N, 3K] matrix whose column p K + k holds plane p of
 //     W[:, k] (and back, summing the planes).
+//   * bf16 W -> 16 x 16 tiles in the A-fragment order of the m16n8k16
+//     warp MMA, for the few-token GEMV (and back).
 // The tile and record layouts are defined in kernels.h.
 #include <cuda_bf16.h>
 
@@ -284,6 +286,50 @@ __global__ void unpack_planes_kernel(const uint8_t* __restrict__ src, int N, int
   }
 }
 
+// One thread per 16-byte fragment: tile (rb, kb) of 16 rows x 16 k at
+// (rb K/16 + kb) x 512 B, lane l's four words at l x 16: rows g = l / 4 and
+// g + 8, columns c = 2 (l % 4) (+1) and c + 8 (+1), as kernels.h states.
+__global__ void pack_frag16_kernel(const uint16_t* __restrict__ W, int N, int K,
+                                   uint32_t* __restrict__ dst) {
+  const int KT = K / 16;
+  const int64_t frags = static_cast<int64_t>(N / 16) * KT * 32;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < frags;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t tile = i / 32;
+    const int l = static_cast<int>(i % 32);
+    const int rb = static_cast<int>(tile / KT), kb = static_cast<int>(tile % KT);
+    const int g = l >> 2, c = (l & 3) * 2;
+    const uint16_t* r0 = W + static_cast<size_t>(rb * 16 + g) * K + kb * 16 + c;
+    const uint16_t* r8 = r0 + static_cast<size_t>(8) * K;
+    uint4 v;
+    v.x = *reinterpret_cast<const uint32_t*>(r0);
+    v.y = *reinterpret_cast<const uint32_t*>(r8);
+    v.z = *reinterpret_cast<const uint32_t*>(r0 + 8);
+    v.w = *reinterpret_cast<const uint32_t*>(r8 + 8);
+    reinterpret_cast<uint4*>(dst)[i] = v;
+  }
+}
+
+__global__ void unpack_frag16_kernel(const uint32_t* __restrict__ src, int N, int K,
+                                     uint16_t* __restrict__ W) {
+  const int KT = K / 16;
+  const int64_t frags = static_cast<int64_t>(N / 16) * KT * 32;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < frags;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t tile = i / 32;
+    const int l = static_cast<int>(i % 32);
+    const int rb = static_cast<int>(tile / KT), kb = static_cast<int>(tile % KT);
+    const int g = l >> 2, c = (l & 3) * 2;
+    uint16_t* r0 = W + static_cast<size_t>(rb * 16 + g) * K + kb * 16 + c;
+    uint16_t* r8 = r0 + static_cast<size_t>(8) * K;
+    const uint4 v = reinterpret_cast<const uint4*>(src)[i];
+    *reinterpret_cast<uint32_t*>(r0) = v.x;
+    *reinterpret_cast<uint32_t*>(r8) = v.y;
+    *reinterpret_cast<uint32_t*>(r0 + 8) = v.z;
+    *reinterpret_cast<uint32_t*>(r8 + 8) = v.w;
+  }
+}
+
 constexpr int kPrepBlock = 256;
 constexpr int kPrepGrid = 152 * 8;
 
@@ -314,6 +360,16 @@ cudaError_t decode_expwin12(const uint8_t* src, int N, int K, int e0, uint16_t* 
                             cudaStream_t s) {
   const uint32_t e0x4 = static_cast<uint32_t>(e0) * 0x01010101u;
   decode_expwin12_kernel<<<kPrepGrid, kPrepBlock, 0, s>>>(src, N, K, e0x4, W);
+  return cudaGetLastError();
+}
+
+cudaError_t pack_frag16(const uint16_t* W, int N, int K, uint32_t* dst, cudaStream_t s) {
+  pack_frag16_kernel<<<kPrepGrid, kPrepBlock, 0, s>>>(W, N, K, dst);
+  return cudaGetLastError();
+}
+
+cudaError_t unpack_frag16(const uint32_t* src, int N, int K, uint16_t* W, cudaStream_t s) {
+  unpack_frag16_kernel<<<kPrepGrid, kPrepBlock, 0, s>>>(src, N, K, W);
   return cudaGetLastError();
 }
 

@@ -113,6 +113,11 @@ enum proj_kernel {
     PROJ_KERNEL_GEMV = 1,   /* row-streaming CUDA-core GEMV, m <= 2 */
     PROJ_KERNEL_TILE = 2,   /* tiled kernels: tensor cores (bf16) / FMA tiles (router),
                                split-K across CTAs through global memory */
+    PROJ_KERNEL_MMA = 5,    /* bf16 layers, m <= 8: weight-streaming GEMV on the warp-level
+                               tensor-core MMA (mma.sync m16n8k16) from a copy of W in
+                               fragment order; CTAs own whole 16-row blocks (at most 4),
+                               proj_run_opts.grid = CTAs; the dispatch form at
+                               3 <= m <= 8 */
     PROJ_KERNEL_GEMV_REG = 4, /* m <= 2: CUDA-core GEMV with the weights loaded straight
                                  into registers (PROJ_KERNEL_GEMV: through a shared-
                                  memory ring fed by bulk copies) */
@@ -221,8 +226,11 @@ int proj_describe(proj_handle h, int64_t m, char *buf, size_t cap);
  * decodes that copy, so a bitwise comparison with the original W checks
  * that the recode is lossless.  For the router, PROJ_VARIANT_PLANES3 sums
  * the three bf16 planes back to fp32 (the same check for the plane split).
- * Enqueued on `stream`.
+ * variant = PROJ_UNPACK_FRAG16 decodes the bf16 layers' copy in warp-MMA
+ * fragment order (the few-token GEMV's layout; PROJ_EUNSUPPORTED where it
+ * was not built).  Enqueued on `stream`.
  */
+#define PROJ_UNPACK_FRAG16 16
 int proj_unpack_weights(proj_handle h, int variant, void *W_out, proj_stream stream);
 
 /* Read and clear the handle's device status word (synchronises `stream`).

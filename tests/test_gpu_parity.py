@@ -182,6 +182,49 @@ def test_cluster_groups_and_determinism(dev, layer, m):
     assert B.proj_device_status(h) == 0
 
 
+@pytest.mark.parametrize("m", [1, 2, 3, 5, 7, 8])
+@pytest.mark.parametrize("layer", ["qkv_gate", "o", "pooler", "unpooler"])
+def test_mma_gemv(dev, layer, m):
+    """The bf16 layers' few-token GEMV on the warp-level tensor-core MMA (W in
+    fragment order, whole 16-row blocks per CTA): the dispatch form at
+    3 <= m <= 8, forced at m <= 8 and at several CTA counts (up to four
+    blocks per CTA); meets the contract and is bitwise reproducible."""
+    for seed in (0, 1):
+        h, W, _ = prepared(layer, seed)
+        nb = B.proj_out_features(h, m) // 16
+        if m >= 3 and layer != "pooler":
+            assert "gemv_mma" in B.proj_describe(h, m)
+        for kw in (dict(), dict(kernel=B.PROJ_KERNEL_MMA),
+                   dict(kernel=B.PROJ_KERNEL_MMA, grid=-(-nb // 4)),
+                   dict(kernel=B.PROJ_KERNEL_MMA, grid=37)):
+            if m <= 2 and not kw:
+                continue
+            if kw.get("grid") and -(-nb // kw["grid"]) > 4:
+                continue
+            a = check_case(layer, seed, seed == 1, m, h=h, W=W, **kw)
+            b = check_case(layer, seed, seed == 1, m, h=h, W=W, **kw)
+            assert np.array_equal(a, b), (layer, m, seed, kw)
+        assert B.proj_device_status(h) == 0
+
+
+def test_mma_gemv_rejections(dev):
+    h, _, _ = prepared("pooler", 0)
+    x = torch.zeros((16, 8192), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros((16, 4096), dtype=torch.bfloat16, device="cuda")
+    for m, kw in ((9, dict(kernel=B.PROJ_KERNEL_MMA)),
+                  (8, dict(kernel=B.PROJ_KERNEL_MMA, grid=16)),   # 16 blocks per CTA
+                  (8, dict(kernel=B.PROJ_KERNEL_MMA, variant=B.PROJ_VARIANT_EXPWIN12))):
+        with pytest.raises(B.ProjError) as e:
+            B.proj_run_ex(h, x, m, out, **kw)
+        assert e.value.status == B.PROJ_EUNSUPPORTED
+    hr, _, _ = prepared("router", 0)
+    xr = torch.zeros((8, 8192), dtype=torch.bfloat16, device="cuda")
+    orr = torch.zeros((8, 256), dtype=torch.float32, device="cuda")
+    with pytest.raises(B.ProjError) as e:
+        B.proj_run_ex(hr, xr, 8, orr, kernel=B.PROJ_KERNEL_MMA)
+    assert e.value.status == B.PROJ_EUNSUPPORTED
+
+
 @pytest.mark.parametrize("m", [1, 3, 16, 130, 256])
 def test_router_planes_variant(dev, m):
     """The router's opt-in tensor-core form -- its fp32 weights as three exact
@@ -311,6 +354,14 @@ def test_unpack_is_lossless(dev, layer):
         B.proj_unpack_weights(h, B.PROJ_VARIANT_PLANES3, back)
         torch.cuda.synchronize()
         assert torch.equal(back.view(torch.int32), Wd.view(torch.int32))
+        with pytest.raises(B.ProjError):
+            B.proj_unpack_weights(h, B.PROJ_UNPACK_FRAG16, back)
+    else:
+        # the few-token GEMV's copy in warp-MMA fragment order
+        back.zero_()
+        B.proj_unpack_weights(h, B.PROJ_UNPACK_FRAG16, back)
+        torch.cuda.synchronize()
+        assert torch.equal(back.view(torch.int16), Wd.view(torch.int16))
 
 
 @pytest.mark.parametrize("layer", ["qkv_gate", "o", "pooler", "unpooler"])
@@ -384,7 +435,8 @@ def test_edge_arguments(dev):
     assert B.proj_out_features(prepared("unpooler", 0)[0], 8) == 1024
     assert B.proj_out_features(prepared("unpooler", 0)[0], 9) == 8192
     assert "gemv" in B.proj_describe(h, 1)
-    assert "BN=16" in B.proj_describe(h, 3)
+    assert "gemv_mma" in B.proj_describe(h, 3)
+    assert "BN=16" in B.proj_describe(h, 9)
     with pytest.raises(B.ProjError) as e:  # a run longer than the register form keeps
         B.proj_run_ex(h, x, 1, out, grid=1, kernel=B.PROJ_KERNEL_GEMV_REG)
     assert e.value.status == B.PROJ_EUNSUPPORTED
