@@ -363,14 +363,19 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
     const int64_t nb = pl->n_out / 16;
     int64_t G = std::min<int64_t>(nb, h->num_sms);
     if (opts && opts->grid > 0) G = std::min<int64_t>(opts->grid, nb);
+    const int nt = m <= 8 ? 1 : (m <= 16 ? 2 : 4);  // tiles of 8 tokens
     const bool mma_ok = !pl->router && h->w_frag && m <= kGemvMmaMaxM &&
+                        gemv_mma_fits(nt, static_cast<int>(h->K)) &&
                         (variant == PROJ_VARIANT_AUTO || variant == PROJ_VARIANT_DENSE) &&
                         pl->n_out % 16 == 0 && G > 0 && (nb + G - 1) / G <= kGemvMmaMaxBlocks;
-    // (measured: faster than the cluster kernel at 3..8 tokens on qkv_gate,
-    // o and the unpooler slice; the pooler's 256 blocks over 152 CTAs leave
-    // it behind -- whole blocks per CTA, two for most)
-    const bool mma_auto = kern == PROJ_KERNEL_AUTO && m >= kGemvMmaMinM &&
-                          (nb % G == 0 || (nb + G - 1) / G == 1 || h->K <= 4096) &&
+    // Measured against the cluster kernel on GB300: faster at 3..8 tokens
+    // on qkv_gate (one block per CTA), o and the unpooler slice, and at 9..16
+    // tokens on o (K = 1024: the cluster kernel's fixed costs dominate its
+    // short stream); slower on the pooler (256 blocks over 152 CTAs, two for
+    // most) and on the full unpooler (long streams over uneven blocks).
+    const bool mma_shape = m <= 8 ? (nb % G == 0 || (nb + G - 1) / G == 1 || h->K <= 4096)
+                                  : (m <= 16 && h->K <= 1024);
+    const bool mma_auto = kern == PROJ_KERNEL_AUTO && m >= kGemvMmaMinM && mma_shape &&
                           (!opts || (opts->grid == 0 && opts->groups == 0 &&
                                      opts->tile_n == 0 && opts->reduce == PROJ_REDUCE_AUTO));
     if (kern == PROJ_KERNEL_MMA && !mma_ok) return PROJ_EUNSUPPORTED;
@@ -378,7 +383,7 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
       pl->gemv_mma = true;
       pl->expwin = false;
       pl->reduce = 0;
-      pl->bn = kGemvMmaMaxM;
+      pl->bn = nt;
       pl->T = pl->KB = pl->MT = 0;
       pl->G = static_cast<int>(G);
       return PROJ_OK;
@@ -768,7 +773,7 @@ int proj_run_ex(proj_handle h, const void* x, int64_t m, void* out, proj_stream 
     g.n_rows = static_cast<int>(pl.n_out);
     g.K = static_cast<int>(h->K);
     g.G = pl.G;
-    e = gemv_mma_launch(g, s);
+    e = gemv_mma_launch(pl.bn, g, s);
     if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
     return PROJ_OK;
   }
@@ -875,7 +880,8 @@ int proj_describe(proj_handle h, int64_t m, char* buf, size_t cap) {
     std::snprintf(buf, cap, "gemv%s_%s MT=%d G=%d n_rows=%lld", pl.gemv_reg ? "_reg" : "",
                   pl.router ? "f32w" : "bf16w", pl.bn, pl.G, static_cast<long long>(pl.n_out));
   } else if (pl.gemv_mma) {
-    std::snprintf(buf, cap, "gemv_mma16x8 G=%d blocks_per_cta<=%lld n_rows=%lld", pl.G,
+    std::snprintf(buf, cap, "gemv_mma16x8 tokens<=%d G=%d blocks_per_cta<=%lld n_rows=%lld",
+                  8 * pl.bn, pl.G,
                   static_cast<long long>((pl.n_out / 16 + pl.G - 1) / pl.G),
                   static_cast<long long>(pl.n_out));
   } else if (pl.cluster) {

@@ -36,9 +36,11 @@ namespace {
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 constexpr int kU = 8;  // fragments per batch per warp
-constexpr int kXBytes = 8192 / 16 * 256;                          // K <= 8192
-constexpr int kRedBytes = kWarps * kGemvMmaMaxBlocks * 32 * 4 * 4;  // [warp][block][lane][4]
-constexpr int kSmem = kXBytes + kRedBytes;
+// Shared memory for NT tiles of 8 tokens: x in B-fragment order (K / 16
+// k-tiles x NT x 256 B) and the warps' partial tiles ([warp][block][NT][lane][4]).
+constexpr int red_bytes(int nt) { return kWarps * kGemvMmaMaxBlocks * nt * 32 * 4 * 4; }
+constexpr int smem_bytes(int nt, int K) { return K / 16 * nt * 256 + red_bytes(nt); }
+constexpr int kSmemLimit = 227 * 1024;
 
 __device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
   uint4 v;
@@ -85,10 +87,12 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint4& a, const ui
       : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y));
 }
 
+template <int NT>
 __global__ void __launch_bounds__(kThreads, 1) gemv_mma_kernel(const GemvMmaParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
-  const uint32_t sX = smem_u32(smem_raw);       // [K/16 k-tiles][32 lanes][2 words], xfrag_off
-  const uint32_t sRed = sX + kXBytes;           // [warp][block][lane][4] fp32
+  // [K/16 k-tiles][NT][32 lanes][2 words], fragment (kt, nt) at xfrag_off(kt NT + nt, ...)
+  const uint32_t sX = smem_u32(smem_raw);
+  const uint32_t sRed = sX + static_cast<uint32_t>(p.K / 16 * NT * 256);  // [warp][block][NT][lane][4]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -111,16 +115,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_mma_kernel(const GemvMmaPara
       if (u < u1) a[j] = ldg_stream(W + static_cast<size_t>(u) * 32);
     }
   };
+  auto red_at = [&](int w, int q, int nt, int l) {
+    return sRed + static_cast<uint32_t>((((w * kGemvMmaMaxBlocks + q) * NT + nt) * 32 + l) * 16);
+  };
   // Partial tiles, zero where a warp has no unit of a block.
 #pragma unroll
   for (int q = 0; q < kGemvMmaMaxBlocks; ++q)
-    st_shared_f32x4(sRed + static_cast<uint32_t>(((warp * kGemvMmaMaxBlocks + q) * 32 + lane) * 16),
-                    0.f, 0.f, 0.f, 0.f);
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) st_shared_f32x4(red_at(warp, q, nt, lane), 0.f, 0.f, 0.f, 0.f);
+  float acc[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
   int cur = u0 / KT;  // block of the accumulator (local index)
   auto flush = [&]() {
-    st_shared_f32x4(sRed + static_cast<uint32_t>(((warp * kGemvMmaMaxBlocks + cur) * 32 + lane) * 16),
-                    acc[0], acc[1], acc[2], acc[3]);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+      st_shared_f32x4(red_at(warp, cur, nt, lane), acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
   };
   auto compute_batch = [&](int base, const uint4 (&a)[kU]) {
 #pragma unroll
@@ -132,10 +142,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_mma_kernel(const GemvMmaPara
       if (bl != cur) {  // warp-uniform; at most once per warp
         flush();
         cur = bl;
-        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
       }
-      const uint2 b = ld_shared_u2(sX + xfrag_off(kt, lane, 0));
-      mma16816(acc, a[j], b);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const uint2 b = ld_shared_u2(sX + xfrag_off(kt * NT + nt, lane, 0));
+        mma16816(acc[nt], a[j], b);
+      }
     }
   };
 
@@ -168,11 +182,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_mma_kernel(const GemvMmaPara
         if (i >= n8) break;
         const int n = i / (p.K / 8);
         const int h = i - n * (p.K / 8);  // 16-byte chunk within the row
-        const int kt = h >> 1;
-        st_shared_u32(sX + xfrag_off(kt, 4 * n + 0, h & 1), xv[j].x);
-        st_shared_u32(sX + xfrag_off(kt, 4 * n + 1, h & 1), xv[j].y);
-        st_shared_u32(sX + xfrag_off(kt, 4 * n + 2, h & 1), xv[j].z);
-        st_shared_u32(sX + xfrag_off(kt, 4 * n + 3, h & 1), xv[j].w);
+        const int f = (h >> 1) * NT + (n >> 3);  // fragment (k-tile, token tile)
+        const int l4 = 4 * (n & 7);
+        st_shared_u32(sX + xfrag_off(f, l4 + 0, h & 1), xv[j].x);
+        st_shared_u32(sX + xfrag_off(f, l4 + 1, h & 1), xv[j].y);
+        st_shared_u32(sX + xfrag_off(f, l4 + 2, h & 1), xv[j].z);
+        st_shared_u32(sX + xfrag_off(f, l4 + 3, h & 1), xv[j].w);
       }
     }
   }
@@ -193,42 +208,64 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_mma_kernel(const GemvMmaPara
   // Each (block, row, token) summed over the warps' partial tiles in warp
   // order.
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
-  for (int idx = threadIdx.x; idx < (b1 - b0) * 128; idx += kThreads) {
-    const int q = idx / 128;          // block
+  for (int idx = threadIdx.x; idx < (b1 - b0) * NT * 128; idx += kThreads) {
+    const int q = idx / (NT * 128);   // block
+    const int nt = (idx / 128) % NT;  // token tile
     const int l = (idx / 4) % 32;     // fragment lane
     const int e = idx % 4;            // fragment element
     float s = 0.f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w)
-      s += ld_shared_f32(sRed + static_cast<uint32_t>(((w * kGemvMmaMaxBlocks + q) * 32 + l) * 16 +
-                                                      e * 4));
+    for (int w = 0; w < kWarps; ++w) s += ld_shared_f32(red_at(w, q, nt, l) + e * 4);
     // element e of lane l: row l / 4 (+ 8 for e >= 2), token 2 (l % 4) + e % 2
     const int row = (l >> 2) + (e >= 2 ? 8 : 0);
-    const int tok = 2 * (l & 3) + (e & 1);
+    const int tok = nt * 8 + 2 * (l & 3) + (e & 1);
     if (tok < p.m)
       out[static_cast<size_t>(tok) * p.n_rows + (b0 + q) * 16 + row] = __float2bfloat16_rn(s);
   }
 }
 
-}  // namespace
 
-cudaError_t gemv_mma_init_attributes() {
-  return cudaFuncSetAttribute(gemv_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kSmem);
+template <int NT>
+cudaError_t set_attr() {
+  return cudaFuncSetAttribute(gemv_mma_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kSmemLimit);
 }
 
-cudaError_t gemv_mma_launch(const GemvMmaParams& p, cudaStream_t s) {
+template <int NT>
+cudaError_t launch(const GemvMmaParams& p, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.G);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmem;
+  cfg.dynamicSmemBytes = gemv_mma_smem(NT, p.K);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemv_mma_kernel, p);
+  return cudaLaunchKernelEx(&cfg, gemv_mma_kernel<NT>, p);
+}
+
+}  // namespace
+
+int gemv_mma_smem(int nt, int K) { return smem_bytes(nt, K); }
+
+bool gemv_mma_fits(int nt, int K) { return smem_bytes(nt, K) <= kSmemLimit; }
+
+cudaError_t gemv_mma_init_attributes() {
+  cudaError_t e;
+  if ((e = set_attr<1>()) != cudaSuccess) return e;
+  if ((e = set_attr<2>()) != cudaSuccess) return e;
+  return set_attr<4>();
+}
+
+cudaError_t gemv_mma_launch(int nt, const GemvMmaParams& p, cudaStream_t s) {
+  switch (nt) {
+    case 1: return launch<1>(p, s);
+    case 2: return launch<2>(p, s);
+    case 4: return launch<4>(p, s);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace proj

@@ -158,15 +158,17 @@ struct GemvMmaParams {
   const void* x;    // bf16 [m, K]
   void* out;        // bf16 [m, n_rows]
   uint32_t* status;
-  int m;            // <= 8
+  int m;            // <= 8 x nt
   int n_rows;       // rows computed, multiple of 16
   int K;            // multiple of 256, <= 8192
   int G;            // CTAs: CTA c computes 16-row blocks [c NB / G, (c + 1) NB / G)
 };
-constexpr int kGemvMmaMaxM = 8;
+constexpr int kGemvMmaMaxM = 32;
 constexpr int kGemvMmaMaxBlocks = 4;  // 16-row blocks per CTA, at most
+int gemv_mma_smem(int nt, int K);   // dynamic shared memory at nt tiles of 8 tokens
+bool gemv_mma_fits(int nt, int K);  // it fits one CTA's shared memory
 cudaError_t gemv_mma_init_attributes();
-cudaError_t gemv_mma_launch(const GemvMmaParams& p, cudaStream_t s);
+cudaError_t gemv_mma_launch(int nt, const GemvMmaParams& p, cudaStream_t s);
 cudaError_t pack_router_fma_tiles(const float* W, int N, int K, uint8_t* dst, cudaStream_t s);
 cudaError_t unpack_router_fma_tiles(const uint8_t* src, int N, int K, float* W, cudaStream_t s);
 // Router W -> bf16 planes hi, mid, lo (hi + mid + lo == W) packed as the bf16

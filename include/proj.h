@@ -113,11 +113,12 @@ enum proj_kernel {
     PROJ_KERNEL_GEMV = 1,   /* row-streaming CUDA-core GEMV, m <= 2 */
     PROJ_KERNEL_TILE = 2,   /* tiled kernels: tensor cores (bf16) / FMA tiles (router),
                                split-K across CTAs through global memory */
-    PROJ_KERNEL_MMA = 5,    /* bf16 layers, m <= 8: weight-streaming GEMV on the warp-level
-                               tensor-core MMA (mma.sync m16n8k16) from a copy of W in
-                               fragment order; CTAs own whole 16-row blocks (at most 4),
-                               proj_run_opts.grid = CTAs; the dispatch form at
-                               3 <= m <= 8 */
+    PROJ_KERNEL_MMA = 5,    /* bf16 layers, m <= 32 (as far as x fits shared memory: K <=
+                               8192 / 4096 / 1024 at 8 / 16 / 32 tokens): weight-streaming
+                               GEMV on the warp-level tensor-core MMA (mma.sync m16n8k16)
+                               from a copy of W in fragment order; CTAs own whole 16-row
+                               blocks (at most 4), proj_run_opts.grid = CTAs; the dispatch
+                               form at 3 <= m <= 8 (not the pooler) and on o to 16 */
     PROJ_KERNEL_GEMV_REG = 4, /* m <= 2: CUDA-core GEMV with the weights loaded straight
                                  into registers (PROJ_KERNEL_GEMV: through a shared-
                                  memory ring fed by bulk copies) */

@@ -182,8 +182,10 @@ def test_cluster_groups_and_determinism(dev, layer, m):
     assert B.proj_device_status(h) == 0
 
 
-@pytest.mark.parametrize("m", [1, 2, 3, 5, 7, 8])
-@pytest.mark.parametrize("layer", ["qkv_gate", "o", "pooler", "unpooler"])
+@pytest.mark.parametrize("layer,m", [(l, m) for l in ("qkv_gate", "o", "pooler", "unpooler")
+                                     for m in (1, 2, 3, 5, 7, 8)] +
+                         [("o", 9), ("o", 16), ("o", 17), ("o", 32), ("unpooler", 9),
+                          ("unpooler", 16)])
 def test_mma_gemv(dev, layer, m):
     """The bf16 layers' few-token GEMV on the warp-level tensor-core MMA (W in
     fragment order, whole 16-row blocks per CTA): the dispatch form at
@@ -192,7 +194,7 @@ def test_mma_gemv(dev, layer, m):
     for seed in (0, 1):
         h, W, _ = prepared(layer, seed)
         nb = B.proj_out_features(h, m) // 16
-        if m >= 3 and layer != "pooler":
+        if (3 <= m <= 8 and layer != "pooler") or (layer == "o" and 9 <= m <= 16):
             assert "gemv_mma" in B.proj_describe(h, m)
         for kw in (dict(), dict(kernel=B.PROJ_KERNEL_MMA),
                    dict(kernel=B.PROJ_KERNEL_MMA, grid=-(-nb // 4)),
@@ -211,7 +213,7 @@ def test_mma_gemv_rejections(dev):
     h, _, _ = prepared("pooler", 0)
     x = torch.zeros((16, 8192), dtype=torch.bfloat16, device="cuda")
     out = torch.zeros((16, 4096), dtype=torch.bfloat16, device="cuda")
-    for m, kw in ((9, dict(kernel=B.PROJ_KERNEL_MMA)),
+    for m, kw in ((9, dict(kernel=B.PROJ_KERNEL_MMA)),    # x for 16 tokens does not fit at K = 8192
                   (8, dict(kernel=B.PROJ_KERNEL_MMA, grid=16)),   # 16 blocks per CTA
                   (8, dict(kernel=B.PROJ_KERNEL_MMA, variant=B.PROJ_VARIANT_EXPWIN12))):
         with pytest.raises(B.ProjError) as e:
@@ -436,7 +438,8 @@ def test_edge_arguments(dev):
     assert B.proj_out_features(prepared("unpooler", 0)[0], 9) == 8192
     assert "gemv" in B.proj_describe(h, 1)
     assert "gemv_mma" in B.proj_describe(h, 3)
-    assert "BN=16" in B.proj_describe(h, 9)
+    assert "gemv_mma" in B.proj_describe(h, 9)
+    assert "BN=32" in B.proj_describe(h, 17)
     with pytest.raises(B.ProjError) as e:  # a run longer than the register form keeps
         B.proj_run_ex(h, x, 1, out, grid=1, kernel=B.PROJ_KERNEL_GEMV_REG)
     assert e.value.status == B.PROJ_EUNSUPPORTED
