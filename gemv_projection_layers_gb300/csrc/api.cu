@@ -122,6 +122,8 @@ constexpr int64_t kExpwinMaxM = 32;
 constexpr int64_t kTcOwnerMaxM = 8;
 
 constexpr int64_t kGemvMaxM = 2;
+// The router's few-token GEMV is the dispatch form up to this many tokens.
+constexpr int64_t kRouterGemvAutoMaxM = 8;
 // From three tokens to kGemvMmaMaxM the bf16 layers take the warp-MMA
 // weight stream (measured faster than the tcgen05 cluster kernel there).
 constexpr int64_t kGemvMmaMinM = 3;
@@ -227,6 +229,7 @@ struct Plan {
   bool gemv;
   bool gemv_reg = false;  // m <= 2: register-streaming form
   bool gemv_mma = false;  // bf16, m <= 8: warp-MMA weight stream
+  bool router_gemv = false;  // router, m <= 16: FP32-FMA weight stream
   bool cluster;
   bool planes = false;  // router on the tensor cores (three bf16 planes)
   int KG = 1;  // cluster kernel: clusters per output tile
@@ -334,7 +337,8 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
   // Streaming GEMV: small m, uncompressed weights.
   const bool gemv_ok =
       m <= kGemvMaxM && (variant == PROJ_VARIANT_AUTO || variant == PROJ_VARIANT_DENSE);
-  if ((kern == PROJ_KERNEL_GEMV || kern == PROJ_KERNEL_GEMV_REG) && !gemv_ok)
+  if ((kern == PROJ_KERNEL_GEMV || kern == PROJ_KERNEL_GEMV_REG) && !gemv_ok &&
+      !(kern == PROJ_KERNEL_GEMV_REG && pl->router && m <= kRouterGemvMaxM))
     return PROJ_EUNSUPPORTED;
   if (gemv_ok && (kern == PROJ_KERNEL_GEMV || kern == PROJ_KERNEL_GEMV_REG ||
                   (kern == PROJ_KERNEL_AUTO && tile_n == 0))) {
@@ -358,6 +362,27 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
   }
   pl->gemv = false;
   pl->cluster = false;
+  // The router at 3..8 tokens (or on request, as the register form, to 16):
+  // FP32 FMAs on a weight stream, whole rows per CTA.  (Measured on GB300:
+  // 4.6-6.5 us against the cluster kernel's 8.6 at 3..8 tokens; a second
+  // pass of eight tokens makes it slower than the cluster kernel.)
+  if (pl->router && m <= kRouterGemvMaxM &&
+      (kern == PROJ_KERNEL_GEMV_REG ||
+       (kern == PROJ_KERNEL_AUTO && variant == PROJ_VARIANT_AUTO && m <= kRouterGemvAutoMaxM &&
+        (!opts || (opts->grid == 0 && opts->groups == 0 && opts->tile_n == 0 &&
+                   opts->reduce == PROJ_REDUCE_AUTO))))) {
+    int64_t G = std::min<int64_t>(pl->n_out, h->num_sms);
+    if (opts && opts->grid > 0) G = std::min<int64_t>(opts->grid, pl->n_out);
+    if (h->K % 1024 || h->K > 8192 || (pl->n_out + G - 1) / G * (h->K / 1024) > 16)
+      return PROJ_EUNSUPPORTED;
+    pl->router_gemv = true;
+    pl->expwin = false;
+    pl->reduce = 0;
+    pl->bn = 8;
+    pl->T = pl->KB = pl->MT = 0;
+    pl->G = static_cast<int>(G);
+    return PROJ_OK;
+  }
   // A few tokens on the bf16 layers: the warp-MMA weight stream.
   {
     const int64_t nb = pl->n_out / 16;
@@ -571,6 +596,7 @@ proj_handle proj_prepare_ex(int layer, const void* W, int64_t N, int64_t K, int 
   if ((e = gemv_init_attributes()) != cudaSuccess) return bail_cuda(e, "gemv attributes");
   if ((e = gemv_reg_init_attributes()) != cudaSuccess) return bail_cuda(e, "gemv attributes");
   if ((e = gemv_mma_init_attributes()) != cudaSuccess) return bail_cuda(e, "gemv attributes");
+  if ((e = router_gemv_init_attributes()) != cudaSuccess) return bail_cuda(e, "gemv attributes");
   if ((e = cluster_init_attributes()) != cudaSuccess) return bail_cuda(e, "cluster attributes");
   {
     const int bns[5] = {16, 32, 64, 128, 256};
@@ -763,6 +789,20 @@ int proj_run_ex(proj_handle h, const void* x, int64_t m, void* out, proj_stream 
     if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
     return PROJ_OK;
   }
+  if (pl.router_gemv) {
+    RouterGemvParams r;
+    r.w = h->w_rows;
+    r.x = x;
+    r.out = out;
+    r.status = h->status;
+    r.m = static_cast<int>(m);
+    r.N = static_cast<int>(pl.n_out);
+    r.K = static_cast<int>(h->K);
+    r.G = pl.G;
+    e = router_gemv_launch(r, s);
+    if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
+    return PROJ_OK;
+  }
   if (pl.gemv_mma) {
     GemvMmaParams g;
     g.w = reinterpret_cast<const uint4*>(h->w_frag);
@@ -879,6 +919,9 @@ int proj_describe(proj_handle h, int64_t m, char* buf, size_t cap) {
   if (pl.gemv) {
     std::snprintf(buf, cap, "gemv%s_%s MT=%d G=%d n_rows=%lld", pl.gemv_reg ? "_reg" : "",
                   pl.router ? "f32w" : "bf16w", pl.bn, pl.G, static_cast<long long>(pl.n_out));
+  } else if (pl.router_gemv) {
+    std::snprintf(buf, cap, "router_gemv_f32w passes_of_8 G=%d n_rows=%lld", pl.G,
+                  static_cast<long long>(pl.n_out));
   } else if (pl.gemv_mma) {
     std::snprintf(buf, cap, "gemv_mma16x8 tokens<=%d G=%d blocks_per_cta<=%lld n_rows=%lld",
                   8 * pl.bn, pl.G,

@@ -132,6 +132,21 @@ cudaError_t cluster_launch(int BN, const CUtensorMap& tmap_x, const ClusterParam
                            cudaStream_t s);
 
 // FP32-FMA router on the cluster split-K skeleton: BN in {16, 32, 64}.
+// The router at a few tokens: whole rows per CTA, fp32 weights straight to
+// registers, x in passes of eight tokens (router_gemv.cu).
+struct RouterGemvParams {
+  const void* w;    // fp32 row-major [N, K]
+  const void* x;    // bf16 [m, K]
+  void* out;        // fp32 [m, N]
+  uint32_t* status;
+  int m;            // <= kRouterGemvMaxM
+  int N;
+  int K;            // multiple of 1024, <= 8192
+  int G;            // CTAs: CTA c computes rows [c N / G, (c + 1) N / G), at most 16 chunks
+};
+constexpr int kRouterGemvMaxM = 16;
+cudaError_t router_gemv_init_attributes();
+cudaError_t router_gemv_launch(const RouterGemvParams& p, cudaStream_t s);
 cudaError_t router_cluster_init_attributes();
 int router_cluster_max_active(int BN, int cs);
 int router_cluster_stages(int BN);

@@ -119,9 +119,12 @@ enum proj_kernel {
                                from a copy of W in fragment order; CTAs own whole 16-row
                                blocks (at most 4), proj_run_opts.grid = CTAs; the dispatch
                                form at 3 <= m <= 8 (not the pooler) and on o to 16 */
-    PROJ_KERNEL_GEMV_REG = 4, /* m <= 2: CUDA-core GEMV with the weights loaded straight
-                                 into registers (PROJ_KERNEL_GEMV: through a shared-
-                                 memory ring fed by bulk copies) */
+    PROJ_KERNEL_GEMV_REG = 4, /* m <= 2 (the router: m <= 16): CUDA-core GEMV with the
+                                 weights loaded straight into registers, whole rows per
+                                 CTA (PROJ_KERNEL_GEMV: through a shared-memory ring fed
+                                 by bulk copies); for the router at 3 <= m <= 16, FP32
+                                 FMAs with x in passes of eight tokens (the dispatch
+                                 form at 3 <= m <= 8) */
     PROJ_KERNEL_CLUSTER = 3 /* tensor cores (dense bf16 weights; the router's bf16 planes),
                                split-K inside a thread-block cluster combined through
                                distributed shared memory, and optionally across several

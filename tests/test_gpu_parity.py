@@ -142,7 +142,7 @@ def test_cluster_sizes_and_determinism(dev, layer, m):
     meets the contract and is bitwise reproducible; for the router this is the
     FP32-FMA cluster kernel (fp32 weights as they are)."""
     h, W, _ = prepared(layer, 0)
-    if m >= (3 if layer == "router" else 33):
+    if m >= (9 if layer == "router" else 33):
         assert "cluster" in B.proj_describe(h, m)
     for cs in range(1, 17):
         kw = dict(grid=cs, kernel=B.PROJ_KERNEL_CLUSTER)
@@ -225,6 +225,31 @@ def test_mma_gemv_rejections(dev):
     with pytest.raises(B.ProjError) as e:
         B.proj_run_ex(hr, xr, 8, orr, kernel=B.PROJ_KERNEL_MMA)
     assert e.value.status == B.PROJ_EUNSUPPORTED
+
+
+@pytest.mark.parametrize("m", [3, 5, 7, 8, 9, 15, 16])
+def test_router_gemv(dev, m):
+    """The router's few-token FP32-FMA GEMV (whole rows per CTA, weights in
+    registers, x in passes of eight tokens): the dispatch form at
+    3 <= m <= 8 (forced to 16), at several CTA counts; meets the router's 1e-4
+    contract (probe rows exactly) and is bitwise reproducible."""
+    for seed in (0, 1):
+        h, W, _ = prepared("router", seed)
+        assert ("router_gemv" in B.proj_describe(h, m)) == (m <= 8)
+        for kw in (dict(), dict(kernel=B.PROJ_KERNEL_GEMV_REG, grid=128),
+                   dict(kernel=B.PROJ_KERNEL_GEMV_REG, grid=150)):
+            a = check_case("router", seed, seed == 1, m, h=h, W=W, **kw)
+            b = check_case("router", seed, seed == 1, m, h=h, W=W, **kw)
+            assert np.array_equal(a, b), (m, seed, kw)
+        assert B.proj_device_status(h) == 0
+    h, _, _ = prepared("router", 0)
+    x = torch.zeros((32, 8192), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros((32, 256), dtype=torch.float32, device="cuda")
+    for mm, kw in ((17, dict(kernel=B.PROJ_KERNEL_GEMV_REG)),
+                   (8, dict(kernel=B.PROJ_KERNEL_GEMV_REG, grid=64))):  # 32 chunks per CTA
+        with pytest.raises(B.ProjError) as e:
+            B.proj_run_ex(h, x, mm, out, **kw)
+        assert e.value.status == B.PROJ_EUNSUPPORTED
 
 
 @pytest.mark.parametrize("m", [1, 3, 16, 130, 256])
