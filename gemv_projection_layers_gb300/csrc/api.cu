@@ -122,6 +122,12 @@ constexpr int64_t kExpwinMaxM = 32;
 constexpr int64_t kTcOwnerMaxM = 8;
 
 constexpr int64_t kGemvMaxM = 2;
+// m <= 2 with the 12-bit row-chunk records built: the dispatch table keeps
+// the dense register GEMV (measured on GB300 at m = 1, 2 on the four bf16
+// layers: the 12-bit form within +-0.6 us of it either way -- both are bound
+// by the per-warp chain of load round trips, not by the bytes), so the
+// records serve variant = EXPWIN12.
+constexpr bool kRc12Auto = false;
 // The router's few-token GEMV is the dispatch form up to this many tokens.
 constexpr int64_t kRouterGemvAutoMaxM = 8;
 // From three tokens to kGemvMmaMaxM the bf16 layers take the warp-MMA
@@ -261,6 +267,8 @@ struct proj_ctx {
   int rcluster_active[5][kClusterMaxCS] = {};  // the same for the FP32-FMA router kernel
   uint8_t* w_exp = nullptr;
   size_t w_exp_bytes = 0;
+  uint8_t* w_rc12 = nullptr;       // 12-bit row-chunk records (register GEMV, m <= 2)
+  uint32_t* rc12_esc = nullptr;    // their escape blocks
   int e0 = 0;
   int64_t n_esc = 0;
   int exp_declined = 0;
@@ -294,6 +302,8 @@ void free_ctx(proj_ctx* h) {
   cudaFree(h->gemv_flags);
   cudaFree(h->gemv_ws);
   cudaFree(h->w_exp);
+  cudaFree(h->w_rc12);
+  cudaFree(h->rc12_esc);
   cudaFree(h->ws);
   cudaFree(h->counters);
   cudaFree(h->status);
@@ -336,7 +346,8 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
   pl->n_out = out_rows(h, m);
   // Streaming GEMV: small m, uncompressed weights.
   const bool gemv_ok =
-      m <= kGemvMaxM && (variant == PROJ_VARIANT_AUTO || variant == PROJ_VARIANT_DENSE);
+      m <= kGemvMaxM && (variant == PROJ_VARIANT_AUTO || variant == PROJ_VARIANT_DENSE ||
+                         (variant == PROJ_VARIANT_EXPWIN12 && h->w_rc12));
   if ((kern == PROJ_KERNEL_GEMV || kern == PROJ_KERNEL_GEMV_REG) && !gemv_ok &&
       !(kern == PROJ_KERNEL_GEMV_REG && pl->router && m <= kRouterGemvMaxM))
     return PROJ_EUNSUPPORTED;
@@ -358,6 +369,10 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
     const bool reg_ok = (pl->n_out + pl->G - 1) / pl->G * (h->K / 1024) <= kGemvRegMaxChunks;
     if (kern == PROJ_KERNEL_GEMV_REG && !reg_ok) return PROJ_EUNSUPPORTED;
     pl->gemv_reg = kern == PROJ_KERNEL_GEMV_REG || (kern == PROJ_KERNEL_AUTO && reg_ok);
+    // The 12-bit records are read by the register form only.
+    pl->expwin = h->w_rc12 && pl->gemv_reg &&
+                 (variant == PROJ_VARIANT_EXPWIN12 || (variant == PROJ_VARIANT_AUTO && kRc12Auto));
+    if (variant == PROJ_VARIANT_EXPWIN12 && !pl->expwin) return PROJ_EUNSUPPORTED;
     return PROJ_OK;
   }
   pl->gemv = false;
@@ -706,6 +721,35 @@ proj_handle proj_prepare_ex(int layer, const void* W, int64_t N, int64_t K, int 
         h->w_exp_bytes = 0;
         h->exp_declined = 1;
       }
+      // The register GEMV's row-chunk records, same window.
+      if (K % kRc12Chunk == 0 && K <= 8192) {
+        const size_t chunks = static_cast<size_t>(N) * (K / kRc12Chunk);
+        uint32_t* dev_over = nullptr;
+        uint32_t over = 0;
+        bool ok12 = (e = dmalloc(&dev_over, 4)) == cudaSuccess &&
+                    (e = dmalloc(&h->w_rc12, chunks * kRc12Bytes)) == cudaSuccess &&
+                    (e = dmalloc(&h->rc12_esc, chunks * kRc12EscWords * 4)) == cudaSuccess &&
+                    (e = cudaMemsetAsync(dev_over, 0, 4, s)) == cudaSuccess &&
+                    (e = cudaMemsetAsync(h->rc12_esc, 0, chunks * kRc12EscWords * 4, s)) ==
+                        cudaSuccess &&
+                    (e = encode_rc12(static_cast<const uint16_t*>(W), static_cast<int>(N),
+                                     static_cast<int>(K), h->e0, h->w_rc12, h->rc12_esc, dev_over,
+                                     s)) == cudaSuccess &&
+                    (e = cudaMemcpyAsync(&over, dev_over, 4, cudaMemcpyDeviceToHost, s)) ==
+                        cudaSuccess &&
+                    (e = cudaStreamSynchronize(s)) == cudaSuccess;
+        cudaFree(dev_over);
+        if (!ok12) {
+          done();
+          return bail_cuda(e, "12-bit row-chunk encode");
+        }
+        if (over) {  // some chunk has more escapes than its block holds
+          cudaFree(h->w_rc12);
+          cudaFree(h->rc12_esc);
+          h->w_rc12 = nullptr;
+          h->rc12_esc = nullptr;
+        }
+      }
     }
     const int bn_max = bn_for_m(std::min<int64_t>(m_max, 256));
     h->ws_bytes = static_cast<size_t>(2 * sms) * bn_max * kTileRows * 4;
@@ -774,7 +818,9 @@ int proj_run_ex(proj_handle h, const void* x, int64_t m, void* out, proj_stream 
   cudaError_t e;
   if (pl.gemv) {
     GemvParams g;
-    g.w = h->w_rows;
+    g.w = pl.expwin ? static_cast<const void*>(h->w_rc12) : h->w_rows;
+    g.esc = h->rc12_esc;
+    g.e0x4 = static_cast<uint32_t>(h->e0) * 0x01010101u;
     g.x = x;
     g.out = out;
     g.ws = h->gemv_ws;
@@ -785,7 +831,9 @@ int proj_run_ex(proj_handle h, const void* x, int64_t m, void* out, proj_stream 
     g.K = static_cast<int>(h->K);
     g.G = pl.G;
     g.out_f32 = pl.router ? 1 : 0;
-    e = pl.gemv_reg ? gemv_reg_launch(pl.router, pl.bn, g, s) : gemv_launch(pl.router, pl.bn, g, s);
+    e = pl.expwin     ? gemv_reg12_launch(pl.bn, g, s)
+        : pl.gemv_reg ? gemv_reg_launch(pl.router, pl.bn, g, s)
+                      : gemv_launch(pl.router, pl.bn, g, s);
     if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
     return PROJ_OK;
   }
@@ -918,7 +966,8 @@ int proj_describe(proj_handle h, int64_t m, char* buf, size_t cap) {
   if (st != PROJ_OK) return fail(st);
   if (pl.gemv) {
     std::snprintf(buf, cap, "gemv%s_%s MT=%d G=%d n_rows=%lld", pl.gemv_reg ? "_reg" : "",
-                  pl.router ? "f32w" : "bf16w", pl.bn, pl.G, static_cast<long long>(pl.n_out));
+                  pl.router ? "f32w" : (pl.expwin ? "expwin12rc" : "bf16w"), pl.bn, pl.G,
+                  static_cast<long long>(pl.n_out));
   } else if (pl.router_gemv) {
     std::snprintf(buf, cap, "router_gemv_f32w passes_of_8 G=%d n_rows=%lld", pl.G,
                   static_cast<long long>(pl.n_out));
@@ -950,12 +999,13 @@ int proj_unpack_weights(proj_handle h, int variant, void* W_out, proj_stream str
   if (!h || !W_out) return fail(PROJ_EINVAL);
   if (!aligned16(W_out)) return fail(PROJ_EALIGN);
   if ((variant < PROJ_VARIANT_AUTO || variant > PROJ_VARIANT_PLANES3) &&
-      variant != PROJ_UNPACK_FRAG16)
+      variant != PROJ_UNPACK_FRAG16 && variant != PROJ_UNPACK_RC12)
     return fail(PROJ_EINVAL);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (h->layer == PROJ_ROUTER) {
-    if (variant == PROJ_VARIANT_EXPWIN12 || variant == PROJ_UNPACK_FRAG16)
+    if (variant == PROJ_VARIANT_EXPWIN12 || variant == PROJ_UNPACK_FRAG16 ||
+        variant == PROJ_UNPACK_RC12)
       return fail(PROJ_EUNSUPPORTED);
     if (variant == PROJ_VARIANT_PLANES3)
       e = unpack_router_planes(h->w_planes, static_cast<int>(h->N), static_cast<int>(h->K),
@@ -965,6 +1015,10 @@ int proj_unpack_weights(proj_handle h, int variant, void* W_out, proj_stream str
                                   static_cast<float*>(W_out), s);
   } else if (variant == PROJ_VARIANT_PLANES3) {
     return fail(PROJ_EUNSUPPORTED);
+  } else if (variant == PROJ_UNPACK_RC12) {
+    if (!h->w_rc12) return fail(PROJ_EUNSUPPORTED);
+    e = decode_rc12(h->w_rc12, h->rc12_esc, static_cast<int>(h->N), static_cast<int>(h->K), h->e0,
+                    static_cast<uint16_t*>(W_out), s);
   } else if (variant == PROJ_UNPACK_FRAG16) {
     if (!h->w_frag) return fail(PROJ_EUNSUPPORTED);
     e = unpack_frag16(h->w_frag, static_cast<int>(h->N), static_cast<int>(h->K),

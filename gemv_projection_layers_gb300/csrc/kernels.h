@@ -38,6 +38,24 @@ constexpr int kRecNibOff = 8192;
 constexpr int kRecEscOff = 12288;
 constexpr int kEscCap = 15;
 
+// 12-bit row-chunk records for the register GEMV (m <= 2), same nibble and
+// escape conventions: W [N, K] row-major cut into 1024-column chunks, chunk
+// q = n K / 1024 + c covering W[n, 1024 c .. 1024 c + 1023], record q at
+// q x 1536 bytes.  Lane l of the warp that reads a chunk holds its groups
+// j = 0..3, group j being columns 1024 c + 8 (l + 32 j) .. + 7:
+//   [0, 1024)     low bytes: the 16 bytes at 16 (l + 32 i), i = 0, 1, hold
+//                 groups 2i and 2i + 1 of lane l (8 bytes each, column order);
+//   [1024, 1536)  nibbles: the 16 bytes at 1024 + 16 l, word j for group j,
+//                 byte b holding the nibble of the group's column b in bits
+//                 0-3 and that of column b + 4 in bits 4-7.
+// Escapes sit in a separate array, 8 words per chunk at q x 32 bytes: word 0
+// = count (<= kRc12EscCap), then (position << 8 | original high byte), the
+// position being the column within the chunk, in increasing order.
+constexpr int kRc12Chunk = 1024;
+constexpr int kRc12Bytes = 1536;
+constexpr int kRc12EscWords = 8;
+constexpr int kRc12EscCap = kRc12EscWords - 1;
+
 // Router (fp32) tiles for the FMA kernel: 128 rows x 64 columns, 32768
 // bytes, tile (t, kb) at (t * K / 64 + kb) * 32768; row r at r * 256, its
 // 16-byte chunk c (columns 4c .. 4c+3) at slot c ^ (r & 15).
@@ -76,6 +94,8 @@ struct GemvParams {
   int K;                // multiple of 1024, <= 8192
   int G;                // CTAs, <= n_rows
   int out_f32;
+  const uint32_t* esc;  // 12-bit register form: escape blocks of the records in w
+  uint32_t e0x4;        // 12-bit register form: window base replicated into 4 bytes
 };
 cudaError_t gemv_init_attributes();
 // Register-streaming GEMV (m <= 2), same parameters (ws and flags unused);
@@ -84,6 +104,8 @@ cudaError_t gemv_init_attributes();
 constexpr int kGemvRegMaxChunks = 2048;
 cudaError_t gemv_reg_init_attributes();
 cudaError_t gemv_reg_launch(bool f32w, int MT, const GemvParams& p, cudaStream_t s);
+// The same form on 12-bit row-chunk records (bf16 weights, bf16 output).
+cudaError_t gemv_reg12_launch(int MT, const GemvParams& p, cudaStream_t s);
 // Record a failing status (and its text) for proj_last_status /
 // proj_last_cuda_error; both return the status.
 int record_status(int status, const char* text);
@@ -161,6 +183,12 @@ cudaError_t encode_expwin12(const uint16_t* W, int N, int K, int e0, uint8_t* ds
                             uint32_t* overflow, unsigned long long* n_esc, cudaStream_t s);
 cudaError_t decode_expwin12(const uint8_t* src, int N, int K, int e0, uint16_t* W,
                             cudaStream_t s);
+// Row-chunk records (K % 1024 == 0); esc must be zeroed before the encode,
+// *overflow is set when a chunk has more than kRc12EscCap escapes.
+cudaError_t encode_rc12(const uint16_t* W, int N, int K, int e0, uint8_t* rec, uint32_t* esc,
+                        uint32_t* overflow, cudaStream_t s);
+cudaError_t decode_rc12(const uint8_t* rec, const uint32_t* esc, int N, int K, int e0,
+                        uint16_t* W, cudaStream_t s);
 // Few-token GEMV layout: bf16 W [N, K] as 16 x 16 tiles in the A-fragment
 // order of mma.sync m16n8k16 (row-major A): tile (rb, kb) at
 // (rb K/16 + kb) x 512 bytes, lane l's 16 bytes at l x 16 holding the pairs

@@ -8,7 +8,9 @@
 //     bf16 tiles of a [N, 3K] matrix whose column p K + k holds plane p of
 //     W[:, k] (and back, summing the planes).
 //   * bf16 W -> 16 x 16 tiles in the A-fragment order of the m16n8k16
-//     warp MMA, for the few-token GEMV (and back).
+//     warp MMA, for the few-token GEMV (and back);
+//   * bf16 W -> 12-bit row-chunk records (same window, nibbles and escapes as
+//     the tile records) for the register GEMV (and back).
 // The tile and record layouts are defined in kernels.h.
 #include <cuda_bf16.h>
 
@@ -333,6 +335,114 @@ __global__ void unpack_frag16_kernel(const uint32_t* __restrict__ src, int N, in
 constexpr int kPrepBlock = 256;
 constexpr int kPrepGrid = 152 * 8;
 
+// Row-chunk records for the register GEMV: one warp per 1024-column chunk,
+// lane l encoding its groups j = 0..3 (columns 8 (l + 32 j) .. + 7); escapes
+// are numbered in column order (group, then lane, then column) by a warp
+// prefix sum, so the records do not depend on scheduling.
+__global__ void encode_rc12_kernel(const uint16_t* __restrict__ W, int N, int K, int e0,
+                                   uint8_t* __restrict__ rec, uint32_t* __restrict__ esc,
+                                   uint32_t* overflow) {
+  const int lane = threadIdx.x & 31;
+  const int64_t chunks = static_cast<int64_t>(N) * (K / kRc12Chunk);
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
+  for (int64_t q = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) / 32; q < chunks;
+       q += nwarps) {
+    const uint16_t* src = W + q * kRc12Chunk;  // chunks are contiguous in row-major W
+    uint8_t* r = rec + q * kRc12Bytes;
+    uint32_t* eb = esc + q * kRc12EscWords;
+    uint32_t nibw[4];
+    uint32_t base = 0;  // escapes numbered so far
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int col = (lane + 32 * j) * 8;
+      const uint4 v = *reinterpret_cast<const uint4*>(src + col);
+      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+      uint32_t lo0 = 0, lo1 = 0, nb = 0, emask = 0;
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        const uint32_t wb = (wv[b >> 1] >> (16 * (b & 1))) & 0xFFFFu;
+        const int h7 = static_cast<int>((wb >> 8) & 0x7F);
+        int code = h7 - e0;
+        if (code < 0 || code > 7) emask |= 1u << b;
+        code = code < 0 ? 0 : (code > 7 ? 7 : code);
+        const uint32_t nib = ((wb >> 15) << 3) | static_cast<uint32_t>(code);
+        if (b < 4) {
+          lo0 |= (wb & 0xFF) << (8 * b);
+          nb |= nib << (8 * b);
+        } else {
+          lo1 |= (wb & 0xFF) << (8 * (b - 4));
+          nb |= nib << (8 * (b - 4) + 4);
+        }
+      }
+      *reinterpret_cast<uint2*>(r + (lane + 32 * (j >> 1)) * 16 + (j & 1) * 8) =
+          make_uint2(lo0, lo1);
+      nibw[j] = nb;
+      const uint32_t cnt = __popc(emask);
+      uint32_t incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      uint32_t slot = base + incl - cnt;
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        if ((emask >> b) & 1u) {
+          const uint32_t wb = (wv[b >> 1] >> (16 * (b & 1))) & 0xFFFFu;
+          if (slot < static_cast<uint32_t>(kRc12EscCap))
+            eb[1 + slot] = (static_cast<uint32_t>(col + b) << 8) | (wb >> 8);
+          ++slot;
+        }
+      }
+      base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    *reinterpret_cast<uint4*>(r + kRc12Chunk + lane * 16) =
+        make_uint4(nibw[0], nibw[1], nibw[2], nibw[3]);
+    if (lane == 0) {
+      eb[0] = min(base, static_cast<uint32_t>(kRc12EscCap));
+      if (base > static_cast<uint32_t>(kRc12EscCap)) atomicOr(overflow, 1u);
+    }
+  }
+}
+
+// Row-chunk records back to row-major bf16: the register GEMV's decode, then
+// the escape patch.
+__global__ void decode_rc12_kernel(const uint8_t* __restrict__ rec,
+                                   const uint32_t* __restrict__ esc, int N, int K, uint32_t e0x4,
+                                   uint16_t* __restrict__ W) {
+  const int lane = threadIdx.x & 31;
+  const int64_t chunks = static_cast<int64_t>(N) * (K / kRc12Chunk);
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
+  for (int64_t q = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) / 32; q < chunks;
+       q += nwarps) {
+    const uint8_t* r = rec + q * kRc12Bytes;
+    const uint32_t* eb = esc + q * kRc12EscWords;
+    const uint4 nib = *reinterpret_cast<const uint4*>(r + kRc12Chunk + lane * 16);
+    const uint32_t nibw[4] = {nib.x, nib.y, nib.z, nib.w};
+    const uint32_t cnt = min(eb[0], static_cast<uint32_t>(kRc12EscCap));
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int col = (lane + 32 * j) * 8;
+      const uint2 lo = *reinterpret_cast<const uint2*>(r + (lane + 32 * (j >> 1)) * 16 + (j & 1) * 8);
+      const uint32_t nb = nibw[j];
+      const uint32_t hl = ((nb & 0x07070707u) + e0x4) | ((nb << 4) & 0x80808080u);
+      const uint32_t hh = (((nb >> 4) & 0x07070707u) + e0x4) | (nb & 0x80808080u);
+      uint32_t o[4] = {__byte_perm(lo.x, hl, 0x5140), __byte_perm(lo.x, hl, 0x7362),
+                       __byte_perm(lo.y, hh, 0x5140), __byte_perm(lo.y, hh, 0x7362)};
+      for (uint32_t e = 0; e < cnt; ++e) {
+        const uint32_t ent = eb[1 + e];
+        const int b = static_cast<int>(ent >> 8) - col;
+        if (b >= 0 && b < 8) {
+#pragma unroll
+          for (int w = 0; w < 4; ++w)
+            if (w == (b >> 1)) o[w] = __byte_perm(o[w], ent, (b & 1) ? 0x4210 : 0x3240);
+        }
+      }
+      *reinterpret_cast<uint4*>(W + q * kRc12Chunk + col) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t pack_bf16_tiles(const uint16_t* W, int N, int K, uint8_t* dst, cudaStream_t s) {
@@ -360,6 +470,19 @@ cudaError_t decode_expwin12(const uint8_t* src, int N, int K, int e0, uint16_t* 
                             cudaStream_t s) {
   const uint32_t e0x4 = static_cast<uint32_t>(e0) * 0x01010101u;
   decode_expwin12_kernel<<<kPrepGrid, kPrepBlock, 0, s>>>(src, N, K, e0x4, W);
+  return cudaGetLastError();
+}
+
+cudaError_t encode_rc12(const uint16_t* W, int N, int K, int e0, uint8_t* rec, uint32_t* esc,
+                        uint32_t* overflow, cudaStream_t s) {
+  encode_rc12_kernel<<<kPrepGrid, kPrepBlock, 0, s>>>(W, N, K, e0, rec, esc, overflow);
+  return cudaGetLastError();
+}
+
+cudaError_t decode_rc12(const uint8_t* rec, const uint32_t* esc, int N, int K, int e0,
+                        uint16_t* W, cudaStream_t s) {
+  const uint32_t e0x4 = static_cast<uint32_t>(e0) * 0x01010101u;
+  decode_rc12_kernel<<<kPrepGrid, kPrepBlock, 0, s>>>(rec, esc, N, K, e0x4, W);
   return cudaGetLastError();
 }
 

@@ -75,7 +75,11 @@ enum proj_flags {
      * per-tile escape list.  Results are bit-identical to the uncompressed
      * kernel.  If any tile holds more escapes than the format's per-tile
      * capacity, the encoding is declined and the handle runs uncompressed
-     * (proj_info reports it). */
+     * (proj_info reports it).  Where K is a multiple of 1024 (<= 8192) a
+     * second 12-bit copy in 1024-column row chunks (same window, escapes per
+     * chunk, at most 7, else that copy is declined) serves the register GEMV
+     * at m <= 2, bit-identical to its dense form; proj_describe names it
+     * "expwin12rc". */
     PROJ_ENCODE_EXPWIN12 = 1u << 0
 };
 
@@ -93,7 +97,9 @@ enum proj_status {
 enum proj_variant {
     PROJ_VARIANT_AUTO = 0,      /* the dispatch table's choice */
     PROJ_VARIANT_DENSE = 1,     /* uncompressed weights */
-    PROJ_VARIANT_EXPWIN12 = 2,  /* 12-bit weights (handle must hold them) */
+    PROJ_VARIANT_EXPWIN12 = 2,  /* 12-bit weights (handle must hold them): the row-chunk
+                                   copy on the register GEMV at m <= 2 where it was built,
+                                   else the tile records on the tensor cores (m <= 32) */
     PROJ_VARIANT_PLANES3 = 3    /* router only: the fp32 weights as three bf16 planes,
                                    hi + mid + lo == W exactly, on the tensor cores */
 };
@@ -232,9 +238,12 @@ int proj_describe(proj_handle h, int64_t m, char *buf, size_t cap);
  * the three bf16 planes back to fp32 (the same check for the plane split).
  * variant = PROJ_UNPACK_FRAG16 decodes the bf16 layers' copy in warp-MMA
  * fragment order (the few-token GEMV's layout; PROJ_EUNSUPPORTED where it
- * was not built).  Enqueued on `stream`.
+ * was not built), and variant = PROJ_UNPACK_RC12 the 12-bit row-chunk copy
+ * (bf16 layers with PROJ_ENCODE_EXPWIN12; PROJ_EUNSUPPORTED where it was
+ * not built or was declined).  Enqueued on `stream`.
  */
 #define PROJ_UNPACK_FRAG16 16
+#define PROJ_UNPACK_RC12 32
 int proj_unpack_weights(proj_handle h, int variant, void *W_out, proj_stream stream);
 
 /* Read and clear the handle's device status word (synchronises `stream`).

@@ -416,7 +416,7 @@ def test_expwin12_lossless_and_bit_identical(dev, layer):
                 a = run(layer, h, x, m, variant=B.PROJ_VARIANT_DENSE, grid=grid, reduce=reduce,
                         kernel=B.PROJ_KERNEL_TILE)
                 b = run(layer, h, x, m, variant=B.PROJ_VARIANT_EXPWIN12, grid=grid,
-                        reduce=reduce)
+                        reduce=reduce, kernel=B.PROJ_KERNEL_TILE)
                 assert torch.equal(a.view(torch.int16), b.view(torch.int16)), \
                     (layer, seed, m, grid, reduce)
             check_case(layer, seed, True, m, h=h, W=W, variant=B.PROJ_VARIANT_EXPWIN12)
@@ -430,6 +430,105 @@ def test_expwin12_lossless_and_bit_identical(dev, layer):
         for i, c in enumerate(cols):
             assert np.array_equal(o[i], oracle.bf16_bits_to_f64(W[:o.shape[1], c]))
         assert B.proj_device_status(h) == 0
+
+
+@pytest.mark.parametrize("layer", ["qkv_gate", "o", "pooler", "unpooler"])
+def test_expwin12_register_gemv(dev, layer):
+    """The 12-bit row-chunk records on the register GEMV (m <= 2): the copy
+    decodes to W bit for bit, and the outputs are bit-identical to the dense
+    register GEMV at the same partition (same products, same order)."""
+    for seed in (0, 1):
+        h, W, Wd = prepared(layer, seed, B.PROJ_ENCODE_EXPWIN12)
+        back = torch.zeros_like(Wd)
+        B.proj_unpack_weights(h, B.PROJ_UNPACK_RC12, back)
+        torch.cuda.synchronize()
+        assert torch.equal(back.view(torch.int16), Wd.view(torch.int16))
+        for m in (1, 2):
+            act = wl.make_activations(layer, m, seed + 3, outliers=True)
+            x = to_dev_x(act.x_bits)
+            for grid in (0, 37, 151):
+                a = run(layer, h, x, m, variant=B.PROJ_VARIANT_DENSE,
+                        kernel=B.PROJ_KERNEL_GEMV_REG, grid=grid)
+                b = run(layer, h, x, m, variant=B.PROJ_VARIANT_EXPWIN12, grid=grid)
+                assert torch.equal(a.view(torch.int16), b.view(torch.int16)), (layer, seed, m, grid)
+            check_case(layer, seed, True, m, h=h, W=W, variant=B.PROJ_VARIANT_EXPWIN12)
+            # the dispatch table keeps the dense register form at m <= 2
+            assert B.proj_describe(h, m).startswith("gemv_reg_bf16w")
+        assert B.proj_device_status(h) == 0
+
+
+def _planted_escape_weights(n_per_chunk, seed=0):
+    """o's weights with escapes planted at chosen columns of each 1024-column
+    chunk (row): large values above the window, signed zeros below it, at
+    even and odd columns of every lane and group position."""
+    spec = wl.LAYER_BY_NAME["o"]
+    W = wl.make_weights(spec, seed).copy()
+    # the matrix's own escapes move into the window (2^-7, same sign), so
+    # every chunk holds exactly the planted ones
+    e0 = oracle.expwin12_window(W)
+    h7 = (W >> 8) & 0x7F
+    nat = (h7 < e0) | (h7 > e0 + 7)
+    W[nat] = 0x3C00 | (W[nat] & 0x8000)
+    rng = np.random.default_rng(seed + 11)
+    fixed = np.array([0, 1, 9, 255, 263, 767, 1023, 512])
+    vals = np.array([0x4080, 0xC0A0, 0x0000, 0x8000, 0x4200, 0xC110, 0x0000, 0x4080], np.uint16)
+    for n in range(spec.N):
+        if n == 0:
+            cols = fixed[:n_per_chunk]
+        else:
+            cols = rng.choice(1024, size=int(rng.integers(0, n_per_chunk + 1)), replace=False)
+        W[n, cols] = vals[rng.integers(0, len(vals), size=len(cols))]
+    return spec, W
+
+
+def test_expwin12_register_gemv_planted_escapes(dev):
+    """Chunks with up to the block's 7 escapes decode exactly and give the
+    dense register GEMV's outputs bit for bit; one chunk with 8 escapes makes
+    prepare decline the row-chunk copy (the dense forms serve instead)."""
+    spec, W = _planted_escape_weights(7)
+    Wd = torch.from_numpy(W.view(np.int16)).cuda().view(torch.bfloat16)
+    h = B.proj_prepare_ex(spec.index, Wd, spec.N, spec.K, B.PROJ_BF16, B.PROJ_ENCODE_EXPWIN12, 64)
+    try:
+        back = torch.zeros_like(Wd)
+        B.proj_unpack_weights(h, B.PROJ_UNPACK_RC12, back)
+        torch.cuda.synchronize()
+        assert torch.equal(back.view(torch.int16), Wd.view(torch.int16))
+        for m in (1, 2):
+            act = wl.make_activations(spec, m, 4, outliers=False)
+            x = to_dev_x(act.x_bits)
+            a = run("o", h, x, m, variant=B.PROJ_VARIANT_DENSE, kernel=B.PROJ_KERNEL_GEMV_REG)
+            b = run("o", h, x, m, variant=B.PROJ_VARIANT_EXPWIN12)
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16)), m
+            ref = oracle.reference("o", act.x_bits, W)
+            res = oracle.check("o", out_f64(b), ref, [])
+            assert res["ok"], res
+        # one-hot rows on the planted columns of row 0 reproduce W's column
+        for c in (0, 1, 9, 255, 263, 767, 1023):
+            x = np.zeros((1, spec.K), np.uint16)
+            x[0, c] = 0x3F80
+            o = out_f64(run("o", h, to_dev_x(x), 1, variant=B.PROJ_VARIANT_EXPWIN12))
+            assert np.array_equal(o[0], oracle.bf16_bits_to_f64(W[:, c])), c
+        assert B.proj_device_status(h) == 0
+    finally:
+        B.proj_destroy(h)
+    spec, W = _planted_escape_weights(8)
+    Wd = torch.from_numpy(W.view(np.int16)).cuda().view(torch.bfloat16)
+    h = B.proj_prepare_ex(spec.index, Wd, spec.N, spec.K, B.PROJ_BF16, B.PROJ_ENCODE_EXPWIN12, 64)
+    try:
+        assert B.proj_info(h)["expwin12_declined"] == 1  # the tile records overflow too
+        back = torch.zeros_like(Wd)
+        with pytest.raises(B.ProjError) as e:
+            B.proj_unpack_weights(h, B.PROJ_UNPACK_RC12, back)
+        assert e.value.status == B.PROJ_EUNSUPPORTED
+        act = wl.make_activations(spec, 1, 4, outliers=False)
+        with pytest.raises(B.ProjError) as e:
+            run("o", h, to_dev_x(act.x_bits), 1, variant=B.PROJ_VARIANT_EXPWIN12)
+        assert e.value.status == B.PROJ_EUNSUPPORTED
+        out = run("o", h, to_dev_x(act.x_bits), 1)
+        res = oracle.check("o", out_f64(out), oracle.reference("o", act.x_bits, W), [])
+        assert res["ok"], res
+    finally:
+        B.proj_destroy(h)
 
 
 def test_run_host_matches_device_run(dev):
