@@ -303,6 +303,50 @@ def time_router_forms(B, torch, S, flush, sink, stream, reps):
     return res
 
 
+def time_compressed(B, torch, flush, stream, ms=(1, 8, 16)):
+    """The decode shapes with the bf16 weights losslessly recoded to 12 bits
+    (prepare flag PROJ_ENCODE_EXPWIN12): each layer's device time with
+    variant=EXPWIN12 (the router has no 12-bit form and runs as in the
+    loads) beside the same handle's dispatch-table form, per token count,
+    with the bytes each reads.  m <= 2: the register GEMV on the row-chunk
+    records; 3..32: the stream-K tile kernel on the tile records."""
+    flush_fn = lambda: flush(stream)
+    layers = setup_layers(B, torch, expwin=True)
+    res = {}
+    try:
+        for m in ms:
+            row = {"x12_us": {}, "auto_us": {}, "x12_kernels": {}, "x12_weight_bytes": {}}
+            for L in layers:
+                S = Shape(B, torch, L, m)
+                x12 = L.spec.weight_dtype != "fp32"
+                v = B.PROJ_VARIANT_EXPWIN12 if x12 else B.PROJ_VARIANT_AUTO
+                launch = lambda S=S, v=v: B.proj_run_ex(S.h, S.x, S.m, S.out, stream, variant=v)
+                launch()
+                torch.cuda.synchronize()
+                if B.proj_device_status(S.h) != 0:
+                    raise RuntimeError(f"device status after {L.spec.name} m={m}")
+                row["x12_us"][L.spec.name] = round(time_device_us(torch, launch, flush_fn, stream), 2)
+                row["auto_us"][L.spec.name] = round(time_device_us(
+                    torch, lambda S=S: B.proj_run(S.h, S.x, S.m, S.out, stream), flush_fn, stream), 2)
+                kern = S.desc
+                if x12:
+                    rc = m <= 2
+                    nw = S.n_out * L.spec.K
+                    row["x12_weight_bytes"][L.spec.name] = int(
+                        nw * 1.5 + (nw // 1024 * 32 if rc else
+                                    L.info["expwin12_escapes"] * S.n_out / L.spec.N * 4))
+                    kern = ("gemv_reg12 (row-chunk records)" if rc
+                            else "tc_kernel expwin12 (tile records)")
+                row["x12_kernels"][L.spec.name] = kern
+            row["x12_sum_us"] = round(sum(row["x12_us"].values()), 2)
+            row["auto_sum_us"] = round(sum(row["auto_us"].values()), 2)
+            res[f"m{m}"] = row
+    finally:
+        for L in layers:
+            B.proj_destroy(L.h)
+    return res
+
+
 def time_load(B, torch, lg, flush, sink, steps, breakdown=False):
     outer, per = [], []
     for _ in range(steps):
@@ -675,6 +719,7 @@ def run_ours(args):
                 loads_out[ld]["router_forms_single_graph_us"] = time_router_forms(
                     B, torch, rs, flush, sink, stream, nrep)
         result["loads"] = loads_out
+        result["compressed_12bit_device_us"] = time_compressed(B, torch, flush, stream)
 
     if not args.no_extras and rank == 0:
         e2e_us, h2d, d2h = time_e2e(B, torch, lg.shapes, flush, sink, stream, args.steps)
