@@ -122,6 +122,12 @@ constexpr int64_t kExpwinMaxM = 32;
 constexpr int64_t kTcOwnerMaxM = 8;
 
 constexpr int64_t kGemvMaxM = 2;
+// The split-K router GEMV serves these token counts by default (measured on
+// GB300, device time, cold L2: 0.4-2.2 us faster than the whole-row router
+// GEMV at 5..8 tokens and than the FP32-FMA cluster kernel at 9..24; at 3
+// tokens the whole-row form, at 32 the cluster kernel are faster).
+constexpr int64_t kRouterGemvCcAutoMinM = 5;
+constexpr int64_t kRouterGemvCcAutoMaxM = 24;
 // m <= 2 with the 12-bit row-chunk records built: the dispatch table keeps
 // the dense register GEMV (measured on GB300 at m = 1, 2 on the four bf16
 // layers: the 12-bit form within +-0.6 us of it either way -- both are bound
@@ -129,7 +135,7 @@ constexpr int64_t kGemvMaxM = 2;
 // records serve variant = EXPWIN12.
 constexpr bool kRc12Auto = false;
 // The router's few-token GEMV is the dispatch form up to this many tokens.
-constexpr int64_t kRouterGemvAutoMaxM = 8;
+constexpr int64_t kRouterGemvAutoMaxM = 4;
 // From three tokens to kGemvMmaMaxM the bf16 layers take the warp-MMA
 // weight stream (measured faster than the tcgen05 cluster kernel there).
 constexpr int64_t kGemvMmaMinM = 3;
@@ -236,6 +242,7 @@ struct Plan {
   bool gemv_reg = false;  // m <= 2: register-streaming form
   bool gemv_mma = false;  // bf16, m <= 8: warp-MMA weight stream
   bool router_gemv = false;  // router, m <= 16: FP32-FMA weight stream
+  bool router_gemv_cc = false;  // router, m <= 32: the same with K split across a cluster
   bool cluster;
   bool planes = false;  // router on the tensor cores (three bf16 planes)
   int KG = 1;  // cluster kernel: clusters per output tile
@@ -265,6 +272,7 @@ struct proj_ctx {
   uint32_t* w_frag = nullptr;      // bf16 layers: 16 x 16 MMA-fragment tiles (few tokens)
   int cluster_active[5][kClusterMaxCS] = {};   // co-resident clusters: BN 16..256 x size 1..16
   int rcluster_active[5][kClusterMaxCS] = {};  // the same for the FP32-FMA router kernel
+  int rgcc_active = 0;  // co-resident clusters of the split-K router GEMV
   uint8_t* w_exp = nullptr;
   size_t w_exp_bytes = 0;
   uint8_t* w_rc12 = nullptr;       // 12-bit row-chunk records (register GEMV, m <= 2)
@@ -336,7 +344,7 @@ int64_t out_rows(const proj_ctx* h, int64_t m) {
 int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl) {
   const int variant = opts ? opts->variant : PROJ_VARIANT_AUTO;
   const int kern = opts ? opts->kernel : PROJ_KERNEL_AUTO;
-  if (kern < PROJ_KERNEL_AUTO || kern > PROJ_KERNEL_MMA) return PROJ_EINVAL;
+  if (kern < PROJ_KERNEL_AUTO || kern > PROJ_KERNEL_GEMV_SPLITK) return PROJ_EINVAL;
   if (variant < PROJ_VARIANT_AUTO || variant > PROJ_VARIANT_PLANES3) return PROJ_EINVAL;
   const int tile_n = opts ? opts->tile_n : 0;
   if (tile_n != 0 && tile_n != 16 && tile_n != 32 && tile_n != 64 && tile_n != 128 &&
@@ -377,7 +385,30 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
   }
   pl->gemv = false;
   pl->cluster = false;
-  // The router at 3..8 tokens (or on request, as the register form, to 16):
+  // The router GEMV with K split across a cluster (one 1024-column chunk
+  // per CTA, eight rows per cluster): x staged per CTA is 1/8 of the
+  // whole-row form's.
+  if (kern == PROJ_KERNEL_GEMV_SPLITK ||
+      (pl->router && kern == PROJ_KERNEL_AUTO && variant == PROJ_VARIANT_AUTO &&
+       m >= kRouterGemvCcAutoMinM && m <= kRouterGemvCcAutoMaxM &&
+       (!opts || (opts->grid == 0 && opts->groups == 0 && opts->tile_n == 0 &&
+                  opts->reduce == PROJ_REDUCE_AUTO)))) {
+    const int64_t clusters = (pl->n_out + 7) / 8;
+    const bool ok = pl->router && m <= kRouterGemvCcMaxM && h->K % 1024 == 0 && h->K <= 8192 &&
+                    (variant == PROJ_VARIANT_AUTO || variant == PROJ_VARIANT_DENSE) &&
+                    h->rgcc_active >= clusters;
+    if (ok) {
+      pl->router_gemv_cc = true;
+      pl->expwin = false;
+      pl->reduce = 0;
+      pl->bn = 8;
+      pl->T = pl->KB = pl->MT = 0;
+      pl->G = static_cast<int>(h->K / 1024);  // cluster size
+      return PROJ_OK;
+    }
+    if (kern == PROJ_KERNEL_GEMV_SPLITK) return PROJ_EUNSUPPORTED;
+  }
+  // The router at 3 and 4 tokens (or on request, as the register form, to 16):
   // FP32 FMAs on a weight stream, whole rows per CTA.  (Measured on GB300:
   // 4.6-6.5 us against the cluster kernel's 8.6 at 3..8 tokens; a second
   // pass of eight tokens makes it slower than the cluster kernel.)
@@ -624,6 +655,8 @@ proj_handle proj_prepare_ex(int layer, const void* W, int64_t N, int64_t K, int 
         h->rcluster_active[b][c] = router_cluster_max_active(bns[b], c + 1);
       }
   }
+  if (layer == PROJ_ROUTER && K % 1024 == 0 && K <= 8192)
+    h->rgcc_active = router_gemv_cc_max_active(static_cast<int>(N), static_cast<int>(K));
   if (!encode_fn()) return bail_cuda(cudaErrorNotSupported, "cuTensorMapEncodeTiled");
 
   cudaStream_t s;
@@ -837,7 +870,7 @@ int proj_run_ex(proj_handle h, const void* x, int64_t m, void* out, proj_stream 
     if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
     return PROJ_OK;
   }
-  if (pl.router_gemv) {
+  if (pl.router_gemv || pl.router_gemv_cc) {
     RouterGemvParams r;
     r.w = h->w_rows;
     r.x = x;
@@ -847,7 +880,7 @@ int proj_run_ex(proj_handle h, const void* x, int64_t m, void* out, proj_stream 
     r.N = static_cast<int>(pl.n_out);
     r.K = static_cast<int>(h->K);
     r.G = pl.G;
-    e = router_gemv_launch(r, s);
+    e = pl.router_gemv_cc ? router_gemv_cc_launch(r, s) : router_gemv_launch(r, s);
     if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
     return PROJ_OK;
   }
@@ -971,6 +1004,9 @@ int proj_describe(proj_handle h, int64_t m, char* buf, size_t cap) {
   } else if (pl.router_gemv) {
     std::snprintf(buf, cap, "router_gemv_f32w passes_of_8 G=%d n_rows=%lld", pl.G,
                   static_cast<long long>(pl.n_out));
+  } else if (pl.router_gemv_cc) {
+    std::snprintf(buf, cap, "router_gemv_splitk_f32w CS=%d clusters=%lld n_rows=%lld", pl.G,
+                  static_cast<long long>((pl.n_out + 7) / 8), static_cast<long long>(pl.n_out));
   } else if (pl.gemv_mma) {
     std::snprintf(buf, cap, "gemv_mma16x8 tokens<=%d G=%d blocks_per_cta<=%lld n_rows=%lld",
                   8 * pl.bn, pl.G,

@@ -169,6 +169,12 @@ struct RouterGemvParams {
 constexpr int kRouterGemvMaxM = 16;
 cudaError_t router_gemv_init_attributes();
 cudaError_t router_gemv_launch(const RouterGemvParams& p, cudaStream_t s);
+// The router GEMV with K split across a cluster (router_gemv.cu): cluster
+// size K / 1024 (<= 8), rank q takes columns [1024 q, 1024 q + 1024) of 8
+// rows (one per warp); ceil(N / 8) clusters; G unused.  m <= 32.
+constexpr int kRouterGemvCcMaxM = 32;
+cudaError_t router_gemv_cc_launch(const RouterGemvParams& p, cudaStream_t s);
+int router_gemv_cc_max_active(int N, int K);  // co-resident clusters (occupancy query)
 cudaError_t router_cluster_init_attributes();
 int router_cluster_max_active(int BN, int cs);
 int router_cluster_stages(int BN);

@@ -142,7 +142,7 @@ def test_cluster_sizes_and_determinism(dev, layer, m):
     meets the contract and is bitwise reproducible; for the router this is the
     FP32-FMA cluster kernel (fp32 weights as they are)."""
     h, W, _ = prepared(layer, 0)
-    if m >= (9 if layer == "router" else 33):
+    if m >= (25 if layer == "router" else 33):
         assert "cluster" in B.proj_describe(h, m)
     for cs in range(1, 17):
         kw = dict(grid=cs, kernel=B.PROJ_KERNEL_CLUSTER)
@@ -230,12 +230,14 @@ def test_mma_gemv_rejections(dev):
 @pytest.mark.parametrize("m", [3, 5, 7, 8, 9, 15, 16])
 def test_router_gemv(dev, m):
     """The router's few-token FP32-FMA GEMV (whole rows per CTA, weights in
-    registers, x in passes of eight tokens): the dispatch form at
-    3 <= m <= 8 (forced to 16), at several CTA counts; meets the router's 1e-4
-    contract (probe rows exactly) and is bitwise reproducible."""
+    registers, x in passes of eight tokens): the dispatch form at m = 3, 4
+    (forced to 16), at several CTA counts; meets the router's 1e-4 contract
+    (probe rows exactly) and is bitwise reproducible."""
     for seed in (0, 1):
         h, W, _ = prepared("router", seed)
-        assert ("router_gemv" in B.proj_describe(h, m)) == (m <= 8)
+        desc = B.proj_describe(h, m)
+        assert desc.startswith("router_gemv_f32w") == (m <= 4), desc
+        assert desc.startswith("router_gemv_splitk") == (5 <= m <= 24), desc
         for kw in (dict(), dict(kernel=B.PROJ_KERNEL_GEMV_REG, grid=128),
                    dict(kernel=B.PROJ_KERNEL_GEMV_REG, grid=150)):
             a = check_case("router", seed, seed == 1, m, h=h, W=W, **kw)
@@ -250,6 +252,37 @@ def test_router_gemv(dev, m):
         with pytest.raises(B.ProjError) as e:
             B.proj_run_ex(h, x, mm, out, **kw)
         assert e.value.status == B.PROJ_EUNSUPPORTED
+
+
+@pytest.mark.parametrize("m", [1, 2, 3, 8, 9, 16, 17, 31, 32])
+def test_router_gemv_splitk(dev, m):
+    """The router GEMV with K split across a cluster (one 1024-column chunk
+    per CTA, eight rows per cluster, partials summed in rank order through
+    distributed shared memory; the dispatch form at 5 <= m <= 24): the 1e-4
+    contract, probe rows exactly, and bitwise reproducible; refused for the
+    bf16 layers and above 32 tokens."""
+    for seed in (0, 1):
+        h, W, _ = prepared("router", seed)
+        assert B.proj_describe(h, m).startswith("router_gemv_splitk") == (5 <= m <= 24)
+        kw = dict(kernel=B.PROJ_KERNEL_GEMV_SPLITK)
+        a = check_case("router", seed, seed == 1, m, h=h, W=W, **kw)
+        b = check_case("router", seed, seed == 1, m, h=h, W=W, **kw)
+        assert np.array_equal(a, b), (m, seed)
+        assert B.proj_device_status(h) == 0
+    h, _, _ = prepared("router", 0)
+    x = torch.zeros((33, 8192), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros((33, 256), dtype=torch.float32, device="cuda")
+    for mm, kw in ((33, dict(kernel=B.PROJ_KERNEL_GEMV_SPLITK)),
+                   (8, dict(kernel=B.PROJ_KERNEL_GEMV_SPLITK, variant=B.PROJ_VARIANT_PLANES3))):
+        with pytest.raises(B.ProjError) as e:
+            B.proj_run_ex(h, x, mm, out, **kw)
+        assert e.value.status == B.PROJ_EUNSUPPORTED
+    hq, _, _ = prepared("o", 0)
+    xq = torch.zeros((8, 1024), dtype=torch.bfloat16, device="cuda")
+    oq = torch.zeros((8, 8192), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(B.ProjError) as e:
+        B.proj_run_ex(hq, xq, 8, oq, kernel=B.PROJ_KERNEL_GEMV_SPLITK)
+    assert e.value.status == B.PROJ_EUNSUPPORTED
 
 
 @pytest.mark.parametrize("m", [1, 3, 16, 130, 256])
