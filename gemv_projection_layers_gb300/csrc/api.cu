@@ -123,10 +123,12 @@ constexpr int64_t kTcOwnerMaxM = 8;
 
 constexpr int64_t kGemvMaxM = 2;
 // The split-K router GEMV serves these token counts by default (measured on
-// GB300, device time, cold L2: 0.4-2.2 us faster than the whole-row router
-// GEMV at 5..8 tokens and than the FP32-FMA cluster kernel at 9..24; at 3
-// tokens the whole-row form, at 32 the cluster kernel are faster).
-constexpr int64_t kRouterGemvCcAutoMinM = 5;
+// GB300, device time, cold L2: 1-2.2 us faster than the FP32-FMA cluster
+// kernel at 9..24 tokens, slower at 32; at 5..8 tokens 0.4-1 us faster than
+// the whole-row router GEMV alone, but a load with it last ran 1.5 us
+// slower -- the cluster launch overlaps less with the previous kernel's
+// tail -- so the whole-row form keeps 3..8).
+constexpr int64_t kRouterGemvCcAutoMinM = 9;
 constexpr int64_t kRouterGemvCcAutoMaxM = 24;
 // m <= 2 with the 12-bit row-chunk records built: the dispatch table keeps
 // the dense register GEMV (measured on GB300 at m = 1, 2 on the four bf16
@@ -135,7 +137,7 @@ constexpr int64_t kRouterGemvCcAutoMaxM = 24;
 // records serve variant = EXPWIN12.
 constexpr bool kRc12Auto = false;
 // The router's few-token GEMV is the dispatch form up to this many tokens.
-constexpr int64_t kRouterGemvAutoMaxM = 4;
+constexpr int64_t kRouterGemvAutoMaxM = 8;
 // From three tokens to kGemvMmaMaxM the bf16 layers take the warp-MMA
 // weight stream (measured faster than the tcgen05 cluster kernel there).
 constexpr int64_t kGemvMmaMinM = 3;
@@ -408,7 +410,7 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
     }
     if (kern == PROJ_KERNEL_GEMV_SPLITK) return PROJ_EUNSUPPORTED;
   }
-  // The router at 3 and 4 tokens (or on request, as the register form, to 16):
+  // The router at 3..8 tokens (or on request, as the register form, to 16):
   // FP32 FMAs on a weight stream, whole rows per CTA.  (Measured on GB300:
   // 4.6-6.5 us against the cluster kernel's 8.6 at 3..8 tokens; a second
   // pass of eight tokens makes it slower than the cluster kernel.)

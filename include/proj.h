@@ -130,13 +130,13 @@ enum proj_kernel {
                                  CTA (PROJ_KERNEL_GEMV: through a shared-memory ring fed
                                  by bulk copies); for the router at 3 <= m <= 16, FP32
                                  FMAs with x in passes of eight tokens (the dispatch
-                                 form at m = 3, 4) */
+                                 form at 3 <= m <= 8) */
     PROJ_KERNEL_GEMV_SPLITK = 6, /* router, m <= 32: the FP32-FMA weight-streaming GEMV with K
                                     split across a thread-block cluster (K / 1024 CTAs, one
                                     1024-column chunk of eight rows each, x staged per CTA for
                                     its chunk only), partials summed in rank order through
                                     distributed shared memory; the dispatch form at
-                                    5 <= m <= 24; PROJ_EUNSUPPORTED elsewhere */
+                                    9 <= m <= 24; PROJ_EUNSUPPORTED elsewhere */
     PROJ_KERNEL_CLUSTER = 3 /* tensor cores (dense bf16 weights; the router's bf16 planes),
                                split-K inside a thread-block cluster combined through
                                distributed shared memory, and optionally across several

@@ -230,14 +230,14 @@ def test_mma_gemv_rejections(dev):
 @pytest.mark.parametrize("m", [3, 5, 7, 8, 9, 15, 16])
 def test_router_gemv(dev, m):
     """The router's few-token FP32-FMA GEMV (whole rows per CTA, weights in
-    registers, x in passes of eight tokens): the dispatch form at m = 3, 4
+    registers, x in passes of eight tokens): the dispatch form at 3 <= m <= 8
     (forced to 16), at several CTA counts; meets the router's 1e-4 contract
     (probe rows exactly) and is bitwise reproducible."""
     for seed in (0, 1):
         h, W, _ = prepared("router", seed)
         desc = B.proj_describe(h, m)
-        assert desc.startswith("router_gemv_f32w") == (m <= 4), desc
-        assert desc.startswith("router_gemv_splitk") == (5 <= m <= 24), desc
+        assert desc.startswith("router_gemv_f32w") == (m <= 8), desc
+        assert desc.startswith("router_gemv_splitk") == (9 <= m <= 24), desc
         for kw in (dict(), dict(kernel=B.PROJ_KERNEL_GEMV_REG, grid=128),
                    dict(kernel=B.PROJ_KERNEL_GEMV_REG, grid=150)):
             a = check_case("router", seed, seed == 1, m, h=h, W=W, **kw)
@@ -258,12 +258,12 @@ def test_router_gemv(dev, m):
 def test_router_gemv_splitk(dev, m):
     """The router GEMV with K split across a cluster (one 1024-column chunk
     per CTA, eight rows per cluster, partials summed in rank order through
-    distributed shared memory; the dispatch form at 5 <= m <= 24): the 1e-4
+    distributed shared memory; the dispatch form at 9 <= m <= 24): the 1e-4
     contract, probe rows exactly, and bitwise reproducible; refused for the
     bf16 layers and above 32 tokens."""
     for seed in (0, 1):
         h, W, _ = prepared("router", seed)
-        assert B.proj_describe(h, m).startswith("router_gemv_splitk") == (5 <= m <= 24)
+        assert B.proj_describe(h, m).startswith("router_gemv_splitk") == (9 <= m <= 24)
         kw = dict(kernel=B.PROJ_KERNEL_GEMV_SPLITK)
         a = check_case("router", seed, seed == 1, m, h=h, W=W, **kw)
         b = check_case("router", seed, seed == 1, m, h=h, W=W, **kw)
