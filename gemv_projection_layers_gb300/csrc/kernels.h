@@ -228,6 +228,11 @@ cudaError_t unpack_router_planes(const uint8_t* src, int N, int K, float* W, cud
 // Streaming read (read.cu).
 cudaError_t read_floor_launch(const void* buf, int64_t bytes, uint32_t* sink, int grid, int mode,
                               cudaStream_t s);
+// bytes / 16 16-byte words from src to dst (both 16-byte aligned, device-
+// accessible: device memory or the device mapping of page-locked host memory),
+// as a programmatic dependent launch that touches memory only after the
+// dependency wait.
+cudaError_t copy16_launch(void* dst, const void* src, int64_t bytes, int sms, cudaStream_t s);
 
 // Split-K partition shared by every kernel: CTA c owns work units
 // [c U / G, (c + 1) U / G) of the linear order (tile, k-block).

@@ -89,7 +89,36 @@ __global__ void __launch_bounds__(32)
   sink[blockIdx.x] = acc;
 }
 
+// 16-byte copy, grid-stride (proj_run_host: host-mapped buffers <-> device),
+// launched as a programmatic dependent launch: it may start during the
+// previous kernel's tail, but reads and writes only after it (the source may
+// be that kernel's output, even through host memory).
+__global__ void __launch_bounds__(256) copy16_kernel(uint4* __restrict__ dst,
+                                                     const uint4* __restrict__ src, int64_t n16) {
+  griddep_launch_dependents();
+  griddep_wait();
+  for (int64_t i = blockIdx.x * 256ll + threadIdx.x; i < n16; i += gridDim.x * 256ll) dst[i] = src[i];
+}
+
 }  // namespace
+
+cudaError_t copy16_launch(void* dst, const void* src, int64_t bytes, int sms, cudaStream_t s) {
+  const int64_t n16 = bytes / 16;
+  if (n16 == 0) return cudaSuccess;
+  int64_t grid = (n16 + 255) / 256;
+  if (grid > 4ll * sms) grid = 4ll * sms;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, copy16_kernel, static_cast<uint4*>(dst),
+                            static_cast<const uint4*>(src), n16);
+}
 
 cudaError_t read_floor_launch(const void* buf, int64_t bytes, uint32_t* sink, int grid, int mode,
                               cudaStream_t s) {

@@ -216,9 +216,12 @@ int proj_run_ex(proj_handle h, const void *x, int64_t m, void *out, proj_stream 
 /*
  * End-to-end call on HOST buffers: copies x_host [m, K] bf16 to a
  * handle-owned device buffer, runs the projection, and copies the result to
- * out_host [m, proj_out_features(h, m)], all enqueued on `stream`.  The
- * copies are asynchronous for page-locked host memory; the caller
- * synchronises `stream` before reading out_host.  Same m rules as proj_run.
+ * out_host [m, proj_out_features(h, m)], all enqueued on `stream`.  For
+ * page-locked host buffers (16-byte aligned) the transfers are copy kernels
+ * reading and writing the buffers' device mapping; other host memory goes
+ * through cudaMemcpyAsync (asynchronous only for page-locked memory).  The
+ * caller synchronises `stream` before reading out_host.  Same m rules as
+ * proj_run.
  */
 int proj_run_host(proj_handle h, const void *x_host, int64_t m, void *out_host,
                   proj_stream stream);

@@ -564,17 +564,35 @@ def test_expwin12_register_gemv_planted_escapes(dev):
         B.proj_destroy(h)
 
 
-def test_run_host_matches_device_run(dev):
+@pytest.mark.parametrize("pinned", [True, False])
+def test_run_host_matches_device_run(dev, pinned):
+    """proj_run_host equals proj_run bit for bit: page-locked buffers move
+    through copy kernels on their device mapping, pageable ones through
+    cudaMemcpyAsync (then synchronous)."""
     for layer, m in (("o", 1), ("router", 16), ("unpooler", 8), ("pooler", 130)):
         spec = wl.LAYER_BY_NAME[layer]
         h, W, _ = prepared(layer, 0)
         act = wl.make_activations(layer, m, 3, False)
         dev_out = run(layer, h, to_dev_x(act.x_bits), m)
-        x_host = torch.from_numpy(act.x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
-        host_out = torch.empty(dev_out.shape, dtype=dev_out.dtype).pin_memory()
+        x_host = torch.from_numpy(act.x_bits.view(np.int16).copy()).view(torch.bfloat16)
+        host_out = torch.full(dev_out.shape, float("nan"), dtype=dev_out.dtype)
+        if pinned:
+            x_host, host_out = x_host.pin_memory(), host_out.pin_memory()
         s = torch.cuda.current_stream()
-        B.proj_run_host(h, x_host, m, host_out, s)
+        for _ in range(2):  # the second call overwrites the first call's buffers
+            B.proj_run_host(h, x_host, m, host_out, s)
         s.synchronize()
+        if pinned and layer == "o":
+            # one call's host output is the next call's host input (o's 8192
+            # outputs feed qkv_gate's K = 8192): the copy in must see it
+            hq, Wq, _ = prepared("qkv_gate", 0)
+            chained = torch.full((m, 2304), float("nan"), dtype=torch.bfloat16).pin_memory()
+            host_out.fill_(float("nan"))  # the chain must see the new output, not a stale one
+            B.proj_run_host(h, x_host, m, host_out, s)
+            B.proj_run_host(hq, host_out, m, chained, s)
+            s.synchronize()
+            ref = run("qkv_gate", hq, dev_out, m)
+            assert torch.equal(chained.view(torch.int16), ref.cpu().view(torch.int16))
         assert torch.equal(host_out.view(torch.int16) if spec.out_dtype == "bf16" else host_out,
                            dev_out.cpu().view(torch.int16) if spec.out_dtype == "bf16"
                            else dev_out.cpu())
