@@ -129,6 +129,8 @@ extern "C" int proj_gemv_static(const void* W, int w_dtype, int64_t N, int64_t K
   g.K = static_cast<int>(K);
   g.G = static_cast<int>(G);
   g.out_f32 = w_dtype == PROJ_FP32 ? 1 : 0;
+  g.esc = nullptr;  // dense weights only
+  g.e0x4 = 0;
   e = gemv_launch(w_dtype == PROJ_FP32, static_cast<int>(m), g, s);
   if (e != cudaSuccess) return record_cuda(e, "proj_gemv_static: kernel launch");
   return PROJ_OK;
