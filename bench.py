@@ -303,6 +303,17 @@ def time_router_forms(B, torch, S, flush, sink, stream, reps):
     return res
 
 
+def read_floor_us(B, torch, nbytes, flush, stream, sink2, buf):
+    """The read floor for nbytes (device time, cold L2): the fastest of the
+    streaming-read kernel's launch shapes, launched as the projections are."""
+    sms = B.proj_num_sms()
+    nb = int(nbytes) - int(nbytes) % 16
+    return min(time_device_us(
+        torch, lambda md=md, g=g: B.proj_read_floor(buf, nb, sink2, g, md | B.PROJ_READ_PDL,
+                                                    stream), lambda: flush(stream), stream)
+        for md, g in ((0, 2 * sms), (0, 3 * sms), (0, 4 * sms), (1, sms)))
+
+
 def time_compressed(B, torch, flush, stream, ms=(1, 8, 16)):
     """The decode shapes with the bf16 weights losslessly recoded to 12 bits
     (prepare flag PROJ_ENCODE_EXPWIN12): each layer's device time with
@@ -340,6 +351,17 @@ def time_compressed(B, torch, flush, stream, ms=(1, 8, 16)):
                 row["x12_kernels"][L.spec.name] = kern
             row["x12_sum_us"] = round(sum(row["x12_us"].values()), 2)
             row["auto_sum_us"] = round(sum(row["auto_us"].values()), 2)
+            # each 12-bit shape against the read floor of the bytes it reads
+            nmax = max(row["x12_weight_bytes"].values())
+            buf = torch.ones(nmax // 4 + 16, dtype=torch.int32, device="cuda")
+            sink2 = torch.zeros(4 * B.proj_num_sms() + 8, dtype=torch.int32, device="cuda")
+            row["x12_read_floor_us"] = {}
+            row["x12_floor_fraction"] = {}
+            for name, nb in row["x12_weight_bytes"].items():
+                fl = read_floor_us(B, torch, nb, flush, stream, sink2, buf)
+                row["x12_read_floor_us"][name] = round(fl, 2)
+                row["x12_floor_fraction"][name] = round(fl / row["x12_us"][name], 3)
+            del buf
             res[f"m{m}"] = row
     finally:
         for L in layers:
@@ -492,16 +514,25 @@ def device_times(B, torch, shapes, flush, sink, stream):
     return dev, floor
 
 
-def shape_targets(S, m, dev_us, floor_us, hbm_gbs, bf16_tf):
+def shape_targets(S, m, dev_us, floor_us, hbm_gbs, bf16_tf, sms=152):
     """The shape's score against its target: m <= 32 -> read floor / kernel;
-    m >= 128 -> max(weight bytes / HBM peak, FLOPs / bf16 tensor peak) / kernel."""
+    m >= 128 -> max(weight bytes / HBM peak, FLOPs / bf16 tensor peak) / kernel.
+    The FP32-FMA router at m >= 128 also gets the bound its own arithmetic
+    sets, max(weight bytes / HBM peak, FLOPs / FP32 FMA peak)."""
     if m <= 32:
         return {"kind": "read_floor", "fraction": round(floor_us / dev_us, 3)}
     bpe, ne = weight_bytes(S)
     nbytes = S.n_out * S.spec.K * bpe + ne * 4
-    t = max(nbytes / (hbm_gbs * 1e9), 2.0 * m * S.n_out * S.spec.K / (bf16_tf * 1e12)) * 1e6
-    return {"kind": "max(bytes/HBM, FLOPs/bf16 peak)", "bound_us": round(t, 3),
-            "fraction": round(t / dev_us, 3)}
+    flops = 2.0 * m * S.n_out * S.spec.K
+    t = max(nbytes / (hbm_gbs * 1e9), flops / (bf16_tf * 1e12)) * 1e6
+    res = {"kind": "max(bytes/HBM, FLOPs/bf16 peak)", "bound_us": round(t, 3),
+           "fraction": round(t / dev_us, 3)}
+    if S.spec.weight_dtype == "fp32":
+        alu = sms * 128 * 2 * FP32_PEAK_CLOCK_GHZ * 1e9
+        ta = max(nbytes / (hbm_gbs * 1e9), flops / alu) * 1e6
+        res["fp32_fma_bound_us"] = round(ta, 3)
+        res["fp32_fma_fraction"] = round(ta / dev_us, 3)
+    return res
 
 
 def weight_bytes(S) -> tuple[float, int]:
@@ -678,7 +709,8 @@ def run_ours(args):
         "per_layer_device_us": {n: round(dev_us[n], 3) for n in names},
         "read_floor_device_us": {n: round(floor_us[n], 3) for n in names},
         "shape_targets": {S.spec.name: shape_targets(S, m, dev_us[S.spec.name],
-                                                     floor_us[S.spec.name], hbm_gbs, bf16_tf)
+                                                     floor_us[S.spec.name], hbm_gbs, bf16_tf,
+                                                     B.proj_num_sms())
                           for S in lg.shapes},
         "kernels": {S.spec.name: S.desc for S in lg.shapes},
         "roofline": {
@@ -711,7 +743,8 @@ def run_ours(args):
                              "per_layer_device_us": {k: round(v, 2) for k, v in dv.items()},
                              "read_floor_device_us": {k: round(v, 2) for k, v in fl.items()},
                              "shape_targets": {S.spec.name: shape_targets(
-                                 S, mm, dv[S.spec.name], fl[S.spec.name], hbm_gbs, bf16_tf)
+                                 S, mm, dv[S.spec.name], fl[S.spec.name], hbm_gbs, bf16_tf,
+                                 B.proj_num_sms())
                                  for S in graphs[ld].shapes},
                              "kernels": {S.spec.name: S.desc for S in graphs[ld].shapes}}
             rs = graphs[ld].shapes[-1]
