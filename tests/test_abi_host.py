@@ -63,3 +63,21 @@ def test_status_strings(lib):
     assert B.status_string(99) == "unknown status"
     with pytest.raises(B.ProjError):
         B.proj_run(0, 16, 1, 16)
+
+
+def test_binding_constants_match_the_header():
+    """Every PROJ_* constant the binding defines has the header's value
+    (enumerators written `NAME = value` and `#define NAME value`)."""
+    import re
+    text = open(B.HEADER_PATH).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    declared = {}
+    for name, val in re.findall(r"\b(PROJ_[A-Z0-9_]+)\s*=\s*([0-9]+u?(?:\s*<<\s*[0-9]+)?)", text):
+        declared[name] = eval(val.replace("u", ""))
+    for name, val in re.findall(r"#define\s+(PROJ_[A-Z0-9_]+)\s+([0-9]+)", text):
+        declared[name] = int(val)
+    consts = {n: getattr(B, n) for n in dir(B) if n.startswith("PROJ_") and isinstance(getattr(B, n), int)}
+    assert len(consts) >= 30
+    for n, v in consts.items():
+        assert n in declared, n
+        assert declared[n] == v, (n, declared[n], v)
