@@ -320,7 +320,9 @@ def time_compressed(B, torch, flush, stream, ms=(1, 8, 16)):
     variant=EXPWIN12 (the router has no 12-bit form and runs as in the
     loads) beside the same handle's dispatch-table form, per token count,
     with the bytes each reads.  m <= 2: the register GEMV on the row-chunk
-    records; 3..32: the stream-K tile kernel on the tile records."""
+    records; from 3 tokens the warp-MMA GEMV on the recoded fragment copy
+    where x fits its shared memory, else the stream-K tile kernel on the tile
+    records."""
     flush_fn = lambda: flush(stream)
     layers = setup_layers(B, torch, expwin=True)
     res = {}
@@ -341,13 +343,12 @@ def time_compressed(B, torch, flush, stream, ms=(1, 8, 16)):
                     torch, lambda S=S: B.proj_run(S.h, S.x, S.m, S.out, stream), flush_fn, stream), 2)
                 kern = S.desc
                 if x12:
-                    rc = m <= 2
+                    kern = B.proj_describe_ex(S.h, m, variant=v)
+                    rc = "expwin12rc" in kern  # 12-bit records of 1024 weights + 32-B escape block
                     nw = S.n_out * L.spec.K
                     row["x12_weight_bytes"][L.spec.name] = int(
                         nw * 1.5 + (nw // 1024 * 32 if rc else
                                     L.info["expwin12_escapes"] * S.n_out / L.spec.N * 4))
-                    kern = ("gemv_reg12 (row-chunk records)" if rc
-                            else "tc_kernel expwin12 (tile records)")
                 row["x12_kernels"][L.spec.name] = kern
             row["x12_sum_us"] = round(sum(row["x12_us"].values()), 2)
             row["auto_sum_us"] = round(sum(row["auto_us"].values()), 2)

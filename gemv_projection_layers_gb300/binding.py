@@ -90,6 +90,9 @@ def load() -> ctypes.CDLL:
     lib.proj_info.argtypes = [vp, ctypes.POINTER(proj_info_t)]
     lib.proj_describe.restype = i32
     lib.proj_describe.argtypes = [vp, i64, ctypes.c_char_p, ctypes.c_size_t]
+    lib.proj_describe_ex.restype = i32
+    lib.proj_describe_ex.argtypes = [vp, i64, ctypes.POINTER(proj_run_opts), ctypes.c_char_p,
+                                     ctypes.c_size_t]
     lib.proj_unpack_weights.restype = i32
     lib.proj_unpack_weights.argtypes = [vp, i32, vp, vp]
     lib.proj_device_status.restype = i32
@@ -198,6 +201,16 @@ def proj_info(h: int) -> dict:
 def proj_describe(h: int, m: int) -> str:
     buf = ctypes.create_string_buffer(256)
     _check(load().proj_describe(h, int(m), buf, 256), "proj_describe")
+    return buf.value.decode()
+
+
+def proj_describe_ex(h: int, m: int, variant: int = PROJ_VARIANT_AUTO, grid: int = 0,
+                     reduce: int = PROJ_REDUCE_AUTO, kernel: int = PROJ_KERNEL_AUTO,
+                     groups: int = 0, tile_n: int = 0) -> str:
+    opts = proj_run_opts(int(variant), int(grid), int(reduce), int(kernel), int(groups),
+                         int(tile_n))
+    buf = ctypes.create_string_buffer(256)
+    _check(load().proj_describe_ex(h, int(m), ctypes.byref(opts), buf, 256), "proj_describe_ex")
     return buf.value.decode()
 
 

@@ -279,6 +279,8 @@ struct proj_ctx {
   size_t w_exp_bytes = 0;
   uint8_t* w_rc12 = nullptr;       // 12-bit row-chunk records (register GEMV, m <= 2)
   uint32_t* rc12_esc = nullptr;    // their escape blocks
+  uint8_t* w_frag12 = nullptr;     // the fragment-order copy as 12-bit records (warp-MMA GEMV)
+  uint32_t* frag12_esc = nullptr;  // their escape blocks
   int e0 = 0;
   int64_t n_esc = 0;
   int exp_declined = 0;
@@ -314,6 +316,8 @@ void free_ctx(proj_ctx* h) {
   cudaFree(h->w_exp);
   cudaFree(h->w_rc12);
   cudaFree(h->rc12_esc);
+  cudaFree(h->w_frag12);
+  cudaFree(h->frag12_esc);
   cudaFree(h->ws);
   cudaFree(h->counters);
   cudaFree(h->status);
@@ -437,9 +441,11 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
     int64_t G = std::min<int64_t>(nb, h->num_sms);
     if (opts && opts->grid > 0) G = std::min<int64_t>(opts->grid, nb);
     const int nt = m <= 8 ? 1 : (m <= 16 ? 2 : 4);  // tiles of 8 tokens
+    // 12-bit weights: the recoded fragment copy, wherever the form fits
+    const bool x12 = variant == PROJ_VARIANT_EXPWIN12 && h->w_frag12;
     const bool mma_ok = !pl->router && h->w_frag && m <= kGemvMmaMaxM &&
                         gemv_mma_fits(nt, static_cast<int>(h->K)) &&
-                        (variant == PROJ_VARIANT_AUTO || variant == PROJ_VARIANT_DENSE) &&
+                        (variant == PROJ_VARIANT_AUTO || variant == PROJ_VARIANT_DENSE || x12) &&
                         pl->n_out % 16 == 0 && G > 0 && (nb + G - 1) / G <= kGemvMmaMaxBlocks;
     // Measured against the cluster kernel on GB300: faster at 3..8 tokens
     // on qkv_gate (one block per CTA), o and the unpooler slice, and at 9..16
@@ -452,9 +458,10 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
                           (!opts || (opts->grid == 0 && opts->groups == 0 &&
                                      opts->tile_n == 0 && opts->reduce == PROJ_REDUCE_AUTO));
     if (kern == PROJ_KERNEL_MMA && !mma_ok) return PROJ_EUNSUPPORTED;
-    if (mma_ok && (kern == PROJ_KERNEL_MMA || mma_auto)) {
+    if (mma_ok && (kern == PROJ_KERNEL_MMA || mma_auto ||
+                   (x12 && kern == PROJ_KERNEL_AUTO && tile_n == 0))) {
       pl->gemv_mma = true;
-      pl->expwin = false;
+      pl->expwin = x12;
       pl->reduce = 0;
       pl->bn = nt;
       pl->T = pl->KB = pl->MT = 0;
@@ -785,6 +792,36 @@ proj_handle proj_prepare_ex(int layer, const void* W, int64_t N, int64_t K, int 
           h->rc12_esc = nullptr;
         }
       }
+      // The warp-MMA GEMV's fragment-order copy, recoded the same way: its
+      // stream of 16 x 16 tiles viewed as rows of 1024 elements (four tiles).
+      if (h->w_frag) {
+        const size_t chunks = static_cast<size_t>(N) * K / kRc12Chunk;
+        uint32_t* dev_over = nullptr;
+        uint32_t over = 0;
+        bool okf = (e = dmalloc(&dev_over, 4)) == cudaSuccess &&
+                   (e = dmalloc(&h->w_frag12, chunks * kRc12Bytes)) == cudaSuccess &&
+                   (e = dmalloc(&h->frag12_esc, chunks * kRc12EscWords * 4)) == cudaSuccess &&
+                   (e = cudaMemsetAsync(dev_over, 0, 4, s)) == cudaSuccess &&
+                   (e = cudaMemsetAsync(h->frag12_esc, 0, chunks * kRc12EscWords * 4, s)) ==
+                       cudaSuccess &&
+                   (e = encode_rc12(reinterpret_cast<const uint16_t*>(h->w_frag),
+                                    static_cast<int>(chunks), kRc12Chunk, h->e0, h->w_frag12,
+                                    h->frag12_esc, dev_over, s)) == cudaSuccess &&
+                   (e = cudaMemcpyAsync(&over, dev_over, 4, cudaMemcpyDeviceToHost, s)) ==
+                       cudaSuccess &&
+                   (e = cudaStreamSynchronize(s)) == cudaSuccess;
+        cudaFree(dev_over);
+        if (!okf) {
+          done();
+          return bail_cuda(e, "12-bit fragment encode");
+        }
+        if (over) {
+          cudaFree(h->w_frag12);
+          cudaFree(h->frag12_esc);
+          h->w_frag12 = nullptr;
+          h->frag12_esc = nullptr;
+        }
+      }
     }
     const int bn_max = bn_for_m(std::min<int64_t>(m_max, 256));
     h->ws_bytes = static_cast<size_t>(2 * sms) * bn_max * kTileRows * 4;
@@ -889,6 +926,9 @@ int proj_run_ex(proj_handle h, const void* x, int64_t m, void* out, proj_stream 
   if (pl.gemv_mma) {
     GemvMmaParams g;
     g.w = reinterpret_cast<const uint4*>(h->w_frag);
+    g.rec = h->w_frag12;
+    g.esc = h->frag12_esc;
+    g.e0x4 = static_cast<uint32_t>(h->e0) * 0x01010101u;
     g.x = x;
     g.out = out;
     g.status = h->status;
@@ -896,7 +936,7 @@ int proj_run_ex(proj_handle h, const void* x, int64_t m, void* out, proj_stream 
     g.n_rows = static_cast<int>(pl.n_out);
     g.K = static_cast<int>(h->K);
     g.G = pl.G;
-    e = gemv_mma_launch(pl.bn, g, s);
+    e = gemv_mma_launch(pl.bn, pl.expwin, g, s);
     if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
     return PROJ_OK;
   }
@@ -1022,9 +1062,13 @@ int proj_info(proj_handle h, proj_info_t* info) {
 }
 
 int proj_describe(proj_handle h, int64_t m, char* buf, size_t cap) {
+  return proj_describe_ex(h, m, nullptr, buf, cap);
+}
+
+int proj_describe_ex(proj_handle h, int64_t m, const proj_run_opts* opts, char* buf, size_t cap) {
   if (!h || !buf || cap == 0 || m < 1) return fail(PROJ_EINVAL);
   Plan pl;
-  int st = make_plan(h, m, nullptr, &pl);
+  int st = make_plan(h, m, opts, &pl);
   if (st != PROJ_OK) return fail(st);
   if (pl.gemv) {
     std::snprintf(buf, cap, "gemv%s_%s MT=%d G=%d n_rows=%lld", pl.gemv_reg ? "_reg" : "",
@@ -1037,8 +1081,8 @@ int proj_describe(proj_handle h, int64_t m, char* buf, size_t cap) {
     std::snprintf(buf, cap, "router_gemv_splitk_f32w CS=%d clusters=%lld n_rows=%lld", pl.G,
                   static_cast<long long>((pl.n_out + 7) / 8), static_cast<long long>(pl.n_out));
   } else if (pl.gemv_mma) {
-    std::snprintf(buf, cap, "gemv_mma16x8 tokens<=%d G=%d blocks_per_cta<=%lld n_rows=%lld",
-                  8 * pl.bn, pl.G,
+    std::snprintf(buf, cap, "gemv_mma16x8%s tokens<=%d G=%d blocks_per_cta<=%lld n_rows=%lld",
+                  pl.expwin ? "_expwin12rc" : "", 8 * pl.bn, pl.G,
                   static_cast<long long>((pl.n_out / 16 + pl.G - 1) / pl.G),
                   static_cast<long long>(pl.n_out));
   } else if (pl.cluster) {

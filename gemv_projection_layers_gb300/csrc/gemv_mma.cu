@@ -25,6 +25,15 @@
 //   the sixteen warps' tiles are summed in warp order (deterministic) and
 //   rounded to bf16.
 // Products are exact and accumulate in fp32 on the tensor cores.
+//
+// The 12-bit form reads the fragment-order copy recoded as 12-bit records
+// (four consecutive fragment tiles of a block per 1536-byte record, the
+// row-chunk record layout of kernels.h applied to the fragment stream, so
+// that a lane's decoded words are exactly its four A fragments), decodes
+// them in registers with the same byte permutes as the register GEMV,
+// restores the escapes, and runs the same MMAs in the same order: its
+// outputs are bit-identical to the dense form at the same partition.  Warps
+// then take runs of whole records (four k-tiles).
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -87,7 +96,46 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint4& a, const ui
       : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y));
 }
 
-template <int NT>
+__device__ __forceinline__ uint32_t ldg_stream_u32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+// Lane l's four fragments of a 12-bit record: low-byte words lo[0..1],
+// nibble word nb, escape word e (lane l holds word l % 8 of the block).
+__device__ __forceinline__ void decode_frag12(const uint4 (&r)[3], uint32_t e, uint32_t e0x4,
+                                              int lane, uint4 (&a)[4]) {
+  uint32_t pw[16];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t lo0 = (j & 1) ? r[j >> 1].z : r[j >> 1].x;
+    const uint32_t lo1 = (j & 1) ? r[j >> 1].w : r[j >> 1].y;
+    const uint32_t nb = j == 0 ? r[2].x : (j == 1 ? r[2].y : (j == 2 ? r[2].z : r[2].w));
+    const uint32_t hl = ((nb & 0x07070707u) + e0x4) | ((nb << 4) & 0x80808080u);
+    const uint32_t hh = (((nb >> 4) & 0x07070707u) + e0x4) | (nb & 0x80808080u);
+    pw[4 * j + 0] = __byte_perm(lo0, hl, 0x5140);
+    pw[4 * j + 1] = __byte_perm(lo0, hl, 0x7362);
+    pw[4 * j + 2] = __byte_perm(lo1, hh, 0x5140);
+    pw[4 * j + 3] = __byte_perm(lo1, hh, 0x7362);
+  }
+  const uint32_t cnt = min(__shfl_sync(0xffffffffu, e, 0), static_cast<uint32_t>(kRc12EscCap));
+  for (uint32_t k = 0; k < cnt; ++k) {  // warp-uniform
+    const uint32_t ent = __shfl_sync(0xffffffffu, e, static_cast<int>(1 + k));
+    const uint32_t pos = ent >> 8;  // 256 (tile) + 8 (lane) + element
+    if (static_cast<int>((pos >> 3) & 31) == lane) {
+      const uint32_t wi = (pos >> 8) * 4 + ((pos >> 1) & 3);
+      const uint32_t sel = (pos & 1) ? 0x4210u : 0x3240u;
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (static_cast<uint32_t>(i) == wi) pw[i] = __byte_perm(pw[i], ent, sel);
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < 4; ++t) a[t] = make_uint4(pw[4 * t], pw[4 * t + 1], pw[4 * t + 2], pw[4 * t + 3]);
+}
+
+template <int NT, bool kX12>
 __global__ void __launch_bounds__(kThreads, 1) gemv_mma_kernel(const GemvMmaParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   // [K/16 k-tiles][NT][32 lanes][2 words], fragment (kt, nt) at xfrag_off(kt NT + nt, ...)
@@ -102,17 +150,39 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_mma_kernel(const GemvMmaPara
   const int b1 = static_cast<int>((static_cast<uint32_t>(blockIdx.x) + 1u) * NB / p.G);
   const int nu = (b1 - b0) * KT;  // units (block, k-tile) of this CTA, block-major
   // Warp w takes the contiguous units [u0, u1): consecutive k-tiles (4 KB
-  // contiguous per batch), at most one block change on the way.
-  const int u0 = static_cast<int>(static_cast<uint32_t>(warp) * nu / kWarps);
-  const int u1 = static_cast<int>(static_cast<uint32_t>(warp + 1) * nu / kWarps);
+  // contiguous per batch), at most one block change on the way; whole
+  // records of four k-tiles in the 12-bit form (KT is a multiple of 16).
+  constexpr int kGran = kX12 ? 4 : 1;
+  const int u0 = kGran * static_cast<int>(static_cast<uint32_t>(warp) * (nu / kGran) / kWarps);
+  const int u1 = kGran * static_cast<int>(static_cast<uint32_t>(warp + 1) * (nu / kGran) / kWarps);
   // unit u: block b0 + u / KT, k-tile u % KT; its fragment for this lane
   const uint4* W = p.w + static_cast<size_t>(b0) * KT * 32 + lane;
 
+  // The 12-bit records of this CTA's first unit onwards: record r covers
+  // units 4 r .. 4 r + 3.
+  const uint8_t* R = kX12 ? p.rec + static_cast<size_t>(b0) * KT / 4 * kRc12Bytes : nullptr;
+  const uint32_t* E = kX12 ? p.esc + static_cast<size_t>(b0) * KT / 4 * kRc12EscWords : nullptr;
   auto load_batch = [&](int base, uint4 (&a)[kU]) {
+    if constexpr (kX12) {
+      // kU / 4 records: a[3 g .. 3 g + 2] their three 16-byte words, the
+      // escape word in a[6 + g].x
 #pragma unroll
-    for (int j = 0; j < kU; ++j) {
-      const int u = base + j;
-      if (u < u1) a[j] = ldg_stream(W + static_cast<size_t>(u) * 32);
+      for (int g = 0; g < kU / 4; ++g) {
+        const int u = base + 4 * g;
+        if (u < u1) {
+          const uint8_t* src = R + static_cast<size_t>(u / 4) * kRc12Bytes;
+          a[3 * g + 0] = ldg_stream(reinterpret_cast<const uint4*>(src) + lane);
+          a[3 * g + 1] = ldg_stream(reinterpret_cast<const uint4*>(src) + lane + 32);
+          a[3 * g + 2] = ldg_stream(reinterpret_cast<const uint4*>(src + kRc12Chunk) + lane);
+          a[6 + g].x = ldg_stream_u32(E + static_cast<size_t>(u / 4) * kRc12EscWords + (lane & 7));
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < kU; ++j) {
+        const int u = base + j;
+        if (u < u1) a[j] = ldg_stream(W + static_cast<size_t>(u) * 32);
+      }
     }
   };
   auto red_at = [&](int w, int q, int nt, int l) {
@@ -132,23 +202,40 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_mma_kernel(const GemvMmaPara
     for (int nt = 0; nt < NT; ++nt)
       st_shared_f32x4(red_at(warp, cur, nt, lane), acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
   };
+  // One unit's MMAs (block change handled first).
+  auto mma_unit = [&](int u, const uint4& frag) {
+    const int bl = u / KT;
+    const int kt = u - bl * KT;
+    if (bl != cur) {  // warp-uniform; at most once per warp
+      flush();
+      cur = bl;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const uint2 b = ld_shared_u2(sX + xfrag_off(kt * NT + nt, lane, 0));
+      mma16816(acc[nt], frag, b);
+    }
+  };
   auto compute_batch = [&](int base, const uint4 (&a)[kU]) {
+    if constexpr (kX12) {
+      // record by record: decode its four fragments, then their MMAs
 #pragma unroll
-    for (int j = 0; j < kU; ++j) {
-      const int u = base + j;
-      if (u >= u1) break;
-      const int bl = u / KT;
-      const int kt = u - bl * KT;
-      if (bl != cur) {  // warp-uniform; at most once per warp
-        flush();
-        cur = bl;
+      for (int g = 0; g < kU / 4; ++g) {
+        if (base + 4 * g >= u1) break;
+        const uint4 r[3] = {a[3 * g], a[3 * g + 1], a[3 * g + 2]};
+        uint4 d[4];
+        decode_frag12(r, a[6 + g].x, p.e0x4, lane, d);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+        for (int t = 0; t < 4; ++t) mma_unit(base + 4 * g + t, d[t]);
       }
+    } else {
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const uint2 b = ld_shared_u2(sX + xfrag_off(kt * NT + nt, lane, 0));
-        mma16816(acc[nt], a[j], b);
+      for (int j = 0; j < kU; ++j) {
+        const int u = base + j;
+        if (u >= u1) break;
+        mma_unit(u, a[j]);
       }
     }
   };
@@ -227,11 +314,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_mma_kernel(const GemvMmaPara
 
 template <int NT>
 cudaError_t set_attr() {
-  return cudaFuncSetAttribute(gemv_mma_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kSmemLimit);
+  cudaError_t e = cudaFuncSetAttribute(gemv_mma_kernel<NT, false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(gemv_mma_kernel<NT, true>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
 }
 
-template <int NT>
+template <int NT, bool kX12>
 cudaError_t launch(const GemvMmaParams& p, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.G);
@@ -243,7 +333,7 @@ cudaError_t launch(const GemvMmaParams& p, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemv_mma_kernel<NT>, p);
+  return cudaLaunchKernelEx(&cfg, gemv_mma_kernel<NT, kX12>, p);
 }
 
 }  // namespace
@@ -259,11 +349,11 @@ cudaError_t gemv_mma_init_attributes() {
   return set_attr<4>();
 }
 
-cudaError_t gemv_mma_launch(int nt, const GemvMmaParams& p, cudaStream_t s) {
+cudaError_t gemv_mma_launch(int nt, bool x12, const GemvMmaParams& p, cudaStream_t s) {
   switch (nt) {
-    case 1: return launch<1>(p, s);
-    case 2: return launch<2>(p, s);
-    case 4: return launch<4>(p, s);
+    case 1: return x12 ? launch<1, true>(p, s) : launch<1, false>(p, s);
+    case 2: return x12 ? launch<2, true>(p, s) : launch<2, false>(p, s);
+    case 4: return x12 ? launch<4, true>(p, s) : launch<4, false>(p, s);
   }
   return cudaErrorInvalidValue;
 }

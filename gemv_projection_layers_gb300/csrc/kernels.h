@@ -204,6 +204,9 @@ cudaError_t pack_frag16(const uint16_t* W, int N, int K, uint32_t* dst, cudaStre
 cudaError_t unpack_frag16(const uint32_t* src, int N, int K, uint16_t* W, cudaStream_t s);
 struct GemvMmaParams {
   const uint4* w;   // frag16 layout of the rows computed (and more)
+  const uint8_t* rec;   // 12-bit form: the frag16 stream as row-chunk records (1024 elements each)
+  const uint32_t* esc;  // 12-bit form: their escape blocks
+  uint32_t e0x4;        // 12-bit form: window base replicated into 4 bytes
   const void* x;    // bf16 [m, K]
   void* out;        // bf16 [m, n_rows]
   uint32_t* status;
@@ -217,7 +220,7 @@ constexpr int kGemvMmaMaxBlocks = 4;  // 16-row blocks per CTA, at most
 int gemv_mma_smem(int nt, int K);   // dynamic shared memory at nt tiles of 8 tokens
 bool gemv_mma_fits(int nt, int K);  // it fits one CTA's shared memory
 cudaError_t gemv_mma_init_attributes();
-cudaError_t gemv_mma_launch(int nt, const GemvMmaParams& p, cudaStream_t s);
+cudaError_t gemv_mma_launch(int nt, bool x12, const GemvMmaParams& p, cudaStream_t s);
 cudaError_t pack_router_fma_tiles(const float* W, int N, int K, uint8_t* dst, cudaStream_t s);
 cudaError_t unpack_router_fma_tiles(const uint8_t* src, int N, int K, float* W, cudaStream_t s);
 // Router W -> bf16 planes hi, mid, lo (hi + mid + lo == W) packed as the bf16

@@ -239,6 +239,11 @@ int proj_info(proj_handle h, proj_info_t *info);
  */
 int proj_describe(proj_handle h, int64_t m, char *buf, size_t cap);
 
+/* The same for proj_run_ex with these options (opts may be NULL): the kernel
+ * and launch shape that call would use, or the status it would refuse with
+ * (PROJ_EINVAL / PROJ_EUNSUPPORTED, nothing written). */
+int proj_describe_ex(proj_handle h, int64_t m, const proj_run_opts *opts, char *buf, size_t cap);
+
 /*
  * Decode the handle's packed weights back to row-major [N, K] at W_out
  * (device, same dtype as prepared).  With the 12-bit copy present it

@@ -490,6 +490,79 @@ def test_expwin12_register_gemv(dev, layer):
         assert B.proj_device_status(h) == 0
 
 
+@pytest.mark.parametrize("layer,m", [("qkv_gate", 3), ("qkv_gate", 8), ("o", 5), ("o", 16),
+                                     ("o", 32), ("pooler", 8), ("unpooler", 8),
+                                     ("unpooler", 16)])
+def test_expwin12_mma_gemv(dev, layer, m):
+    """The warp-MMA GEMV on the 12-bit recode of its fragment-order copy:
+    outputs bit-identical to the dense warp-MMA GEMV at the same partition
+    (the same MMAs on the same decoded fragments), and the oracle's contract."""
+    for seed in (0, 1):
+        h, W, Wd = prepared(layer, seed, B.PROJ_ENCODE_EXPWIN12)
+        desc = B.proj_describe_ex(h, m, variant=B.PROJ_VARIANT_EXPWIN12)
+        assert desc.startswith("gemv_mma16x8_expwin12rc"), desc
+        act = wl.make_activations(layer, m, seed + 7, outliers=True)
+        x = to_dev_x(act.x_bits)
+        a = run(layer, h, x, m, variant=B.PROJ_VARIANT_DENSE, kernel=B.PROJ_KERNEL_MMA)
+        b = run(layer, h, x, m, variant=B.PROJ_VARIANT_EXPWIN12)
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), (layer, seed, m)
+        check_case(layer, seed, True, m, h=h, W=W, variant=B.PROJ_VARIANT_EXPWIN12)
+        assert B.proj_device_status(h) == 0
+
+
+def _fragment_positions():
+    """(row, column) within a 16 x 16 tile of lane l's eight A-fragment
+    elements of mma.sync m16n8k16 (row-major A), in register order."""
+    l = np.arange(32)
+    g, c = l // 4, 2 * (l % 4)
+    rows = np.stack([g, g, g + 8, g + 8, g, g, g + 8, g + 8], 1)
+    cols = np.stack([c, c + 1, c, c + 1, c + 8, c + 9, c + 8, c + 9], 1)
+    return rows, cols
+
+
+def test_expwin12_mma_gemv_planted_escapes(dev):
+    """o's weights with up to 7 escapes in every 12-bit fragment record (four
+    16 x 16 tiles of a row block) at every tile, lane and register position:
+    the 12-bit warp-MMA GEMV equals the dense one bit for bit at 3..32 tokens;
+    8 escapes in one record make prepare decline that copy."""
+    spec = wl.LAYER_BY_NAME["o"]
+    rows, cols = _fragment_positions()
+    for cap in (7, 8):
+        W = wl.make_weights(spec, 2).copy()
+        e0 = oracle.expwin12_window(W)
+        h7 = (W >> 8) & 0x7F
+        nat = (h7 < e0) | (h7 > e0 + 7)
+        W[nat] = 0x3C00 | (W[nat] & 0x8000)
+        rng = np.random.default_rng(21 + cap)
+        KT = spec.K // 16
+        vals = np.array([0x4080, 0xC0A0, 0x0000, 0x8000, 0x4200, 0xC110], np.uint16)
+        n_rec = spec.N * spec.K // 1024
+        for r in range(n_rec):
+            n = cap if r == 0 else int(rng.integers(0, 8))
+            pos = rng.choice(1024, size=n, replace=False)  # 256 tile + 8 lane + element
+            t, ln, b = pos >> 8, (pos >> 3) & 31, pos & 7
+            rb, kb = (4 * r) // KT, (4 * r) % KT + t
+            W[rb * 16 + rows[ln, b], kb * 16 + cols[ln, b]] = vals[rng.integers(0, len(vals), n)]
+        Wd = torch.from_numpy(W.view(np.int16)).cuda().view(torch.bfloat16)
+        h = B.proj_prepare_ex(spec.index, Wd, spec.N, spec.K, B.PROJ_BF16,
+                              B.PROJ_ENCODE_EXPWIN12, 64)
+        try:
+            for m in (3, 8, 16, 32):
+                x = to_dev_x(wl.make_activations(spec, m, 5, outliers=True).x_bits)
+                try:
+                    desc = B.proj_describe_ex(h, m, variant=B.PROJ_VARIANT_EXPWIN12)
+                except B.ProjError:
+                    desc = ""
+                assert desc.startswith("gemv_mma16x8_expwin12rc") == (cap == 7), (cap, m, desc)
+                if cap == 7:
+                    a = run("o", h, x, m, variant=B.PROJ_VARIANT_DENSE, kernel=B.PROJ_KERNEL_MMA)
+                    b = run("o", h, x, m, variant=B.PROJ_VARIANT_EXPWIN12)
+                    assert torch.equal(a.view(torch.int16), b.view(torch.int16)), m
+            assert B.proj_device_status(h) == 0
+        finally:
+            B.proj_destroy(h)
+
+
 def _planted_escape_weights(n_per_chunk, seed=0):
     """o's weights with escapes planted at chosen columns of each 1024-column
     chunk (row): large values above the window, signed zeros below it, at
