@@ -78,8 +78,9 @@ enum proj_flags {
      * (proj_info reports it).  Where K is a multiple of 1024 (<= 8192) a
      * second 12-bit copy in 1024-column row chunks (same window, escapes per
      * chunk, at most 7, else that copy is declined) serves the register GEMV
-     * at m <= 2, bit-identical to its dense form; proj_describe names it
-     * "expwin12rc". */
+     * at m <= 2, and the same format over the warp-MMA GEMV's fragment-order
+     * copy serves that GEMV from 3 tokens; both are bit-identical to their
+     * dense forms, and proj_describe_ex names them "expwin12rc". */
     PROJ_ENCODE_EXPWIN12 = 1u << 0
 };
 
@@ -98,8 +99,10 @@ enum proj_variant {
     PROJ_VARIANT_AUTO = 0,      /* the dispatch table's choice */
     PROJ_VARIANT_DENSE = 1,     /* uncompressed weights */
     PROJ_VARIANT_EXPWIN12 = 2,  /* 12-bit weights (handle must hold them): the row-chunk
-                                   copy on the register GEMV at m <= 2 where it was built,
-                                   else the tile records on the tensor cores (m <= 32) */
+                                   copy on the register GEMV at m <= 2, the recoded
+                                   fragment copy on the warp-MMA GEMV where x fits its
+                                   shared memory (m <= 32), else the tile records on the
+                                   tensor cores (m <= 32); each where it was built */
     PROJ_VARIANT_PLANES3 = 3    /* router only: the fp32 weights as three bf16 planes,
                                    hi + mid + lo == W exactly, on the tensor cores */
 };
