@@ -29,6 +29,7 @@ PROJ_REDUCE_AUTO, PROJ_REDUCE_OWNER, PROJ_REDUCE_DISTRIBUTED = range(3)
  PROJ_KERNEL_MMA, PROJ_KERNEL_GEMV_SPLITK) = range(7)
 PROJ_UNPACK_FRAG16 = 16  # proj_unpack_weights: the few-token GEMV's fragment-order copy
 PROJ_UNPACK_RC12 = 32  # proj_unpack_weights: the register GEMV's 12-bit row-chunk copy
+PROJ_UNPACK_FRAG12 = 64  # proj_unpack_weights: the warp-MMA GEMV's 12-bit fragment copy
 PROJ_READ_PDL = 4  # proj_read_floor mode flag: launched as a programmatic dependent launch
 
 LAYER_INDEX = {"qkv_gate": 0, "o": 1, "pooler": 2, "unpooler": 3, "router": 4}

@@ -1108,13 +1108,14 @@ int proj_unpack_weights(proj_handle h, int variant, void* W_out, proj_stream str
   if (!h || !W_out) return fail(PROJ_EINVAL);
   if (!aligned16(W_out)) return fail(PROJ_EALIGN);
   if ((variant < PROJ_VARIANT_AUTO || variant > PROJ_VARIANT_PLANES3) &&
-      variant != PROJ_UNPACK_FRAG16 && variant != PROJ_UNPACK_RC12)
+      variant != PROJ_UNPACK_FRAG16 && variant != PROJ_UNPACK_RC12 &&
+      variant != PROJ_UNPACK_FRAG12)
     return fail(PROJ_EINVAL);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (h->layer == PROJ_ROUTER) {
     if (variant == PROJ_VARIANT_EXPWIN12 || variant == PROJ_UNPACK_FRAG16 ||
-        variant == PROJ_UNPACK_RC12)
+        variant == PROJ_UNPACK_RC12 || variant == PROJ_UNPACK_FRAG12)
       return fail(PROJ_EUNSUPPORTED);
     if (variant == PROJ_VARIANT_PLANES3)
       e = unpack_router_planes(h->w_planes, static_cast<int>(h->N), static_cast<int>(h->K),
@@ -1124,6 +1125,19 @@ int proj_unpack_weights(proj_handle h, int variant, void* W_out, proj_stream str
                                   static_cast<float*>(W_out), s);
   } else if (variant == PROJ_VARIANT_PLANES3) {
     return fail(PROJ_EUNSUPPORTED);
+  } else if (variant == PROJ_UNPACK_FRAG12) {
+    // records -> the fragment stream (a temporary) -> row-major
+    if (!h->w_frag12) return fail(PROJ_EUNSUPPORTED);
+    uint16_t* tmp = nullptr;
+    const size_t nk = static_cast<size_t>(h->N) * h->K;
+    if ((e = dmalloc(&tmp, nk * 2)) != cudaSuccess) return fail_cuda(e, "unpack temporary");
+    if ((e = decode_rc12(h->w_frag12, h->frag12_esc, static_cast<int>(nk / kRc12Chunk), kRc12Chunk,
+                         h->e0, tmp, s)) == cudaSuccess &&
+        (e = unpack_frag16(reinterpret_cast<const uint32_t*>(tmp), static_cast<int>(h->N),
+                           static_cast<int>(h->K), static_cast<uint16_t*>(W_out), s)) ==
+            cudaSuccess)
+      e = cudaStreamSynchronize(s);
+    cudaFree(tmp);
   } else if (variant == PROJ_UNPACK_RC12) {
     if (!h->w_rc12) return fail(PROJ_EUNSUPPORTED);
     e = decode_rc12(h->w_rc12, h->rc12_esc, static_cast<int>(h->N), static_cast<int>(h->K), h->e0,

@@ -257,10 +257,14 @@ int proj_describe_ex(proj_handle h, int64_t m, const proj_run_opts *opts, char *
  * fragment order (the few-token GEMV's layout; PROJ_EUNSUPPORTED where it
  * was not built), and variant = PROJ_UNPACK_RC12 the 12-bit row-chunk copy
  * (bf16 layers with PROJ_ENCODE_EXPWIN12; PROJ_EUNSUPPORTED where it was
- * not built or was declined).  Enqueued on `stream`.
+ * not built or was declined), and variant = PROJ_UNPACK_FRAG12 the 12-bit
+ * recode of the fragment-order copy (same conditions; it uses a temporary
+ * device buffer of N x K bf16 and synchronises `stream`).  Otherwise
+ * enqueued on `stream`.
  */
 #define PROJ_UNPACK_FRAG16 16
 #define PROJ_UNPACK_RC12 32
+#define PROJ_UNPACK_FRAG12 64
 int proj_unpack_weights(proj_handle h, int variant, void *W_out, proj_stream stream);
 
 /* Read and clear the handle's device status word (synchronises `stream`).

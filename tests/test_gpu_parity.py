@@ -499,6 +499,10 @@ def test_expwin12_mma_gemv(dev, layer, m):
     (the same MMAs on the same decoded fragments), and the oracle's contract."""
     for seed in (0, 1):
         h, W, Wd = prepared(layer, seed, B.PROJ_ENCODE_EXPWIN12)
+        back = torch.zeros_like(Wd)
+        B.proj_unpack_weights(h, B.PROJ_UNPACK_FRAG12, back)
+        torch.cuda.synchronize()
+        assert torch.equal(back.view(torch.int16), Wd.view(torch.int16))
         desc = B.proj_describe_ex(h, m, variant=B.PROJ_VARIANT_EXPWIN12)
         assert desc.startswith("gemv_mma16x8_expwin12rc"), desc
         act = wl.make_activations(layer, m, seed + 7, outliers=True)
@@ -554,6 +558,11 @@ def test_expwin12_mma_gemv_planted_escapes(dev):
                 except B.ProjError:
                     desc = ""
                 assert desc.startswith("gemv_mma16x8_expwin12rc") == (cap == 7), (cap, m, desc)
+                if cap == 7 and m == 3:
+                    back = torch.zeros_like(Wd)
+                    B.proj_unpack_weights(h, B.PROJ_UNPACK_FRAG12, back)
+                    torch.cuda.synchronize()
+                    assert torch.equal(back.view(torch.int16), Wd.view(torch.int16))
                 if cap == 7:
                     a = run("o", h, x, m, variant=B.PROJ_VARIANT_DENSE, kernel=B.PROJ_KERNEL_MMA)
                     b = run("o", h, x, m, variant=B.PROJ_VARIANT_EXPWIN12)
