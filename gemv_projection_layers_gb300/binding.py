@@ -26,7 +26,7 @@ PROJ_ENCODE_EXPWIN12 = 1
 PROJ_VARIANT_AUTO, PROJ_VARIANT_DENSE, PROJ_VARIANT_EXPWIN12, PROJ_VARIANT_PLANES3 = range(4)
 PROJ_REDUCE_AUTO, PROJ_REDUCE_OWNER, PROJ_REDUCE_DISTRIBUTED = range(3)
 (PROJ_KERNEL_AUTO, PROJ_KERNEL_GEMV, PROJ_KERNEL_TILE, PROJ_KERNEL_CLUSTER, PROJ_KERNEL_GEMV_REG,
- PROJ_KERNEL_MMA, PROJ_KERNEL_GEMV_SPLITK) = range(7)
+ PROJ_KERNEL_MMA, PROJ_KERNEL_GEMV_SPLITK, PROJ_KERNEL_PAIR) = range(8)
 PROJ_UNPACK_FRAG16 = 16  # proj_unpack_weights: the few-token GEMV's fragment-order copy
 PROJ_UNPACK_RC12 = 32  # proj_unpack_weights: the register GEMV's 12-bit row-chunk copy
 PROJ_UNPACK_FRAG12 = 64  # proj_unpack_weights: the warp-MMA GEMV's 12-bit fragment copy

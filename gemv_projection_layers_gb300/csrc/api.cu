@@ -104,6 +104,23 @@ bool make_x_map(CUtensorMap* map, const void* x, int64_t m, int64_t K, int box_r
   return r == CUDA_SUCCESS;
 }
 
+// The packed bf16 weight tiles (kTileBytes each, already the shared-memory
+// image of the 128-byte swizzle) as a [tiles x 128][64] bf16 matrix: a box
+// of 64 x 128 with no swizzle copies one tile verbatim.
+bool make_w_map(CUtensorMap* map, const void* w, int64_t tiles) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kTileK),
+                              static_cast<cuuint64_t>(tiles) * kTileRows};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kTileK) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileK), static_cast<cuuint32_t>(kTileRows)};
+  const cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int bn_for_m(int64_t m) {
   if (m <= 16) return 16;
   if (m <= 32) return 32;
@@ -144,6 +161,8 @@ constexpr int64_t kGemvMmaMinM = 3;
 // From three tokens on every layer goes to a cluster split-K kernel (the
 // router to its FP32-FMA one); below that, the GEMV.
 constexpr int64_t kClusterMinM = 3;
+// From this many tokens on the bf16 layers take the CTA-pair kernel.
+constexpr int64_t kPairMinM = 65;
 constexpr int64_t kRouterClusterMinM = 3;
 constexpr int kRouterMaxBN = 64;  // widest token tile of the FP32-FMA router kernel
 
@@ -237,6 +256,48 @@ ClusterShape pick_cluster(int64_t m, int T, int KB, const ClusterCost& cost, int
   }
   return best;
 }
+// Launch shape of the CTA-pair kernel: token tile bn (the smallest covering
+// m, or its half) and pairs per pair tile kg.  Scored like the cluster
+// kernels: the stream is the slower of an SM's ingest per k-block (16 KB of
+// weights plus bn / 2 x 128 B of x), the pair MMAs per k-block (4 MMAs of
+// 128 x bn x 16 per SM at ~4096 multiply-adds per clock) and the weight
+// bytes at the HBM rate; kg > 1 adds the counter barrier and the exchange of
+// the partials' remote part through L2.  Every pair is co-resident (the
+// combine's barrier needs it) and holds at least kMinKbPerCta k-blocks.
+struct PairShape {
+  int bn, kg;
+};
+int pair_bn_index(int bn) { return bn == 64 ? 0 : bn == 128 ? 1 : 2; }
+PairShape pick_pair(int64_t m, int T, int KB, int sms, const int* active, int bn_hi, int bn_lo,
+                    int kg_force) {
+  constexpr double kHbm = 6.4e12;      // bytes/s, streaming reads
+  constexpr double kIngest = 135e9;    // bytes/s per SM into shared memory
+  constexpr double kMmaClock = 1.9e9;  // SM clock under load, Hz
+  constexpr double kL2 = 100e9;        // bytes/s per SM, partials through L2
+  constexpr double kSync = 1.0e-6;     // s, the counter barrier
+  const double weight_bytes = static_cast<double>(T) * kTileRows * KB * kTileK * 2;
+  PairShape best{0, 0};
+  double best_t = 1e30;
+  for (int bn = bn_hi; bn >= bn_lo && bn >= 64; bn /= 2) {
+    const int64_t tiles = static_cast<int64_t>(T / 2) * ((m + bn - 1) / bn);
+    const int64_t cap = std::min<int64_t>(active[pair_bn_index(bn)], sms / 2);
+    for (int kg = 1; kg <= kPairMaxKG; ++kg) {
+      if (kg_force && kg != kg_force) continue;
+      if (tiles * kg > cap) continue;
+      if (kg > 1 && KB / kg < kMinKbPerCta) continue;
+      const double nk = static_cast<double>((KB + kg - 1) / kg);
+      const double t_kb = std::max((kTileBytes + 64.0 * bn) / kIngest, 2.0 * bn / kMmaClock);
+      double t = std::max(nk * t_kb, weight_bytes / kHbm);
+      if (kg > 1) t += kSync + 2.0 * (kg - 1.0) / kg * (128.0 * bn * 4) / kL2;
+      if (t < best_t * 0.999 || (t < best_t * 1.001 && kg < best.kg)) {
+        best_t = t;
+        best = PairShape{bn, kg};
+      }
+    }
+  }
+  return best;
+}
+
 int mt_for_gemv(int64_t m) { return m <= 1 ? 1 : 2; }
 
 struct Plan {
@@ -247,7 +308,8 @@ struct Plan {
   bool router_gemv_cc = false;  // router, m <= 32: the same with K split across a cluster
   bool cluster;
   bool planes = false;  // router on the tensor cores (three bf16 planes)
-  int KG = 1;  // cluster kernel: clusters per output tile
+  bool pair = false;    // CTA-pair tensor-core kernel (bf16 layers, wide token tiles)
+  int KG = 1;  // cluster kernel: clusters per output tile; pair kernel: pairs per pair tile
   bool router;
   bool expwin;
   int reduce;   // 0 owner, 1 distributed
@@ -275,6 +337,11 @@ struct proj_ctx {
   int cluster_active[5][kClusterMaxCS] = {};   // co-resident clusters: BN 16..256 x size 1..16
   int rcluster_active[5][kClusterMaxCS] = {};  // the same for the FP32-FMA router kernel
   int rgcc_active = 0;  // co-resident clusters of the split-K router GEMV
+  int pair_active[3] = {};  // co-resident CTA pairs of the pair kernel: BN 64, 128, 256
+  bool wmap_ok = false;     // tmap_w describes w_dense (bf16 layers)
+  CUtensorMap tmap_w;       // the packed weight tiles as [tiles x 128][64] bf16
+  uint32_t* pair_sync = nullptr;  // pair kernel: counter barrier words, zero at prepare
+  size_t pair_sync_words = 0;
   uint8_t* w_exp = nullptr;
   size_t w_exp_bytes = 0;
   uint8_t* w_rc12 = nullptr;       // 12-bit row-chunk records (register GEMV, m <= 2)
@@ -308,6 +375,7 @@ void free_ctx(proj_ctx* h) {
   cudaFree(h->w_dense);
   cudaFree(h->w_planes);
   cudaFree(h->cl_counters);
+  cudaFree(h->pair_sync);
   cudaFree(h->xch);
   cudaFree(h->w_frag);
   cudaFree(h->w_rows);
@@ -350,7 +418,7 @@ int64_t out_rows(const proj_ctx* h, int64_t m) {
 int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl) {
   const int variant = opts ? opts->variant : PROJ_VARIANT_AUTO;
   const int kern = opts ? opts->kernel : PROJ_KERNEL_AUTO;
-  if (kern < PROJ_KERNEL_AUTO || kern > PROJ_KERNEL_GEMV_SPLITK) return PROJ_EINVAL;
+  if (kern < PROJ_KERNEL_AUTO || kern > PROJ_KERNEL_PAIR) return PROJ_EINVAL;
   if (variant < PROJ_VARIANT_AUTO || variant > PROJ_VARIANT_PLANES3) return PROJ_EINVAL;
   const int tile_n = opts ? opts->tile_n : 0;
   if (tile_n != 0 && tile_n != 16 && tile_n != 32 && tile_n != 64 && tile_n != 128 &&
@@ -466,6 +534,40 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
       pl->bn = nt;
       pl->T = pl->KB = pl->MT = 0;
       pl->G = static_cast<int>(G);
+      return PROJ_OK;
+    }
+  }
+  // Wide token tiles on the bf16 layers: the CTA-pair kernel (M = 256 per
+  // pair, half the x bytes per weight byte of a single CTA).
+  {
+    const int T = static_cast<int>(pl->n_out / kTileRows);
+    const int KB = static_cast<int>(h->K / kTileK);
+    const bool pair_req = kern == PROJ_KERNEL_PAIR;
+    const bool pair_ok = !pl->router && h->wmap_ok && T % 2 == 0 &&
+                         (variant == PROJ_VARIANT_AUTO || variant == PROJ_VARIANT_DENSE) &&
+                         (tile_n == 0 || pair_supported(tile_n)) &&
+                         (!opts || (opts->grid == 0 && opts->reduce == PROJ_REDUCE_AUTO &&
+                                    opts->groups >= 0 && opts->groups <= kPairMaxKG));
+    const bool pair_auto = kern == PROJ_KERNEL_AUTO && m >= kPairMinM &&
+                           (!opts || (opts->grid == 0 && opts->groups == 0 &&
+                                      opts->tile_n == 0 && opts->reduce == PROJ_REDUCE_AUTO));
+    if (pair_req && !pair_ok) return PROJ_EUNSUPPORTED;
+    if (pair_ok && (pair_req || pair_auto)) {
+      const int bn_hi = tile_n ? tile_n : std::max(64, bn_for_cluster(m));
+      const int bn_lo = tile_n ? tile_n : std::max(64, bn_hi / 2);
+      const PairShape ps = pick_pair(m, T, KB, h->num_sms, h->pair_active, bn_hi, bn_lo,
+                                     opts ? opts->groups : 0);
+      if (ps.bn == 0) return PROJ_EUNSUPPORTED;  // no co-resident shape
+      pl->pair = true;
+      pl->cluster = false;
+      pl->expwin = false;
+      pl->reduce = 0;
+      pl->bn = ps.bn;
+      pl->KG = ps.kg;
+      pl->T = T;
+      pl->KB = KB;
+      pl->MT = static_cast<int>((m + ps.bn - 1) / ps.bn);
+      pl->G = (T / 2) * pl->MT * ps.kg * 2;  // CTAs
       return PROJ_OK;
     }
   }
@@ -653,6 +755,8 @@ proj_handle proj_prepare_ex(int layer, const void* W, int64_t N, int64_t K, int 
   if ((e = gemv_mma_init_attributes()) != cudaSuccess) return bail_cuda(e, "gemv attributes");
   if ((e = router_gemv_init_attributes()) != cudaSuccess) return bail_cuda(e, "gemv attributes");
   if ((e = cluster_init_attributes()) != cudaSuccess) return bail_cuda(e, "cluster attributes");
+  if ((e = pair_init_attributes()) != cudaSuccess) return bail_cuda(e, "pair attributes");
+  for (int b = 0; b < 3; ++b) h->pair_active[b] = pair_max_active(64 << b);
   {
     const int bns[5] = {16, 32, 64, 128, 256};
     for (int b = 0; b < 5; ++b)
@@ -706,6 +810,20 @@ proj_handle proj_prepare_ex(int layer, const void* W, int64_t N, int64_t K, int 
                              static_cast<int>(K), h->w_dense, s)) != cudaSuccess) {
       done();
       return bail_cuda(e, "pack bf16");
+    }
+    h->wmap_ok = make_w_map(&h->tmap_w, h->w_dense, (N / kTileRows) * (K / kTileK));
+    if (!h->wmap_ok) {
+      done();
+      return bail_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(weights)");
+    }
+    {
+      // pair kernel barrier words: [pair tiles x token tiles of 64][2 halves][2]
+      h->pair_sync_words = static_cast<size_t>(N / 256 + 1) * ((m_max + 63) / 64) * 4;
+      if ((e = dmalloc(&h->pair_sync, h->pair_sync_words * 4)) != cudaSuccess ||
+          (e = cudaMemsetAsync(h->pair_sync, 0, h->pair_sync_words * 4, s)) != cudaSuccess) {
+        done();
+        return bail_cuda(e, "cudaMalloc(pair counters)");
+      }
     }
     if (N % 16 == 0 && K % 256 == 0 && K <= 8192) {
       if ((e = dmalloc(&h->w_frag, static_cast<size_t>(N) * K * 2)) != cudaSuccess ||
@@ -940,6 +1058,26 @@ int proj_run_ex(proj_handle h, const void* x, int64_t m, void* out, proj_stream 
     if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
     return PROJ_OK;
   }
+  if (pl.pair) {
+    const CUtensorMap* xmap = get_map(h, x, m, pl.bn / 2, true);
+    if (!xmap) return fail_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(x)");
+    PairParams q;
+    q.out = out;
+    q.status = h->status;
+    q.xch = h->xch;
+    q.sync = h->pair_sync;
+    q.m = static_cast<int>(m);
+    q.n_out = static_cast<int>(pl.n_out);
+    q.KB = pl.KB;
+    q.KBx = static_cast<int>(h->K / kTileK);
+    q.MT = pl.MT;
+    q.KG = pl.KG;
+    q.out_f32 = 0;
+    q.w_evict_first = pl.MT == 1 ? 1 : 0;
+    e = pair_launch(pl.bn, h->tmap_w, *xmap, q, pl.T / 2, s);
+    if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
+    return PROJ_OK;
+  }
   const CUtensorMap* map = get_map(h, x, m, pl.bn, true);
   if (!map) return fail_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(x)");
   if (pl.cluster) {
@@ -1085,6 +1223,12 @@ int proj_describe_ex(proj_handle h, int64_t m, const proj_run_opts* opts, char* 
                   pl.expwin ? "_expwin12rc" : "", 8 * pl.bn, pl.G,
                   static_cast<long long>((pl.n_out / 16 + pl.G - 1) / pl.G),
                   static_cast<long long>(pl.n_out));
+  } else if (pl.pair) {
+    std::snprintf(buf, cap,
+                  "tc_pair BN=%d stages=%d KG=%d CTAs=%d pair_tiles=%d KB=%d MT=%d n_out=%lld "
+                  "resident_pairs=%d",
+                  pl.bn, pair_stages(pl.bn), pl.KG, pl.G, pl.T / 2, pl.KB, pl.MT,
+                  static_cast<long long>(pl.n_out), h->pair_active[pair_bn_index(pl.bn)]);
   } else if (pl.cluster) {
     const bool fma = pl.router && !pl.planes;
     std::snprintf(buf, cap,

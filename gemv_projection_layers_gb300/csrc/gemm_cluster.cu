@@ -1,6 +1,9 @@
 // gemm_cluster.cu -- tensor-core GEMM, split-K inside a thread-block
 // cluster, combined through distributed shared memory: the bf16 layers at
-// wide token tiles and the router (fp32 weights as three exact bf16 planes).
+// 3..64 tokens (the pooler from 3; the CTA-pair kernel takes wider tiles) and,
+// on request only (PROJ_VARIANT_PLANES3), the router with its fp32 weights as
+// three exact bf16 planes.  The router's dispatch form is the FP32-FMA path
+// at every token count (router_cluster.cu and the router GEMVs).
 //
 // out[i, n] = sum_k x[i, k] W[n, k]            (muse_bf16_proj guide, ch. 1, §1.1)
 //
@@ -22,11 +25,12 @@
 // n. 20 "Hopper pipelines and block clusters", distributed shared-memory
 // reduction), here on tcgen05 and for the wide token tiles.
 //
-// Router: W (fp32) was split at prepare into bf16 planes hi + mid + lo == W
-// exactly, stored as the tiles of a [N, 3K] bf16 matrix.  Weight k-block kb
-// meets x k-block kb % KBx, so x @ [hi | mid | lo].T accumulates the three
-// exact bf16 x bf16 products of every weight in fp32 -- the same sum as
-// fp32 weights, without TF32 truncation -- and the result is stored as fp32.
+// Router, opt-in form: W (fp32) was split at prepare into bf16 planes
+// hi + mid + lo == W exactly, stored as the tiles of a [N, 3K] bf16 matrix.
+// Weight k-block kb meets x k-block kb % KBx, so x @ [hi | mid | lo].T
+// accumulates the three exact bf16 x bf16 products of every weight in fp32
+// -- the same sum as fp32 weights, without TF32 truncation -- and the
+// result is stored as fp32.
 #include <cuda_bf16.h>
 
 #include "cluster_common.cuh"

@@ -114,7 +114,12 @@ extern "C" int proj_gemv_static(const void* W, int w_dtype, int64_t N, int64_t K
   if (G > N) G = N;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // The flags and the status word must start at zero; the partial row sums
-  // are always written before they are read.
+  // are always written before they are read.  The memset is also what keeps
+  // the caller's W safe: the GEMV is a programmatic dependent launch that
+  // streams its (constant) weights before its dependency wait, and W here
+  // belongs to the caller, who may have written it in the kernel just before.
+  // A memset node is an ordinary dependency, so the GEMV starts only after
+  // everything earlier on the stream has completed.
   e = cudaMemsetAsync(d->scratch + kFlagsWord, 0, (kStatusWord + 1) * sizeof(uint32_t), s);
   if (e != cudaSuccess) return record_cuda(e, "proj_gemv_static: clearing the scratch flags");
   GemvParams g;

@@ -17,11 +17,13 @@
  *
  * Accumulation is in fp32; the dense layers round the fp32 sum to bf16
  * (round-to-nearest-even) on output.  The router keeps fp32 weights and an
- * fp32 sum: at m <= 2 the bf16 input (widened exactly) meets the fp32
- * weights in fp32 fused multiply-adds; from m = 3 on the weights run on the
- * tensor cores as three bf16 planes with hi + mid + lo == W exactly, so
- * every product x * plane is exact and only the fp32 accumulation rounds
- * (no TF32 truncation anywhere).
+ * fp32 sum: at every token count the dispatch runs it on the CUDA cores, the
+ * bf16 input (widened exactly) meeting the fp32 weights in fp32 fused
+ * multiply-adds (no TF32 truncation anywhere).  On request only
+ * (PROJ_VARIANT_PLANES3) the router runs on the tensor cores instead, its
+ * weights split at prepare into three bf16 planes with hi + mid + lo == W
+ * exactly, so every product x * plane is exact and only the fp32
+ * accumulation rounds.
  *
  * Interface shape (guide ch. 1, §1.6 "Rules that shaped the code"):
  * prepare(weights) runs once, untimed, and may repack or losslessly recode
@@ -140,12 +142,20 @@ enum proj_kernel {
                                     its chunk only), partials summed in rank order through
                                     distributed shared memory; the dispatch form at
                                     9 <= m <= 24; PROJ_EUNSUPPORTED elsewhere */
-    PROJ_KERNEL_CLUSTER = 3 /* tensor cores (dense bf16 weights; the router's bf16 planes),
+    PROJ_KERNEL_CLUSTER = 3, /* tensor cores (dense bf16 weights; the router's bf16 planes),
                                split-K inside a thread-block cluster combined through
                                distributed shared memory, and optionally across several
                                clusters per tile through global memory:
                                proj_run_opts.grid = cluster size (1..16),
                                proj_run_opts.groups = clusters per tile (1..8) */
+    PROJ_KERNEL_PAIR = 7    /* bf16 layers (dense weights): tensor cores on CTA pairs
+                               (tcgen05 cta_group::2, 256 weight rows per MMA, each CTA
+                               holding half of the token tile's x), K split across
+                               proj_run_opts.groups pairs per 256-row tile (1..16; 0 = cost
+                               model) whose partials meet in L2; proj_run_opts.tile_n = 64,
+                               128 or 256 tokens per tile; grid and reduce must be 0; the
+                               dispatch form from 65 tokens; PROJ_EUNSUPPORTED where no
+                               shape keeps every pair co-resident */
 };
 
 typedef struct proj_run_opts {
@@ -155,6 +165,7 @@ typedef struct proj_run_opts {
     int reduce;     /* enum proj_reduce (tiled kernels); owner needs m <= 32 on bf16 */
     int kernel;     /* enum proj_kernel */
     int groups;     /* PROJ_KERNEL_CLUSTER: clusters sharing one output tile's K
+                       (1..16); PROJ_KERNEL_PAIR: pairs sharing one 256-row tile's K
                        (1..16); 0 = dispatch table */
     int tile_n;     /* token tile width of the tensor-core kernels (16, 32, 64, 128
                        or 256; the 12-bit kernel 16 or 32); 0 = dispatch table */
@@ -321,8 +332,10 @@ int proj_num_sms(void);
  *   m       : 0, 1 or 2 (0 returns PROJ_OK and launches nothing).
  *   out     : device, row-major [m, N], 16-byte aligned; every element written.
  *
- * The kernel is the streaming GEMV of proj_run at m <= 2 (same partition of
- * W over min(SMs, N, 256) CTAs, same summation order).  Its scratch is a
+ * The kernel is the ring-form streaming GEMV that proj_run_ex runs with
+ * kernel = PROJ_KERNEL_GEMV: with grid = min(SMs, 256) that call splits W over
+ * the same min(SMs, 256, N) CTAs and gives bit-identical results (on devices
+ * of at most 256 SMs the default grid is the same).  Its scratch is a
  * 4 KB static device array inside the library (hand-off flags, partial row
  * sums and a status word for at most 256 CTAs); each device that loads the
  * library holds it until the process exits.  Nothing is allocated by any

@@ -8,11 +8,13 @@ run time).  Its scratch is a small static array inside the library, shared
 by every call on a device.
 
 Each case calls it twice in a row on fresh inputs -- so the second call
-runs on the scratch the first one left behind -- and compares both outputs
-with proj_run's on the same inputs, under the same tolerance contract as the
-parity tests (relative L2, per-row bound, probe rows).  This file is named
-to be collected last; it passes alone in a fresh process and after the rest
-of the suite.
+runs on the scratch the first one left behind -- and checks both outputs
+against the FP64 oracle under the parity tests' contract (relative L2,
+per-row bound, probe rows equal to the scaled weight column), against
+proj_run's output under the same contract, and bit for bit against the
+ring-form GEMV of proj_run_ex, which runs the same kernel on the same
+partition of W.  This file is named to be collected last; it passes alone
+in a fresh process and after the rest of the suite.
 """
 import numpy as np
 import pytest
@@ -53,13 +55,25 @@ def test_static_scratch_gemv_matches_proj_run(layer, m):
         ref = [torch.full((m, n_out), float("nan"), dtype=odt, device="cuda") for _ in xs]
         for x, o in zip(xs, ref):
             B.proj_run(h, x, m, o)
+        # the ring-form GEMV over the same partition (min(SMs, 256, N) CTAs)
+        ring = [torch.full((m, n_out), float("nan"), dtype=odt, device="cuda") for _ in xs]
+        grid = min(B.proj_num_sms(), 256)
+        for x, o in zip(xs, ring):
+            B.proj_run_ex(h, x, m, o, kernel=B.PROJ_KERNEL_GEMV, grid=grid)
         torch.cuda.synchronize()
         assert B.proj_device_status(h) == 0
-        for call, (a, g, r) in enumerate(zip(acts, got, ref)):
+        W = wl.make_weights(spec, 3)
+        for call, (a, g, r, q) in enumerate(zip(acts, got, ref, ring)):
             g64 = g.float().cpu().numpy().astype(np.float64)
+            exact = oracle.reference(layer, a.x_bits, W)[:, :n_out]
+            res = oracle.check(layer, g64, exact, a.probe_rows)
+            assert res["ok"], (layer, m, call, "oracle", res)
             r64 = r.float().cpu().numpy().astype(np.float64)
             res = oracle.check(layer, g64, r64, a.probe_rows)
-            assert res["ok"], (layer, m, call, res)
+            assert res["ok"], (layer, m, call, "proj_run", res)
+            assert torch.equal(g.view(torch.int32 if odt == torch.float32 else torch.int16),
+                               q.view(torch.int32 if odt == torch.float32 else torch.int16)), \
+                (layer, m, call, "ring-form GEMV differs")
     finally:
         B.proj_destroy(h)
 
