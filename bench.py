@@ -456,7 +456,50 @@ def time_e2e(B, torch, shapes, flush, sink, stream, steps):
             b.record(stream)
     stream.synchronize()
     ts = [a.elapsed_time(b) * 1e3 for a, b in evs]
-    return float(np.mean(ts)), h2d, d2h
+    # host wall clock: the flush completes first; then the five calls and a
+    # stream synchronize, timed with perf_counter (the host's enqueue cost,
+    # hidden behind the flush in the event figure, is in this one)
+    walls = []
+    for _ in range(steps):
+        flush(stream)
+        stream.synchronize()
+        t0 = time.perf_counter()
+        for S, (xh, oh) in zip(shapes, hosts):
+            B.proj_run_host(S.h, xh, S.m, oh, stream)
+        stream.synchronize()
+        walls.append((time.perf_counter() - t0) * 1e6)
+    return float(np.mean(ts)), h2d, d2h, float(np.median(walls))
+
+
+def read_floor_curve(B, torch, flush, stream, hbm_gbs,
+                     sizes_mb=(8, 17, 38, 67, 256, 1024)):
+    """The read floor against the bytes read (cold L2, device time as
+    time_device_us, the fastest of four launch shapes) and a least-squares fit
+    t = t0 + bytes / BW: t0 is the fixed cost of a launch (ramp, tail, the gap
+    after the flush), BW the asymptotic streaming rate."""
+    sms = B.proj_num_sms()
+    buf = torch.ones(max(sizes_mb) * (1 << 20) // 4 + 16, dtype=torch.int32, device="cuda")
+    sink2 = torch.zeros(4 * sms + 8, dtype=torch.int32, device="cuda")
+    flush_fn = lambda: flush(stream)
+    pts = {}
+    for mb in sizes_mb:
+        nb = mb * (1 << 20)
+        pts[mb] = {}
+        for name, md, g in (("regs_2x", 0, 2 * sms), ("regs_4x", 0, 4 * sms),
+                            ("bulk_1x", 1, sms)):
+            pts[mb][name] = round(time_device_us(
+                torch, lambda md=md, g=g: B.proj_read_floor(buf, nb, sink2, g,
+                                                            md | B.PROJ_READ_PDL, stream),
+                flush_fn, stream), 3)
+    xs = np.array([mb * (1 << 20) for mb in sizes_mb], dtype=np.float64)
+    ys = np.array([min(pts[mb].values()) for mb in sizes_mb], dtype=np.float64)
+    slope, t0 = np.polyfit(xs, ys, 1)
+    del buf
+    return {"sizes_mb": list(sizes_mb), "us": {str(k): v for k, v in pts.items()},
+            "fit_fixed_us": round(float(t0), 3),
+            "fit_asymptotic_gbs": round(1e-3 / float(slope), 1),
+            "copy_gbs_measured": hbm_gbs,
+            "asymptote_over_copy": round(1e-3 / float(slope) / hbm_gbs, 3)}
 
 
 def time_device_us(torch, launch, flush_fn, stream, n=25, reps=5):
@@ -527,7 +570,7 @@ def shape_targets(S, m, dev_us, floor_us, hbm_gbs, bf16_tf, sms=152):
     flops = 2.0 * m * S.n_out * S.spec.K
     t = max(nbytes / (hbm_gbs * 1e9), flops / (bf16_tf * 1e12)) * 1e6
     res = {"kind": "max(bytes/HBM, FLOPs/bf16 peak)", "bound_us": round(t, 3),
-           "fraction": round(t / dev_us, 3)}
+           "fraction": round(t / dev_us, 3), "read_floor_fraction": round(floor_us / dev_us, 3)}
     if S.spec.weight_dtype == "fp32":
         alu = sms * 128 * 2 * FP32_PEAK_CLOCK_GHZ * 1e9
         ta = max(nbytes / (hbm_gbs * 1e9), flops / alu) * 1e6
@@ -560,6 +603,60 @@ def cpu_baseline(load_m: int, budget_s: float = 10.0, seed: int = 0):
             break
     dt = time.perf_counter() - t0
     return dt / n * 1e6, oracle.threads(), n
+
+
+def load_config(load: str, world: int) -> dict:
+    """The workload and measurement conditions of a load, printed identically
+    by both arms."""
+    m = wl.LOAD_M[load]
+    slice_rows = 1024 if m <= 8 else 8192
+    return {
+        "workload": f"{load} load: m={m} through qkv_gate 2304x8192, o 8192x1024, "
+                    f"pooler 4096x8192, unpooler {slice_rows}x4096, router fp32 256x8192",
+        "m": m,
+        "l2": "flushed before every step (a write of 2x L2, then a read of 4x L2), outside "
+              "the events",
+        "timing": "one CUDA graph per load (5 kernels); value = mean of an event pair "
+                  "around each replay (includes one graph launch); per-layer = a second "
+                  "pass with event nodes between the kernels",
+        "weights": "dense bf16; router fp32 on FP32 FMAs (its opt-in bf16x3-planes tensor-core "
+                   "form is timed per load under loads.*.router_forms_single_graph_us)",
+        "parallelism": f"replicas x{world}",
+    }
+
+
+def cpu_baseline_shapes(reps: int = 3, seed: int = 0):
+    """The oracle as it stands, per shape and per load for all six loads, on
+    all host cores and on one core.  A shape is timed on a sample of its token
+    rows (all of them up to 8 tokens, else 9: the oracle's work is linear in
+    the tokens, one FP64 dot product per output, and 9 rows keep the
+    unpooler's full width) and scaled to the load's token count; best of
+    `reps`."""
+    from oracle import oracle
+    Ws = {s.name: wl.make_weights(s, seed) for s in wl.LAYERS}
+    all_cores = oracle.threads()
+    out = {}
+    for cores in (all_cores, 1):
+        oracle.set_threads(cores)
+        per_load = {}
+        for ld, m in wl.LOADS:
+            r = m if m <= 8 else 9
+            shapes = {}
+            for s in wl.LAYERS:
+                xb = wl.make_activations(s, r, seed).x_bits
+                best = 1e30
+                for _ in range(reps):
+                    t0 = time.perf_counter()
+                    oracle.reference(s.name, xb, Ws[s.name])
+                    best = min(best, time.perf_counter() - t0)
+                shapes[s.name] = round(best * 1e6 * m / r, 1)
+            per_load[ld] = {"per_shape_us": shapes, "load_us": round(sum(shapes.values()), 1)}
+        out[f"cores_{cores}"] = per_load
+    oracle.set_threads(all_cores)
+    out["cores"] = {"all": all_cores, "one": 1}
+    out["sample"] = ("per shape: min(m, 8) or 9 token rows through the FP64 C oracle, best of "
+                     f"{reps}, scaled by m / rows")
+    return out
 
 
 def max_over_ranks(torch, value: float, device) -> float:
@@ -676,7 +773,6 @@ def run_ours(args):
                     "peak_source": f"derived: {sms} SMs x 128 FP32 lanes x 2 FLOP x "
                                    f"{FP32_PEAK_CLOCK_GHZ} GHz (maximum SM clock)",
                     "flops": flops}
-    slice_rows = lg.shapes[3].n_out
 
     result = {
         "metric": METRIC,
@@ -691,19 +787,8 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded: x ~ N(0,1) bf16, W ~ N(0,1/K))",
-        "config": {
-            "workload": f"{args.load} load: m={m} through qkv_gate 2304x8192, o 8192x1024, "
-                        f"pooler 4096x8192, unpooler {slice_rows}x4096, router fp32 256x8192",
-            "m": m,
-            "l2": f"flushed before every step ({flush.desc}), outside the events",
-            "timing": "one CUDA graph per load (5 kernels); value = mean of an event pair "
-                      "around each replay (includes one graph launch); per-layer = a second "
-                      "pass with event nodes between the kernels" + (
-                          "" if lg.inner else " (here: per-layer graphs)"),
-            "weights": "dense bf16; router fp32 on FP32 FMAs (its opt-in bf16x3-planes tensor-core "
-                       "form is timed per load under loads.*.router_forms_single_graph_us)",
-            "parallelism": f"replicas x{world}",
-        },
+        "config": load_config(args.load, world),
+        "flush": flush.desc + ("" if lg.inner else "; per-layer graphs"),
         "median_us": round(float(np.median(outer)), 3),
         "kernel_sum_us": round(float(layer_us.sum()), 3),
         "per_layer_us": {S.spec.name: round(float(u), 3) for S, u in zip(lg.shapes, layer_us)},
@@ -756,9 +841,15 @@ def run_ours(args):
         result["compressed_12bit_device_us"] = time_compressed(B, torch, flush, stream)
 
     if not args.no_extras and rank == 0:
-        e2e_us, h2d, d2h = time_e2e(B, torch, lg.shapes, flush, sink, stream, args.steps)
+        e2e_us, h2d, d2h, wall_us = time_e2e(B, torch, lg.shapes, flush, sink, stream,
+                                             args.steps)
         result["e2e"] = {"value": round(e2e_us, 3), "unit": UNIT,
-                         "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+                         "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                         "host_wall_us": round(wall_us, 3),
+                         "method": "value: event pair on the stream around the five "
+                                   "proj_run_host calls (queued behind the flush); host_wall_us: "
+                                   "perf_counter around the five calls and a stream synchronize"}
+        result["read_floor_curve"] = read_floor_curve(B, torch, flush, stream, hbm_gbs)
         wb = {}
         for S in lg.shapes:
             bpe, ne = weight_bytes(S)
@@ -775,7 +866,8 @@ def run_ours(args):
         result["cpu_baseline"] = {"value": round(cb_us, 1), "unit": UNIT, "cores": cores,
                                   "kind": "oracle",
                                   "sample": f"{n} whole {args.load} loads (FP64 C oracle, "
-                                            f"{args.cpu_seconds:.0f} s budget)"}
+                                            f"{args.cpu_seconds:.0f} s budget)",
+                                  "per_shape": cpu_baseline_shapes()}
     for L in layers:
         B.proj_destroy(L.h)
     if rank == 0:
@@ -841,7 +933,7 @@ def run_reference(args):
         "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(v / 1e3, 4), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{args.load} load: m={m}, five layers", "m": m},
+        "config": load_config(args.load, int(os.environ.get("WORLD_SIZE", "1"))),
         "cpu_baseline": {"value": round(v, 1), "unit": UNIT, "cores": oracle.threads(),
                          "kind": "oracle", "sample": f"one whole {args.load} load per step"},
         "e2e": {"value": round(v, 1), "unit": UNIT, "h2d_bytes_per_step": 0,

@@ -161,8 +161,14 @@ constexpr int64_t kGemvMmaMinM = 3;
 // From three tokens on every layer goes to a cluster split-K kernel (the
 // router to its FP32-FMA one); below that, the GEMV.
 constexpr int64_t kClusterMinM = 3;
-// From this many tokens on the bf16 layers take the CTA-pair kernel.
-constexpr int64_t kPairMinM = 65;
+// The CTA-pair kernel is the dispatch form above 128 tokens on layers whose
+// K needs no split (K <= 1024: o).  Measured on GB300 (device time, cold
+// L2): o at 256 tokens 10.5 us against the cluster kernel's 11.7; at 128
+// tokens, and on the K = 4096 / 8192 layers, where the pairs must split K
+// across clusters of up to 16 CTAs (at most 15 clusters of 8 are resident),
+// the cluster kernel was as fast or faster (pooler 128: 17.3 vs 20.3 us).
+constexpr int64_t kPairMinM = 129;
+constexpr int64_t kPairMaxK = 1024;
 constexpr int64_t kRouterClusterMinM = 3;
 constexpr int kRouterMaxBN = 64;  // widest token tile of the FP32-FMA router kernel
 
@@ -257,38 +263,42 @@ ClusterShape pick_cluster(int64_t m, int T, int KB, const ClusterCost& cost, int
   return best;
 }
 // Launch shape of the CTA-pair kernel: token tile bn (the smallest covering
-// m, or its half) and pairs per pair tile kg.  Scored like the cluster
-// kernels: the stream is the slower of an SM's ingest per k-block (16 KB of
-// weights plus bn / 2 x 128 B of x), the pair MMAs per k-block (4 MMAs of
-// 128 x bn x 16 per SM at ~4096 multiply-adds per clock) and the weight
-// bytes at the HBM rate; kg > 1 adds the counter barrier and the exchange of
-// the partials' remote part through L2.  Every pair is co-resident (the
-// combine's barrier needs it) and holds at least kMinKbPerCta k-blocks.
+// m, or its half) and pairs per pair tile kg (one cluster of 2 kg CTAs).
+// Scored like the cluster kernels: the stream is the slower of an SM's
+// ingest per k-block (16 KB of weights plus bn / 2 x 128 B of x), the pair
+// MMAs per k-block (4 MMAs of 128 x bn x 16 per SM at ~4096 multiply-adds
+// per clock) and the weight bytes at the HBM rate, times the waves of
+// clusters; kg > 1 adds a cluster barrier and the exchange of the partials'
+// remote part through L2.  At least kMinKbPerCta k-blocks per CTA.  With
+// kg > 1 the grid is at most one CTA per SM: the exchange slots are indexed
+// by CTA and sized for that.
 struct PairShape {
   int bn, kg;
 };
 int pair_bn_index(int bn) { return bn == 64 ? 0 : bn == 128 ? 1 : 2; }
-PairShape pick_pair(int64_t m, int T, int KB, int sms, const int* active, int bn_hi, int bn_lo,
-                    int kg_force) {
-  constexpr double kHbm = 6.4e12;      // bytes/s, streaming reads
+PairShape pick_pair(int64_t m, int T, int KB, int sms, const int (*active)[kPairMaxKG],
+                    int bn_hi, int bn_lo, int kg_force) {
+  constexpr double kHbm = 7.0e12;      // bytes/s, streaming reads
   constexpr double kIngest = 135e9;    // bytes/s per SM into shared memory
   constexpr double kMmaClock = 1.9e9;  // SM clock under load, Hz
   constexpr double kL2 = 100e9;        // bytes/s per SM, partials through L2
-  constexpr double kSync = 1.0e-6;     // s, the counter barrier
+  constexpr double kBarrier = 0.4e-6;  // s, a cluster barrier
   const double weight_bytes = static_cast<double>(T) * kTileRows * KB * kTileK * 2;
   PairShape best{0, 0};
   double best_t = 1e30;
   for (int bn = bn_hi; bn >= bn_lo && bn >= 64; bn /= 2) {
     const int64_t tiles = static_cast<int64_t>(T / 2) * ((m + bn - 1) / bn);
-    const int64_t cap = std::min<int64_t>(active[pair_bn_index(bn)], sms / 2);
     for (int kg = 1; kg <= kPairMaxKG; ++kg) {
       if (kg_force && kg != kg_force) continue;
-      if (tiles * kg > cap) continue;
       if (kg > 1 && KB / kg < kMinKbPerCta) continue;
+      if (kg > 1 && tiles * kg * 2 > sms) continue;
+      const int act = active[pair_bn_index(bn)][kg - 1];
+      if (act <= 0) continue;
+      const double waves = static_cast<double>((tiles + act - 1) / act);
       const double nk = static_cast<double>((KB + kg - 1) / kg);
       const double t_kb = std::max((kTileBytes + 64.0 * bn) / kIngest, 2.0 * bn / kMmaClock);
-      double t = std::max(nk * t_kb, weight_bytes / kHbm);
-      if (kg > 1) t += kSync + 2.0 * (kg - 1.0) / kg * (128.0 * bn * 4) / kL2;
+      double t = std::max(nk * t_kb * waves, weight_bytes / kHbm);
+      if (kg > 1) t += kBarrier + 2.0 * (kg - 1.0) / kg * (128.0 * bn * 4) / kL2;
       if (t < best_t * 0.999 || (t < best_t * 1.001 && kg < best.kg)) {
         best_t = t;
         best = PairShape{bn, kg};
@@ -337,11 +347,9 @@ struct proj_ctx {
   int cluster_active[5][kClusterMaxCS] = {};   // co-resident clusters: BN 16..256 x size 1..16
   int rcluster_active[5][kClusterMaxCS] = {};  // the same for the FP32-FMA router kernel
   int rgcc_active = 0;  // co-resident clusters of the split-K router GEMV
-  int pair_active[3] = {};  // co-resident CTA pairs of the pair kernel: BN 64, 128, 256
+  int pair_active[3][kPairMaxKG] = {};  // co-resident pair-kernel clusters: BN 64..256 x kg
   bool wmap_ok = false;     // tmap_w describes w_dense (bf16 layers)
   CUtensorMap tmap_w;       // the packed weight tiles as [tiles x 128][64] bf16
-  uint32_t* pair_sync = nullptr;  // pair kernel: counter barrier words, zero at prepare
-  size_t pair_sync_words = 0;
   uint8_t* w_exp = nullptr;
   size_t w_exp_bytes = 0;
   uint8_t* w_rc12 = nullptr;       // 12-bit row-chunk records (register GEMV, m <= 2)
@@ -375,7 +383,6 @@ void free_ctx(proj_ctx* h) {
   cudaFree(h->w_dense);
   cudaFree(h->w_planes);
   cudaFree(h->cl_counters);
-  cudaFree(h->pair_sync);
   cudaFree(h->xch);
   cudaFree(h->w_frag);
   cudaFree(h->w_rows);
@@ -548,7 +555,7 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
                          (tile_n == 0 || pair_supported(tile_n)) &&
                          (!opts || (opts->grid == 0 && opts->reduce == PROJ_REDUCE_AUTO &&
                                     opts->groups >= 0 && opts->groups <= kPairMaxKG));
-    const bool pair_auto = kern == PROJ_KERNEL_AUTO && m >= kPairMinM &&
+    const bool pair_auto = kern == PROJ_KERNEL_AUTO && m >= kPairMinM && h->K <= kPairMaxK &&
                            (!opts || (opts->grid == 0 && opts->groups == 0 &&
                                       opts->tile_n == 0 && opts->reduce == PROJ_REDUCE_AUTO));
     if (pair_req && !pair_ok) return PROJ_EUNSUPPORTED;
@@ -557,7 +564,7 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
       const int bn_lo = tile_n ? tile_n : std::max(64, bn_hi / 2);
       const PairShape ps = pick_pair(m, T, KB, h->num_sms, h->pair_active, bn_hi, bn_lo,
                                      opts ? opts->groups : 0);
-      if (ps.bn == 0) return PROJ_EUNSUPPORTED;  // no co-resident shape
+      if (ps.bn == 0) return PROJ_EUNSUPPORTED;  // no shape (k-blocks per CTA, residency)
       pl->pair = true;
       pl->cluster = false;
       pl->expwin = false;
@@ -756,7 +763,8 @@ proj_handle proj_prepare_ex(int layer, const void* W, int64_t N, int64_t K, int 
   if ((e = router_gemv_init_attributes()) != cudaSuccess) return bail_cuda(e, "gemv attributes");
   if ((e = cluster_init_attributes()) != cudaSuccess) return bail_cuda(e, "cluster attributes");
   if ((e = pair_init_attributes()) != cudaSuccess) return bail_cuda(e, "pair attributes");
-  for (int b = 0; b < 3; ++b) h->pair_active[b] = pair_max_active(64 << b);
+  for (int b = 0; b < 3; ++b)
+    for (int kg = 1; kg <= kPairMaxKG; ++kg) h->pair_active[b][kg - 1] = pair_max_active(64 << b, kg);
   {
     const int bns[5] = {16, 32, 64, 128, 256};
     for (int b = 0; b < 5; ++b)
@@ -815,15 +823,6 @@ proj_handle proj_prepare_ex(int layer, const void* W, int64_t N, int64_t K, int 
     if (!h->wmap_ok) {
       done();
       return bail_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(weights)");
-    }
-    {
-      // pair kernel barrier words: [pair tiles x token tiles of 64][2 halves][2]
-      h->pair_sync_words = static_cast<size_t>(N / 256 + 1) * ((m_max + 63) / 64) * 4;
-      if ((e = dmalloc(&h->pair_sync, h->pair_sync_words * 4)) != cudaSuccess ||
-          (e = cudaMemsetAsync(h->pair_sync, 0, h->pair_sync_words * 4, s)) != cudaSuccess) {
-        done();
-        return bail_cuda(e, "cudaMalloc(pair counters)");
-      }
     }
     if (N % 16 == 0 && K % 256 == 0 && K <= 8192) {
       if ((e = dmalloc(&h->w_frag, static_cast<size_t>(N) * K * 2)) != cudaSuccess ||
@@ -1065,7 +1064,6 @@ int proj_run_ex(proj_handle h, const void* x, int64_t m, void* out, proj_stream 
     q.out = out;
     q.status = h->status;
     q.xch = h->xch;
-    q.sync = h->pair_sync;
     q.m = static_cast<int>(m);
     q.n_out = static_cast<int>(pl.n_out);
     q.KB = pl.KB;
@@ -1074,6 +1072,8 @@ int proj_run_ex(proj_handle h, const void* x, int64_t m, void* out, proj_stream 
     q.KG = pl.KG;
     q.out_f32 = 0;
     q.w_evict_first = pl.MT == 1 ? 1 : 0;
+    // the exchange slots hold one [256][128] fp32 partial per SM
+    if (pl.KG > 1 && pl.G > h->num_sms) return fail(PROJ_EUNSUPPORTED);
     e = pair_launch(pl.bn, h->tmap_w, *xmap, q, pl.T / 2, s);
     if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
     return PROJ_OK;
@@ -1225,10 +1225,11 @@ int proj_describe_ex(proj_handle h, int64_t m, const proj_run_opts* opts, char* 
                   static_cast<long long>(pl.n_out));
   } else if (pl.pair) {
     std::snprintf(buf, cap,
-                  "tc_pair BN=%d stages=%d KG=%d CTAs=%d pair_tiles=%d KB=%d MT=%d n_out=%lld "
-                  "resident_pairs=%d",
-                  pl.bn, pair_stages(pl.bn), pl.KG, pl.G, pl.T / 2, pl.KB, pl.MT,
-                  static_cast<long long>(pl.n_out), h->pair_active[pair_bn_index(pl.bn)]);
+                  "tc_pair BN=%d stages=%d KG=%d cluster=%d CTAs=%d pair_tiles=%d KB=%d MT=%d "
+                  "n_out=%lld resident_clusters=%d",
+                  pl.bn, pair_stages(pl.bn), pl.KG, 2 * pl.KG, pl.G, pl.T / 2, pl.KB, pl.MT,
+                  static_cast<long long>(pl.n_out),
+                  h->pair_active[pair_bn_index(pl.bn)][pl.KG - 1]);
   } else if (pl.cluster) {
     const bool fma = pl.router && !pl.planes;
     std::snprintf(buf, cap,

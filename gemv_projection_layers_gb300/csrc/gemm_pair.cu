@@ -15,20 +15,19 @@
 //
 // Work split: a pair tile is 256 weight rows x BN tokens; KG pairs split its
 // K into equal k-block ranges.  Each CTA ends with a [BN][128] fp32 partial
-// in tensor memory.  With KG > 1 the KG CTAs that hold the same 128 rows
-// combine through L2: each stores the tokens it does not own to its
-// exchange slot (and stages its own in shared memory), arrives on a counter
-// barrier, and after the last arrival sums its 1/KG of the tokens over the
-// KG partials in split order (deterministic), rounds to bf16 (the router's
-// planes keep fp32) and stores.  Every CTA of the grid is resident at once
-// (the dispatch keeps the grid within the co-resident pair count), so the
-// barrier cannot wait on a CTA that has not started; all waits are bounded.
+// in tensor memory, staged to shared memory after the last MMA.  The KG
+// pairs of a pair tile form one thread-block cluster of 2 KG CTAs (pair i =
+// ranks 2i, 2i + 1).  With KG > 1 the KG CTAs that hold the same 128 rows
+// combine through L2: each stores the tokens it does not own to its exchange
+// slot, a cluster barrier orders those stores, and each sums its 1/KG of the
+// tokens over the KG partials in split order (deterministic), rounds to bf16
+// and stores.  Nothing waits on another cluster.
 //
 // Pipeline per CTA: warp 0 copies (one 2-D TMA of a prepacked 16 KB weight
 // tile and one of the CTA's x rows per k-block, both counted on the even
 // CTA's "full" barrier), warp 1 of the even CTA issues the pair MMAs and
 // commits each stage to both CTAs' "empty" barriers, warps 4..7 drain the
-// accumulator; all eight warps combine.
+// accumulator to shared memory; all eight warps store and combine.
 #include <cuda_bf16.h>
 
 #include "cluster_common.cuh"
@@ -97,10 +96,11 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t h = cluster_rank();  // 0: the even CTA, which issues the MMAs
-  const int pair = static_cast<int>(blockIdx.x) >> 1;
-  const int g = pair % p.KG;          // K split of this pair
-  const int tm = pair / p.KG;         // (pair tile, token tile)
+  const uint32_t rank = cluster_rank();
+  const uint32_t h = rank & 1u;       // 0: the even CTA of the pair, which issues the MMAs
+  const uint32_t lead = rank & ~1u;   // that CTA's rank
+  const int g = static_cast<int>(rank >> 1);                 // K split of this pair
+  const int tm = static_cast<int>(blockIdx.x) / (2 * p.KG);  // (pair tile, token tile): the cluster
   const int mt = tm % p.MT;
   const int tp = tm / p.MT;
   const int t = 2 * tp + static_cast<int>(h);  // this CTA's 128-row weight tile
@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint32_t full_lead = map_to_rank(full0, 0);  // the even CTA's barriers
+      const uint32_t full_lead = map_to_rank(full0, lead);  // the even CTA's barriers
       const uint64_t pol_w = p.w_evict_first ? policy_evict_first() : policy_evict_normal();
       const uint64_t pol_x = policy_evict_normal();
       const int pre = min(nk, S);
@@ -178,6 +178,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
     if (h == 0 && lane == 0) {
+      const uint16_t pair_mask = static_cast<uint16_t>(0x3u << lead);
       for (int j = 0; j < nk; ++j) {
         const int s = j % S;
         if (!mbar_wait(full0 + 8 * s, static_cast<uint32_t>((j / S) & 1), p.status,
@@ -190,110 +191,95 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         for (int k = 0; k < kTileK / 16; ++k)
           tc_mma_f16_pair(tmem, smem_desc_sw128(a + 32 * k), smem_desc_sw128(b + 32 * k),
                           C::kIdesc, (j > 0 || k > 0) ? 1u : 0u);
-        tc_commit_pair(empty0 + 8 * s, 0x3);
+        tc_commit_pair(empty0 + 8 * s, pair_mask);
       }
       // arrives once every MMA issued above has completed (also after an
       // aborted loop)
-      tc_commit_pair(accf, 0x3);
+      tc_commit_pair(accf, pair_mask);
     }
   } else if (warp >= 4) {
-    // ------------------------------------------ drain: accumulator -> out
+    // ---------------------------- drain: accumulator -> shared-memory staging
+    // [BN tokens][128 rows] fp32 at red_base (the ring, free once every MMA
+    // has completed): for each token the warp's 32 lanes write 128
+    // consecutive bytes.  (Storing straight from these registers to global
+    // memory -- 64-128 bytes per warp instruction, one token at a time --
+    // measured 5-12 us for a tile; the coalesced vector stores below take a
+    // fraction of that.)
     const int q = warp & 3;  // the tensor-memory lane quarter this warp may read
     const int r = q * 32 + lane;
-    const int row = t * kTileRows + r;
     if (mbar_wait_sleep(accf, 0, p.status, kStatusTimeoutEpilogue)) {
       tc_fence_after();
       const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
-      griddep_wait();  // before the first global write
-      const int jo0 = g * BN / p.KG;
-      const int jo1 = (g + 1) * BN / p.KG;
-      float* slot = p.xch + static_cast<size_t>(blockIdx.x) * BN * kTileRows;
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        if (c0 >= mv) break;
+      for (int c0 = 0; c0 < mv; c0 += 32) {
         float v[16], u[16];
         tmem_ld16(taddr + c0, v);
         tmem_ld16(taddr + c0 + 16, u);
         tmem_ld_wait();
-        auto put = [&](int j, float val) {
-          if (j >= mv) return;
-          if (p.KG == 1) {
-            const size_t o = static_cast<size_t>(mt * BN + j) * p.n_out + row;
-            if (p.out_f32)
-              static_cast<float*>(p.out)[o] = val;
-            else
-              static_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(val);
-          } else if (j >= jo0 && j < jo1) {
-            st_shared_f32(red_base + static_cast<uint32_t>(((j - jo0) * kTileRows + r) * 4), val);
-          } else {
-            slot[j * kTileRows + r] = val;  // 128 contiguous bytes per warp store
-          }
-        };
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) put(c0 + jj, v[jj]);
+        for (int jj = 0; jj < 16; ++jj)
+          st_shared_f32(red_base + static_cast<uint32_t>(((c0 + jj) * kTileRows + r) * 4), v[jj]);
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) put(c0 + 16 + jj, u[jj]);
+        for (int jj = 0; jj < 16; ++jj)
+          st_shared_f32(red_base + static_cast<uint32_t>(((c0 + 16 + jj) * kTileRows + r) * 4),
+                        u[jj]);
       }
     }
   }
   tc_fence_before();
   __syncwarp();
-  // Both CTAs are done with their tensor memory (and the pair's MMAs with
-  // both CTAs' shared memory): free the columns.
+  __syncthreads();  // the staging is complete; every tensor-memory read is done
+  griddep_wait();   // before the first global write
+  const int tid = static_cast<int>(threadIdx.x);
+  // An item is 4 consecutive rows of one token (float4 of the staging).
+  auto staged = [&](int j, int r4) {
+    return ld_shared_v4(red_base + static_cast<uint32_t>((j * kTileRows + r4) * 4));
+  };
+  // CTA g owns tokens [g BN / KG, (g + 1) BN / KG).
+  const int jo0 = g * BN / p.KG;
+  const int jo1 = (g + 1) * BN / p.KG;
+  if (p.KG == 1) {
+    for (int idx = tid; idx < mv * 32; idx += kPairThreads) {
+      const int j = idx >> 5, r4 = (idx & 31) * 4;
+      store_out4(p, mt * BN + j, t * kTileRows + r4, staged(j, r4));
+    }
+  } else {
+    // The valid tokens this CTA does not own go to its exchange slot
+    // ([BN][128] fp32, 512 contiguous bytes per token).
+    float* slot = p.xch + static_cast<size_t>(blockIdx.x) * BN * kTileRows;
+    const int lo = min(jo0, mv);  // valid tokens before the owned range
+    const int n_other = lo + max(mv - jo1, 0);
+    for (int idx = tid; idx < n_other * 32; idx += kPairThreads) {
+      const int jj = idx >> 5, r4 = (idx & 31) * 4;
+      const int j = jj < lo ? jj : jj - lo + jo1;
+      *reinterpret_cast<float4*>(slot + j * kTileRows + r4) = staged(j, r4);
+    }
+  }
+  // Every CTA of the cluster is done with its tensor memory (and the pair's
+  // MMAs with both CTAs' shared memory); with KG > 1 the barrier's release /
+  // acquire also orders every CTA's exchange stores before the loads below.
   cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc_pair(tmem, C::kTmemCols);
   }
-  if (p.KG == 1) return;
+  if (p.KG == 1 || jo0 >= mv) return;
 
-  // ------------------------------------------------ combine across KG pairs
-  griddep_wait();
-  __shared__ uint32_t s_ok;
-  if (threadIdx.x == 0) {
-    // Counter barrier of the KG CTAs holding these 128 rows: the last to
-    // arrive resets the count and advances the generation word that the
-    // others wait on.  (The barrier's release/acquire, together with the CTA
-    // barriers around it, orders every CTA's exchange stores before the
-    // loads below.)
-    uint32_t* cnt = p.sync + 2 * (tm * 2 + static_cast<int>(h));
-    uint32_t* gen = cnt + 1;
-    const uint32_t g0 = ld_acquire_gpu_u32(gen);
-    const uint32_t old = atom_add_acq_rel_gpu(cnt, 1u);
-    uint32_t ok = 1;
-    if (old == static_cast<uint32_t>(p.KG - 1)) {
-      *cnt = 0u;
-      st_release_gpu_u32(gen, g0 + 1u);
-    } else {
-      const uint64_t t0 = globaltimer_ns();
-      while (ld_acquire_gpu_u32(gen) == g0) {
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-          atomicOr(p.status, kStatusTimeoutEpilogue);
-          ok = 0;
-          break;
-        }
-        __nanosleep(64);
-      }
-    }
-    s_ok = ok;
-  }
-  __syncthreads();
-  if (!s_ok) return;
-  // Sum tokens [jo0, jo1) over the KG partials in split order; an item is 4
-  // consecutive rows of one token (float4).
-  const int jo0 = g * BN / p.KG;
-  const int jo1 = min((g + 1) * BN / p.KG, mv);
-  const int n_items = max(jo1 - jo0, 0) * 32;
+  // ------------------------------------- combine across the cluster's pairs
+  // Sum the owned tokens over the KG partials of these 128 rows (cluster
+  // ranks 2 g' + h) in split order.  No CTA reads another's shared memory,
+  // so none has to wait for the others before leaving.
+  const int n_items = (min(jo1, mv) - jo0) * 32;
   const float* slot0 = p.xch + static_cast<size_t>(tm) * p.KG * 2 * BN * kTileRows;
   constexpr int kItems = 4;
-  for (int base = threadIdx.x; base < n_items; base += kItems * kPairThreads) {
+  for (int base = tid; base < n_items; base += kItems * kPairThreads) {
     float4 acc[kItems];
     int jl[kItems], r4[kItems];
 #pragma unroll
     for (int u = 0; u < kItems; ++u) {
       acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
       const int idx = min(base + u * kPairThreads, n_items - 1);
-      jl[u] = idx >> 5;
+      jl[u] = jo0 + (idx >> 5);
       r4[u] = (idx & 31) * 4;
     }
     for (int g0 = 0; g0 < p.KG; g0 += 4) {
@@ -304,11 +290,11 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         for (int gg = 0; gg < 4; ++gg) {
           const int src = g0 + gg;
           if (src == g)
-            v[u][gg] = ld_shared_v4(red_base + static_cast<uint32_t>((jl[u] * kTileRows + r4[u]) * 4));
+            v[u][gg] = staged(jl[u], r4[u]);
           else if (src < p.KG)
             v[u][gg] = ld_global_cg_v4(slot0 +
                                        (static_cast<size_t>(src) * 2 + h) * BN * kTileRows +
-                                       static_cast<size_t>(jo0 + jl[u]) * kTileRows + r4[u]);
+                                       static_cast<size_t>(jl[u]) * kTileRows + r4[u]);
         }
 #pragma unroll
       for (int u = 0; u < kItems; ++u)
@@ -325,7 +311,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     for (int u = 0; u < kItems; ++u) {
       const int idx = base + u * kPairThreads;
       if (idx >= n_items) break;
-      store_out4(p, mt * BN + jo0 + jl[u], t * kTileRows + r4[u], acc[u]);
+      store_out4(p, mt * BN + jl[u], t * kTileRows + r4[u], acc[u]);
     }
   }
 }
@@ -335,18 +321,20 @@ cudaError_t set_attr() {
   cudaError_t e = cudaFuncSetAttribute(tc_pair_kernel<BN>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(PCfg<BN>::kSmem));
-  return e;
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(tc_pair_kernel<BN>, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                              1);
 }
 
 template <int BN>
-cudaLaunchConfig_t make_cfg(int ctas, cudaStream_t s, cudaLaunchAttribute* attr) {
+cudaLaunchConfig_t make_cfg(int ctas, int cluster, cudaStream_t s, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(ctas));
   cfg.blockDim = dim3(kPairThreads);
   cfg.dynamicSmemBytes = PCfg<BN>::kSmem;
   cfg.stream = s;
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
@@ -358,7 +346,7 @@ template <int BN>
 cudaError_t launch(const CUtensorMap& tw, const CUtensorMap& tx, const PairParams& p,
                    int pair_tiles, cudaStream_t s) {
   cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = make_cfg<BN>(pair_tiles * p.MT * p.KG * 2, s, attr);
+  cudaLaunchConfig_t cfg = make_cfg<BN>(pair_tiles * p.MT * p.KG * 2, 2 * p.KG, s, attr);
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.numAttrs = 2;
@@ -366,9 +354,9 @@ cudaError_t launch(const CUtensorMap& tw, const CUtensorMap& tx, const PairParam
 }
 
 template <int BN>
-int max_active() {
+int max_active(int kg) {
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = make_cfg<BN>(2, nullptr, attr);
+  cudaLaunchConfig_t cfg = make_cfg<BN>(2 * kg, 2 * kg, nullptr, attr);
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, tc_pair_kernel<BN>, &cfg) != cudaSuccess) {
     cudaGetLastError();
@@ -388,11 +376,11 @@ cudaError_t pair_init_attributes() {
   return set_attr<256>();
 }
 
-int pair_max_active(int BN) {
+int pair_max_active(int BN, int kg) {
   switch (BN) {
-    case 64: return max_active<64>();
-    case 128: return max_active<128>();
-    case 256: return max_active<256>();
+    case 64: return max_active<64>(kg);
+    case 128: return max_active<128>(kg);
+    case 256: return max_active<256>(kg);
   }
   return 0;
 }

@@ -155,29 +155,28 @@ cudaError_t cluster_launch(int BN, const CUtensorMap& tmap_x, const ClusterParam
 
 // CTA-pair tensor-core path (tcgen05 cta_group::2): BN in {64, 128, 256}.
 // A pair tile is 256 weight rows (packed tiles 2 tp and 2 tp + 1) x BN
-// tokens; the two CTAs of a cluster of 2 each hold one 128-row tile and half
-// of the tokens' x.  KG pairs split a pair tile's K; their fp32 partials meet
-// in L2 (exchange slots) after a counter barrier among the KG CTAs holding
-// the same 128 rows, and each sums 1/KG of the tokens in split order.
+// tokens; the two CTAs of a pair each hold one 128-row tile and half of the
+// tokens' x.  KG pairs split a pair tile's K and form one cluster of 2 KG
+// CTAs; their fp32 partials meet in L2 (exchange slots) behind a cluster
+// barrier, and each CTA sums 1/KG of the tokens in split order.
 struct PairParams {
   void* out;            // [m, n_out], bf16 or fp32 (out_f32)
   uint32_t* status;
-  float* xch;           // KG > 1: [CTA][BN][128] fp32 exchange slots
-  uint32_t* sync;       // KG > 1: [pair tiles x MT][2 halves][2 words], zero at prepare
+  float* xch;           // KG > 1: [CTA][BN][128] fp32 exchange slots (grid <= SMs)
   int m;
   int n_out;
   int KB;               // weight k-blocks per tile row
   int KBx;              // x k-blocks (K / 64); weight k-block kb meets x k-block kb % KBx
   int MT;               // token tiles: ceil(m / BN)
-  int KG;               // pairs per pair tile (K split)
+  int KG;               // pairs per pair tile (K split), 1..kPairMaxKG
   int out_f32;
   int w_evict_first;    // the weights are read once (MT == 1): evict them first from L2
 };
-constexpr int kPairMaxKG = 16;
+constexpr int kPairMaxKG = 8;  // clusters of at most 16 CTAs
 constexpr int kPairThreads = 256;
 bool pair_supported(int BN);
 cudaError_t pair_init_attributes();
-int pair_max_active(int BN);  // co-resident clusters of 2 (occupancy query)
+int pair_max_active(int BN, int kg);  // co-resident clusters of 2 kg CTAs (occupancy query)
 int pair_stages(int BN);
 // tmap_w: the packed weight tiles viewed as a [tiles x 128 rows][64] bf16
 // matrix (box 64 x 128, no swizzle: each tile is already the shared-memory

@@ -273,15 +273,16 @@ __device__ __forceinline__ uint64_t policy_evict_normal() {
   return p;
 }
 
-__device__ __forceinline__ uint32_t ld_acquire_gpu_u32(const uint32_t* p) {
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 
-__device__ __forceinline__ void st_release_gpu_u32(uint32_t* p, uint32_t v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+__device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+
 
 // 32 lanes x 32 bits, 16 consecutive columns: thread t of the warp gets
 // lane (base lane + t), columns [col, col + 16).

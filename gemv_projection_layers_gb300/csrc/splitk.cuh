@@ -32,16 +32,6 @@ namespace proj {
 
 enum : uint32_t { kStatusTimeoutSplitK = 1u << 7 };
 
-__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
 // Spin (bounded) until *p >= target.
 __device__ __forceinline__ bool spin_until_ge(const uint32_t* p, uint32_t target,
                                               uint32_t* status) {

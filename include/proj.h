@@ -151,11 +151,13 @@ enum proj_kernel {
     PROJ_KERNEL_PAIR = 7    /* bf16 layers (dense weights): tensor cores on CTA pairs
                                (tcgen05 cta_group::2, 256 weight rows per MMA, each CTA
                                holding half of the token tile's x), K split across
-                               proj_run_opts.groups pairs per 256-row tile (1..16; 0 = cost
-                               model) whose partials meet in L2; proj_run_opts.tile_n = 64,
-                               128 or 256 tokens per tile; grid and reduce must be 0; the
-                               dispatch form from 65 tokens; PROJ_EUNSUPPORTED where no
-                               shape keeps every pair co-resident */
+                               proj_run_opts.groups pairs per 256-row tile (1..8; 0 = cost
+                               model), one thread-block cluster of 2 x groups CTAs whose
+                               partials meet in L2; proj_run_opts.tile_n = 64, 128 or 256
+                               tokens per tile; grid and reduce must be 0; groups > 1
+                               needs the grid within one CTA per SM (the partials'
+                               exchange is sized for that), else PROJ_EUNSUPPORTED; the
+                               dispatch form on o above 128 tokens */
 };
 
 typedef struct proj_run_opts {
@@ -166,7 +168,7 @@ typedef struct proj_run_opts {
     int kernel;     /* enum proj_kernel */
     int groups;     /* PROJ_KERNEL_CLUSTER: clusters sharing one output tile's K
                        (1..16); PROJ_KERNEL_PAIR: pairs sharing one 256-row tile's K
-                       (1..16); 0 = dispatch table */
+                       (1..8); 0 = dispatch table */
     int tile_n;     /* token tile width of the tensor-core kernels (16, 32, 64, 128
                        or 256; the 12-bit kernel 16 or 32); 0 = dispatch table */
 } proj_run_opts;

@@ -5,8 +5,9 @@ relative L2 per output <= 1e-2 (router 1e-4), probe rows within 1e-3 (and,
 stronger, exactly equal to the scaled weight column), no row over 5x the
 bound, no NaN/Inf.  Shapes: the five layers at the six scored token counts
 and the awkward ones (§1.2), two weight seeds, normal and outlier inputs.
-Small m is compared in full; large m on sampled token rows (all of their
-outputs), which always include the probe rows.
+Small m and the scored 128 and 256 tokens are compared in full; the other
+large m on sampled token rows (all of their outputs), which always include
+the probe rows.
 """
 import numpy as np
 import pytest
@@ -20,6 +21,7 @@ from oracle import oracle
 pytestmark = pytest.mark.gpu
 
 FULL_ORACLE_MAX_M = 33
+FULL_ORACLE_M = (128, 256)  # the scored wide token counts: every output checked
 SAMPLED_ROWS = 20
 M_SCORED = (1, 8, 16, 32, 128, 256)
 M_AWKWARD = (2, 3, 5, 7, 9, 33, 130, 512, 1000)
@@ -82,7 +84,7 @@ def check_case(layer, seed, outliers, m, h=None, W=None, **kw):
         h, W, _ = prepared(layer, seed)
     act = wl.make_activations(layer, m, seed, outliers)
     out = out_f64(run(layer, h, to_dev_x(act.x_bits), m, **kw))
-    if m <= FULL_ORACLE_MAX_M:
+    if m <= FULL_ORACLE_MAX_M or m in FULL_ORACLE_M:
         rows = np.arange(m)
     else:
         rng = np.random.default_rng(m * 7 + seed)
@@ -107,7 +109,7 @@ def check_case(layer, seed, outliers, m, h=None, W=None, **kw):
 @pytest.mark.parametrize("layer", [s.name for s in wl.LAYERS])
 def test_parity_all_shapes(dev, layer, m):
     combos = [(0, False), (1, True)]
-    if m <= FULL_ORACLE_MAX_M:
+    if m <= FULL_ORACLE_MAX_M or m in FULL_ORACLE_M:
         combos += [(0, True), (1, False)]
     for seed, outl in combos:
         check_case(layer, seed, outl, m)
@@ -142,7 +144,11 @@ def test_cluster_sizes_and_determinism(dev, layer, m):
     meets the contract and is bitwise reproducible; for the router this is the
     FP32-FMA cluster kernel (fp32 weights as they are)."""
     h, W, _ = prepared(layer, 0)
-    if m >= (25 if layer == "router" else 33):
+    if layer == "router" and m >= 25:
+        assert "cluster" in B.proj_describe(h, m)
+    elif layer == "o" and m >= 129:
+        assert B.proj_describe(h, m).startswith("tc_pair")
+    elif layer != "router" and m >= 33:
         assert "cluster" in B.proj_describe(h, m)
     for cs in range(1, 17):
         kw = dict(grid=cs, kernel=B.PROJ_KERNEL_CLUSTER)
@@ -180,6 +186,55 @@ def test_cluster_groups_and_determinism(dev, layer, m):
         ran += 1
     assert ran >= 1
     assert B.proj_device_status(h) == 0
+
+
+@pytest.mark.parametrize("layer,m", [("o", 128), ("qkv_gate", 128), ("pooler", 256),
+                                     ("unpooler", 256), ("qkv_gate", 130), ("pooler", 65),
+                                     ("o", 512), ("unpooler", 1000), ("qkv_gate", 33),
+                                     ("unpooler", 96)])
+def test_pair_shapes_and_determinism(dev, layer, m):
+    """The CTA-pair tensor-core kernel (two CTAs per M = 256 MMA, K split
+    across the pairs of a cluster whose partials meet in L2): the dispatch
+    form on o above 128 tokens; at every token tile and several K splits it
+    meets the contract and is bitwise reproducible (two calls in a row)."""
+    for seed in (0, 1):
+        h, W, _ = prepared(layer, seed)
+        assert B.proj_describe(h, m).startswith("tc_pair") == (layer == "o" and m >= 129)
+        ran = 0
+        for bn in (64, 128, 256):
+            for kg in (0, 1, 2, 3, 5, 8):
+                kw = dict(kernel=B.PROJ_KERNEL_PAIR, tile_n=bn, groups=kg)
+                try:
+                    B.proj_describe_ex(h, m, **kw)
+                except B.ProjError as e:  # < 4 k-blocks per CTA, or a split over > 1 wave
+                    assert e.status == B.PROJ_EUNSUPPORTED
+                    continue
+                a = check_case(layer, seed, seed == 1, m, h=h, W=W, **kw)
+                b = check_case(layer, seed, seed == 1, m, h=h, W=W, **kw)
+                assert np.array_equal(a, b), (layer, m, seed, kw)
+                ran += 1
+        assert ran >= 3
+        assert B.proj_device_status(h) == 0
+
+
+def test_pair_rejections(dev):
+    h, _, _ = prepared("o", 0)
+    x = torch.zeros((128, 1024), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros((128, 8192), dtype=torch.bfloat16, device="cuda")
+    for kw in (dict(kernel=B.PROJ_KERNEL_PAIR, tile_n=32),        # token tiles of 64..256
+               dict(kernel=B.PROJ_KERNEL_PAIR, grid=4),           # no grid for the pair kernel
+               dict(kernel=B.PROJ_KERNEL_PAIR, groups=9),         # clusters of at most 16 CTAs
+               dict(kernel=B.PROJ_KERNEL_PAIR, groups=5),         # o: 16 k-blocks, < 4 per CTA
+               dict(kernel=B.PROJ_KERNEL_PAIR, variant=B.PROJ_VARIANT_EXPWIN12)):
+        with pytest.raises(B.ProjError) as e:
+            B.proj_run_ex(h, x, 128, out, **kw)
+        assert e.value.status == B.PROJ_EUNSUPPORTED, kw
+    hr, _, _ = prepared("router", 0)
+    xr = torch.zeros((128, 8192), dtype=torch.bfloat16, device="cuda")
+    orr = torch.zeros((128, 256), dtype=torch.float32, device="cuda")
+    with pytest.raises(B.ProjError) as e:
+        B.proj_run_ex(hr, xr, 128, orr, kernel=B.PROJ_KERNEL_PAIR)
+    assert e.value.status == B.PROJ_EUNSUPPORTED
 
 
 @pytest.mark.parametrize("layer,m", [(l, m) for l in ("qkv_gate", "o", "pooler", "unpooler")
