@@ -18,11 +18,15 @@
 //   16-byte chunks swizzled by row so that 16 consecutive rows read
 //   conflict-free) with one bulk copy each, and the x tile with the same
 //   128-byte-swizzled 2-D TMA load as the tensor-core kernel.
-// * Eight compute warps.  A thread owns 8 rows x 4 tokens; per 4 k it loads
-//   its 8 rows' weights (16-byte loads) and its 4 tokens' x (8-byte loads,
-//   widened exactly), and issues fma.rn.f32x2 on (even k, odd k) pairs, so
-//   each output keeps two fp32 partial sums (even and odd k) added at the
-//   end.  Narrow token tiles split each stage's 64 k among warp groups
+// * Eight compute warps.  At each stage a warp first widens (exactly) the
+//   bf16 x of its 8 tokens over its k-range to fp32 in a private shared-memory
+//   scratch.  A thread owns 8 rows x 4 tokens; per 4 k it loads its 8 rows'
+//   weights and its 4 tokens' x (16-byte loads each, no per-step widening or
+//   swizzle arithmetic on x), and issues fma.rn.f32x2 on (even k, odd k)
+//   pairs, so each output keeps two fp32 partial sums (even and odd k) added
+//   at the end.  (Widening inside the 4-k step instead measured 3-10 %
+//   slower at 64..512 tokens: its integer work sits between the loads and the
+//   FMAs.)  Narrow token tiles split each stage's 64 k among warp groups
 //   inside the CTA; their partial tiles are added in group order.  Nine
 //   warps put three on one of the SM's four schedulers, whose quarter of the
 //   register file then holds about 170 registers per thread, which sets the
@@ -47,17 +51,23 @@ struct RCfg {
   static_assert(BN >= 16 && BN <= 64, "token tile");
   static constexpr int kXBytes = BN * 128;  // bf16 [BN][64]
   static constexpr int kStage = kRfBytes + kXBytes;
-  static constexpr int kFit = (kSmemMax - 1024 - 1024) / kStage;
-  static constexpr int S = kFit > 8 ? 8 : kFit;
   static constexpr int kComputeWarps = 8;
   static constexpr int kThreads = (kComputeWarps + 1) * 32;  // warp 0: producer
   static constexpr int kWpt = BN / 8;                // warps per token tile
   static constexpr int kKGroups = kComputeWarps / kWpt;  // k-groups inside the CTA
   static constexpr int kKPerGroup = kRfK / kKGroups;     // k of a stage per warp
+  static constexpr int kScrAll = kComputeWarps * 8 * (kKPerGroup * 4 + 16);
+  static constexpr int kFit = (kSmemMax - 1024 - 1024 - kScrAll) / kStage;
+  static constexpr int S = kFit > 8 ? 8 : kFit;
+  // per compute warp: its 8 tokens' x for its k-range of a stage, widened to
+  // fp32 ([8][kKPerGroup + 4] floats: the 16-byte pad puts the two token
+  // halves of a warp on different banks)
+  static constexpr int kScrStride = kKPerGroup * 4 + 16;  // bytes per token row
+  static constexpr int kScrWarp = 8 * kScrStride;
   static constexpr size_t kRing = static_cast<size_t>(S) * kStage;
   static constexpr size_t kPart = static_cast<size_t>(kKGroups) * BN * kTileRows * 4;
   static constexpr size_t kData = kRing > kPart ? kRing : kPart;
-  static constexpr size_t kSmem = 1024 + kData + (2 * S) * 8 + 16;
+  static constexpr size_t kSmem = 1024 + kData + kScrAll + (2 * S) * 8 + 16;
   static_assert(S >= 3, "pipeline too shallow");
   static_assert(kSmem <= kSmemMax, "shared memory budget");
   static_assert(kKPerGroup % 4 == 0, "k step");
@@ -65,15 +75,6 @@ struct RCfg {
 
 __device__ __forceinline__ void ld_shared_2x64(uint32_t addr, uint64_t& a, uint64_t& b) {
   asm volatile("ld.shared.v2.u64 {%0,%1}, [%2];" : "=l"(a), "=l"(b) : "r"(addr));
-}
-__device__ __forceinline__ uint2 ld_shared_u2(uint32_t addr) {
-  uint2 v;
-  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
-  return v;
-}
-// Two bf16 (low half first) widened exactly to an fp32 pair.
-__device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t v) {
-  return (static_cast<uint64_t>(v & 0xFFFF0000u) << 32) | (v << 16);
 }
 // (acc.lo, acc.hi) += (w.lo, w.hi) * (x.lo, x.hi)
 __device__ __forceinline__ void ffma2(uint64_t& acc, uint64_t w, uint64_t x) {
@@ -97,7 +98,8 @@ __global__ void __launch_bounds__(RCfg<BN>::kThreads, 1)
   // the CTA's partial tile that the combine reads.
   const uint32_t part_base = sW;
   const uint32_t red_base = sW;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kData);
+  const uint32_t sScr = sW + static_cast<uint32_t>(C::kData);  // per-warp fp32 x
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kData + C::kScrAll);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * S;
 
@@ -193,6 +195,27 @@ __global__ void __launch_bounds__(RCfg<BN>::kThreads, 1)
       }
       const uint32_t wst = sW + s * kRfBytes;
       const uint32_t xst = sX + s * C::kXBytes;
+      // Widen this warp's 8 tokens x its k-range of the stage to fp32 once
+      // (16-byte chunks of the 128-byte-swizzled bf16 tile).
+      const uint32_t scr = sScr + static_cast<uint32_t>(cw * C::kScrWarp);
+      {
+        constexpr int kCh = C::kKPerGroup / 8;  // 16-byte bf16 chunks per token
+#pragma unroll
+        for (int idx = lane; idx < 8 * kCh; idx += 32) {
+          const int t8 = idx / kCh, cc = idx % kCh;
+          const int jt = 8 * tt + t8;
+          const int kc = kg * kCh + cc;
+          const uint4 v = ld_shared_u4(xst + jt * 128 + ((kc ^ (jt & 7)) << 4));
+          const uint32_t a = scr + t8 * C::kScrStride + cc * 32;
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(v.x << 16),
+                       "r"(v.x & 0xFFFF0000u), "r"(v.y << 16), "r"(v.y & 0xFFFF0000u)
+                       : "memory");
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(a + 16), "r"(v.z << 16),
+                       "r"(v.z & 0xFFFF0000u), "r"(v.w << 16), "r"(v.w & 0xFFFF0000u)
+                       : "memory");
+        }
+        __syncwarp();
+      }
       // fully unrolled over the stage: the next steps' shared-memory loads
       // issue under this step's FMAs (measured 2-4 % faster than unrolling
       // by two at 256-512 tokens, no change below)
@@ -208,13 +231,8 @@ __global__ void __launch_bounds__(RCfg<BN>::kThreads, 1)
         }
         uint64_t x01[4], x23[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int jt = 8 * tt + 4 * tg + u;
-          const uint2 xv = ld_shared_u2(xst + jt * 128 + ((((k0 >> 3) ^ (jt & 7))) << 4) +
-                                        ((k0 >> 2) & 1) * 8);
-          x01[u] = bf16x2_to_f32x2(xv.x);
-          x23[u] = bf16x2_to_f32x2(xv.y);
-        }
+        for (int u = 0; u < 4; ++u)
+          ld_shared_2x64(scr + (4 * tg + u) * C::kScrStride + kk * 4, x01[u], x23[u]);
         // 32 independent pair-FMAs, then the 32 that depend on them
 #pragma unroll
         for (int i = 0; i < 8; ++i)
