@@ -26,10 +26,12 @@ PROJ_ENCODE_EXPWIN12 = 1
 PROJ_VARIANT_AUTO, PROJ_VARIANT_DENSE, PROJ_VARIANT_EXPWIN12, PROJ_VARIANT_PLANES3 = range(4)
 PROJ_REDUCE_AUTO, PROJ_REDUCE_OWNER, PROJ_REDUCE_DISTRIBUTED = range(3)
 (PROJ_KERNEL_AUTO, PROJ_KERNEL_GEMV, PROJ_KERNEL_TILE, PROJ_KERNEL_CLUSTER, PROJ_KERNEL_GEMV_REG,
- PROJ_KERNEL_MMA, PROJ_KERNEL_GEMV_SPLITK, PROJ_KERNEL_PAIR) = range(8)
+ PROJ_KERNEL_MMA, PROJ_KERNEL_GEMV_SPLITK, PROJ_KERNEL_PAIR, PROJ_KERNEL_ROWS) = range(9)
 PROJ_UNPACK_FRAG16 = 16  # proj_unpack_weights: the few-token GEMV's fragment-order copy
 PROJ_UNPACK_RC12 = 32  # proj_unpack_weights: the register GEMV's 12-bit row-chunk copy
 PROJ_UNPACK_FRAG12 = 64  # proj_unpack_weights: the warp-MMA GEMV's 12-bit fragment copy
+PROJ_UNPACK_RUNS = 128  # proj_unpack_weights: the row-run GEMV's copy (all N rows)
+PROJ_UNPACK_RUNS_SLICE = 256  # proj_unpack_weights: the unpooler's row-run copy of its slice
 PROJ_READ_PDL = 4  # proj_read_floor mode flag: launched as a programmatic dependent launch
 
 LAYER_INDEX = {"qkv_gate": 0, "o": 1, "pooler": 2, "unpooler": 3, "router": 4}
@@ -49,7 +51,7 @@ class NativeLibraryMissing(ImportError):
 class proj_run_opts(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int), ("grid", ctypes.c_int),
                 ("reduce", ctypes.c_int), ("kernel", ctypes.c_int), ("groups", ctypes.c_int),
-                ("tile_n", ctypes.c_int)]
+                ("tile_n", ctypes.c_int), ("stamps", ctypes.c_void_p)]
 
 
 class proj_info_t(ctypes.Structure):
@@ -177,9 +179,10 @@ def proj_run(h: int, x, m: int, out, stream=None) -> None:
 
 def proj_run_ex(h: int, x, m: int, out, stream=None, variant: int = PROJ_VARIANT_AUTO,
                 grid: int = 0, reduce: int = PROJ_REDUCE_AUTO,
-                kernel: int = PROJ_KERNEL_AUTO, groups: int = 0, tile_n: int = 0) -> None:
+                kernel: int = PROJ_KERNEL_AUTO, groups: int = 0, tile_n: int = 0,
+                stamps=None) -> None:
     opts = proj_run_opts(int(variant), int(grid), int(reduce), int(kernel), int(groups),
-                         int(tile_n))
+                         int(tile_n), _addr(stamps))
     _check(load().proj_run_ex(h, _addr(x), int(m), _addr(out), _stream(stream),
                               ctypes.byref(opts)), "proj_run_ex")
 

@@ -104,6 +104,50 @@ bool make_x_map(CUtensorMap* map, const void* x, int64_t m, int64_t K, int box_r
   return r == CUDA_SUCCESS;
 }
 
+// A row-major bf16 [rows, K] matrix viewed as (32 columns, rows, K / 32
+// steps): a box (32, box_rows, box_steps) lands as [step][row][64 bytes].
+bool make_rows3_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows,
+                    int box_steps) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {32u, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(K / 32)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, 64u};
+  const cuuint32_t box[3] = {32u, static_cast<cuuint32_t>(box_rows),
+                             static_cast<cuuint32_t>(box_steps)};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Ring shape of the row-run GEMV: steps per stage KS = SPW x (16 / block
+// slots) for SPW in {1, 2, 4} (each consumer warp takes SPW steps of every
+// stage), KS dividing K / 32, and the stages that fit shared memory (at
+// most kGemvRowsMaxStages).  The longest stages that still leave three in
+// the ring (or hold the whole run) win: measured on GB300, each stage costs
+// a fixed hand-off (consumer release, producer re-issue) and each consumer
+// warp's x loads are hidden better across more steps, so 4 steps per warp
+// beat 1 by 1-4 us on every bf16 layer at 8 tokens although fewer bytes are
+// in flight.
+void rows_ring_shape(int nt, int nr_hi, int64_t K, int* ks_out, int* spw_out, int* s_out) {
+  const int steps = static_cast<int>(K / 32);
+  const int wpb = kGemvRowsConsumers / gemv_rows_block_slots(nr_hi);
+  *ks_out = *spw_out = *s_out = 0;
+  for (int spw = 1; spw <= 4; spw *= 2) {
+    const int ks = spw * wpb;
+    if (ks > steps || steps % ks) continue;
+    int s = kGemvRowsMaxStages;
+    while (s >= 2 && gemv_rows_smem(nt, ks, s, nr_hi) > static_cast<size_t>(kGemvRowsSmemMax)) --s;
+    if (s < 2) continue;
+    const int nst = steps / ks;
+    if (s < 3 && nst > s) continue;
+    *ks_out = ks;
+    *spw_out = spw;
+    *s_out = s;
+  }
+}
+
 // The packed bf16 weight tiles (kTileBytes each, already the shared-memory
 // image of the 128-byte swizzle) as a [tiles x 128][64] bf16 matrix: a box
 // of 64 x 128 with no swizzle copies one tile verbatim.
@@ -314,6 +358,8 @@ struct Plan {
   bool gemv;
   bool gemv_reg = false;  // m <= 2: register-streaming form
   bool gemv_mma = false;  // bf16, m <= 8: warp-MMA weight stream
+  bool gemv_rows = false;  // bf16, m <= 32: row-run warp-MMA weight stream
+  int bpw = 1;             // gemv_rows: 32-column steps per ring stage
   bool router_gemv = false;  // router, m <= 16: FP32-FMA weight stream
   bool router_gemv_cc = false;  // router, m <= 32: the same with K split across a cluster
   bool cluster;
@@ -344,6 +390,11 @@ struct proj_ctx {
   uint32_t* cl_counters = nullptr; // cluster groups: [SMs][16], zero between calls
   float* xch = nullptr;            // cluster partials' exchange: [SMs][256][128] fp32
   uint32_t* w_frag = nullptr;      // bf16 layers: 16 x 16 MMA-fragment tiles (few tokens)
+  uint8_t* w_runs = nullptr;       // bf16 layers: the row-run layout of all N rows over runs_G CTAs
+  int runs_G = 0;
+  uint8_t* w_runs_slice = nullptr; // unpooler: the same for the slice's runs_slice_rows rows
+  int runs_slice_G = 0;
+  int64_t runs_slice_rows = 0;
   int cluster_active[5][kClusterMaxCS] = {};   // co-resident clusters: BN 16..256 x size 1..16
   int rcluster_active[5][kClusterMaxCS] = {};  // the same for the FP32-FMA router kernel
   int rgcc_active = 0;  // co-resident clusters of the split-K router GEMV
@@ -374,6 +425,13 @@ struct proj_ctx {
     CUtensorMap map;
   } maps[8];
   int n_maps = 0, next_map = 0;
+  struct RowsMapEntry {
+    const void* base;
+    int64_t rows;
+    int box_rows, box_steps;
+    CUtensorMap map;
+  } rmaps[16];
+  int n_rmaps = 0, next_rmap = 0;
 };
 
 namespace {
@@ -385,6 +443,8 @@ void free_ctx(proj_ctx* h) {
   cudaFree(h->cl_counters);
   cudaFree(h->xch);
   cudaFree(h->w_frag);
+  cudaFree(h->w_runs);
+  cudaFree(h->w_runs_slice);
   cudaFree(h->w_rows);
   cudaFree(h->gemv_flags);
   cudaFree(h->gemv_ws);
@@ -417,6 +477,24 @@ const CUtensorMap* get_map(proj_ctx* h, const void* x, int64_t m, int box, bool 
   return &e.map;
 }
 
+const CUtensorMap* get_rows_map(proj_ctx* h, const void* base, int64_t rows, int box_rows,
+                                int box_steps) {
+  for (int i = 0; i < h->n_rmaps; ++i) {
+    auto& e = h->rmaps[i];
+    if (e.base == base && e.rows == rows && e.box_rows == box_rows && e.box_steps == box_steps)
+      return &e.map;
+  }
+  auto& e = h->rmaps[h->next_rmap];
+  if (!make_rows3_map(&e.map, base, rows, h->K, box_rows, box_steps)) return nullptr;
+  e.base = base;
+  e.rows = rows;
+  e.box_rows = box_rows;
+  e.box_steps = box_steps;
+  h->next_rmap = (h->next_rmap + 1) % 16;
+  h->n_rmaps = std::min(h->n_rmaps + 1, 16);
+  return &e.map;
+}
+
 int64_t out_rows(const proj_ctx* h, int64_t m) {
   if (h->layer == PROJ_UNPOOLER && m <= kUnpoolerSliceMaxM) return kUnpoolerSliceRows;
   return h->N;
@@ -425,7 +503,7 @@ int64_t out_rows(const proj_ctx* h, int64_t m) {
 int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl) {
   const int variant = opts ? opts->variant : PROJ_VARIANT_AUTO;
   const int kern = opts ? opts->kernel : PROJ_KERNEL_AUTO;
-  if (kern < PROJ_KERNEL_AUTO || kern > PROJ_KERNEL_PAIR) return PROJ_EINVAL;
+  if (kern < PROJ_KERNEL_AUTO || kern > PROJ_KERNEL_ROWS) return PROJ_EINVAL;
   if (variant < PROJ_VARIANT_AUTO || variant > PROJ_VARIANT_PLANES3) return PROJ_EINVAL;
   const int tile_n = opts ? opts->tile_n : 0;
   if (tile_n != 0 && tile_n != 16 && tile_n != 32 && tile_n != 64 && tile_n != 128 &&
@@ -509,6 +587,57 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
     pl->T = pl->KB = pl->MT = 0;
     pl->G = static_cast<int>(G);
     return PROJ_OK;
+  }
+  // A few tokens on the bf16 layers: the row-run warp-MMA weight stream
+  // (whole row runs per CTA fed by tensor copies into a shared-memory ring).
+  {
+    int64_t G = std::min<int64_t>(pl->n_out, h->num_sms);
+    if (opts && opts->grid > 0) G = std::min<int64_t>(opts->grid, pl->n_out);
+    const int nt = m <= 8 ? 1 : (m <= 16 ? 2 : 4);  // tiles of 8 tokens
+    const int64_t nr_hi = G > 0 ? (pl->n_out + G - 1) / G : 0;
+    int ks = 0, spw = 0, stages = 0;
+    if (nr_hi >= 1 && nr_hi <= kGemvRowsMaxRows && h->K % 32 == 0)
+      rows_ring_shape(nt, static_cast<int>(nr_hi), h->K, &ks, &spw, &stages);
+    if (opts && opts->groups > 0 && ks > 0) {  // forced steps per consumer warp and stage
+      const int want = opts->groups;
+      const int wpb = kGemvRowsConsumers / gemv_rows_block_slots(static_cast<int>(nr_hi));
+      ks = (want == 1 || want == 2 || want == 4) && (h->K / 32) % (want * wpb) == 0 ? want * wpb
+                                                                                   : 0;
+      spw = want;
+      if (ks) {
+        stages = kGemvRowsMaxStages;
+        while (stages >= 2 && gemv_rows_smem(nt, ks, stages, static_cast<int>(nr_hi)) >
+                                  static_cast<size_t>(kGemvRowsSmemMax))
+          --stages;
+        if (stages < 2) ks = 0;
+      }
+    }
+    const bool rows_ok = !pl->router && h->w_rows && m <= kGemvRowsMaxM && ks > 0 &&
+                         (variant == PROJ_VARIANT_AUTO || variant == PROJ_VARIANT_DENSE);
+    // Measured on GB300 (device time, cold L2) against the forms it replaces:
+    // faster on the K = 8192 layers at 3..8 tokens (qkv_gate 10.4-10.7 us
+    // against the warp-MMA GEMV's 10.6-11.6; pooler 14.6-15.0 against the
+    // cluster kernel's 15.3-15.6), slower on o and the unpooler slice and
+    // from 9 tokens on (each CTA reads all of x from L2: m x 16 KB at K =
+    // 8192, on each consumer warp's critical path).
+    const bool rows_auto = kern == PROJ_KERNEL_AUTO && m >= kGemvMmaMinM && m <= 8 &&
+                           h->K >= 8192 &&
+                           (!opts || (opts->grid == 0 && opts->groups == 0 &&
+                                      opts->tile_n == 0 && opts->reduce == PROJ_REDUCE_AUTO));
+    if (kern == PROJ_KERNEL_ROWS && !rows_ok) return PROJ_EUNSUPPORTED;
+    if (rows_ok && (kern == PROJ_KERNEL_ROWS || rows_auto)) {
+      pl->gemv_rows = true;
+      pl->expwin = false;
+      pl->reduce = 0;
+      pl->bn = nt;
+      pl->bpw = ks;
+      pl->KG = stages;
+      pl->MT = spw;
+      pl->T = static_cast<int>(nr_hi);
+      pl->KB = 0;
+      pl->G = static_cast<int>(G);
+      return PROJ_OK;
+    }
   }
   // A few tokens on the bf16 layers: the warp-MMA weight stream.
   {
@@ -760,6 +889,7 @@ proj_handle proj_prepare_ex(int layer, const void* W, int64_t N, int64_t K, int 
   if ((e = gemv_init_attributes()) != cudaSuccess) return bail_cuda(e, "gemv attributes");
   if ((e = gemv_reg_init_attributes()) != cudaSuccess) return bail_cuda(e, "gemv attributes");
   if ((e = gemv_mma_init_attributes()) != cudaSuccess) return bail_cuda(e, "gemv attributes");
+  if ((e = gemv_rows_init_attributes()) != cudaSuccess) return bail_cuda(e, "gemv attributes");
   if ((e = router_gemv_init_attributes()) != cudaSuccess) return bail_cuda(e, "gemv attributes");
   if ((e = cluster_init_attributes()) != cudaSuccess) return bail_cuda(e, "cluster attributes");
   if ((e = pair_init_attributes()) != cudaSuccess) return bail_cuda(e, "pair attributes");
@@ -830,6 +960,31 @@ proj_handle proj_prepare_ex(int layer, const void* W, int64_t N, int64_t K, int 
                            static_cast<int>(K), h->w_frag, s)) != cudaSuccess) {
         done();
         return bail_cuda(e, "pack fragment tiles");
+      }
+    }
+    // The row-run layout of the few-token GEMV, for its default partition
+    // (one CTA per SM); the unpooler also for its first 1024 rows.
+    if (K % 32 == 0) {
+      h->runs_G = static_cast<int>(std::min<int64_t>(N, h->num_sms));
+      if ((N + h->runs_G - 1) / h->runs_G <= kGemvRowsMaxRows) {
+        if ((e = dmalloc(&h->w_runs, static_cast<size_t>(N) * K * 2)) != cudaSuccess ||
+            (e = pack_runs(static_cast<const uint16_t*>(W), static_cast<int>(N),
+                           static_cast<int>(K), h->runs_G, h->w_runs, s)) != cudaSuccess) {
+          done();
+          return bail_cuda(e, "pack row runs");
+        }
+      }
+      if (layer == PROJ_UNPOOLER) {
+        h->runs_slice_rows = kUnpoolerSliceRows;
+        h->runs_slice_G = static_cast<int>(std::min<int64_t>(kUnpoolerSliceRows, h->num_sms));
+        if ((e = dmalloc(&h->w_runs_slice, static_cast<size_t>(kUnpoolerSliceRows) * K * 2)) !=
+                cudaSuccess ||
+            (e = pack_runs(static_cast<const uint16_t*>(W), static_cast<int>(kUnpoolerSliceRows),
+                           static_cast<int>(K), h->runs_slice_G, h->w_runs_slice, s)) !=
+                cudaSuccess) {
+          done();
+          return bail_cuda(e, "pack row runs");
+        }
       }
     }
     if (flags & PROJ_ENCODE_EXPWIN12) {
@@ -1040,6 +1195,39 @@ int proj_run_ex(proj_handle h, const void* x, int64_t m, void* out, proj_stream 
     if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
     return PROJ_OK;
   }
+  if (pl.gemv_rows) {
+    const int nt = pl.bn, ks = pl.bpw, nr_hi = pl.T;
+    // Each map is copied out at once: a later insertion into the cache may
+    // reuse the slot a hit pointed to.
+    CUtensorMap tw_hi, tw_lo;
+    const CUtensorMap* mp = get_rows_map(h, h->w_rows, h->N, nr_hi, ks);
+    if (!mp) return fail_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(rows)");
+    tw_hi = *mp;
+    mp = nr_hi > 1 ? get_rows_map(h, h->w_rows, h->N, nr_hi - 1, ks) : &tw_hi;
+    if (!mp) return fail_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(rows)");
+    tw_lo = *mp;
+
+    GemvRowsParams g;
+    g.w_runs = nullptr;
+    if (pl.n_out == h->N && h->w_runs && pl.G == h->runs_G) g.w_runs = h->w_runs;
+    if (pl.n_out != h->N && h->w_runs_slice && pl.n_out == h->runs_slice_rows &&
+        pl.G == h->runs_slice_G)
+      g.w_runs = h->w_runs_slice;
+    g.x = static_cast<const uint16_t*>(x);
+    g.out = out;
+    g.status = h->status;
+    g.stamps = opts ? static_cast<uint64_t*>(opts->stamps) : nullptr;
+    g.m = static_cast<int>(m);
+    g.n_rows = static_cast<int>(pl.n_out);
+    g.K = static_cast<int>(h->K);
+    g.G = pl.G;
+    g.KS = ks;
+    g.S = pl.KG;
+    g.nr_hi = nr_hi;
+    e = gemv_rows_launch(nt, pl.MT, tw_hi, tw_lo, g, s);
+    if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
+    return PROJ_OK;
+  }
   if (pl.gemv_mma) {
     GemvMmaParams g;
     g.w = reinterpret_cast<const uint4*>(h->w_frag);
@@ -1218,6 +1406,14 @@ int proj_describe_ex(proj_handle h, int64_t m, const proj_run_opts* opts, char* 
   } else if (pl.router_gemv_cc) {
     std::snprintf(buf, cap, "router_gemv_splitk_f32w CS=%d clusters=%lld n_rows=%lld", pl.G,
                   static_cast<long long>((pl.n_out + 7) / 8), static_cast<long long>(pl.n_out));
+  } else if (pl.gemv_rows) {
+    std::snprintf(buf, cap,
+                  "gemv_rows_mma tokens<=%d steps_per_stage=%d steps_per_warp=%d stages=%d G=%d "
+                  "rows_per_cta<=%d n_rows=%lld %s",
+                  8 * pl.bn, pl.bpw, pl.MT, pl.KG, pl.G, pl.T, static_cast<long long>(pl.n_out),
+                  (pl.n_out == h->N ? (h->w_runs && pl.G == h->runs_G)
+                                    : (h->w_runs_slice && pl.G == h->runs_slice_G))
+                      ? "packed_runs" : "row_major_tma");
   } else if (pl.gemv_mma) {
     std::snprintf(buf, cap, "gemv_mma16x8%s tokens<=%d G=%d blocks_per_cta<=%lld n_rows=%lld",
                   pl.expwin ? "_expwin12rc" : "", 8 * pl.bn, pl.G,
@@ -1254,13 +1450,15 @@ int proj_unpack_weights(proj_handle h, int variant, void* W_out, proj_stream str
   if (!aligned16(W_out)) return fail(PROJ_EALIGN);
   if ((variant < PROJ_VARIANT_AUTO || variant > PROJ_VARIANT_PLANES3) &&
       variant != PROJ_UNPACK_FRAG16 && variant != PROJ_UNPACK_RC12 &&
-      variant != PROJ_UNPACK_FRAG12)
+      variant != PROJ_UNPACK_FRAG12 && variant != PROJ_UNPACK_RUNS &&
+      variant != PROJ_UNPACK_RUNS_SLICE)
     return fail(PROJ_EINVAL);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (h->layer == PROJ_ROUTER) {
     if (variant == PROJ_VARIANT_EXPWIN12 || variant == PROJ_UNPACK_FRAG16 ||
-        variant == PROJ_UNPACK_RC12 || variant == PROJ_UNPACK_FRAG12)
+        variant == PROJ_UNPACK_RC12 || variant == PROJ_UNPACK_FRAG12 ||
+        variant == PROJ_UNPACK_RUNS || variant == PROJ_UNPACK_RUNS_SLICE)
       return fail(PROJ_EUNSUPPORTED);
     if (variant == PROJ_VARIANT_PLANES3)
       e = unpack_router_planes(h->w_planes, static_cast<int>(h->N), static_cast<int>(h->K),
@@ -1287,6 +1485,14 @@ int proj_unpack_weights(proj_handle h, int variant, void* W_out, proj_stream str
     if (!h->w_rc12) return fail(PROJ_EUNSUPPORTED);
     e = decode_rc12(h->w_rc12, h->rc12_esc, static_cast<int>(h->N), static_cast<int>(h->K), h->e0,
                     static_cast<uint16_t*>(W_out), s);
+  } else if (variant == PROJ_UNPACK_RUNS) {
+    if (!h->w_runs) return fail(PROJ_EUNSUPPORTED);
+    e = unpack_runs(h->w_runs, static_cast<int>(h->N), static_cast<int>(h->K), h->runs_G,
+                    static_cast<uint16_t*>(W_out), s);
+  } else if (variant == PROJ_UNPACK_RUNS_SLICE) {
+    if (!h->w_runs_slice) return fail(PROJ_EUNSUPPORTED);
+    e = unpack_runs(h->w_runs_slice, static_cast<int>(h->runs_slice_rows), static_cast<int>(h->K),
+                    h->runs_slice_G, static_cast<uint16_t*>(W_out), s);
   } else if (variant == PROJ_UNPACK_FRAG16) {
     if (!h->w_frag) return fail(PROJ_EUNSUPPORTED);
     e = unpack_frag16(h->w_frag, static_cast<int>(h->N), static_cast<int>(h->K),

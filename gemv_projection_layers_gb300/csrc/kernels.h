@@ -252,6 +252,68 @@ int gemv_mma_smem(int nt, int K);   // dynamic shared memory at nt tiles of 8 to
 bool gemv_mma_fits(int nt, int K);  // it fits one CTA's shared memory
 cudaError_t gemv_mma_init_attributes();
 cudaError_t gemv_mma_launch(int nt, bool x12, const GemvMmaParams& p, cudaStream_t s);
+// Row-run warp-MMA GEMV (gemv_rows.cu): bf16 layers, m <= 8 NT (NT in
+// {1, 2, 4} tiles of 8 tokens).  CTA c of G owns rows [c N / G, (c + 1) N / G)
+// of W (nr_hi = ceil(N / G) rows or one fewer, at most kGemvRowsMaxRows);
+// one thread streams them into a ring of S stages of KS 32-column steps:
+// from the packed run layout with one bulk copy per stage, or -- for another
+// grid -- through tw_hi / tw_lo, W viewed as (32 columns, N rows, K / 32
+// steps) with boxes (32, nr_hi or nr_hi - 1, KS).  The 16 consumer warps
+// take 16 / NB per 16-row block (NB = ceil(rows / 16)) and SPW = KS NB / 16
+// steps of every stage each, loading their x fragments from global memory.
+struct GemvRowsParams {
+  const uint8_t* w_runs;  // the rows' run layout for this (n_rows, G) (pack_runs), or null:
+                          // W through the tensor maps instead
+  const uint16_t* x;    // bf16 [m, K]
+  void* out;            // bf16 [m, n_rows]
+  uint32_t* status;
+  uint64_t* stamps;     // optional: [G][4] %globaltimer at entry, after the dependency
+                        // wait, after the main loop, at exit (null: none)
+  int m;
+  int n_rows;
+  int K;                // multiple of 32 KS
+  int G;
+  int KS;               // steps per stage
+  int S;                // ring stages
+  int nr_hi;            // ceil(n_rows / G)
+};
+constexpr int kGemvRowsMaxM = 32;
+constexpr int kGemvRowsMaxRows = 64;     // rows per CTA: at most four 16-row blocks
+constexpr int kGemvRowsConsumers = 16;   // consumer warps
+constexpr int kGemvRowsRowPitch = 20;    // fp32 per staged tile row (bank-spread stores)
+constexpr int kGemvRowsMaxStages = 16;
+constexpr int kGemvRowsSmemMax = 227 * 1024;
+// Consumer warps are dealt to 1, 2 or 4 block slots (the 16-row blocks of
+// the longest run, rounded up to a power of two), 16 / slots per block.
+__host__ __device__ inline int gemv_rows_block_slots(int nr_hi) {
+  const int nb = (nr_hi + 15) >> 4;
+  return nb <= 1 ? 1 : (nb <= 2 ? 2 : 4);
+}
+// Stages of x fragments a consumer warp keeps in flight (registers:
+// D x SPW x NT x 4).
+__host__ __device__ constexpr int gemv_rows_x_depth(int nt, int spw) {
+  return (nt == 1 ? 8 : (nt == 2 ? 6 : 4)) / spw < 2 ? 2 : (nt == 1 ? 8 : (nt == 2 ? 6 : 4)) / spw;
+}
+// A stage: KS steps of the run's rows, [step][row][64 B], padded to 128 B.
+__host__ __device__ inline uint32_t gemv_rows_stage_bytes(int ks, int nr_hi) {
+  return (static_cast<uint32_t>(ks) * nr_hi * 64 + 127u) & ~127u;
+}
+// Byte offset of the barriers: after the ring, or after the accumulator
+// staging that reuses it, whichever is longer.
+__host__ __device__ inline uint32_t gemv_rows_bar_offset(int nt, int ks, int stages, int nr_hi) {
+  const uint32_t ring = static_cast<uint32_t>(stages) * gemv_rows_stage_bytes(ks, nr_hi);
+  const uint32_t red = static_cast<uint32_t>(kGemvRowsConsumers) * 8 * nt * kGemvRowsRowPitch * 4;
+  return ((ring > red ? ring : red) + 7u) & ~7u;
+}
+size_t gemv_rows_smem(int nt, int ks, int stages, int nr_hi);
+cudaError_t gemv_rows_init_attributes();
+cudaError_t gemv_rows_launch(int nt, int spw, const CUtensorMap& tw_hi, const CUtensorMap& tw_lo,
+                             const GemvRowsParams& p, cudaStream_t s);
+// The row-run layout: rows [0, Nr) of a row-major bf16 [*, K] matrix for the
+// partition over G CTAs; CTA c's run [c Nr / G, (c + 1) Nr / G) at byte
+// offset (c Nr / G) K 2, laid out [K / 32 steps][run rows][32 columns].
+cudaError_t pack_runs(const uint16_t* W, int Nr, int K, int G, uint8_t* dst, cudaStream_t s);
+cudaError_t unpack_runs(const uint8_t* src, int Nr, int K, int G, uint16_t* W, cudaStream_t s);
 cudaError_t pack_router_fma_tiles(const float* W, int N, int K, uint8_t* dst, cudaStream_t s);
 cudaError_t unpack_router_fma_tiles(const uint8_t* src, int N, int K, float* W, cudaStream_t s);
 // Router W -> bf16 planes hi, mid, lo (hi + mid + lo == W) packed as the bf16

@@ -332,6 +332,43 @@ __global__ void unpack_frag16_kernel(const uint32_t* __restrict__ src, int N, in
   }
 }
 
+// Row-run layout of the few-token GEMV (gemv_rows.cu): CTA c of G owns rows
+// [r0, r1) = [c Nr / G, (c + 1) Nr / G); its run sits at byte r0 K 2 as
+// [K / 32 steps][r1 - r0 rows][32 columns].  16-byte unit (row r, columns
+// 8u .. 8u + 7) of the row-major source goes to
+// r0 K 2 + (u / 4) (r1 - r0) 64 + (r - r0) 64 + (u % 4) 16.
+__device__ __forceinline__ size_t runs_offset(int r, int u, int Nr, int K, int G) {
+  const int c = static_cast<int>(part_owner(r, Nr, G));
+  const int r0 = static_cast<int>(part_begin(c, Nr, G));
+  const int r1 = static_cast<int>(part_begin(c + 1, Nr, G));
+  return static_cast<size_t>(r0) * K * 2 + static_cast<size_t>(u >> 2) * (r1 - r0) * 64 +
+         static_cast<size_t>(r - r0) * 64 + (u & 3) * 16;
+}
+
+__global__ void pack_runs_kernel(const uint16_t* __restrict__ W, int Nr, int K, int G,
+                                 uint8_t* __restrict__ dst) {
+  const int U = K / 8;
+  const int64_t n = static_cast<int64_t>(Nr) * U;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int r = static_cast<int>(i / U), u = static_cast<int>(i % U);
+    *reinterpret_cast<uint4*>(dst + runs_offset(r, u, Nr, K, G)) =
+        *reinterpret_cast<const uint4*>(W + static_cast<size_t>(r) * K + 8 * u);
+  }
+}
+
+__global__ void unpack_runs_kernel(const uint8_t* __restrict__ src, int Nr, int K, int G,
+                                   uint16_t* __restrict__ W) {
+  const int U = K / 8;
+  const int64_t n = static_cast<int64_t>(Nr) * U;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int r = static_cast<int>(i / U), u = static_cast<int>(i % U);
+    *reinterpret_cast<uint4*>(W + static_cast<size_t>(r) * K + 8 * u) =
+        *reinterpret_cast<const uint4*>(src + runs_offset(r, u, Nr, K, G));
+  }
+}
+
 constexpr int kPrepBlock = 256;
 constexpr int kPrepGrid = 152 * 8;
 
@@ -493,6 +530,16 @@ cudaError_t pack_frag16(const uint16_t* W, int N, int K, uint32_t* dst, cudaStre
 
 cudaError_t unpack_frag16(const uint32_t* src, int N, int K, uint16_t* W, cudaStream_t s) {
   unpack_frag16_kernel<<<kPrepGrid, kPrepBlock, 0, s>>>(src, N, K, W);
+  return cudaGetLastError();
+}
+
+cudaError_t pack_runs(const uint16_t* W, int Nr, int K, int G, uint8_t* dst, cudaStream_t s) {
+  pack_runs_kernel<<<kPrepGrid, kPrepBlock, 0, s>>>(W, Nr, K, G, dst);
+  return cudaGetLastError();
+}
+
+cudaError_t unpack_runs(const uint8_t* src, int Nr, int K, int G, uint16_t* W, cudaStream_t s) {
+  unpack_runs_kernel<<<kPrepGrid, kPrepBlock, 0, s>>>(src, Nr, K, G, W);
   return cudaGetLastError();
 }
 

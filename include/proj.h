@@ -148,6 +148,15 @@ enum proj_kernel {
                                clusters per tile through global memory:
                                proj_run_opts.grid = cluster size (1..16),
                                proj_run_opts.groups = clusters per tile (1..8) */
+    PROJ_KERNEL_ROWS = 8,   /* bf16 layers, m <= 32: weight-streaming GEMV on the warp-level
+                               tensor-core MMA over whole row runs per CTA (CTA c of
+                               proj_run_opts.grid, default the SM count, owns rows
+                               [c N / grid, (c + 1) N / grid), at most 64), W and x
+                               brought from their row-major layouts into a shared-memory
+                               ring by tensor copies; proj_run_opts.groups = 32-column
+                               steps per ring stage (a power of two dividing K / 32, at
+                               most 64; 0 = chosen for the most bytes in flight);
+                               PROJ_EUNSUPPORTED elsewhere */
     PROJ_KERNEL_PAIR = 7    /* bf16 layers (dense weights): tensor cores on CTA pairs
                                (tcgen05 cta_group::2, 256 weight rows per MMA, each CTA
                                holding half of the token tile's x), K split across
@@ -171,6 +180,11 @@ typedef struct proj_run_opts {
                        (1..8); 0 = dispatch table */
     int tile_n;     /* token tile width of the tensor-core kernels (16, 32, 64, 128
                        or 256; the 12-bit kernel 16 or 32); 0 = dispatch table */
+    void *stamps;   /* optional, for measurement: a device buffer of at least
+                       grid x 4 uint64 that the row-run kernel (PROJ_KERNEL_ROWS)
+                       fills with %globaltimer readings per CTA (entry, after the
+                       wait on the previous kernel of the stream, after the main
+                       loop, exit); NULL = none; ignored by the other kernels */
 } proj_run_opts;
 
 typedef struct proj_info_t {
@@ -272,12 +286,18 @@ int proj_describe_ex(proj_handle h, int64_t m, const proj_run_opts *opts, char *
  * (bf16 layers with PROJ_ENCODE_EXPWIN12; PROJ_EUNSUPPORTED where it was
  * not built or was declined), and variant = PROJ_UNPACK_FRAG12 the 12-bit
  * recode of the fragment-order copy (same conditions; it uses a temporary
- * device buffer of N x K bf16 and synchronises `stream`).  Otherwise
- * enqueued on `stream`.
+ * device buffer of N x K bf16 and synchronises `stream`).  variant =
+ * PROJ_UNPACK_RUNS decodes the row-run copy of the few-token GEMV
+ * (PROJ_KERNEL_ROWS: each CTA's rows as [K / 32 steps][rows][32 columns])
+ * into all N rows, and PROJ_UNPACK_RUNS_SLICE the unpooler's copy of its
+ * first 1024 rows into [1024, K] (PROJ_EUNSUPPORTED where not built).
+ * Otherwise enqueued on `stream`.
  */
 #define PROJ_UNPACK_FRAG16 16
 #define PROJ_UNPACK_RC12 32
 #define PROJ_UNPACK_FRAG12 64
+#define PROJ_UNPACK_RUNS 128
+#define PROJ_UNPACK_RUNS_SLICE 256
 int proj_unpack_weights(proj_handle h, int variant, void *W_out, proj_stream stream);
 
 /* Read and clear the handle's device status word (synchronises `stream`).

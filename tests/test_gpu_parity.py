@@ -249,7 +249,7 @@ def test_mma_gemv(dev, layer, m):
     for seed in (0, 1):
         h, W, _ = prepared(layer, seed)
         nb = B.proj_out_features(h, m) // 16
-        if (3 <= m <= 8 and layer != "pooler") or (layer == "o" and 9 <= m <= 16):
+        if (3 <= m <= 8 and layer in ("o", "unpooler")) or (layer == "o" and 9 <= m <= 16):
             assert "gemv_mma" in B.proj_describe(h, m)
         for kw in (dict(), dict(kernel=B.PROJ_KERNEL_MMA),
                    dict(kernel=B.PROJ_KERNEL_MMA, grid=-(-nb // 4)),
@@ -279,6 +279,89 @@ def test_mma_gemv_rejections(dev):
     orr = torch.zeros((8, 256), dtype=torch.float32, device="cuda")
     with pytest.raises(B.ProjError) as e:
         B.proj_run_ex(hr, xr, 8, orr, kernel=B.PROJ_KERNEL_MMA)
+    assert e.value.status == B.PROJ_EUNSUPPORTED
+
+
+def check_outputs(layer, seed, outliers, m, h, W, configs):
+    """Run every config (proj_run_ex keyword sets) on one seeded input; check
+    each against one FP64 reference, probe rows exactly, each config twice
+    for bitwise reproducibility.  Configs the library rejects with
+    PROJ_EUNSUPPORTED are skipped; returns the configs that ran."""
+    act = wl.make_activations(layer, m, seed, outliers)
+    x = to_dev_x(act.x_bits)
+    ref = oracle.reference(layer, act.x_bits, W)
+    ran = []
+    for kw in configs:
+        try:
+            B.proj_describe_ex(h, m, **{k: v for k, v in kw.items() if k != "stamps"})
+        except B.ProjError as e:
+            assert e.status == B.PROJ_EUNSUPPORTED, (layer, m, kw)
+            continue
+        a = out_f64(run(layer, h, x, m, **kw))
+        b = out_f64(run(layer, h, x, m, **kw))
+        assert np.array_equal(a, b), (layer, m, seed, kw)
+        res = oracle.check(layer, a, ref, list(act.probe_rows))
+        assert res["ok"], (layer, seed, outliers, m, kw, res)
+        n_out = a.shape[1]
+        for r, c, e, sg in zip(act.probe_rows, act.probe_cols, act.probe_exp, act.probe_sign):
+            col = oracle.bf16_bits_to_f64(W[:n_out, c])
+            assert np.array_equal(a[r], float(sg) * 2.0 ** int(e) * col), (layer, m, kw, int(r))
+        ran.append(kw)
+    return ran
+
+
+@pytest.mark.parametrize("m", [3, 5, 7, 8, 9, 16, 17, 31, 32])
+@pytest.mark.parametrize("layer", ["qkv_gate", "o", "pooler", "unpooler"])
+def test_rows_gemv(dev, layer, m):
+    """The row-run warp-MMA GEMV (whole row runs per CTA streamed into a
+    shared-memory ring -- from the packed run layout at the SM-count grid,
+    through 3-D tensor copies of the row-major W at other grids -- and x
+    fragments from global memory, the in-step column assignment shared by
+    both operands): the chosen ring shape and forced stages of 1 and 2 steps
+    per warp (many ring laps), the SM-count grid and two odd grids (runs one
+    row shorter than the longest, partial last blocks), all four
+    seed/outlier inputs; the contract, exact probe rows, bitwise
+    reproducibility."""
+    sms = B.proj_num_sms()
+    if layer in ("qkv_gate", "pooler") and 3 <= m <= 8:  # the dispatch form there
+        assert B.proj_describe(prepared(layer, 0)[0], m).startswith("gemv_rows")
+    for seed, outl in ((0, False), (0, True), (1, False), (1, True)):
+        h, W, _ = prepared(layer, seed)
+        configs = [dict(kernel=B.PROJ_KERNEL_ROWS, groups=ks, grid=grid)
+                   for ks in (0, 1, 2) for grid in (0, sms - 3, 131)]
+        ran = check_outputs(layer, seed, outl, m, h, W, configs)
+        assert any(kw["grid"] == 0 and kw["groups"] == 0 for kw in ran), (layer, m)
+        assert B.proj_device_status(h) == 0
+
+
+def test_rows_gemv_stamps_and_rejections(dev):
+    """The phase stamps are written per CTA in order; shapes outside the
+    kernel's range are rejected before any launch."""
+    h, W, _ = prepared("pooler", 0)
+    m = 16
+    act = wl.make_activations("pooler", m, 0, False)
+    x = to_dev_x(act.x_bits)
+    G = B.proj_num_sms()
+    st = torch.zeros((G, 4), dtype=torch.int64, device="cuda")
+    out = run("pooler", h, x, m, kernel=B.PROJ_KERNEL_ROWS, stamps=st)
+    ref = oracle.reference("pooler", act.x_bits, W)
+    assert oracle.check("pooler", out_f64(out), ref, list(act.probe_rows))["ok"]
+    t = st.cpu().numpy()
+    assert (t > 0).all()
+    assert (np.diff(t, axis=1) >= 0).all()
+    x33 = torch.zeros((33, 8192), dtype=torch.bfloat16, device="cuda")
+    o33 = torch.zeros((33, 4096), dtype=torch.bfloat16, device="cuda")
+    for mm, kw in ((33, dict(kernel=B.PROJ_KERNEL_ROWS)),             # more than 32 tokens
+                   (8, dict(kernel=B.PROJ_KERNEL_ROWS, grid=40)),     # 103 rows per CTA
+                   (8, dict(kernel=B.PROJ_KERNEL_ROWS, groups=3)),    # not a power of two
+                   (8, dict(kernel=B.PROJ_KERNEL_ROWS, variant=B.PROJ_VARIANT_EXPWIN12))):
+        with pytest.raises(B.ProjError) as e:
+            B.proj_run_ex(h, x33, mm, o33, **kw)
+        assert e.value.status == B.PROJ_EUNSUPPORTED, (mm, kw)
+    hr, _, _ = prepared("router", 0)
+    with pytest.raises(B.ProjError) as e:
+        B.proj_run_ex(hr, x33, 8, torch.zeros((8, 256), dtype=torch.float32, device="cuda"),
+                      kernel=B.PROJ_KERNEL_ROWS)
     assert e.value.status == B.PROJ_EUNSUPPORTED
 
 
@@ -477,6 +560,19 @@ def test_unpack_is_lossless(dev, layer):
         B.proj_unpack_weights(h, B.PROJ_UNPACK_FRAG16, back)
         torch.cuda.synchronize()
         assert torch.equal(back.view(torch.int16), Wd.view(torch.int16))
+        # the row-run GEMV's copy (each CTA's rows step-major)
+        back.zero_()
+        B.proj_unpack_weights(h, B.PROJ_UNPACK_RUNS, back)
+        torch.cuda.synchronize()
+        assert torch.equal(back.view(torch.int16), Wd.view(torch.int16))
+        if layer == "unpooler":
+            part = torch.zeros((1024, Wd.shape[1]), dtype=Wd.dtype, device="cuda")
+            B.proj_unpack_weights(h, B.PROJ_UNPACK_RUNS_SLICE, part)
+            torch.cuda.synchronize()
+            assert torch.equal(part.view(torch.int16), Wd[:1024].view(torch.int16))
+        else:
+            with pytest.raises(B.ProjError):
+                B.proj_unpack_weights(h, B.PROJ_UNPACK_RUNS_SLICE, back)
 
 
 @pytest.mark.parametrize("layer", ["qkv_gate", "o", "pooler", "unpooler"])
