@@ -1260,6 +1260,7 @@ int proj_run_ex(proj_handle h, const void* x, int64_t m, void* out, proj_stream 
     q.KG = pl.KG;
     q.out_f32 = 0;
     q.w_evict_first = pl.MT == 1 ? 1 : 0;
+    q.stamps = opts ? static_cast<uint64_t*>(opts->stamps) : nullptr;
     // the exchange slots hold one [256][128] fp32 partial per SM
     if (pl.KG > 1 && pl.G > h->num_sms) return fail(PROJ_EUNSUPPORTED);
     e = pair_launch(pl.bn, h->tmap_w, *xmap, q, pl.T / 2, s);
@@ -1284,6 +1285,7 @@ int proj_run_ex(proj_handle h, const void* x, int64_t m, void* out, proj_stream 
     c.KG = pl.KG;
     c.ws = reinterpret_cast<float*>(h->ws);
     c.counters = h->cl_counters;
+    c.stamps = (opts && !(pl.router && !pl.planes)) ? static_cast<uint64_t*>(opts->stamps) : nullptr;
     // The cluster kernels exchange their partials through L2 when three or
     // more CTAs share a tile and every CTA has a slot (one wave: at most one
     // CTA per SM); otherwise through distributed shared memory (~33 GB/s per

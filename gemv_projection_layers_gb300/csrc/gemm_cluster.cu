@@ -41,6 +41,14 @@ namespace proj {
 namespace {
 
 constexpr int kSmemLimit = 232448;
+// Weight stages the producer issues before the wait on the previous kernel
+// of the stream; the rest of the first ring follows x.  Measured on GB300
+// (device time after an L2 flush): issuing the whole ring early queues the
+// first x tiles behind every SM's weight burst -- the first MMA started
+// ~2.7 us after entry at 256 tokens -- and two early stages took 1.0-1.5 us
+// off each bf16 layer at 128 tokens (qkv_gate 15.2 -> 14.0 us, pooler
+// 18.5 -> 17.0); zero early stages was no better than two.
+constexpr int kClusterEarlyStages = 2;
 
 template <int BN>
 struct CCfg {
@@ -93,6 +101,8 @@ __global__ void __launch_bounds__(CCfg<BN>::kThreads, CCfg<BN>::kBlocksPerSm)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  uint64_t* const stamp = p.stamps ? p.stamps + blockIdx.x * 8 : nullptr;
+  if (stamp && threadIdx.x == 0) stamp[kStampEntry] = globaltimer_ns();
   const uint32_t rank = cluster_rank();
   const int cluster = static_cast<int>(blockIdx.x) / p.CS;
   const int tile = cluster / p.KG;   // output tile (t, mt)
@@ -106,10 +116,11 @@ __global__ void __launch_bounds__(CCfg<BN>::kThreads, CCfg<BN>::kBlocksPerSm)
   const int mv = min(BN, p.m - mt * BN);
 
   // Thread 0 (the producer) sets up the barriers and issues the weights of
-  // the first ring's worth of stages before the CTA barrier: they are
+  // the first kClusterEarlyStages stages before the CTA barrier: they are
   // constant, so they stream before the wait on the previous kernel of the
   // stream; x and every global write come after that wait.
   const int pre = min(kb1 - kb0, S);
+  const int pre_w = min(pre, kClusterEarlyStages);  // weight stages issued before the wait
   uint64_t pol = 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -119,7 +130,7 @@ __global__ void __launch_bounds__(CCfg<BN>::kThreads, CCfg<BN>::kBlocksPerSm)
     mbar_init(accf, 1);
     fence_mbar_init();
     pol = policy_evict_first();
-    for (int j = 0; j < pre; ++j) {
+    for (int j = 0; j < pre_w; ++j) {
       const uint32_t fb = full0 + 8 * j;
       mbar_arrive_expect_tx(fb, kTileBytes + C::kXBytes);
       bulk_g2s(smem_u32(sA + j * kTileBytes),
@@ -149,9 +160,19 @@ __global__ void __launch_bounds__(CCfg<BN>::kThreads, CCfg<BN>::kBlocksPerSm)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       griddep_wait();
-      for (int j = 0; j < pre; ++j)
+      if (stamp) stamp[kStampDepWait] = globaltimer_ns();
+      for (int j = 0; j < pre_w; ++j)
         tma_load_2d(smem_u32(sB + j * C::kXBytes), &tmap_x, ((kb0 + j) % p.KBx) * kTileK,
                     mt * BN, full0 + 8 * j);
+      for (int j = pre_w; j < pre; ++j) {  // the rest of the first ring: weights, then x
+        const uint32_t fb = full0 + 8 * j;
+        mbar_arrive_expect_tx(fb, kTileBytes + C::kXBytes);
+        bulk_g2s(smem_u32(sA + j * kTileBytes),
+                 p.w + (static_cast<size_t>(t) * p.KB + kb0 + j) * kTileBytes, kTileBytes, fb,
+                 pol);
+        tma_load_2d(smem_u32(sB + j * C::kXBytes), &tmap_x, ((kb0 + j) % p.KBx) * kTileK,
+                    mt * BN, fb);
+      }
       int64_t issued = pre;
       for (int kb = kb0 + pre; kb < kb1; ++kb) {
         const int s = static_cast<int>(issued % S);
@@ -184,6 +205,7 @@ __global__ void __launch_bounds__(CCfg<BN>::kThreads, CCfg<BN>::kBlocksPerSm)
         if (!mbar_wait(full0 + 8 * s, static_cast<uint32_t>((j / S) & 1), p.status,
                        kStatusTimeoutMma))
           break;
+        if (stamp && j == 0) stamp[kStampFirstFull] = globaltimer_ns();
         tc_fence_after();
         const uint32_t a = smem_u32(sA + s * kTileBytes);
         const uint32_t b = smem_u32(sB + s * C::kXBytes);
@@ -195,6 +217,7 @@ __global__ void __launch_bounds__(CCfg<BN>::kThreads, CCfg<BN>::kBlocksPerSm)
         tc_commit(empty0 + 8 * s);
       }
       tc_commit(accf);  // also covers an aborted loop: arrives once prior MMAs finish
+      if (stamp) stamp[kStampLastMma] = globaltimer_ns();
     }
   } else if (warp < 2 + C::kDrainWarps) {
     // ------------------------------------- epilogue: accumulator -> smem
@@ -204,6 +227,7 @@ __global__ void __launch_bounds__(CCfg<BN>::kThreads, CCfg<BN>::kBlocksPerSm)
     constexpr int kCols = BN / kParts;
     const int r = q * 32 + lane;
     if (part < kParts && mbar_wait(accf, 0, p.status, kStatusTimeoutEpilogue)) {
+      if (stamp && warp == 2 && lane == 0) stamp[kStampAccReady] = globaltimer_ns();
       tc_fence_after();
       const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
       const int c_beg = part * kCols;
@@ -251,6 +275,7 @@ __global__ void __launch_bounds__(CCfg<BN>::kThreads, CCfg<BN>::kBlocksPerSm)
         });
       }
       tc_fence_before();
+      if (stamp && warp == 2 && lane == 0) stamp[kStampDrained] = globaltimer_ns();
     }
   }
   __syncwarp();
@@ -258,6 +283,7 @@ __global__ void __launch_bounds__(CCfg<BN>::kThreads, CCfg<BN>::kBlocksPerSm)
   // L2 exchange, in its exchange slot; the barrier's release/acquire orders
   // those global stores too).
   cluster_sync_all();
+  if (stamp && threadIdx.x == 0) stamp[kStampCombine] = globaltimer_ns();
   griddep_wait();  // before the first global write of this thread
   if constexpr (kXch) {
     cluster_combine_l2<BN, C::kThreads>(p, red_base, cluster, tile, t, mt, rank, mv);
@@ -270,6 +296,7 @@ __global__ void __launch_bounds__(CCfg<BN>::kThreads, CCfg<BN>::kBlocksPerSm)
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+  if (stamp && threadIdx.x == 0) stamp[kStampExit] = globaltimer_ns();
 }
 
 template <int BN, bool kXch>

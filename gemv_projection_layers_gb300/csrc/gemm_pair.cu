@@ -96,6 +96,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  uint64_t* const stamp = p.stamps ? p.stamps + blockIdx.x * 8 : nullptr;
+  if (stamp && threadIdx.x == 0) stamp[kStampEntry] = globaltimer_ns();
   const uint32_t rank = cluster_rank();
   const uint32_t h = rank & 1u;       // 0: the even CTA of the pair, which issues the MMAs
   const uint32_t lead = rank & ~1u;   // that CTA's rank
@@ -148,6 +150,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                          (t * p.KB + kb0 + j) * kTileRows, full_lead + 8 * j, pol_w);
       }
       griddep_wait();
+      if (stamp) stamp[kStampDepWait] = globaltimer_ns();
       for (int j = 0; j < pre; ++j)
         tma_load_2d_pair(smem_u32(sB + j * C::kXBytes), &tmap_x, ((kb0 + j) % p.KBx) * kTileK,
                          mt * BN + static_cast<int>(h) * C::kHalf, full_lead + 8 * j, pol_x);
@@ -184,6 +187,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         if (!mbar_wait(full0 + 8 * s, static_cast<uint32_t>((j / S) & 1), p.status,
                        kStatusTimeoutMma))
           break;
+        if (stamp && j == 0) stamp[kStampFirstFull] = globaltimer_ns();
         tc_fence_after();
         const uint32_t a = smem_u32(sA + s * kTileBytes);
         const uint32_t b = smem_u32(sB + s * C::kXBytes);
@@ -196,6 +200,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       // arrives once every MMA issued above has completed (also after an
       // aborted loop)
       tc_commit_pair(accf, pair_mask);
+      if (stamp) stamp[kStampLastMma] = globaltimer_ns();
     }
   } else if (warp >= 4) {
     // ---------------------------- drain: accumulator -> shared-memory staging
@@ -208,6 +213,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     const int q = warp & 3;  // the tensor-memory lane quarter this warp may read
     const int r = q * 32 + lane;
     if (mbar_wait_sleep(accf, 0, p.status, kStatusTimeoutEpilogue)) {
+      if (stamp && warp == 4 && lane == 0) stamp[kStampAccReady] = globaltimer_ns();
       tc_fence_after();
       const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
 #pragma unroll 1
@@ -229,6 +235,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   tc_fence_before();
   __syncwarp();
   __syncthreads();  // the staging is complete; every tensor-memory read is done
+  if (stamp && threadIdx.x == 0) stamp[kStampDrained] = globaltimer_ns();
   griddep_wait();   // before the first global write
   const int tid = static_cast<int>(threadIdx.x);
   // An item is 4 consecutive rows of one token (float4 of the staging).
@@ -259,11 +266,15 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   // MMAs with both CTAs' shared memory); with KG > 1 the barrier's release /
   // acquire also orders every CTA's exchange stores before the loads below.
   cluster_sync_all();
+  if (stamp && threadIdx.x == 0) stamp[kStampCombine] = globaltimer_ns();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc_pair(tmem, C::kTmemCols);
   }
-  if (p.KG == 1 || jo0 >= mv) return;
+  if (p.KG == 1 || jo0 >= mv) {
+    if (stamp && threadIdx.x == 0) stamp[kStampExit] = globaltimer_ns();
+    return;
+  }
 
   // ------------------------------------- combine across the cluster's pairs
   // Sum the owned tokens over the KG partials of these 128 rows (cluster
@@ -314,6 +325,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       store_out4(p, mt * BN + jl[u], t * kTileRows + r4[u], acc[u]);
     }
   }
+  if (stamp && threadIdx.x == 0) stamp[kStampExit] = globaltimer_ns();
 }
 
 template <int BN>

@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  if (p.stamps && threadIdx.x == 0) p.stamps[blockIdx.x * 4 + 0] = globaltimer_ns();
+  if (p.stamps && threadIdx.x == 0) p.stamps[blockIdx.x * 8 + kStampEntry] = globaltimer_ns();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int KS = p.KS;
@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(empty0 + 8 * s);
     };
     griddep_wait();  // x may be the previous kernel's output
-    if (p.stamps && threadIdx.x == 0) p.stamps[blockIdx.x * 4 + 1] = globaltimer_ns();
+    if (p.stamps && threadIdx.x == 0) p.stamps[blockIdx.x * 8 + kStampDepWait] = globaltimer_ns();
     // x for stages i .. i + D - 1 in flight (a static register ring: stage
     // i uses slot i % D, refilled with stage i + D right after its MMAs)
     constexpr int D = gemv_rows_x_depth(NT, SPW);
@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         load_x(i + D, xr[d]);
       }
     }
-    if (p.stamps && threadIdx.x == 0) p.stamps[blockIdx.x * 4 + 2] = globaltimer_ns();
+    if (p.stamps && threadIdx.x == 0) p.stamps[blockIdx.x * 8 + kStampDrained] = globaltimer_ns();
     // every stage has been consumed before the ring is reused for the tiles
     named_bar_sync(1, kConsumers * 32);
     if (act) {
@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         sum += ld_shared_f32(ring + static_cast<uint32_t>(((w * 8 * NT + tok) * kRowPitch + row) * 4));
       out[static_cast<size_t>(tok) * p.n_rows + r0 + 16 * qb + row] = __float2bfloat16_rn(sum);
     }
-    if (p.stamps && threadIdx.x == 0) p.stamps[blockIdx.x * 4 + 3] = globaltimer_ns();
+    if (p.stamps && threadIdx.x == 0) p.stamps[blockIdx.x * 8 + kStampExit] = globaltimer_ns();
   }
 }
 

@@ -142,6 +142,18 @@ struct ClusterParams {
   float* xch;           // CS > 1 and every CTA resident: [CTA][BN][128] fp32, the
                         // partials' exchange through L2; null: through distributed
                         // shared memory
+  uint64_t* stamps;     // optional: [CTA][8] %globaltimer phase stamps (kStamp*), or null
+};
+// Phase stamps of the tensor-core kernels (per CTA, 8 slots).
+enum : int {
+  kStampEntry = 0,      // kernel entry
+  kStampDepWait = 1,    // the producer passed the wait on the previous kernel
+  kStampFirstFull = 2,  // the MMA issuer saw the first stage land
+  kStampLastMma = 3,    // the MMA issuer committed the last stage
+  kStampAccReady = 4,   // the drain saw the accumulator complete
+  kStampDrained = 5,    // the accumulator is staged (and exchange stores issued)
+  kStampCombine = 6,    // past the cluster barrier before the combine
+  kStampExit = 7,       // after the combine's last store
 };
 constexpr int kClusterMaxCS = 16;      // CTAs per cluster, at most
 constexpr int kClusterMaxGroups = 16;  // clusters per output tile, at most
@@ -171,6 +183,7 @@ struct PairParams {
   int KG;               // pairs per pair tile (K split), 1..kPairMaxKG
   int out_f32;
   int w_evict_first;    // the weights are read once (MT == 1): evict them first from L2
+  uint64_t* stamps;     // optional: [CTA][8] %globaltimer phase stamps (kStamp*), or null
 };
 constexpr int kPairMaxKG = 8;  // clusters of at most 16 CTAs
 constexpr int kPairThreads = 256;
@@ -267,8 +280,8 @@ struct GemvRowsParams {
   const uint16_t* x;    // bf16 [m, K]
   void* out;            // bf16 [m, n_rows]
   uint32_t* status;
-  uint64_t* stamps;     // optional: [G][4] %globaltimer at entry, after the dependency
-                        // wait, after the main loop, at exit (null: none)
+  uint64_t* stamps;     // optional: [G][8] %globaltimer at entry (slot 0), after the
+                        // dependency wait (1), after the main loop (5), at exit (7); null: none
   int m;
   int n_rows;
   int K;                // multiple of 32 KS

@@ -180,11 +180,16 @@ typedef struct proj_run_opts {
                        (1..8); 0 = dispatch table */
     int tile_n;     /* token tile width of the tensor-core kernels (16, 32, 64, 128
                        or 256; the 12-bit kernel 16 or 32); 0 = dispatch table */
-    void *stamps;   /* optional, for measurement: a device buffer of at least
-                       grid x 4 uint64 that the row-run kernel (PROJ_KERNEL_ROWS)
-                       fills with %globaltimer readings per CTA (entry, after the
-                       wait on the previous kernel of the stream, after the main
-                       loop, exit); NULL = none; ignored by the other kernels */
+    void *stamps;   /* optional, for measurement: a device buffer of 8 uint64 per
+                       CTA of the launch that the row-run kernel (PROJ_KERNEL_ROWS)
+                       and the tensor-core cluster and CTA-pair kernels fill with
+                       %globaltimer readings (ns): [0] entry, [1] the wait on the
+                       previous kernel of the stream passed, [2] first stage landed
+                       (tensor-core issuer), [3] last MMA issued, [4] accumulator
+                       complete, [5] accumulator staged (row-run: main loop done),
+                       [6] past the cluster barrier before the combine, [7] exit;
+                       slots a kernel has no phase for are left as they are;
+                       NULL = none; ignored by the other kernels */
 } proj_run_opts;
 
 typedef struct proj_info_t {

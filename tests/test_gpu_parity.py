@@ -335,20 +335,43 @@ def test_rows_gemv(dev, layer, m):
 
 
 def test_rows_gemv_stamps_and_rejections(dev):
-    """The phase stamps are written per CTA in order; shapes outside the
-    kernel's range are rejected before any launch."""
+    """The phase stamps are written per CTA in order (the row-run kernel and
+    the tensor-core cluster and CTA-pair kernels); shapes outside the
+    row-run kernel's range are rejected before any launch."""
     h, W, _ = prepared("pooler", 0)
     m = 16
     act = wl.make_activations("pooler", m, 0, False)
     x = to_dev_x(act.x_bits)
     G = B.proj_num_sms()
-    st = torch.zeros((G, 4), dtype=torch.int64, device="cuda")
+    st = torch.zeros((G, 8), dtype=torch.int64, device="cuda")
     out = run("pooler", h, x, m, kernel=B.PROJ_KERNEL_ROWS, stamps=st)
     ref = oracle.reference("pooler", act.x_bits, W)
     assert oracle.check("pooler", out_f64(out), ref, list(act.probe_rows))["ok"]
-    t = st.cpu().numpy()
+    t = st.cpu().numpy()[:, [0, 1, 5, 7]]  # entry, wait passed, main loop done, exit
     assert (t > 0).all()
     assert (np.diff(t, axis=1) >= 0).all()
+    # the tensor-core kernels: every phase stamped, in order, per CTA
+    for layer, mm, kw in (("pooler", 128, {}), ("o", 256, {}),
+                          ("pooler", 256, dict(kernel=B.PROJ_KERNEL_PAIR, groups=2))):
+        hh, WW, _ = prepared(layer, 0)
+        desc = B.proj_describe_ex(hh, mm, **kw)
+        ctas = int(desc.split("CTAs=")[1].split()[0])
+        a2 = wl.make_activations(layer, mm, 0, False)
+        st2 = torch.zeros((ctas, 8), dtype=torch.int64, device="cuda")
+        o2 = run(layer, hh, to_dev_x(a2.x_bits), mm, stamps=st2, **kw)
+        rows = np.arange(0, mm, 16)
+        assert oracle.check(layer, out_f64(o2)[rows], oracle.reference(layer, a2.x_bits[rows], WW),
+                            [])["ok"]
+        t2 = st2.cpu().numpy()
+        assert (t2[:, [0, 1, 4, 5, 6, 7]] > 0).all(), (layer, mm, desc)
+        # in order where one thread writes them (thread 0: entry, combine, exit);
+        # %globaltimer readings of different warps need not be ordered
+        assert (np.diff(t2[:, [0, 6, 7]], axis=1) >= 0).all(), (layer, mm, desc)
+        # first stage / last MMA: stamped by the CTAs that issue MMAs (in a CTA
+        # pair, the even one)
+        issuers = t2[:, 2] > 0
+        assert issuers.sum() * (2 if desc.startswith("tc_pair") else 1) == ctas, (layer, mm, desc)
+        assert (t2[issuers][:, 3] > 0).all(), (layer, mm, desc)
     x33 = torch.zeros((33, 8192), dtype=torch.bfloat16, device="cuda")
     o33 = torch.zeros((33, 4096), dtype=torch.bfloat16, device="cuda")
     for mm, kw in ((33, dict(kernel=B.PROJ_KERNEL_ROWS)),             # more than 32 tokens
