@@ -314,7 +314,7 @@ def read_floor_us(B, torch, nbytes, flush, stream, sink2, buf):
         for md, g in ((0, 2 * sms), (0, 3 * sms), (0, 4 * sms), (1, sms)))
 
 
-def time_compressed(B, torch, flush, stream, ms=(1, 8, 16)):
+def time_compressed(B, torch, flush, stream, ms=(1, 8, 16, 128, 256)):
     """The decode shapes with the bf16 weights losslessly recoded to 12 bits
     (prepare flag PROJ_ENCODE_EXPWIN12): each layer's device time with
     variant=EXPWIN12 (the router has no 12-bit form and runs as in the
@@ -322,7 +322,8 @@ def time_compressed(B, torch, flush, stream, ms=(1, 8, 16)):
     with the bytes each reads.  m <= 2: the register GEMV on the row-chunk
     records; from 3 tokens the warp-MMA GEMV on the recoded fragment copy
     where x fits its shared memory, else the stream-K tile kernel on the tile
-    records."""
+    records (128-token tiles at 128 and 256 tokens, beside the same kernel
+    on the dense tiles at the same partition: dense_tile_us)."""
     flush_fn = lambda: flush(stream)
     layers = setup_layers(B, torch, expwin=True)
     res = {}
@@ -350,6 +351,12 @@ def time_compressed(B, torch, flush, stream, ms=(1, 8, 16)):
                         nw * 1.5 + (nw // 1024 * 32 if rc else
                                     L.info["expwin12_escapes"] * S.n_out / L.spec.N * 4))
                 row["x12_kernels"][L.spec.name] = kern
+                if x12 and m > 32:
+                    dense = lambda S=S: B.proj_run_ex(S.h, S.x, S.m, S.out, stream,
+                                                      variant=B.PROJ_VARIANT_DENSE,
+                                                      kernel=B.PROJ_KERNEL_TILE, tile_n=128)
+                    row.setdefault("dense_tile_us", {})[L.spec.name] = round(
+                        time_device_us(torch, dense, flush_fn, stream), 2)
             row["x12_sum_us"] = round(sum(row["x12_us"].values()), 2)
             row["auto_sum_us"] = round(sum(row["auto_us"].values()), 2)
             # each 12-bit shape against the read floor of the bytes it reads

@@ -175,7 +175,10 @@ int bn_for_m(int64_t m) {
 
 // Token counts up to which the 12-bit copy is used by the dispatch table.
 constexpr int64_t kExpwinAutoMaxM = 16;
-constexpr int64_t kExpwinMaxM = 32;
+// The stream-K tile kernel decodes the 12-bit tile records for any m, in
+// token tiles of at most this many tokens (its decoded-tile ring, copy ring
+// and x tiles fit shared memory up to 128).
+constexpr int kExpwinMaxBN = 128;
 
 // Split-K combine by token count: the owner sums the others' partials while
 // its last segment streams (short tail, but one CTA reads S - 1 partials);
@@ -767,7 +770,7 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
   {
     bool use_exp = false;
     if (variant == PROJ_VARIANT_EXPWIN12) {
-      if (!h->w_exp || m > kExpwinMaxM) return PROJ_EUNSUPPORTED;
+      if (!h->w_exp) return PROJ_EUNSUPPORTED;
       use_exp = true;
     } else if (variant == PROJ_VARIANT_AUTO) {
       use_exp = h->w_exp && m <= kExpwinAutoMaxM;
@@ -776,7 +779,8 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
     }
     pl->expwin = use_exp;
     pl->bn = tile_n ? tile_n : bn_for_m(m);
-    if (use_exp && pl->bn > 32) return PROJ_EUNSUPPORTED;
+    if (use_exp && !tile_n && pl->bn > kExpwinMaxBN) pl->bn = kExpwinMaxBN;
+    if (use_exp && pl->bn > kExpwinMaxBN) return PROJ_EUNSUPPORTED;
     pl->T = static_cast<int>(pl->n_out / kTileRows);
     pl->KB = static_cast<int>(h->K / kTileK);
   }

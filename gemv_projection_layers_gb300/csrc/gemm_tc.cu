@@ -516,7 +516,7 @@ cudaError_t launch(const CUtensorMap& tmap, const TcParams& p, cudaStream_t s) {
 }  // namespace
 
 bool tc_supported(int BN, bool expwin) {
-  if (expwin) return BN == 16 || BN == 32;
+  if (expwin) return BN == 16 || BN == 32 || BN == 64 || BN == 128;
   return BN == 16 || BN == 32 || BN == 64 || BN == 128 || BN == 256;
 }
 
@@ -528,6 +528,8 @@ int tc_threads(bool expwin) { return expwin ? 320 : 192; }
       switch (BN) {                                     \
         case 16: { constexpr int kB = 16; constexpr bool kE = true; __VA_ARGS__; } \
         case 32: { constexpr int kB = 32; constexpr bool kE = true; __VA_ARGS__; } \
+        case 64: { constexpr int kB = 64; constexpr bool kE = true; __VA_ARGS__; } \
+        case 128: { constexpr int kB = 128; constexpr bool kE = true; __VA_ARGS__; } \
       }                                                 \
     } else {                                            \
       switch (BN) {                                     \
@@ -559,6 +561,8 @@ cudaError_t tc_init_attributes() {
   if ((e = set_attr<256, false>()) != cudaSuccess) return e;
   if ((e = set_attr<16, true>()) != cudaSuccess) return e;
   if ((e = set_attr<32, true>()) != cudaSuccess) return e;
+  if ((e = set_attr<64, true>()) != cudaSuccess) return e;
+  if ((e = set_attr<128, true>()) != cudaSuccess) return e;
   return cudaSuccess;
 }
 

@@ -112,7 +112,7 @@ int record_status(int status, const char* text);
 int record_cuda(cudaError_t e, const char* what);
 cudaError_t gemv_launch(bool f32w, int MT, const GemvParams& p, cudaStream_t s);
 
-// Tensor-core path: BN in {16, 32, 64, 128, 256}; expwin12 for BN in {16, 32}.
+// Tensor-core path: BN in {16, 32, 64, 128, 256}; expwin12 for BN in {16, 32, 64, 128}.
 bool tc_supported(int BN, bool expwin);
 int tc_threads(bool expwin);
 size_t tc_smem_bytes(int BN, bool expwin);

@@ -104,7 +104,8 @@ enum proj_variant {
                                    copy on the register GEMV at m <= 2, the recoded
                                    fragment copy on the warp-MMA GEMV where x fits its
                                    shared memory (m <= 32), else the tile records on the
-                                   tensor cores (m <= 32); each where it was built */
+                                   tensor cores (stream-K tile kernel, token tiles of
+                                   at most 128: any m); each where it was built */
     PROJ_VARIANT_PLANES3 = 3    /* router only: the fp32 weights as three bf16 planes,
                                    hi + mid + lo == W exactly, on the tensor cores */
 };

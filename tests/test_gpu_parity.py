@@ -602,7 +602,10 @@ def test_unpack_is_lossless(dev, layer):
 def test_expwin12_lossless_and_bit_identical(dev, layer):
     """12-bit exponent-window weights (muse_bf16_proj project report, Round 5):
     window and escapes as the oracle's codec, lossless decode, and outputs
-    bit-identical to the uncompressed kernel at the same partition."""
+    bit-identical to the uncompressed kernel at the same partition -- also at
+    the wide token counts, where the tile kernel decodes records into
+    swizzled bf16 tiles for 64- and 128-token tensor-core tiles (project
+    report, Round 6: decode to shared memory, then the same MMAs)."""
     for seed in (0, 1):
         h, W, Wd = prepared(layer, seed, B.PROJ_ENCODE_EXPWIN12)
         info = B.proj_info(h)
@@ -615,15 +618,18 @@ def test_expwin12_lossless_and_bit_identical(dev, layer):
         B.proj_unpack_weights(h, B.PROJ_VARIANT_EXPWIN12, back)
         torch.cuda.synchronize()
         assert torch.equal(back.view(torch.int16), Wd.view(torch.int16))
-        for m in (1, 8, 16, 32):
+        for m in (1, 8, 16, 32, 64, 128, 130, 256):
             act = wl.make_activations(layer, m, seed + 5, outliers=True)
             x = to_dev_x(act.x_bits)
-            for grid, reduce in ((0, 0), (37, B.PROJ_REDUCE_OWNER),
-                                 (0, B.PROJ_REDUCE_DISTRIBUTED)):
+            combos = ((0, 0), (37, B.PROJ_REDUCE_OWNER), (0, B.PROJ_REDUCE_DISTRIBUTED))
+            if m > 32:  # 64- and 128-token tiles: the distributed combine only
+                combos = ((0, 0), (101, B.PROJ_REDUCE_DISTRIBUTED))
+            tn = 0 if m <= 32 else (64 if m <= 64 else 128)  # the same token tiles
+            for grid, reduce in combos:
                 a = run(layer, h, x, m, variant=B.PROJ_VARIANT_DENSE, grid=grid, reduce=reduce,
-                        kernel=B.PROJ_KERNEL_TILE)
+                        kernel=B.PROJ_KERNEL_TILE, tile_n=tn)
                 b = run(layer, h, x, m, variant=B.PROJ_VARIANT_EXPWIN12, grid=grid,
-                        reduce=reduce, kernel=B.PROJ_KERNEL_TILE)
+                        reduce=reduce, kernel=B.PROJ_KERNEL_TILE, tile_n=tn)
                 assert torch.equal(a.view(torch.int16), b.view(torch.int16)), \
                     (layer, seed, m, grid, reduce)
             check_case(layer, seed, True, m, h=h, W=W, variant=B.PROJ_VARIANT_EXPWIN12)
