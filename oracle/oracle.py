@@ -13,6 +13,8 @@ Contents, each restated from the pages:
 * check(): the correctness contract of guide ch. 1, §1.5 "What counts as
   correct" -- relative L2 per output tensor <= 1 % (router 0.01 %), probe rows
   within 0.1 %, no row over 5x the bound, no NaN/Inf.
+* expwin12_inband_*, expwin12_correction_exact, expwin12_variant_table:
+  the escape designs compared (in-band code 7; the pages' fp32 correction).
 * expwin12_*: the lossless 12-bit exponent-window weight format of the
   project report, "Round 5 -- lossless 12-bit compressed weights", "Format":
   raw low byte + 4-bit (sign, 3-bit window code) + escape list, window of 8
@@ -236,3 +238,103 @@ def expwin12_decode(low: np.ndarray, nib: np.ndarray, esc_index: np.ndarray,
 def expwin12_bytes(n_weights: int, n_escapes: int, escape_entry_bytes: int = 4) -> int:
     """Stream bytes of the format: 1.5 bytes per weight plus the escapes."""
     return (n_weights * 3) // 2 + n_escapes * escape_entry_bytes
+
+
+# --- escape designs compared (project report, "Round 5", "Format" and
+# "Kernel": the exception list; the alternatives the design notes weigh) ---
+
+def expwin12_inband_window(bits: np.ndarray) -> int:
+    """In-band variant: e0 maximising #weights with high7 in [e0, e0 + 6]
+    (code 7 is reserved to mark an escape; smallest e0 on a tie)."""
+    hist = np.bincount(expwin12_high7(bits).ravel(), minlength=128)
+    best_e0, best = 0, -1
+    for e0 in range(127 - 6 + 1):
+        c = int(hist[e0:e0 + EXPWIN_SPAN - 1].sum())
+        if c > best:
+            best_e0, best = e0, c
+    return best_e0
+
+
+def expwin12_inband_encode(bits: np.ndarray, e0: int):
+    """In-band variant: nibble = sign << 3 | code, code = high7 - e0 in 0..6
+    for weights inside the window and 7 for every other weight, whose
+    original high byte goes, in stream order, to the escape list (its
+    position is implied by the code).  Returns (low, nibble, esc_high)."""
+    b = np.asarray(bits, dtype=np.uint16).ravel()
+    low = (b & 0xFF).astype(np.uint8)
+    sign = (b >> 15).astype(np.int64)
+    h7 = (b.astype(np.int64) >> 8) & 0x7F
+    inside = (h7 >= e0) & (h7 <= e0 + EXPWIN_SPAN - 2)
+    code = np.where(inside, h7 - e0, EXPWIN_SPAN - 1)
+    nib = ((sign << 3) | code).astype(np.uint8)
+    esc_high = (b[~inside] >> 8).astype(np.uint8)
+    return low, nib, esc_high
+
+
+def expwin12_inband_decode(low: np.ndarray, nib: np.ndarray, esc_high: np.ndarray,
+                           e0: int) -> np.ndarray:
+    """Inverse of expwin12_inband_encode (flat uint16 bf16 patterns)."""
+    n = nib.astype(np.uint16)
+    code = n & 7
+    high = (((n >> 3) << 7) | (np.uint16(e0) + code)).astype(np.uint16)
+    esc = code == EXPWIN_SPAN - 1
+    high[esc] = esc_high.astype(np.uint16)
+    return ((high << 8) | low.astype(np.uint16)).astype(np.uint16)
+
+
+def expwin12_correction_exact(bits: np.ndarray, e0: int) -> np.ndarray:
+    """The pages' exception design: an escaped weight is stored with its
+    exponent clamped into the window and corrected by an fp32 term
+    delta = w - w_clamped.  True where that delta is exactly an fp32 value
+    (so w_clamped + delta reproduces w), per escaped weight of
+    expwin12_encode (in its order).  The difference is taken in rationals
+    (an FP64 subtraction would itself round when the two are more than 45
+    binades apart); +-inf counts as exact, NaN as not."""
+    from fractions import Fraction
+    b = np.asarray(bits, dtype=np.uint16).ravel()
+    _, nib, esc, _ = expwin12_encode(b, e0)
+    n16 = nib.astype(np.uint16)
+    clamped = (((n16 >> 3) << 15) | ((np.uint16(e0) + (n16 & 7)) << 8) |
+               (b & 0xFF)).astype(np.uint16)
+    w = bf16_bits_to_f64(b[esc])
+    wc = bf16_bits_to_f64(clamped[esc])
+    out = np.zeros(esc.size, dtype=bool)
+    for i in range(esc.size):
+        if np.isinf(w[i]):
+            out[i] = True
+        elif np.isfinite(w[i]):
+            d = Fraction(float(w[i])) - Fraction(float(wc[i]))
+            out[i] = Fraction(float(np.float32(float(d)))) == d
+    return out
+
+
+def expwin12_variant_table(bits: np.ndarray) -> dict:
+    """Escapes and stream bytes per weight of four escape designs on one
+    matrix: the position list (1.5 B + a 4-byte (position, high byte) entry
+    per escape), the in-band code 7 (1.5 B + the 1-byte high byte per
+    escape, window of 7), a bitmap (1.5 B + 1 bit per 8 weights + 2 bytes
+    per escape: in-group position and high byte) and the pages' fp32
+    correction (1.5 B + 8 bytes per escape: position and fp32 delta), with
+    the correction's inexact escapes."""
+    b = np.asarray(bits, dtype=np.uint16).ravel()
+    n = b.size
+    e0 = expwin12_window(b)
+    _, _, esc, _ = expwin12_encode(b, e0)
+    e7 = expwin12_inband_window(b)
+    _, _, esc7 = expwin12_inband_encode(b, e7)
+    exact = expwin12_correction_exact(b, e0)
+    k = esc.size
+    return {
+        "weights": n,
+        "window_e0": e0, "escapes": k, "escape_percent": 100.0 * k / n,
+        "groups_of_8_with_escape_percent": 100.0 * np.unique(esc // 8).size / (n // 8),
+        "inband_window_e0": e7, "inband_escapes": int(esc7.size),
+        "inband_escape_percent": 100.0 * esc7.size / n,
+        "bytes_per_weight": {
+            "position_list": (1.5 * n + 4 * k) / n,
+            "inband_code7": (1.5 * n + 1 * esc7.size) / n,
+            "bitmap": (1.5 * n + n / 64 + 2 * k) / n,
+            "fp32_correction": (1.5 * n + 8 * k) / n,
+        },
+        "fp32_correction_inexact": int((~exact).sum()),
+    }

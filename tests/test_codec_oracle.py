@@ -79,3 +79,52 @@ def test_stream_bytes_ratio():
     n = 4096 * 8192
     b = oracle.expwin12_bytes(n, int(n * 0.00014))
     assert abs(b / (2 * n) - g["bytes_ratio"]) < 0.001
+
+
+@pytest.mark.parametrize("e0", [0, 54, 121])
+def test_inband_code7_round_trips_every_pattern(e0):
+    """The in-band variant (code 7 marks an escape) is lossless for every
+    bf16 pattern, and escapes exactly the patterns outside its 7-wide
+    window."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    low, nib, esc_hi = oracle.expwin12_inband_encode(bits, e0)
+    assert np.array_equal(oracle.expwin12_inband_decode(low, nib, esc_hi, e0), bits)
+    h7 = (bits >> 8) & 0x7F
+    assert esc_hi.size == int(((h7 < e0) | (h7 > e0 + 6)).sum())
+    assert int(((nib & 7) == 7).sum()) == esc_hi.size
+
+
+def test_fp32_correction_is_exact_only_near_the_window():
+    """The pages' correction term w - w_clamped is an fp32 value when the
+    escaped exponent lies at most 14 binades from the window edge (the two
+    8-bit significands then span at most 22 bits), and is not one, for an odd
+    significand, at 18 binades or more (the span exceeds fp32's 24 bits):
+    checked against every bf16 pattern.  The clamped weight keeps the low byte,
+    so the exponent distance is twice the high7 distance."""
+    e0 = 54
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    _, _, esc, _ = oracle.expwin12_encode(bits, e0)
+    exact = oracle.expwin12_correction_exact(bits, e0)
+    h7 = ((bits[esc] >> 8) & 0x7F).astype(np.int64)
+    gap = np.where(h7 < e0, e0 - h7, h7 - (e0 + 7))
+    assert gap.min() == 1
+    assert exact[gap <= 7].all()
+    zero = (bits[esc] & 0x7FFF) == 0                  # +-0: delta = -w_clamped
+    assert exact[zero].all()
+    odd = (bits[esc] & 1) == 1
+    assert not exact[(gap >= 9) & odd].any()
+
+
+def test_escape_designs_on_the_layers():
+    """Escape designs on the synthetic weights: the in-band window of 7 at
+    least doubles the escapes but needs 1 byte each; the position list and
+    the in-band code stay below 1.5006 bytes per weight, the bitmap above
+    1.515; the pages' correction is exact for every escape of these
+    N(0, 1/K) weights."""
+    for layer in ("qkv_gate", "o", "pooler", "unpooler"):
+        t = oracle.expwin12_variant_table(wl.make_weights(layer, 0))
+        assert t["inband_escapes"] >= 2 * t["escapes"], (layer, t)
+        assert t["bytes_per_weight"]["position_list"] < 1.5006, (layer, t)
+        assert t["bytes_per_weight"]["inband_code7"] < 1.5006, (layer, t)
+        assert t["bytes_per_weight"]["bitmap"] > 1.515, (layer, t)
+        assert t["fp32_correction_inexact"] == 0, (layer, t)
