@@ -114,6 +114,8 @@ def load() -> ctypes.CDLL:
     lib.proj_num_sms.argtypes = []
     lib.proj_gemv_static.argtypes = [vp, i32, i64, i64, vp, i64, vp, vp]
     lib.proj_gemv_static.restype = i32
+    lib.proj_gemv_static_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+    lib.proj_gemv_static_status.restype = i32
     _lib = lib
     return lib
 
@@ -270,3 +272,13 @@ def proj_gemv_static(W, w_dtype: int, N: int, K: int, x, m: int, out, stream=Non
                                  _addr(out), _stream(stream))
     if st != PROJ_OK:
         raise ProjError(st, f"proj_gemv_static ({last_cuda_error()})")
+
+
+def proj_gemv_static_status(stream=None) -> int:
+    """Status word of the last proj_gemv_static call on the current device
+    (synchronises `stream`); 0 when every bounded wait completed."""
+    code = ctypes.c_uint32(0)
+    st = load().proj_gemv_static_status(_stream(stream), ctypes.byref(code))
+    if st not in (PROJ_OK, PROJ_EDEVICE):
+        raise ProjError(st, f"proj_gemv_static_status ({last_cuda_error()})")
+    return int(code.value)

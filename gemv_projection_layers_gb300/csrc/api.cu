@@ -209,13 +209,20 @@ constexpr int64_t kGemvMmaMinM = 3;
 // router to its FP32-FMA one); below that, the GEMV.
 constexpr int64_t kClusterMinM = 3;
 // The CTA-pair kernel is the dispatch form above 128 tokens on layers whose
-// K needs no split (K <= 1024: o).  Measured on GB300 (device time, cold
-// L2): o at 256 tokens 10.5 us against the cluster kernel's 11.7; at 128
-// tokens, and on the K = 4096 / 8192 layers, where the pairs must split K
-// across clusters of up to 16 CTAs (at most 15 clusters of 8 are resident),
-// the cluster kernel was as fast or faster (pooler 128: 17.3 vs 20.3 us).
+// K needs no split (K <= 1024: o), and from kPairMinMSplit tokens on the
+// wider-K layers when its shape splits K across at most two pairs (one
+// cluster of four CTAs).  Measured on GB300 (device time, cold L2; pair
+// against cluster kernel): o at 256 tokens 10.6 against 11.7 us; the
+// unpooler at 192 and 256 tokens 21.0 / 21.6 against 22.0 / 22.5 us, at 320-512
+// 27.1-28.1 against 32.0-32.8, at 1000 tokens 51.6 against 61.1; the pooler at
+// 512 tokens 31.3 against 32.7.  Where the pairs must split K three or more
+// ways (the pooler and qkv_gate at 256 tokens: 23.6 / 18.8 against 23.0 /
+// 17.5 us), and below 192 tokens on the wider layers (unpooler at 129: 22.2
+// against 21.4), the cluster kernel stays.
 constexpr int64_t kPairMinM = 129;
 constexpr int64_t kPairMaxK = 1024;
+constexpr int64_t kPairMinMSplit = 192;
+constexpr int kPairMaxAutoKG = 2;
 constexpr int64_t kRouterClusterMinM = 3;
 constexpr int kRouterMaxBN = 64;  // widest token tile of the FP32-FMA router kernel
 
@@ -687,15 +694,26 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
                          (tile_n == 0 || pair_supported(tile_n)) &&
                          (!opts || (opts->grid == 0 && opts->reduce == PROJ_REDUCE_AUTO &&
                                     opts->groups >= 0 && opts->groups <= kPairMaxKG));
-    const bool pair_auto = kern == PROJ_KERNEL_AUTO && m >= kPairMinM && h->K <= kPairMaxK &&
+    const bool pair_auto = kern == PROJ_KERNEL_AUTO && m >= kPairMinM &&
+                           (h->K <= kPairMaxK || m >= kPairMinMSplit) &&
                            (!opts || (opts->grid == 0 && opts->groups == 0 &&
                                       opts->tile_n == 0 && opts->reduce == PROJ_REDUCE_AUTO));
     if (pair_req && !pair_ok) return PROJ_EUNSUPPORTED;
-    if (pair_ok && (pair_req || pair_auto)) {
-      const int bn_hi = tile_n ? tile_n : std::max(64, bn_for_cluster(m));
-      const int bn_lo = tile_n ? tile_n : std::max(64, bn_hi / 2);
-      const PairShape ps = pick_pair(m, T, KB, h->num_sms, h->pair_active, bn_hi, bn_lo,
-                                     opts ? opts->groups : 0);
+    const int bn_hi = tile_n ? tile_n : std::max(64, bn_for_cluster(m));
+    // (automatic choice on the wider-K layers: the widest tile only -- the
+    // 128-token pair tile measured slower there, e.g. the pooler at 256
+    // tokens 26.3 us against 23.6 at 256 and 23.0 for the cluster kernel)
+    const int bn_lo = tile_n ? tile_n
+                      : (pair_auto && h->K > kPairMaxK) ? bn_hi
+                                                         : std::max(64, bn_hi / 2);
+    const PairShape ps = pair_ok && (pair_req || pair_auto)
+                             ? pick_pair(m, T, KB, h->num_sms, h->pair_active, bn_hi, bn_lo,
+                                         opts ? opts->groups : 0)
+                             : PairShape{0, 0};
+    // automatic choice on the wider-K layers: only shapes of at most two pairs per tile
+    const bool pair_take =
+        pair_req || (pair_auto && ps.bn != 0 && (h->K <= kPairMaxK || ps.kg <= kPairMaxAutoKG));
+    if (pair_ok && pair_take) {
       if (ps.bn == 0) return PROJ_EUNSUPPORTED;  // no shape (k-blocks per CTA, residency)
       pl->pair = true;
       pl->cluster = false;

@@ -26,8 +26,9 @@
 // Pipeline per CTA: warp 0 copies (one 2-D TMA of a prepacked 16 KB weight
 // tile and one of the CTA's x rows per k-block, both counted on the even
 // CTA's "full" barrier), warp 1 of the even CTA issues the pair MMAs and
-// commits each stage to both CTAs' "empty" barriers, warps 4..7 drain the
-// accumulator to shared memory; all eight warps store and combine.
+// commits each stage to both CTAs' "empty" barriers; then all eight warps
+// drain the accumulator (own tokens to shared memory, the others to the
+// exchange slot), store and combine.
 #include <cuda_bf16.h>
 
 #include "cluster_common.cuh"
@@ -38,6 +39,7 @@ namespace proj {
 namespace {
 
 constexpr int kPairSmemLimit = 232448;
+constexpr int kPairEarlyStages = 2;
 
 template <int BN>
 struct PCfg {
@@ -141,19 +143,25 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       const uint64_t pol_w = p.w_evict_first ? policy_evict_first() : policy_evict_normal();
       const uint64_t pol_x = policy_evict_normal();
       const int pre = min(nk, S);
+      const int pre_w = min(pre, kPairEarlyStages);
       int issued = 0;
-      // The weights are constant: the first ring's worth streams before the
-      // wait on the previous kernel of the stream; x comes after it.
-      for (int j = 0; j < pre; ++j) {
+      for (int j = 0; j < pre_w; ++j) {
         if (h == 0) mbar_arrive_expect_tx(full0 + 8 * j, 2u * C::kStage);
         tma_load_2d_pair(smem_u32(sA + j * kTileBytes), &tmap_w, 0,
                          (t * p.KB + kb0 + j) * kTileRows, full_lead + 8 * j, pol_w);
       }
       griddep_wait();
       if (stamp) stamp[kStampDepWait] = globaltimer_ns();
-      for (int j = 0; j < pre; ++j)
+      for (int j = 0; j < pre_w; ++j)
         tma_load_2d_pair(smem_u32(sB + j * C::kXBytes), &tmap_x, ((kb0 + j) % p.KBx) * kTileK,
                          mt * BN + static_cast<int>(h) * C::kHalf, full_lead + 8 * j, pol_x);
+      for (int j = pre_w; j < pre; ++j) {
+        if (h == 0) mbar_arrive_expect_tx(full0 + 8 * j, 2u * C::kStage);
+        tma_load_2d_pair(smem_u32(sA + j * kTileBytes), &tmap_w, 0,
+                         (t * p.KB + kb0 + j) * kTileRows, full_lead + 8 * j, pol_w);
+        tma_load_2d_pair(smem_u32(sB + j * C::kXBytes), &tmap_x, ((kb0 + j) % p.KBx) * kTileK,
+                         mt * BN + static_cast<int>(h) * C::kHalf, full_lead + 8 * j, pol_x);
+      }
       issued = pre;
       for (int j = pre; j < nk; ++j) {
         const int s = j % S;
@@ -202,38 +210,50 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       tc_commit_pair(accf, pair_mask);
       if (stamp) stamp[kStampLastMma] = globaltimer_ns();
     }
-  } else if (warp >= 4) {
-    // ---------------------------- drain: accumulator -> shared-memory staging
-    // [BN tokens][128 rows] fp32 at red_base (the ring, free once every MMA
-    // has completed): for each token the warp's 32 lanes write 128
-    // consecutive bytes.  (Storing straight from these registers to global
-    // memory -- 64-128 bytes per warp instruction, one token at a time --
-    // measured 5-12 us for a tile; the coalesced vector stores below take a
-    // fraction of that.)
-    const int q = warp & 3;  // the tensor-memory lane quarter this warp may read
+  }
+  __syncwarp();
+  // ------------------------------------------------------------------ drain
+  // All eight warps, once every MMA has completed: warp w reads tensor-memory
+  // lane quarter w & 3 (rows 32 (w & 3) ..), columns of token half w >> 2.
+  // The tokens this CTA owns go to the shared-memory staging ([BN][128]
+  // fp32 at red_base, the ring, free by then); with KG > 1 the others go
+  // straight from registers to this CTA's exchange slot ([BN][128] fp32: one
+  // warp store is 32 consecutive rows of a token, 128 contiguous bytes).
+  // (A first form drained with four warps into shared memory and copied the
+  // exchange out in a second pass.)
+  const int jo0 = g * BN / p.KG;  // CTA g owns tokens [g BN / KG, (g + 1) BN / KG)
+  const int jo1 = (g + 1) * BN / p.KG;
+  {
+    const int q = warp & 3;
     const int r = q * 32 + lane;
+    const int c_beg = (warp >> 2) * (BN / 2);
+    const int c_end = min(c_beg + BN / 2, mv);
     if (mbar_wait_sleep(accf, 0, p.status, kStatusTimeoutEpilogue)) {
       if (stamp && warp == 4 && lane == 0) stamp[kStampAccReady] = globaltimer_ns();
       tc_fence_after();
       const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+      float* const slot =
+          p.KG > 1 ? p.xch + static_cast<size_t>(blockIdx.x) * BN * kTileRows : nullptr;
+      // (the previous kernel of the stream may be this handle's previous
+      // call, still reading the exchange: wait for it before storing)
+      (void)slot;
+      auto put = [&](int c, float val) {
+        st_shared_f32(red_base + static_cast<uint32_t>((c * kTileRows + r) * 4), val);
+      };
 #pragma unroll 1
-      for (int c0 = 0; c0 < mv; c0 += 32) {
+      for (int c0 = c_beg; c0 < c_end; c0 += 32) {
         float v[16], u[16];
         tmem_ld16(taddr + c0, v);
         tmem_ld16(taddr + c0 + 16, u);
         tmem_ld_wait();
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj)
-          st_shared_f32(red_base + static_cast<uint32_t>(((c0 + jj) * kTileRows + r) * 4), v[jj]);
+        for (int jj = 0; jj < 16; ++jj) put(c0 + jj, v[jj]);
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj)
-          st_shared_f32(red_base + static_cast<uint32_t>(((c0 + 16 + jj) * kTileRows + r) * 4),
-                        u[jj]);
+        for (int jj = 0; jj < 16; ++jj) put(c0 + 16 + jj, u[jj]);
       }
     }
   }
   tc_fence_before();
-  __syncwarp();
   __syncthreads();  // the staging is complete; every tensor-memory read is done
   if (stamp && threadIdx.x == 0) stamp[kStampDrained] = globaltimer_ns();
   griddep_wait();   // before the first global write
@@ -242,19 +262,14 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   auto staged = [&](int j, int r4) {
     return ld_shared_v4(red_base + static_cast<uint32_t>((j * kTileRows + r4) * 4));
   };
-  // CTA g owns tokens [g BN / KG, (g + 1) BN / KG).
-  const int jo0 = g * BN / p.KG;
-  const int jo1 = (g + 1) * BN / p.KG;
   if (p.KG == 1) {
     for (int idx = tid; idx < mv * 32; idx += kPairThreads) {
       const int j = idx >> 5, r4 = (idx & 31) * 4;
       store_out4(p, mt * BN + j, t * kTileRows + r4, staged(j, r4));
     }
   } else {
-    // The valid tokens this CTA does not own go to its exchange slot
-    // ([BN][128] fp32, 512 contiguous bytes per token).
     float* slot = p.xch + static_cast<size_t>(blockIdx.x) * BN * kTileRows;
-    const int lo = min(jo0, mv);  // valid tokens before the owned range
+    const int lo = min(jo0, mv);
     const int n_other = lo + max(mv - jo1, 0);
     for (int idx = tid; idx < n_other * 32; idx += kPairThreads) {
       const int jj = idx >> 5, r4 = (idx & 31) * 4;

@@ -140,3 +140,20 @@ extern "C" int proj_gemv_static(const void* W, int w_dtype, int64_t N, int64_t K
   if (e != cudaSuccess) return record_cuda(e, "proj_gemv_static: kernel launch");
   return PROJ_OK;
 }
+
+extern "C" int proj_gemv_static_status(proj_stream stream, uint32_t* code) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return record_cuda(e, "proj_gemv_static_status: cudaGetDevice");
+  DeviceSlot* d = nullptr;
+  const int st = setup_device(dev, &d);
+  if (st != PROJ_OK) return st;
+  e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return record_cuda(e, "proj_gemv_static_status: stream synchronize");
+  uint32_t word = 0;
+  e = cudaMemcpy(&word, d->scratch + kStatusWord, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return record_cuda(e, "proj_gemv_static_status: reading the status word");
+  if (code) *code = word;
+  return word ? record_status(PROJ_EDEVICE, "proj_gemv_static: a bounded wait gave up")
+              : PROJ_OK;
+}

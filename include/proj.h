@@ -374,8 +374,8 @@ int proj_num_sms(void);
  * launches one kernel.  All calls on a device share the one array, so calls
  * that overlap on the GPU (different streams, or threads without ordering)
  * race and give wrong results; serialise them.  A stall of the kernel's
- * bounded waits is recorded only in that internal status word, which this
- * call does not report.
+ * bounded waits is recorded in that array's status word, which this call
+ * does not report: read it with proj_gemv_static_status.
  *
  * Returns PROJ_OK; PROJ_EINVAL for NULL pointers, N < 1, m < 0 or a bad
  * w_dtype; PROJ_EUNSUPPORTED for m > 2 or K outside the rule above (the
@@ -384,6 +384,15 @@ int proj_num_sms(void);
  */
 int proj_gemv_static(const void *W, int w_dtype, int64_t N, int64_t K, const void *x,
                      int64_t m, void *out, proj_stream stream);
+
+/* The status word of the last proj_gemv_static call on the current device
+ * (each call clears it when it starts; its kernel sets it if a bounded wait
+ * gave up, in which case some rows of `out` are not written).  Synchronises
+ * `stream` -- the stream of that call -- then reads the word; not for use
+ * while `stream` is being captured.  *code receives the raw word if
+ * non-NULL.  Returns PROJ_OK (word zero), PROJ_EDEVICE (non-zero) or
+ * PROJ_ECUDA; allocates nothing. */
+int proj_gemv_static_status(proj_stream stream, uint32_t *code);
 
 #ifdef __cplusplus
 }

@@ -195,11 +195,13 @@ def test_cluster_groups_and_determinism(dev, layer, m):
 def test_pair_shapes_and_determinism(dev, layer, m):
     """The CTA-pair tensor-core kernel (two CTAs per M = 256 MMA, K split
     across the pairs of a cluster whose partials meet in L2): the dispatch
-    form on o above 128 tokens; at every token tile and several K splits it
-    meets the contract and is bitwise reproducible (two calls in a row)."""
+    form on o above 128 tokens and on the unpooler from 192; at every token
+    tile and several K splits it meets the contract and is bitwise
+    reproducible (two calls in a row)."""
+    want_pair = (layer == "o" and m >= 129) or (layer == "unpooler" and m >= 192)
     for seed in (0, 1):
         h, W, _ = prepared(layer, seed)
-        assert B.proj_describe(h, m).startswith("tc_pair") == (layer == "o" and m >= 129)
+        assert B.proj_describe(h, m).startswith("tc_pair") == want_pair, B.proj_describe(h, m)
         ran = 0
         for bn in (64, 128, 256):
             for kg in (0, 1, 2, 3, 5, 8):

@@ -62,6 +62,8 @@ def test_static_scratch_gemv_matches_proj_run(layer, m):
             B.proj_run_ex(h, x, m, o, kernel=B.PROJ_KERNEL_GEMV, grid=grid)
         torch.cuda.synchronize()
         assert B.proj_device_status(h) == 0
+        B.proj_gemv_static(Wd, dt, n_out, spec.K, xs[1], m, got[1])  # the last static call
+        assert B.proj_gemv_static_status() == 0
         W = wl.make_weights(spec, 3)
         for call, (a, g, r, q) in enumerate(zip(acts, got, ref, ring)):
             g64 = g.float().cpu().numpy().astype(np.float64)
@@ -76,6 +78,54 @@ def test_static_scratch_gemv_matches_proj_run(layer, m):
                 (layer, m, call, "ring-form GEMV differs")
     finally:
         B.proj_destroy(h)
+
+
+@pytest.mark.parametrize("m", [1, 2])
+@pytest.mark.parametrize("layer", ["qkv_gate", "router"])
+def test_static_scratch_gemv_in_a_cuda_graph(layer, m):
+    """After one eager call (the per-device set-up), two calls captured on a
+    side stream -- each a memset node and the kernel -- replay with fresh x
+    copied into the captured input buffers and give, bit for bit, the eager
+    call's output on the same x."""
+    assert torch.cuda.is_available()
+    B.load()
+    spec = wl.LAYER_BY_NAME[layer]
+    Wd, dt, odt = _device_weights(spec, 4)
+    N, K = spec.N, spec.K
+    ibits = torch.int32 if odt == torch.float32 else torch.int16
+
+    def xs_for(seed):
+        a = wl.make_activations(spec, m, seed)
+        return torch.from_numpy(a.x_bits.view(np.int16)).cuda().view(torch.bfloat16)
+
+    def eager(x):
+        o = torch.full((m, N), float("nan"), dtype=odt, device="cuda")
+        B.proj_gemv_static(Wd, dt, N, K, x, m, o)
+        torch.cuda.synchronize()
+        return o
+
+    eager(xs_for(10))  # set-up happens outside the capture
+    xin = [torch.empty((m, K), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    outs = [torch.full((m, N), float("nan"), dtype=odt, device="cuda") for _ in range(2)]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for x, o in zip(xin, outs):
+            B.proj_gemv_static(Wd, dt, N, K, x, m, o, stream=s)
+    for replay, seeds in enumerate(((11, 12), (13, 14))):
+        fresh = [xs_for(sd) for sd in seeds]
+        for dst, src in zip(xin, fresh):
+            dst.copy_(src)
+        for o in outs:
+            o.fill_(float("nan"))
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert B.proj_gemv_static_status(s) == 0
+        for x, o in zip(fresh, outs):
+            want = eager(x)
+            assert torch.equal(o.view(ibits), want.view(ibits)), (layer, m, replay)
 
 
 def test_static_scratch_gemv_rejects_sizes_beyond_its_limits():
