@@ -110,6 +110,8 @@ def load() -> ctypes.CDLL:
     lib.proj_last_cuda_error.argtypes = []
     lib.proj_read_floor.restype = i32
     lib.proj_read_floor.argtypes = [vp, i64, vp, i32, i32, vp]
+    lib.proj_fma_peak.restype = i32
+    lib.proj_fma_peak.argtypes = [vp, i32, i32, vp, ctypes.POINTER(ctypes.c_double)]
     lib.proj_num_sms.restype = i32
     lib.proj_num_sms.argtypes = []
     lib.proj_gemv_static.argtypes = [vp, i32, i64, i64, vp, i64, vp, vp]
@@ -259,6 +261,14 @@ proj_last_cuda_error = last_cuda_error
 def proj_read_floor(buf, nbytes: int, sink, grid: int = 0, mode: int = 0, stream=None) -> None:
     _check(load().proj_read_floor(_addr(buf), int(nbytes), _addr(sink), int(grid), int(mode),
                                   _stream(stream)), "proj_read_floor")
+
+
+def proj_fma_peak(sink, iters: int, grid: int = 0, stream=None) -> float:
+    """Enqueue the FP32 FMA probe; returns the launch's FLOPs."""
+    flops = ctypes.c_double(0.0)
+    _check(load().proj_fma_peak(_addr(sink), int(iters), int(grid), _stream(stream),
+                                ctypes.byref(flops)), "proj_fma_peak")
+    return float(flops.value)
 
 
 def proj_num_sms() -> int:

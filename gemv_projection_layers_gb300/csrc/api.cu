@@ -1569,4 +1569,19 @@ int proj_read_floor(const void* buf, int64_t bytes, void* sink, int grid, int mo
   return PROJ_OK;
 }
 
+int proj_fma_peak(void* sink, int iters, int grid, proj_stream stream, double* flops) {
+  if (!sink || iters < 1 || iters > (1 << 24) || grid < 0) return fail(PROJ_EINVAL);
+  if (reinterpret_cast<uintptr_t>(sink) & 3u) return fail(PROJ_EALIGN);
+  if (grid == 0) {
+    const int sms = proj_num_sms();
+    if (sms <= 0) return fail_cuda(cudaErrorNoDevice, "proj_num_sms");
+    grid = 8 * sms;
+  }
+  cudaError_t e = fma_peak_launch(static_cast<uint32_t*>(sink), iters, grid,
+                                  reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "fma peak launch");
+  if (flops) *flops = fma_peak_flops(grid, iters);
+  return PROJ_OK;
+}
+
 }  // extern "C"

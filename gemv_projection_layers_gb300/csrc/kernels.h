@@ -335,6 +335,9 @@ cudaError_t pack_router_planes(const float* W, int N, int K, uint8_t* dst, cudaS
 cudaError_t unpack_router_planes(const uint8_t* src, int N, int K, float* W, cudaStream_t s);
 
 // Streaming read (read.cu).
+// FP32 FMA probe (read.cu): FLOPs of one launch, and the launch.
+double fma_peak_flops(int grid, int iters);
+cudaError_t fma_peak_launch(uint32_t* sink, int iters, int grid, cudaStream_t s);
 cudaError_t read_floor_launch(const void* buf, int64_t bytes, uint32_t* sink, int grid, int mode,
                               cudaStream_t s);
 // bytes / 16 16-byte words from src to dst (both 16-byte aligned, device-

@@ -3,7 +3,9 @@
 // The pages measure the practical ceiling of a weight stream with a
 // hand-written cold-L2 read kernel and a bulk-copy streaming kernel, and find
 // both reach the same time (muse_bf16_proj project report, "Method /
-// tooling" and "Round 2").  Both forms are here: mode 0 streams with 128-bit
+// tooling" and "Round 2").  The file also holds the FP32 FMA probe: the
+// measured ceiling of the CUDA cores' fused multiply-adds, the denominator
+// of the router's FP32-FMA path (guide ch. 1, §1.5: the router in full FP32).  Both forms are here: mode 0 streams with 128-bit
 // non-allocating loads into registers, mode 1 with 1-D bulk copies into a
 // shared-memory ring.  Each CTA reads one contiguous range; a checksum per
 // CTA keeps the loads alive.  Run over a buffer larger than L2 it is also the
@@ -100,7 +102,54 @@ __global__ void __launch_bounds__(256) copy16_kernel(uint4* __restrict__ dst,
   for (int64_t i = blockIdx.x * 256ll + threadIdx.x; i < n16; i += gridDim.x * 256ll) dst[i] = src[i];
 }
 
+// FP32 FMA probe: every thread runs kFmaChains independent dependency chains
+// of packed fp32x2 fused multiply-adds (acc = acc * mul + add, both halves),
+// so the FMA pipes, not latency, set the rate.  mul and add depend on the
+// kernel argument, and the chains' sum decides a store the host never asks
+// for, so nothing is folded or dropped.  Measured on GB300 (eight CTAs of
+// 256 threads per SM, 2070 MHz): 8 chains unrolled 64 deep 78.5 TFLOP/s,
+// 0.97 of SMs x 128 lanes x 2 x clock; a 4-deep unroll 68.7, 12-16 chains
+// 68-72, scalar fma.rn.f32 77.
+constexpr int kFmaThreads = 256;
+constexpr int kFmaChains = 8;
+
+__device__ __forceinline__ uint64_t pack_f2(float lo, float hi) {
+  return (static_cast<uint64_t>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
+}
+
+__global__ void __launch_bounds__(kFmaThreads)
+    fma_peak_kernel(uint32_t* __restrict__ sink, int iters, float seed) {
+  const float base = seed + static_cast<float>(threadIdx.x) * 1e-6f;
+  uint64_t acc[kFmaChains];
+#pragma unroll
+  for (int c = 0; c < kFmaChains; ++c)
+    acc[c] = pack_f2(base + static_cast<float>(c), base - static_cast<float>(c));
+  const uint64_t mul = pack_f2(1.0f - 1e-7f * seed, 1.0f + 1e-7f * seed);
+  const uint64_t add = pack_f2(1e-7f * seed, -1e-7f * seed);
+#pragma unroll 64
+  for (int i = 0; i < iters; ++i) {
+#pragma unroll
+    for (int c = 0; c < kFmaChains; ++c)
+      asm("fma.rn.f32x2 %0, %0, %1, %2;" : "+l"(acc[c]) : "l"(mul), "l"(add));
+  }
+  float sum = 0.f;
+#pragma unroll
+  for (int c = 0; c < kFmaChains; ++c)
+    sum += __uint_as_float(static_cast<uint32_t>(acc[c])) +
+           __uint_as_float(static_cast<uint32_t>(acc[c] >> 32));
+  if (sum == 1.25e30f) sink[0] = __float_as_uint(sum);
+}
+
 }  // namespace
+
+double fma_peak_flops(int grid, int iters) {
+  return static_cast<double>(grid) * kFmaThreads * kFmaChains * 2.0 * 2.0 * iters;
+}
+
+cudaError_t fma_peak_launch(uint32_t* sink, int iters, int grid, cudaStream_t s) {
+  fma_peak_kernel<<<grid, kFmaThreads, 0, s>>>(sink, iters, 1.0f);
+  return cudaGetLastError();
+}
 
 cudaError_t copy16_launch(void* dst, const void* src, int64_t bytes, int sms, cudaStream_t s) {
   const int64_t n16 = bytes / 16;

@@ -337,6 +337,20 @@ const char *proj_last_cuda_error(void);
 int proj_read_floor(const void *buf, int64_t bytes, void *sink, int grid, int mode,
                     proj_stream stream);
 
+/*
+ * FP32 FMA probe: the measured ceiling of the CUDA cores' fp32 fused
+ * multiply-adds, the denominator for the router's FP32-FMA path (guide ch. 1,
+ * §1.5).  Launches `grid` CTAs of 256 threads (grid = 0: eight per SM), each
+ * thread running 8 independent chains of packed `fma.rn.f32x2` for `iters`
+ * steps (1 <= iters <= 2^24); enqueued on `stream`, time it with events
+ * there.  `sink` (device, >= 4 bytes, 4-byte aligned) is never written in
+ * practice: it keeps the arithmetic alive.  *flops (if non-NULL) receives the
+ * launch's floating-point operations, grid x 256 x 8 x 2 x 2 x iters.
+ * Returns PROJ_OK; PROJ_EINVAL (NULL sink, iters or grid out of range);
+ * PROJ_EALIGN; PROJ_ECUDA.
+ */
+int proj_fma_peak(void *sink, int iters, int grid, proj_stream stream, double *flops);
+
 /* Number of SMs of the current device (0 on error). */
 int proj_num_sms(void);
 

@@ -55,6 +55,12 @@ def test_argument_errors_before_any_device_call(lib):
     assert lib.proj_read_floor(16, 16, 16, 0, 8, None) == B.PROJ_EINVAL
     assert lib.proj_read_floor(16, 16, 16, 0, -1, None) == B.PROJ_EINVAL
     assert lib.proj_read_floor(8, 16, 16, 0, 0, None) == B.PROJ_EALIGN
+    # FMA probe argument checks
+    assert lib.proj_fma_peak(None, 16, 0, None, None) == B.PROJ_EINVAL
+    assert lib.proj_fma_peak(16, 0, 4, None, None) == B.PROJ_EINVAL
+    assert lib.proj_fma_peak(16, (1 << 24) + 1, 4, None, None) == B.PROJ_EINVAL
+    assert lib.proj_fma_peak(16, 16, -1, None, None) == B.PROJ_EINVAL
+    assert lib.proj_fma_peak(18, 16, 4, None, None) == B.PROJ_EALIGN
 
 
 def test_status_strings(lib):

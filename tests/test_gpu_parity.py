@@ -939,3 +939,26 @@ def test_dependent_chain_back_to_back(dev, m):
             assert res["ok"], (m, rep, name, res)
             assert B.proj_device_status(h) == 0
             xin = o
+
+
+def test_fma_peak_probe(dev):
+    """The FP32 FMA probe runs, never writes its sink, reports its FLOPs, and
+    measures a rate within the part's range: above half the derived peak
+    (SMs x 128 FMA lanes x 2 FLOP x the maximum SM clock) and at most a
+    little above it."""
+    sms = B.proj_num_sms()
+    sink = torch.zeros(4, dtype=torch.int32, device="cuda")
+    s = torch.cuda.Stream()
+    for _ in range(2):
+        flops = B.proj_fma_peak(sink, 2048, 0, s)
+    assert flops == 8 * sms * 256 * 8 * 2 * 2 * 2048
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    B.proj_fma_peak(sink, 2048, 0, s)
+    e1.record(s)
+    e1.synchronize()
+    tflops = flops / (e0.elapsed_time(e1) * 1e-3) / 1e12
+    derived = sms * 128 * 2 * 2.07e9 / 1e12
+    assert 0.5 * derived < tflops < 1.1 * derived, (tflops, derived)
+    assert int(sink.abs().sum().item()) == 0
+    assert B.proj_fma_peak(sink, 16, 3, s) == 3 * 256 * 8 * 2 * 2 * 16
