@@ -251,13 +251,15 @@ int proj_run_ex(proj_handle h, const void *x, int64_t m, void *out, proj_stream 
 
 /*
  * End-to-end call on HOST buffers: copies x_host [m, K] bf16 to a
- * handle-owned device buffer, runs the projection, and copies the result to
- * out_host [m, proj_out_features(h, m)], all enqueued on `stream`.  For
- * page-locked host buffers (16-byte aligned) the transfers are copy kernels
- * reading and writing the buffers' device mapping; other host memory goes
- * through cudaMemcpyAsync (asynchronous only for page-locked memory).  The
- * caller synchronises `stream` before reading out_host.  Same m rules as
- * proj_run.
+ * handle-owned device buffer, runs the projection, and delivers the result to
+ * out_host [m, proj_out_features(h, m)], all enqueued on `stream`.  For a
+ * page-locked x_host (16-byte aligned) the copy in is a copy kernel reading
+ * the buffer's device mapping; for a page-locked out_host the projection
+ * kernel stores the result straight into its device mapping (every element
+ * written once, as on device memory); other host memory goes through
+ * cudaMemcpyAsync and a handle-owned staging buffer (asynchronous only for
+ * page-locked memory).  The caller synchronises `stream` before reading
+ * out_host.  Same m rules as proj_run.
  */
 int proj_run_host(proj_handle h, const void *x_host, int64_t m, void *out_host,
                   proj_stream stream);

@@ -830,10 +830,15 @@ def test_expwin12_register_gemv_planted_escapes(dev):
 
 @pytest.mark.parametrize("pinned", [True, False])
 def test_run_host_matches_device_run(dev, pinned):
-    """proj_run_host equals proj_run bit for bit: page-locked buffers move
-    through copy kernels on their device mapping, pageable ones through
-    cudaMemcpyAsync (then synchronous)."""
-    for layer, m in (("o", 1), ("router", 16), ("unpooler", 8), ("pooler", 130)):
+    """proj_run_host equals proj_run bit for bit: a page-locked x moves in
+    through a copy kernel on its device mapping and the projection kernel
+    stores straight into a page-locked output's mapping; pageable buffers go
+    through cudaMemcpyAsync (then synchronous).  One shape per kernel family
+    (register GEMV, router GEMVs, warp-MMA and row-run GEMVs, cluster, CTA
+    pair, FP32-FMA router)."""
+    for layer, m in (("o", 1), ("router", 16), ("unpooler", 8), ("pooler", 130),
+                     ("qkv_gate", 8), ("router", 5), ("router", 64), ("o", 256),
+                     ("unpooler", 256), ("qkv_gate", 32)):
         spec = wl.LAYER_BY_NAME[layer]
         h, W, _ = prepared(layer, 0)
         act = wl.make_activations(layer, m, 3, False)
