@@ -19,19 +19,20 @@
 //   conflict-free) with one bulk copy each, and the x tile with the same
 //   128-byte-swizzled 2-D TMA load as the tensor-core kernel.
 // * Eight compute warps.  At each stage a warp first widens (exactly) the
-//   bf16 x of its 8 tokens over its k-range to fp32 in a private shared-memory
-//   scratch.  A thread owns 8 rows x 4 tokens; per 4 k it loads its 8 rows'
-//   weights and its 4 tokens' x (16-byte loads each, no per-step widening or
-//   swizzle arithmetic on x), and issues fma.rn.f32x2 on (even k, odd k)
-//   pairs, so each output keeps two fp32 partial sums (even and odd k) added
-//   at the end.  (Widening inside the 4-k step instead measured 3-10 %
-//   slower at 64..512 tokens: its integer work sits between the loads and the
-//   FMAs.)  Narrow token tiles split each stage's 64 k among warp groups
-//   inside the CTA; their partial tiles are added in group order.  Nine
-//   warps put three on one of the SM's four schedulers, whose quarter of the
-//   register file then holds about 170 registers per thread, which sets the
-//   8 x 4 tile; sixteen compute warps with 4 x 4 tiles measured slower (more
-//   loads per FMA).
+//   bf16 x of its 16 tokens over its k-range to fp32 in a private
+//   shared-memory scratch, k-major (one 64-byte row of 16 tokens per k).  A
+//   thread owns 8 rows x 8 tokens.  Per 4 k it loads its 8 rows' weights
+//   (16-byte loads from the 32 KB tiles) and, per k, its 8 tokens' x as four
+//   token pairs (two 16-byte loads, one address per half-warp), and issues
+//   fma.rn.f32x2 with the weight in both halves against each token pair, so
+//   every output is one fp32 sum in k order.  (The previous thread tile,
+//   8 rows x 4 tokens with (even k, odd k) pairs, needed 36 shared-memory
+//   wavefronts per warp for 64 pair-FMAs against 40 for 128 here; the
+//   token pairs measured 1-2 us faster at 128-256 tokens and 5 us at 512.)
+//   Narrow token tiles split each stage's 64 k among warp groups inside the
+//   CTA; their partial tiles are added in group order.  Nine warps put three
+//   on one of the SM's four schedulers, whose quarter of the register file
+//   then holds about 170 registers per thread: the 8 x 8 tile takes 135-160.
 // The pages' router runs cross-CTA split-K on warp-level FMAs/MMAs with an
 // atomic epilogue (project report, Round 4; notebook n. 28, n. 38); here the
 // combine is deterministic and there is one launch.
@@ -53,32 +54,33 @@ struct RCfg {
   static constexpr int kStage = kRfBytes + kXBytes;
   static constexpr int kComputeWarps = 8;
   static constexpr int kThreads = (kComputeWarps + 1) * 32;  // warp 0: producer
-  static constexpr int kWpt = BN / 8;                // warps per token tile
+  static constexpr int kWpt = BN / 16;               // warps per token tile (16 tokens each)
   static constexpr int kKGroups = kComputeWarps / kWpt;  // k-groups inside the CTA
   static constexpr int kKPerGroup = kRfK / kKGroups;     // k of a stage per warp
-  static constexpr int kScrAll = kComputeWarps * 8 * (kKPerGroup * 4 + 16);
+  // per compute warp: its 16 tokens' x for its k-range of a stage, widened
+  // to fp32, k-major ([kKPerGroup][16] floats, 64 bytes per k)
+  static constexpr int kScrWarp = kKPerGroup * 64;
+  static constexpr int kScrAll = kComputeWarps * kScrWarp;
   static constexpr int kFit = (kSmemMax - 1024 - 1024 - kScrAll) / kStage;
   static constexpr int S = kFit > 8 ? 8 : kFit;
-  // per compute warp: its 8 tokens' x for its k-range of a stage, widened to
-  // fp32 ([8][kKPerGroup + 4] floats: the 16-byte pad puts the two token
-  // halves of a warp on different banks)
-  static constexpr int kScrStride = kKPerGroup * 4 + 16;  // bytes per token row
-  static constexpr int kScrWarp = 8 * kScrStride;
   static constexpr size_t kRing = static_cast<size_t>(S) * kStage;
   static constexpr size_t kPart = static_cast<size_t>(kKGroups) * BN * kTileRows * 4;
   static constexpr size_t kData = kRing > kPart ? kRing : kPart;
   static constexpr size_t kSmem = 1024 + kData + kScrAll + (2 * S) * 8 + 16;
   static_assert(S >= 3, "pipeline too shallow");
   static_assert(kSmem <= kSmemMax, "shared memory budget");
-  static_assert(kKPerGroup % 4 == 0, "k step");
+  static_assert(kKPerGroup % 8 == 0, "k step");
 };
 
 __device__ __forceinline__ void ld_shared_2x64(uint32_t addr, uint64_t& a, uint64_t& b) {
   asm volatile("ld.shared.v2.u64 {%0,%1}, [%2];" : "=l"(a), "=l"(b) : "r"(addr));
 }
-// (acc.lo, acc.hi) += (w.lo, w.hi) * (x.lo, x.hi)
-__device__ __forceinline__ void ffma2(uint64_t& acc, uint64_t w, uint64_t x) {
-  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(w), "l"(x));
+// (acc.lo, acc.hi) += (w, w) * (x.lo, x.hi): one weight times two tokens
+__device__ __forceinline__ void ffma2_bcast(uint64_t& acc, uint32_t w, uint64_t x) {
+  asm("{\n\t.reg .b64 wp;\n\tmov.b64 wp, {%1, %1};\n\t"
+      "fma.rn.f32x2 %0, wp, %2, %0;\n\t}"
+      : "+l"(acc)
+      : "r"(w), "l"(x));
 }
 
 // kXch: the partials are exchanged through L2 (p.xch), else through
@@ -175,15 +177,15 @@ __global__ void __launch_bounds__(RCfg<BN>::kThreads, 1)
 
   // ---------------------------------------------------------- compute warps
   const int cw = warp - 1;
-  const int tt = cw % C::kWpt;        // token sub-tile of 8
+  const int tt = cw % C::kWpt;        // token sub-tile of 16
   const int kg = cw / C::kWpt;        // k-group inside the CTA
   const int rg = lane & 15;           // rows rg + 16 i
-  const int tg = lane >> 4;           // tokens 8 tt + 4 tg + u
+  const int tg = lane >> 4;           // tokens 16 tt + 8 tg + 2 q + {0, 1} (pair q)
   uint64_t acc[8][4];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int u = 0; u < 4; ++u) acc[i][u] = 0ull;
+    for (int q = 0; q < 4; ++q) acc[i][q] = 0ull;
   if (warp > 0) {
     int64_t j = 0;
     for (int kb = kb0; kb < kb1; ++kb, ++j) {
@@ -195,53 +197,49 @@ __global__ void __launch_bounds__(RCfg<BN>::kThreads, 1)
       }
       const uint32_t wst = sW + s * kRfBytes;
       const uint32_t xst = sX + s * C::kXBytes;
-      // Widen this warp's 8 tokens x its k-range of the stage to fp32 once
-      // (16-byte chunks of the 128-byte-swizzled bf16 tile).
+      // Widen this warp's 16 tokens x its k-range of the stage to fp32 once,
+      // k-major (16-byte chunks of the 128-byte-swizzled bf16 tile).
       const uint32_t scr = sScr + static_cast<uint32_t>(cw * C::kScrWarp);
       {
         constexpr int kCh = C::kKPerGroup / 8;  // 16-byte bf16 chunks per token
 #pragma unroll
-        for (int idx = lane; idx < 8 * kCh; idx += 32) {
-          const int t8 = idx / kCh, cc = idx % kCh;
-          const int jt = 8 * tt + t8;
+        for (int idx = lane; idx < 16 * kCh; idx += 32) {
+          const int t16 = idx & 15, cc = idx >> 4;
+          const int jt = 16 * tt + t16;
           const int kc = kg * kCh + cc;
           const uint4 v = ld_shared_u4(xst + jt * 128 + ((kc ^ (jt & 7)) << 4));
-          const uint32_t a = scr + t8 * C::kScrStride + cc * 32;
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(v.x << 16),
-                       "r"(v.x & 0xFFFF0000u), "r"(v.y << 16), "r"(v.y & 0xFFFF0000u)
-                       : "memory");
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(a + 16), "r"(v.z << 16),
-                       "r"(v.z & 0xFFFF0000u), "r"(v.w << 16), "r"(v.w & 0xFFFF0000u)
-                       : "memory");
+          const uint32_t a = scr + static_cast<uint32_t>(cc * 8 * 64 + t16 * 4);
+          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            st_shared_f32(a + (2 * e) * 64, __uint_as_float(w4[e] << 16));
+            st_shared_f32(a + (2 * e + 1) * 64, __uint_as_float(w4[e] & 0xFFFF0000u));
+          }
         }
         __syncwarp();
       }
-      // fully unrolled over the stage: the next steps' shared-memory loads
-      // issue under this step's FMAs (measured 2-4 % faster than unrolling
-      // by two at 256-512 tokens, no change below)
 #pragma unroll
       for (int kk = 0; kk < C::kKPerGroup; kk += 4) {
         const int k0 = kg * C::kKPerGroup + kk;
         const int c = k0 >> 2;  // 16-byte weight chunk
-        uint64_t w01[8], w23[8];
+        uint4 w[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int r = rg + 16 * i;
-          ld_shared_2x64(wst + r * 256 + ((c ^ (r & 15)) << 4), w01[i], w23[i]);
+          w[i] = ld_shared_u4(wst + r * 256 + ((c ^ (r & 15)) << 4));
         }
-        uint64_t x01[4], x23[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          ld_shared_2x64(scr + (4 * tg + u) * C::kScrStride + kk * 4, x01[u], x23[u]);
-        // 32 independent pair-FMAs, then the 32 that depend on them
+        for (int k4 = 0; k4 < 4; ++k4) {
+          uint64_t xq[4];  // token pairs (0,1) (2,3) (4,5) (6,7) of the lane's eight
+          ld_shared_2x64(scr + (kk + k4) * 64 + tg * 32, xq[0], xq[1]);
+          ld_shared_2x64(scr + (kk + k4) * 64 + tg * 32 + 16, xq[2], xq[3]);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t wk = k4 == 0 ? w[i].x : k4 == 1 ? w[i].y : k4 == 2 ? w[i].z : w[i].w;
 #pragma unroll
-          for (int u = 0; u < 4; ++u) ffma2(acc[i][u], w01[i], x01[u]);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-#pragma unroll
-          for (int u = 0; u < 4; ++u) ffma2(acc[i][u], w23[i], x23[u]);
+            for (int q = 0; q < 4; ++q) ffma2_bcast(acc[i][q], wk, xq[q]);
+          }
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * s);
@@ -256,12 +254,13 @@ __global__ void __launch_bounds__(RCfg<BN>::kThreads, 1)
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int q = 0; q < 4; ++q) {
         const int r = rg + 16 * i;
-        const int jt = 8 * tt + 4 * tg + u;
-        const float v = __uint_as_float(static_cast<uint32_t>(acc[i][u])) +
-                        __uint_as_float(static_cast<uint32_t>(acc[i][u] >> 32));
-        st_shared_f32(part_base + static_cast<uint32_t>(((kg * BN + jt) * kTileRows + r) * 4), v);
+        const int jt = 16 * tt + 8 * tg + 2 * q;
+        st_shared_f32(part_base + static_cast<uint32_t>(((kg * BN + jt) * kTileRows + r) * 4),
+                      __uint_as_float(static_cast<uint32_t>(acc[i][q])));
+        st_shared_f32(part_base + static_cast<uint32_t>(((kg * BN + jt + 1) * kTileRows + r) * 4),
+                      __uint_as_float(static_cast<uint32_t>(acc[i][q] >> 32)));
       }
     }
   }
