@@ -316,6 +316,31 @@ ClusterShape pick_cluster(int64_t m, int T, int KB, const ClusterCost& cost, int
   }
   return best;
 }
+// The FP32-FMA router's launch shape, when one wave of clusters of four holds
+// it: token tiles of 16 up to 48 tokens and of 32 above, clusters of four
+// CTAs splitting K, and as many clusters per tile as fill the SMs (at most
+// eight).  A device-time sweep of every shape (token tile 16/32/64 x cluster
+// size 1..8 x clusters per tile 1..16, cold L2) at 25..512 tokens put
+// clusters of four within 0.5 us of the best shape at every token count and
+// found the cost model above 0.7-2.6 us off at 25-48, 96, 256 and 512 tokens:
+// its smooth terms miss how clusters of three, six or seven CTAs pack into
+// the GPU's processing clusters (144 CTAs in clusters of three or six took
+// twice the time of 128 in clusters of four, though the occupancy query
+// admits them).  Returns bn = 0 where the rule does not apply.
+ClusterShape router_fma_shape(int64_t m, int T, int KB, int sms,
+                              const int (*max_active)[kClusterMaxCS]) {
+  constexpr int kCs = 4;
+  constexpr int kMaxKg = 8;
+  const int bn = m <= 48 ? 16 : 32;
+  const int64_t tiles = static_cast<int64_t>(T) * ((m + bn - 1) / bn);
+  int kg = static_cast<int>(std::min<int64_t>(kMaxKg, sms / (kCs * tiles)));
+  while (kg >= 1 && KB / (kCs * kg) < kMinKbPerCtaFma) --kg;
+  if (kg < 1) return ClusterShape{0, 0, 0};
+  const int act = max_active[bn_index(bn)][kCs - 1];
+  if (act > 0 && tiles * kg > act) return ClusterShape{0, 0, 0};
+  return ClusterShape{bn, kCs, kg};
+}
+
 // Launch shape of the CTA-pair kernel: token tile bn (the smallest covering
 // m, or its half) and pairs per pair tile kg (one cluster of 2 kg CTAs).
 // Scored like the cluster kernels: the stream is the slower of an SM's
@@ -766,9 +791,13 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
     const bool forced = opts && (opts->grid > 0 || opts->groups > 0);
     int bn0 = tile_n ? tile_n : bn_for_cluster(m);
     if (fma && bn0 > kRouterMaxBN) bn0 = kRouterMaxBN;
-    const ClusterShape shp =
+    ClusterShape shp =
         pick_cluster(m, pl->T, pl->KB, cost, h->num_sms, bn0, (tile_n || forced) ? bn0 : bn0 / 4,
                      fma ? h->rcluster_active : h->cluster_active);
+    if (fma && !tile_n && !forced) {
+      const ClusterShape r = router_fma_shape(m, pl->T, pl->KB, h->num_sms, h->rcluster_active);
+      if (r.bn) shp = r;
+    }
     pl->bn = shp.bn;
     pl->MT = static_cast<int>((m + pl->bn - 1) / pl->bn);
     int cs = shp.cs, kg = shp.kg;
