@@ -81,6 +81,24 @@ def test_stream_bytes_ratio():
     assert abs(b / (2 * n) - g["bytes_ratio"]) < 0.001
 
 
+def test_stream_bytes_match_the_encoded_fields():
+    """The byte count of the format equals what the encoder emits: one low
+    byte per weight, two 4-bit nibbles per byte, and a 4-byte entry
+    (position, original high byte) per escape."""
+    W = wl.make_weights("pooler", 0)
+    bits = W.ravel()
+    e0 = oracle.expwin12_window(bits)
+    low, nib, esc, esc_high = oracle.expwin12_encode(bits, e0)
+    assert low.dtype == np.uint8 and low.size == bits.size
+    assert int(nib.max()) < 16 and nib.size == bits.size
+    packed = (nib[0::2].astype(np.uint16) | (nib[1::2].astype(np.uint16) << 4))
+    assert int(packed.max()) < 256 and packed.size == bits.size // 2
+    assert esc_high.dtype == np.uint8 and esc_high.size == esc.size
+    emitted = low.size + packed.size + 4 * esc.size
+    assert emitted == oracle.expwin12_bytes(bits.size, esc.size)
+    assert 0.75 < emitted / (2 * bits.size) < 0.7504
+
+
 @pytest.mark.parametrize("e0", [0, 54, 121])
 def test_inband_code7_round_trips_every_pattern(e0):
     """The in-band variant (code 7 marks an escape) is lossless for every
