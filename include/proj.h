@@ -167,7 +167,8 @@ enum proj_kernel {
                                tokens per tile; grid and reduce must be 0; groups > 1
                                needs the grid within one CTA per SM (the partials'
                                exchange is sized for that), else PROJ_EUNSUPPORTED; the
-                               dispatch form on o above 128 tokens */
+                               dispatch form on o above 128 tokens and on the unpooler
+                               from 192 */
 };
 
 typedef struct proj_run_opts {
