@@ -1,9 +1,11 @@
 // gemm_cluster.cu -- tensor-core GEMM, split-K inside a thread-block
-// cluster, combined through distributed shared memory: the bf16 layers at
-// 3..64 tokens (the pooler from 3; the CTA-pair kernel takes wider tiles) and,
-// on request only (PROJ_VARIANT_PLANES3), the router with its fp32 weights as
-// three exact bf16 planes.  The router's dispatch form is the FP32-FMA path
-// at every token count (router_cluster.cu and the router GEMVs).
+// cluster, the partials combined through L2 or distributed shared memory:
+// the dispatch form of the bf16 layers above the few-token GEMVs (qkv_gate
+// and the pooler from 9 tokens, o from 17 to 128, the unpooler from 9 to
+// 191; the CTA-pair kernel takes o above 128 tokens and the unpooler from
+// 192) and, on request only (PROJ_VARIANT_PLANES3), the router with its fp32
+// weights as three exact bf16 planes.  The router's dispatch form is the
+// FP32-FMA path at every token count (router_cluster.cu and the router GEMVs).
 //
 // out[i, n] = sum_k x[i, k] W[n, k]            (muse_bf16_proj guide, ch. 1, §1.1)
 //
