@@ -945,7 +945,8 @@ def run_shape(args):
         B.proj_run_ex(h, x, m, out, variant=variant)
     torch.cuda.synchronize()
     status = B.proj_device_status(h)
-    print(json.dumps({"shape": args.shape, "kernel": B.proj_describe(h, m), "launches": args.steps,
+    print(json.dumps({"shape": args.shape, "kernel": B.proj_describe_ex(h, m, variant=variant),
+                      "launches": args.steps,
                       "device_status": status}))
     B.proj_destroy(h)
 

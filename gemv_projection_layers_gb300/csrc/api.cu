@@ -583,7 +583,8 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
   // per CTA, eight rows per cluster): x staged per CTA is 1/8 of the
   // whole-row form's.
   if (kern == PROJ_KERNEL_GEMV_SPLITK ||
-      (pl->router && kern == PROJ_KERNEL_AUTO && variant == PROJ_VARIANT_AUTO &&
+      (pl->router && kern == PROJ_KERNEL_AUTO &&
+       (variant == PROJ_VARIANT_AUTO || variant == PROJ_VARIANT_DENSE) &&
        m >= kRouterGemvCcAutoMinM && m <= kRouterGemvCcAutoMaxM &&
        (!opts || (opts->grid == 0 && opts->groups == 0 && opts->tile_n == 0 &&
                   opts->reduce == PROJ_REDUCE_AUTO)))) {
@@ -608,7 +609,9 @@ int make_plan(const proj_ctx* h, int64_t m, const proj_run_opts* opts, Plan* pl)
   // pass of eight tokens makes it slower than the cluster kernel.)
   if (pl->router && m <= kRouterGemvMaxM &&
       (kern == PROJ_KERNEL_GEMV_REG ||
-       (kern == PROJ_KERNEL_AUTO && variant == PROJ_VARIANT_AUTO && m <= kRouterGemvAutoMaxM &&
+       (kern == PROJ_KERNEL_AUTO &&
+        (variant == PROJ_VARIANT_AUTO || variant == PROJ_VARIANT_DENSE) &&
+        m <= kRouterGemvAutoMaxM &&
         (!opts || (opts->grid == 0 && opts->groups == 0 && opts->tile_n == 0 &&
                    opts->reduce == PROJ_REDUCE_AUTO))))) {
     int64_t G = std::min<int64_t>(pl->n_out, h->num_sms);

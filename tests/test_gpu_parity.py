@@ -401,6 +401,8 @@ def test_router_gemv(dev, m):
         desc = B.proj_describe(h, m)
         assert desc.startswith("router_gemv_f32w") == (m <= 8), desc
         assert desc.startswith("router_gemv_splitk") == (9 <= m <= 24), desc
+        # fp32 weights as they are: the dense variant is the automatic one
+        assert B.proj_describe_ex(h, m, variant=B.PROJ_VARIANT_DENSE) == desc
         for kw in (dict(), dict(kernel=B.PROJ_KERNEL_GEMV_REG, grid=128),
                    dict(kernel=B.PROJ_KERNEL_GEMV_REG, grid=150)):
             a = check_case("router", seed, seed == 1, m, h=h, W=W, **kw)
